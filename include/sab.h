@@ -1,0 +1,235 @@
+/*
+ * sab.h -- C ABI of libsab.so: streaming chunk attention over a rolling ring
+ * KV cache, for NVIDIA GB300 (sm_103a).
+ *
+ * What the library computes
+ * -------------------------
+ * Streaming autoregressive video-diffusion world models generate a video
+ * chunk by chunk.  Inside every transformer block the queries of the current
+ * chunk attend
+ *   - bidirectionally to the keys of their own chunk, and
+ *   - causally to the keys of the W chunks before it, held in a rolling KV
+ *     cache, plus optionally a permanent sink / reference chunk.
+ * ("WanToFight: Real-Time Generative Game Engine for Multi-Player Combat
+ * Interaction", section 三, table "模型组件", rows "Block-Causal Attention" and
+ * "Rolling KV Cache"; "Matrix-Game 4.0: Harnessing Video Models for Real-Time
+ * Playable Game Worlds", sections "前置知识 / 因果自回归与 KV 缓存" and
+ * "技术新颖性".)  The cache is a ring: chunk c lives in slot c mod R and a new
+ * chunk overwrites the oldest slot in place ("Matrix-Game 4.0", section
+ * "技术新颖性": in-place overwrite of the oldest slot instead of a whole-window
+ * copy).  Optionally the KV cache is stored as FP8 E4M3 with one fp32 scale
+ * per (batch, head, chunk) and tensor ("Matrix-Game 4.0", section
+ * "技术新颖性": 8-bit keys/values per window interval).
+ *
+ * For query token i of chunk c and visible key set J(c):
+ *   s_ij  = softmax_scale * <q_i, k_j>
+ *   O_i   = sum_j softmax_j(s_ij) v_j,   LSE_i = ln sum_{j in J(c)} exp(s_ij)
+ * J(c) = sink tokens (if used) + tokens of chunks max(0, c-W) .. c.
+ *
+ * Conventions for every call
+ * --------------------------
+ * - Element types: Q, K, V, O are bf16 (stored as uint16 bit patterns); LSE is
+ *   fp32; the FP8 cache stores E4M3 codes as uint8 and fp32 scales.
+ * - Token-major tensors ("[B, L, H, D]") are contiguous, row-major, last index
+ *   fastest: element (b, t, h, d) at ((b*L + t)*H + h)*D + d.  This is the
+ *   layout a fused QKV projection produces.
+ * - Pointers named "device" point to device memory of the current CUDA device;
+ *   every device pointer must be 16-byte aligned.  The caller owns all device
+ *   memory (ring, inputs, outputs, workspace); the library owns only the small
+ *   host handle of a ring.
+ * - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call is
+ *   asynchronous on that stream and never synchronises the host, except
+ *   sab_get_last_device_error.  No call allocates device memory.
+ * - Arguments are validated before anything is enqueued: on any error code
+ *   nothing is launched and no memory is touched.  No C++ exception crosses
+ *   this ABI.
+ * - Supported shapes: head_dim D in {64, 128}; chunk_tokens >= 1; every other
+ *   extent >= 1 and small enough that row counts fit in int32.
+ */
+#ifndef SAB_H_
+#define SAB_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SAB_OK = 0,
+  SAB_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad shape or value   */
+  SAB_ERR_UNSUPPORTED = 2,   /* valid request this build does not implement   */
+  SAB_ERR_OUT_OF_RANGE = 3,  /* chunk not held by the ring / bad chunk order  */
+  SAB_ERR_WORKSPACE = 4,     /* workspace missing or smaller than required    */
+  SAB_ERR_CUDA = 5,          /* a CUDA runtime/driver call failed             */
+  SAB_ERR_TIMEOUT = 6        /* a device-side pipeline wait gave up (see sab_get_last_device_error) */
+} sab_status;
+
+typedef enum { SAB_KV_BF16 = 0, SAB_KV_FP8_E4M3 = 1 } sab_kv_dtype;
+
+/* Shape of one ring KV cache with `num_layers` independent per-layer rings. */
+typedef struct {
+  int num_layers;    /* transformer blocks sharing the ring geometry (>= 1)       */
+  int batch;         /* B                                                          */
+  int heads;         /* H                                                          */
+  int head_dim;      /* D, 64 or 128                                               */
+  int chunk_tokens;  /* Lc, tokens per chunk                                       */
+  int ring_slots;    /* R, cached chunks (the rolling window's capacity)          */
+  int has_sink;      /* 1: reserve a permanent sink/reference slot, else 0         */
+  int kv_dtype;      /* sab_kv_dtype                                               */
+} sab_ring_desc;
+
+typedef struct sab_ring sab_ring; /* opaque host handle */
+
+/*
+ * Device memory layout of a ring (informative; use sab_kv_ring_layer_ptrs):
+ * per layer, 256-byte aligned regions
+ *   K codes  [B][H][(has_sink + R) * Lc][D]   (bf16, or uint8 E4M3)
+ *   V codes  same
+ *   K scales [B][H][has_sink + R] fp32        (FP8 only)
+ *   V scales same                             (FP8 only)
+ * Rows [0, Lc) hold the sink when has_sink; slot r holds rows
+ * [(has_sink + r) * Lc, (has_sink + r + 1) * Lc).
+ */
+
+/* Bytes of device memory a ring with this shape needs; 0 if the shape is invalid. */
+size_t sab_kv_ring_bytes(const sab_ring_desc* desc);
+
+/*
+ * Create a ring on caller-owned device memory `dev_mem` (`bytes` >=
+ * sab_kv_ring_bytes, 256-byte aligned).  Enqueues a zero fill of the whole
+ * region on `stream` (so slots never written hold finite zeros) and returns a
+ * new host handle in *out.  The handle records, per layer, the newest chunk
+ * appended (none yet) and whether the sink is set.
+ */
+sab_status sab_kv_ring_create(const sab_ring_desc* desc, void* dev_mem, size_t bytes,
+                              void* stream, sab_ring** out);
+
+/* Free the host handle only (the device memory stays the caller's). NULL is a no-op. */
+sab_status sab_kv_ring_destroy(sab_ring* ring);
+
+/* Copy of the descriptor the ring was created with. */
+sab_status sab_kv_ring_get_desc(const sab_ring* ring, sab_ring_desc* desc);
+
+/*
+ * Device pointers of layer `layer`'s regions (any output may be NULL).  The
+ * scale pointers are NULL for a BF16 ring.  Intended for checkpointing and
+ * tests: the memory is the caller's.
+ */
+sab_status sab_kv_ring_layer_ptrs(const sab_ring* ring, int layer, void** k, void** v,
+                                  float** k_scale, float** v_scale);
+
+/*
+ * Write the sink / reference chunk of `layer` ("Matrix-Game 4.0", section
+ * "前置知识 / 因果自回归与 KV 缓存": recent window plus a reference frame; it is
+ * never evicted).  K, V: device, token-major [B, Lc, H, D] bf16.  For an FP8
+ * ring they are quantised exactly as sab_kv_ring_append does.
+ * Errors: INVALID_ARG (null/misaligned, layer out of range),
+ * UNSUPPORTED (ring has no sink slot).
+ */
+sab_status sab_kv_ring_set_sink(sab_ring* ring, int layer, const void* K, const void* V,
+                                void* stream);
+
+/*
+ * Append chunk `chunk` of layer `layer` into slot chunk mod R, overwriting
+ * that slot in place ("Matrix-Game 4.0", section "技术新颖性").  K, V: device,
+ * token-major [B, Lc, H, D] bf16; they are transposed to the head-major slot
+ * rows.  The copy is bit-exact for a BF16 ring.  For an FP8 ring each (b, h)
+ * block of Lc x D values is quantised with amax = max |x|,
+ * scale = amax / 448 (fp32, round-to-nearest division; 1 when amax = 0),
+ * code = E4M3(x / scale) rounded to nearest even with saturation to +-448;
+ * the scale is stored beside the slot.
+ * `chunk` must be >= 0 and, after the first append of that layer, equal to
+ * the newest appended chunk (an in-place rewrite, e.g. the clean re-run of a
+ * chunk) or one more.  Errors: INVALID_ARG, OUT_OF_RANGE (chunk order).
+ */
+sab_status sab_kv_ring_append(sab_ring* ring, int layer, long long chunk, const void* K,
+                              const void* V, void* stream);
+
+/* Slot of `chunk` in `layer`'s ring: chunk mod R if the chunk is held, else OUT_OF_RANGE. */
+sab_status sab_kv_ring_slot_of(const sab_ring* ring, int layer, long long chunk, int* slot);
+
+/*
+ * Host-side state for checkpoint/resume, one entry per layer: the newest
+ * appended chunk (-1: none), how many chunks the ring holds (0..R; they are
+ * newest-held+1 .. newest) and whether the sink is set.  A caller that saves
+ * the ring's device memory and this state can restore both and continue the
+ * stream.  set_state validates every entry (held <= R, held <= newest+1,
+ * held == 0 iff newest == -1) before changing anything.
+ */
+sab_status sab_kv_ring_get_state(const sab_ring* ring, long long* newest_chunk /*[num_layers]*/,
+                                 int* held /*[num_layers]*/, int* sink_set /*[num_layers]*/);
+sab_status sab_kv_ring_set_state(sab_ring* ring, const long long* newest_chunk, const int* held,
+                                 const int* sink_set);
+
+/*
+ * Workspace bytes sab_chunk_attention needs for `num_splits` KV partitions
+ * (0 when num_splits == 1).  The workspace holds per-split partial outputs
+ * and LSEs plus one arrival counter per query tile; the counters must be zero
+ * before the first call (zero-fill the workspace once after allocating it);
+ * every successful call leaves them zero again.
+ */
+size_t sab_chunk_attention_workspace(const sab_ring* ring, int num_splits);
+
+/*
+ * Attention of chunk `chunk`'s queries over the ring of layer `layer`.
+ *   Q      device, token-major [B, Lc, H, D] bf16 (the chunk's queries).
+ *   K_cur, V_cur
+ *          device, token-major [B, Lc, H, D] bf16: the current chunk's keys
+ *          and values computed fresh at this denoise step; or both NULL when
+ *          the current chunk was already appended to the ring.
+ *   window W >= 0: previous chunks attended (visible chunks c-W .. c).
+ *   use_sink  1 to attend to the sink (the ring must have one, and it must be set).
+ *   num_splits >= 1: KV partitions computed in parallel and merged by
+ *          log-sum-exp inside the same kernel ("Matrix-Game 4.0", section
+ *          "技术新颖性": the window is cut into intervals whose partial outputs
+ *          are merged with log-sum-exp).
+ *   softmax_scale  usually 1/sqrt(D).
+ *   O      device, token-major [B, Lc, H, D] bf16 (output).
+ *   LSE    device, [B, H, Lc] fp32, natural log of sum exp(s) (output; may be NULL).
+ *   workspace/ws_bytes  device scratch, >= sab_chunk_attention_workspace.
+ * Every chunk in max(0, c-W) .. c-1 (and c itself when K_cur is NULL) must be
+ * held by the ring: OUT_OF_RANGE otherwise.  Device-side pipeline waits are
+ * bounded; a wait that gives up is reported by sab_get_last_device_error.
+ */
+sab_status sab_chunk_attention(const sab_ring* ring, int layer, long long chunk, const void* Q,
+                               const void* K_cur, const void* V_cur, int window, int use_sink,
+                               int num_splits, float softmax_scale, void* O, float* LSE,
+                               void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Block-causal attention over whole sequences (training / causal-adaptation
+ * shape; "WanToFight", section "训练流程 / Stage 2": the dense mask is replaced
+ * by a block-causal one, bidirectional inside a chunk, each chunk seeing
+ * itself and the `window` chunks before it).  Token t is in chunk
+ * t / chunk_tokens; query i sees key j iff 0 <= chunk(i) - chunk(j) <= window.
+ *   Q, K, V  device, token-major [B, L, H, D] bf16;  O likewise (output);
+ *   LSE      device, [B, H, L] fp32 (output; may be NULL).
+ *   num_splits / workspace as for sab_chunk_attention (size from
+ *   sab_block_causal_attention_workspace).
+ */
+size_t sab_block_causal_attention_workspace(int B, int L, int H, int D, int num_splits);
+sab_status sab_block_causal_attention(const void* Q, const void* K, const void* V, int B, int L,
+                                      int H, int D, int chunk_tokens, int window, int num_splits,
+                                      float softmax_scale, void* O, float* LSE, void* workspace,
+                                      size_t ws_bytes, void* stream);
+
+/*
+ * Synchronise `stream`, then report and clear the device error word that
+ * bounded pipeline waits set when they give up (SAB_ERR_TIMEOUT), or
+ * SAB_ERR_CUDA if the stream itself reports an error.  SAB_OK otherwise.
+ */
+sab_status sab_get_last_device_error(void* stream);
+
+/* Static, human-readable name of a status code. */
+const char* sab_status_string(sab_status status);
+
+/* Library version string. */
+const char* sab_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SAB_H_ */

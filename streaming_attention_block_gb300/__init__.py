@@ -1,0 +1,35 @@
+"""Streaming chunk attention over a rolling ring KV cache, for GB300 (sm_103a).
+
+Thin Python binding of ``libsab.so`` (C ABI in ``include/sab.h``): argument
+marshalling only.  Every step of the computation runs in the library's CUDA
+kernels; PyTorch is used only to own device memory and to name streams.
+There is no CPU or PyTorch fallback: every call fails loudly when the library
+is missing.
+"""
+
+from ._abi import (  # noqa: F401
+    KV_BF16,
+    KV_FP8_E4M3,
+    KVRing,
+    RingDesc,
+    SabError,
+    block_causal_attention,
+    block_causal_attention_workspace,
+    chunk_attention,
+    chunk_attention_workspace,
+    get_last_device_error,
+    kv_ring_append,
+    kv_ring_bytes,
+    kv_ring_create,
+    kv_ring_destroy,
+    kv_ring_get_desc,
+    kv_ring_get_state,
+    kv_ring_layer_ptrs,
+    kv_ring_set_sink,
+    kv_ring_set_state,
+    kv_ring_slot_of,
+    library,
+    library_path,
+    status_string,
+    version,
+)

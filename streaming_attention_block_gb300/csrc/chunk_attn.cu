@@ -1,0 +1,610 @@
+// Chunk attention over a ring KV cache (streaming) or a whole sequence
+// (block-causal), for sm_103a: TMA tile loads, tcgen05 MMAs with TMEM
+// accumulators, online softmax in registers, split-KV with an in-kernel
+// log-sum-exp merge.
+//
+// What it computes (see include/sab.h): for every query row i of a (b, h)
+// and its visible key set J, O_i = softmax_j(scale * q_i.k_j) V and
+// LSE_i = ln sum_j exp(scale * q_i.k_j).  Visibility follows the block-causal
+// chunk rule of "WanToFight: Real-Time Generative Game Engine for
+// Multi-Player Combat Interaction" (section 三, table "模型组件", row
+// "Block-Causal Attention"): bidirectional inside a chunk, causal over the W
+// previous chunks, plus an optional sink ("Matrix-Game 4.0: Harnessing Video
+// Models for Real-Time Playable Game Worlds", section "前置知识 / 因果自回归与
+// KV 缓存").  The mask is never materialised: in streaming mode every key the
+// host planner hands over is visible and only the ragged end of a key run is
+// masked; in block-causal mode each row derives its key interval from its
+// chunk index.
+//
+// Design (one CTA = QT query tiles of 128 rows x one (b, h) x one KV split):
+//   warp 0      TMA producer: Q once, then K/V tiles through a smem ring of
+//               kStages stages (128-byte swizzle, 64-column boxes).
+//   warp 1      TMEM allocator and single-thread tcgen05 MMA issuer:
+//               S_t = Q_t K^T (M=128, N=128) into TMEM, then O_t += P_t V with
+//               P_t read from TMEM (it overwrites S_t in place, as bf16).
+//   warps 4..   one softmax warpgroup per query tile: thread = row = TMEM
+//               lane; loads S, updates the running max (a rescale of O in
+//               TMEM only when the max grows by more than 2^8, exact in real
+//               arithmetic), writes P, and runs the epilogue.
+// The MMA thread interleaves the two tiles (S_0, PV_1, S_1, PV_0, ...), so one
+// warpgroup's exponentials overlap the other tile's MMAs.  Split partials go
+// to a workspace; the last CTA of a query tile to finish (atomic ticket)
+// merges them by log-sum-exp ("Matrix-Game 4.0", section "技术新颖性": KV
+// window intervals computed in parallel and merged with log-sum-exp).
+//
+// Every mbarrier wait is bounded: on expiry the kernel records the wait site
+// in a device error word, raises a CTA-wide abort flag, drains its own TMA
+// copies and MMAs (again with bounded waits), frees TMEM and returns.
+#include <math.h>
+
+#include "ptx.cuh"
+#include "sab_internal.h"
+
+namespace sab {
+
+__device__ unsigned int g_sab_error_word = 0;
+
+namespace {
+
+using namespace ptx;
+
+constexpr uint32_t kWaitLimit = 1u << 23;  // ~2 s with the 256 ns back-off
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows by > 2^8
+
+template <int D_, int QT_>
+struct Cfg {
+  static constexpr int D = D_, QT = QT_;
+  static constexpr int kBoxes = D / 64;                  // 64-column (128-byte) boxes per row
+  static constexpr uint32_t kBoxBytes = 128u * 128u;     // 128 rows x 128 bytes
+  static constexpr uint32_t kTileBytes = kBoxBytes * kBoxes;
+  static constexpr int kStages = (D == 128) ? 2 : 4;
+  // K stages, V stages, then Q: every operand region is followed by another
+  // operand region inside the allocation.
+  static constexpr uint32_t kKOff = 0;
+  static constexpr uint32_t kVOff = kKOff + kStages * kTileBytes;
+  static constexpr uint32_t kQOff = kVOff + kStages * kTileBytes;
+  static constexpr uint32_t kBarOff = kQOff + QT * kTileBytes;
+  static constexpr int kBarQ = 0;
+  static constexpr int kBarKFull = 1;
+  static constexpr int kBarVFull = kBarKFull + kStages;
+  static constexpr int kBarKVEmpty = kBarVFull + kStages;
+  static constexpr int kBarSFull = kBarKVEmpty + kStages;  // [2]
+  static constexpr int kBarPFull = kBarSFull + 2;          // [2]
+  static constexpr int kBarOFinal = kBarPFull + 2;         // [2]
+  static constexpr int kBarDrain = kBarOFinal + 2;
+  static constexpr int kNumBars = kBarDrain + 1;
+  static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;  // + alignment slack
+  static constexpr int kThreads = 128 + 128 * QT;
+  static constexpr uint32_t kTmemS = 0;          // S_t / P_t at column t * 128
+  static constexpr uint32_t kTmemO = QT * 128;   // O_t at column kTmemO + t * D
+  static constexpr uint32_t kTmemCols = (QT * 128 + QT * D <= 256) ? 256u : 512u;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                             unsigned site) {
+#pragma unroll 1
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (it >= 64) {
+      if (*abort_flag) return false;
+      __nanosleep(it < 4096 ? 32 : 256);
+      if (it >= kWaitLimit) {
+        atomicOr(&g_sab_error_word, 1u << site);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
+// Bounded wait used while draining after an abort (ignores the abort flag).
+__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity) {
+#pragma unroll 1
+  for (uint32_t it = 0; it < kWaitLimit; ++it) {
+    if (mbar_try_wait(bar, parity)) return;
+    if (it >= 64) __nanosleep(256);
+  }
+  atomicOr(&g_sab_error_word, 1u << 31);
+}
+
+struct Tile {
+  int src;    // tensor-map index
+  int row;    // first key row of the tile in the map's row axis
+  int valid;  // keys of the run inside this tile (streaming); 128 otherwise
+};
+
+__device__ __forceinline__ Tile stream_tile(const AttnParams& p, int g) {
+  int s = 0;
+#pragma unroll
+  for (int i = 1; i < kMaxSegments; ++i)
+    if (i < p.nseg && g >= p.seg[i].tile0) s = i;
+  const int t = g - p.seg[s].tile0;
+  Tile ti;
+  ti.src = p.seg[s].src;
+  ti.row = p.seg[s].row0 + t * kTileN;
+  ti.valid = min(kTileN, p.seg[s].nrows - t * kTileN);
+  return ti;
+}
+
+__device__ __forceinline__ Tile tile_at(const AttnParams& p, int g) {
+  if (p.mode == kModeStreaming) return stream_tile(p, g);
+  Tile ti;
+  ti.src = 0;
+  ti.row = g * kTileN;
+  ti.valid = kTileN;
+  return ti;
+}
+
+// KV tiles of this CTA: [first, first + count).
+__device__ __forceinline__ void kv_range(const AttnParams& p, int q0, int qrows, int split,
+                                         int& first, int& count) {
+  int total = 0, base = 0;
+  if (p.mode == kModeStreaming) {
+    total = p.total_tiles;
+  } else {
+    const int q_last = min(p.Lq, q0 + qrows) - 1;
+    if (q_last >= q0) {
+      const int c_lo = q0 / p.chunk_tokens, c_hi = q_last / p.chunk_tokens;
+      const int klo = max(0, c_lo - p.window) * p.chunk_tokens;
+      const int khi = min(p.Lk, (c_hi + 1) * p.chunk_tokens);
+      base = klo / kTileN;
+      total = (khi + kTileN - 1) / kTileN - base;
+    }
+  }
+  const long long a = (long long)total * split / p.splits;
+  const long long e = (long long)total * (split + 1) / p.splits;
+  first = base + (int)a;
+  count = (int)(e - a);
+}
+
+template <int D, int QT>
+__global__ void __launch_bounds__(Cfg<D, QT>::kThreads, 1)
+chunk_attn_kernel(const __grid_constant__ AttnParams p) {
+  using C = Cfg<D, QT>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  const uint32_t base_u32 = (raw_u32 + 1023u) & ~1023u;
+  uint8_t* base = smem_raw + (base_u32 - raw_u32);
+  const uint32_t sQ = base_u32 + C::kQOff;
+  const uint32_t sK = base_u32 + C::kKOff;
+  const uint32_t sV = base_u32 + C::kVOff;
+  const uint32_t bars = base_u32 + C::kBarOff;
+  uint32_t* misc = reinterpret_cast<uint32_t*>(base + C::kMiscOff);  // [0] tmem, [1] abort, [2] ticket
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
+  volatile uint32_t* ticket = misc + 2;
+  auto bar = [&](int i) -> uint32_t { return bars + 8u * (uint32_t)i; };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int qg = blockIdx.x;
+  const int bh = blockIdx.y;
+  const int split = blockIdx.z;
+  const int b = bh / p.H;
+  const int h = bh - b * p.H;
+  const int q0 = qg * QT * kTileM;
+
+  int first = 0, n_tiles = 0;
+  kv_range(p, q0, QT * kTileM, split, first, n_tiles);
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(C::kBarQ), 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(bar(C::kBarKFull + s), 1);
+      mbar_init(bar(C::kBarVFull + s), 1);
+      mbar_init(bar(C::kBarKVEmpty + s), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(C::kBarSFull + t), 1);
+      mbar_init(bar(C::kBarPFull + t), 128);
+      mbar_init(bar(C::kBarOFinal + t), 1);
+    }
+    mbar_init(bar(C::kBarDrain), 1);
+    misc[1] = 0;
+    misc[2] = 0;
+    fence_mbar_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(misc), C::kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&p.q_map);
+    prefetch_tmap(&p.k_map[0]);
+    prefetch_tmap(&p.v_map[0]);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar(C::kBarQ), QT * C::kTileBytes);
+#pragma unroll
+      for (int t = 0; t < QT; ++t)
+#pragma unroll
+        for (int bx = 0; bx < C::kBoxes; ++bx)
+          tma_load_4d(sQ + t * C::kTileBytes + bx * C::kBoxBytes, &p.q_map, bar(C::kBarQ), bx * 64,
+                      q0 + t * kTileM, h, b);
+      int j = 0;
+      for (; j < n_tiles; ++j) {
+        const int st = j % C::kStages;
+        const uint32_t round = (uint32_t)(j / C::kStages);
+        if (j >= C::kStages &&
+            !wait_bounded(bar(C::kBarKVEmpty + st), (round - 1u) & 1u, abort_flag, 0))
+          break;
+        const Tile ti = tile_at(p, first + j);
+        mbar_arrive_expect_tx(bar(C::kBarKFull + st), C::kTileBytes);
+#pragma unroll
+        for (int bx = 0; bx < C::kBoxes; ++bx)
+          tma_load_4d(sK + st * C::kTileBytes + bx * C::kBoxBytes, &p.k_map[ti.src],
+                      bar(C::kBarKFull + st), bx * 64, ti.row, h, b);
+        mbar_arrive_expect_tx(bar(C::kBarVFull + st), C::kTileBytes);
+#pragma unroll
+        for (int bx = 0; bx < C::kBoxes; ++bx)
+          tma_load_4d(sV + st * C::kTileBytes + bx * C::kBoxBytes, &p.v_map[ti.src],
+                      bar(C::kBarVFull + st), bx * 64, ti.row, h, b);
+      }
+      if (*abort_flag) {
+        // let every copy this thread issued land before the CTA exits
+        wait_drain(bar(C::kBarQ), 0);
+        for (int jj = max(0, j - C::kStages); jj < j; ++jj) {
+          const int st = jj % C::kStages;
+          const uint32_t ph = (uint32_t)(jj / C::kStages) & 1u;
+          wait_drain(bar(C::kBarKFull + st), ph);
+          wait_drain(bar(C::kBarVFull + st), ph);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = idesc_bf16_f32(128, kTileN, 0);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 1);
+      bool ok = wait_bounded(bar(C::kBarQ), 0, abort_flag, 1);
+      if (ok) tc_fence_after();
+      auto issue_s = [&](int t, int j) {
+        const int st = j % C::kStages;
+        const uint32_t d = tmem + C::kTmemS + t * 128;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t koff = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
+          const uint64_t a = smem_desc_sw128(sQ + t * C::kTileBytes + koff, 16, 1024);
+          const uint64_t bd = smem_desc_sw128(sK + st * C::kTileBytes + koff, 16, 1024);
+          mma_ss(d, a, bd, idesc_qk, kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_pv = [&](int t, int j) -> bool {
+        if (!wait_bounded(bar(C::kBarPFull + t), (uint32_t)j & 1u, abort_flag, 2 + t)) return false;
+        const int st = j % C::kStages;
+        if (!wait_bounded(bar(C::kBarVFull + st), (uint32_t)(j / C::kStages) & 1u, abort_flag, 4))
+          return false;
+        tc_fence_after();
+        const uint32_t d = tmem + C::kTmemO + t * D;
+#pragma unroll
+        for (int kk = 0; kk < kTileN / 16; ++kk) {
+          const uint32_t a_t = tmem + C::kTmemS + t * 128 + kk * 8;
+          const uint64_t bd = smem_desc_sw128(sV + st * C::kTileBytes + kk * 16 * 128, C::kBoxBytes, 1024);
+          mma_ts(d, a_t, bd, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        return true;
+      };
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        const int st = j % C::kStages;
+        if (j > 0 && !(ok = issue_pv(0, j - 1))) break;
+        if (!(ok = wait_bounded(bar(C::kBarKFull + st), (uint32_t)(j / C::kStages) & 1u, abort_flag, 5)))
+          break;
+        tc_fence_after();
+        issue_s(0, j);
+        mma_commit(bar(C::kBarSFull + 0));
+        if (QT == 2) {
+          if (j > 0 && !(ok = issue_pv(1, j - 1))) break;
+          issue_s(1, j);
+          mma_commit(bar(C::kBarSFull + 1));
+        }
+        if (j > 0) mma_commit(bar(C::kBarKVEmpty + (j - 1) % C::kStages));
+      }
+      if (ok) {
+        if (n_tiles > 0) {
+          ok = issue_pv(0, n_tiles - 1);
+          if (ok) mma_commit(bar(C::kBarOFinal + 0));
+          if (ok && QT == 2) {
+            ok = issue_pv(1, n_tiles - 1);
+            if (ok) mma_commit(bar(C::kBarOFinal + 1));
+          }
+          if (ok) mma_commit(bar(C::kBarKVEmpty + (n_tiles - 1) % C::kStages));
+        } else {
+          mma_commit(bar(C::kBarOFinal + 0));
+          if (QT == 2) mma_commit(bar(C::kBarOFinal + 1));
+        }
+      }
+      if (!ok) {
+        mma_commit(bar(C::kBarDrain));
+        wait_drain(bar(C::kBarDrain), 0);
+      }
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ---------------------------------------------- softmax + epilogue
+    const int t = (warp - 4) >> 2;   // query tile of this warpgroup
+    const int quad = warp & 3;       // TMEM lane quadrant this warp may access
+    const int row = quad * 32 + lane;
+    const int q_row = q0 + t * kTileM + row;
+    const bool row_valid = q_row < p.Lq;
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const uint32_t tS = tmem + lane_off + C::kTmemS + t * 128;
+    const uint32_t tO = tmem + lane_off + C::kTmemO + t * D;
+    int klo = 0, khi = 0;  // block-causal: visible key rows [klo, khi)
+    if (p.mode == kModeBlockCausal && row_valid) {
+      const int qc = q_row / p.chunk_tokens;
+      klo = max(0, qc - p.window) * p.chunk_tokens;
+      khi = min(p.Lk, (qc + 1) * p.chunk_tokens);
+    }
+    const float sl = p.scale_log2;
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_tiles; ++j) {
+      ok = wait_bounded(bar(C::kBarSFull + t), (uint32_t)j & 1u, abort_flag, 6 + t);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t s0[32], s1[32], s2[32], s3[32];
+      tmem_ld32(tS + 0, s0);
+      tmem_ld32(tS + 32, s1);
+      tmem_ld32(tS + 64, s2);
+      tmem_ld32(tS + 96, s3);
+      tmem_wait_ld();
+      int lo, hi;
+      if (p.mode == kModeStreaming) {
+        lo = 0;
+        hi = tile_at(p, first + j).valid;
+      } else {
+        const int kr0 = (first + j) * kTileN;
+        lo = klo - kr0;
+        hi = khi - kr0;
+      }
+      float mx = -INFINITY;
+      if (lo <= 0 && hi >= kTileN) {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          mx = fmaxf(mx, fmaxf(__uint_as_float(s0[c]), __uint_as_float(s1[c])));
+          mx = fmaxf(mx, fmaxf(__uint_as_float(s2[c]), __uint_as_float(s3[c])));
+        }
+      } else {
+        const uint32_t ninf = 0xff800000u;
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          s0[c] = (c >= lo && c < hi) ? s0[c] : ninf;
+          s1[c] = (c + 32 >= lo && c + 32 < hi) ? s1[c] : ninf;
+          s2[c] = (c + 64 >= lo && c + 64 < hi) ? s2[c] : ninf;
+          s3[c] = (c + 96 >= lo && c + 96 < hi) ? s3[c] : ninf;
+          mx = fmaxf(mx, fmaxf(__uint_as_float(s0[c]), __uint_as_float(s1[c])));
+          mx = fmaxf(mx, fmaxf(__uint_as_float(s2[c]), __uint_as_float(s3[c])));
+        }
+      }
+      const float m_new = fmaxf(m_run, mx * sl);
+      const bool need = m_new > m_run + kRescaleThreshold;
+      float alpha = 1.f;
+      if (need) {
+        alpha = ex2(m_run - m_new);  // 0 when m_run is -inf
+        l_run *= alpha;
+        m_run = m_new;
+      }
+      const float mb = (m_run == -INFINITY) ? 0.f : m_run;
+      float sum = 0.f;
+      // P (bf16 pairs) overwrites the first 64 columns of S: column k holds
+      // keys 2k (low half) and 2k+1 (high half).
+      {
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const float a0 = ex2(fmaf(__uint_as_float(s0[2 * c]), sl, -mb));
+          const float a1 = ex2(fmaf(__uint_as_float(s0[2 * c + 1]), sl, -mb));
+          const float b0 = ex2(fmaf(__uint_as_float(s1[2 * c]), sl, -mb));
+          const float b1 = ex2(fmaf(__uint_as_float(s1[2 * c + 1]), sl, -mb));
+          sum += (a0 + a1) + (b0 + b1);
+          pk[c] = pack_bf16(a0, a1);
+          pk[16 + c] = pack_bf16(b0, b1);
+        }
+        tmem_st32(tS + 0, pk);
+      }
+      {
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const float a0 = ex2(fmaf(__uint_as_float(s2[2 * c]), sl, -mb));
+          const float a1 = ex2(fmaf(__uint_as_float(s2[2 * c + 1]), sl, -mb));
+          const float b0 = ex2(fmaf(__uint_as_float(s3[2 * c]), sl, -mb));
+          const float b1 = ex2(fmaf(__uint_as_float(s3[2 * c + 1]), sl, -mb));
+          sum += (a0 + a1) + (b0 + b1);
+          pk[c] = pack_bf16(a0, a1);
+          pk[16 + c] = pack_bf16(b0, b1);
+        }
+        tmem_st32(tS + 32, pk);
+      }
+      l_run += sum;
+      if (j > 0 && __any_sync(0xffffffffu, need)) {
+        // S_t(j) completion implies PV_t(j-1) completed (same-thread commit order)
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld32(tO + c0, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+          tmem_st32(tO + c0, o);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(C::kBarPFull + t));
+    }
+    if (ok) {
+      ok = wait_bounded(bar(C::kBarOFinal + t), 0, abort_flag, 8 + t);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
+    const float lse = (l_run > 0.f) ? (m_run + __log2f(l_run)) * kLn2 : -INFINITY;
+    const int BH = p.B * p.H;
+    if (ok) {
+      tc_fence_after();
+      if (p.splits == 1) {
+        uint16_t* orow = p.O + (((long long)b * p.Lq + q_row) * p.H + h) * D;
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t o[32];
+          if (n_tiles > 0) {
+            tmem_ld32(tO + c0, o);
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) o[c] = 0u;
+          }
+          if (row_valid) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint4 w;
+              w.x = pack_bf16(__uint_as_float(o[8 * v + 0]) * inv_l, __uint_as_float(o[8 * v + 1]) * inv_l);
+              w.y = pack_bf16(__uint_as_float(o[8 * v + 2]) * inv_l, __uint_as_float(o[8 * v + 3]) * inv_l);
+              w.z = pack_bf16(__uint_as_float(o[8 * v + 4]) * inv_l, __uint_as_float(o[8 * v + 5]) * inv_l);
+              w.w = pack_bf16(__uint_as_float(o[8 * v + 6]) * inv_l, __uint_as_float(o[8 * v + 7]) * inv_l);
+              dst[v] = w;
+            }
+          }
+        }
+        if (row_valid && p.LSE != nullptr) p.LSE[(long long)bh * p.Lq + q_row] = lse;
+      } else {
+        const long long prow = ((long long)split * BH + bh) * p.lq_pad + (q_row);
+        float* wrow = p.ws_o + prow * D;
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t o[32];
+          if (n_tiles > 0) {
+            tmem_ld32(tO + c0, o);
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) o[c] = 0u;
+          }
+          float4* dst = reinterpret_cast<float4*>(wrow + c0);
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv_l, __uint_as_float(o[4 * v + 1]) * inv_l,
+                                 __uint_as_float(o[4 * v + 2]) * inv_l, __uint_as_float(o[4 * v + 3]) * inv_l);
+        }
+        p.ws_lse[prow] = lse;
+      }
+    }
+    if (p.splits > 1) {
+      // --------------------------------------- log-sum-exp merge of the splits
+      __threadfence();
+      named_bar_sync(1, 128 * QT);
+      if (threadIdx.x == 128) {
+        *ticket = (*abort_flag) ? 0xffffffffu
+                                : atomicAdd(&p.ws_count[(long long)bh * p.n_qgroups + qg], 1u);
+      }
+      named_bar_sync(1, 128 * QT);
+      if (*ticket == (uint32_t)(p.splits - 1)) {
+        __threadfence();
+        if (row_valid) {
+          const long long stride = (long long)BH * p.lq_pad;
+          const long long r0 = (long long)bh * p.lq_pad + q_row;
+          float M = -INFINITY;
+          for (int s = 0; s < p.splits; ++s) M = fmaxf(M, __ldcg(p.ws_lse + s * stride + r0));
+          float tot = 0.f;
+          if (M != -INFINITY)
+            for (int s = 0; s < p.splits; ++s) tot += ex2((__ldcg(p.ws_lse + s * stride + r0) - M) * kLog2e);
+          const float L = (M == -INFINITY) ? -INFINITY : M + __logf(tot);
+          uint16_t* orow = p.O + (((long long)b * p.Lq + q_row) * p.H + h) * D;
+#pragma unroll 1
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            float acc[32];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) acc[c] = 0.f;
+            if (L != -INFINITY) {
+#pragma unroll 1
+              for (int s = 0; s < p.splits; ++s) {
+                const float ls = __ldcg(p.ws_lse + s * stride + r0);
+                if (ls == -INFINITY) continue;
+                const float w = ex2((ls - L) * kLog2e);
+                const float4* src = reinterpret_cast<const float4*>(p.ws_o + (s * stride + r0) * D + c0);
+#pragma unroll
+                for (int v = 0; v < 8; ++v) {
+                  const float4 x = __ldcg(src + v);
+                  acc[4 * v] = fmaf(w, x.x, acc[4 * v]);
+                  acc[4 * v + 1] = fmaf(w, x.y, acc[4 * v + 1]);
+                  acc[4 * v + 2] = fmaf(w, x.z, acc[4 * v + 2]);
+                  acc[4 * v + 3] = fmaf(w, x.w, acc[4 * v + 3]);
+                }
+              }
+            }
+            uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint4 w;
+              w.x = pack_bf16(acc[8 * v + 0], acc[8 * v + 1]);
+              w.y = pack_bf16(acc[8 * v + 2], acc[8 * v + 3]);
+              w.z = pack_bf16(acc[8 * v + 4], acc[8 * v + 5]);
+              w.w = pack_bf16(acc[8 * v + 6], acc[8 * v + 7]);
+              dst[v] = w;
+            }
+          }
+          if (p.LSE != nullptr) p.LSE[(long long)bh * p.Lq + q_row] = L;
+        }
+        if (threadIdx.x == 128) p.ws_count[(long long)bh * p.n_qgroups + qg] = 0u;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int D, int QT>
+cudaError_t launch_impl(const AttnParams& p, cudaStream_t s) {
+  using C = Cfg<D, QT>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(chunk_attn_kernel<D, QT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  dim3 grid(p.n_qgroups, p.B * p.H, p.splits);
+  chunk_attn_kernel<D, QT><<<grid, C::kThreads, C::kSmemBytes, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_chunk_attention(const AttnParams& p, int q_tiles_per_cta, cudaStream_t s) {
+  if (p.D == 128) return q_tiles_per_cta == 2 ? launch_impl<128, 2>(p, s) : launch_impl<128, 1>(p, s);
+  if (p.D == 64) return q_tiles_per_cta == 2 ? launch_impl<64, 2>(p, s) : launch_impl<64, 1>(p, s);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t read_and_clear_device_error(unsigned int* value) {
+  unsigned int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_sab_error_word, sizeof(v));
+  if (e != cudaSuccess) return e;
+  *value = v;
+  if (v != 0) {
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(g_sab_error_word, &zero, sizeof(zero));
+  }
+  return e;
+}
+
+}  // namespace sab

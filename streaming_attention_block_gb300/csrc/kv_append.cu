@@ -1,0 +1,140 @@
+// KV append into ring slots: BF16 copy and FP8-E4M3 absmax quantisation.
+//
+// A new chunk's K and V (token-major [B, Lc, H, D], as a QKV projection writes
+// them) are written into the ring slot chunk mod R of one layer, head-major
+// [B, H, rows, D], overwriting the oldest chunk in place ("Matrix-Game 4.0:
+// Harnessing Video Models for Real-Time Playable Game Worlds", section
+// "技术新颖性": the ring overwrites the oldest slot instead of copying the
+// window).  Both layouts keep each (b, t, h) row of D elements contiguous, so
+// the transpose is a permutation of 128/256-byte rows: every thread moves
+// 16-byte vectors, reads and writes are fully coalesced, and the kernel is a
+// pure HBM stream (bytes in = bytes out = 2 * B * Lc * H * D * 2).
+//
+// The FP8 variant quantises each (b, h) block of Lc x D values with one fp32
+// scale = amax / 448 (IEEE round-to-nearest division) and E4M3 codes rounded
+// to nearest even with saturation ("Matrix-Game 4.0", section "技术新颖性":
+// 8-bit keys/values per window interval, only the changed interval is
+// re-quantised -- here the changed interval is the appended chunk).
+#include "sab_internal.h"
+
+namespace sab {
+namespace {
+
+constexpr int kAppendThreads = 256;
+
+__global__ void __launch_bounds__(kAppendThreads)
+append_bf16_kernel(const __grid_constant__ AppendParams p) {
+  const int vec_per_row = p.D / 8;  // 16-byte vectors per row
+  const long long per_tensor = (long long)p.B * p.H * p.Lc * vec_per_row;
+  const long long total = 2 * per_tensor;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int tensor = (int)(i / per_tensor);
+    long long r = i - tensor * per_tensor;
+    // destination order (b, h, t, vec): consecutive threads write consecutive bytes
+    const int vec = (int)(r % vec_per_row); r /= vec_per_row;
+    const int t = (int)(r % p.Lc); r /= p.Lc;
+    const int h = (int)(r % p.H);
+    const int b = (int)(r / p.H);
+    const uint4* src = reinterpret_cast<const uint4*>(
+        p.src[tensor] + (((long long)b * p.Lc + t) * p.H + h) * p.D) + vec;
+    uint4* dst = reinterpret_cast<uint4*>(
+        static_cast<uint16_t*>(p.dst[tensor]) +
+        (((long long)b * p.H + h) * p.rows + p.slot_row0 + t) * p.D) + vec;
+    *dst = __ldg(src);
+  }
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Two fp32 values -> two E4M3 codes (RNE, satfinite); `lo` lands in the low byte.
+__device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__global__ void __launch_bounds__(kAppendThreads)
+append_fp8_kernel(const __grid_constant__ AppendParams p) {
+  const int tensor = blockIdx.x;
+  const int bh = blockIdx.y;
+  const int b = bh / p.H, h = bh % p.H;
+  const int vec_per_row = p.D / 8;
+  const int nvec = p.Lc * vec_per_row;
+  const uint16_t* src = p.src[tensor];
+  auto src_vec = [&](int v) -> uint4 {
+    const int t = v / vec_per_row, c = v % vec_per_row;
+    return __ldg(reinterpret_cast<const uint4*>(src + (((long long)b * p.Lc + t) * p.H + h) * p.D) + c);
+  };
+  // pass 1: amax over the (b, h) block
+  float amax = 0.f;
+  for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
+    const uint4 x = src_vec(v);
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[k])), fabsf(bf16_hi(w[k]))));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  __shared__ float red[kAppendThreads / 32];
+  __shared__ float s_scale;
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float m = 0.f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) m = fmaxf(m, red[w]);
+    const float sc = (m == 0.f) ? 1.0f : __fdiv_rn(m, 448.0f);
+    s_scale = sc;
+    p.scale[tensor][(long long)bh * p.scale_stride + p.scale_idx] = sc;
+  }
+  __syncthreads();
+  const float sc = s_scale;
+  // pass 2: quantise (the block is re-read from L2)
+  uint8_t* dst = static_cast<uint8_t*>(p.dst[tensor]) + ((long long)bh * p.rows + p.slot_row0) * p.D;
+  for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
+    const uint4 x = src_vec(v);
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    uint32_t out[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const uint16_t c0 = e4m3x2(__fdiv_rn(bf16_lo(w[2 * k]), sc), __fdiv_rn(bf16_hi(w[2 * k]), sc));
+      const uint16_t c1 = e4m3x2(__fdiv_rn(bf16_lo(w[2 * k + 1]), sc), __fdiv_rn(bf16_hi(w[2 * k + 1]), sc));
+      out[k] = (uint32_t)c0 | ((uint32_t)c1 << 16);
+    }
+    const int t = v / vec_per_row, c = v % vec_per_row;
+    *reinterpret_cast<uint2*>(dst + (long long)t * p.D + c * 8) = make_uint2(out[0], out[1]);
+  }
+}
+
+int num_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+}  // namespace
+
+cudaError_t launch_append_bf16(const AppendParams& p, cudaStream_t s) {
+  const long long vecs = 2LL * p.B * p.H * p.Lc * (p.D / 8);
+  long long blocks = (vecs + kAppendThreads - 1) / kAppendThreads;
+  const long long cap = (long long)num_sms() * 8;  // grid-stride beyond 8 CTAs per SM
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  append_bf16_kernel<<<(unsigned)blocks, kAppendThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_append_fp8(const AppendParams& p, cudaStream_t s) {
+  dim3 grid(2, p.B * p.H);
+  append_fp8_kernel<<<grid, kAppendThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace sab

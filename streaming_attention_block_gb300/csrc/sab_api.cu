@@ -1,0 +1,469 @@
+// Host side of libsab.so: ring handle, argument validation, key-set planner,
+// TMA tensor-map encoding and kernel launches.  No call allocates device
+// memory or synchronises the host (except sab_get_last_device_error).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <algorithm>
+#include <new>
+#include <vector>
+
+#include "../../include/sab.h"
+#include "sab_internal.h"
+
+using namespace sab;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 4-D bf16 map with coordinates (d, row, h, b) and a 64 x 128 box, 128-byte swizzle.
+bool encode_map(CUtensorMap* m, const void* ptr, int D, long long rows, int H, int B, size_t s_row,
+                size_t s_h, size_t s_b) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)rows, (cuuint64_t)H, (cuuint64_t)B};
+  const cuuint64_t strides[3] = {(cuuint64_t)s_row, (cuuint64_t)s_h, (cuuint64_t)s_b};
+  const cuuint32_t box[4] = {64, (cuuint32_t)kTileN, 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Token-major [B, L, H, D] bf16.
+bool encode_token_major(CUtensorMap* m, const void* ptr, int B, int L, int H, int D) {
+  const size_t e = 2;
+  return encode_map(m, ptr, D, L, H, B, (size_t)H * D * e, (size_t)D * e, (size_t)L * H * D * e);
+}
+
+// Head-major [B, H, rows, D] bf16.
+bool encode_head_major(CUtensorMap* m, const void* ptr, int B, int H, long long rows, int D) {
+  const size_t e = 2;
+  return encode_map(m, ptr, D, rows, H, B, (size_t)D * e, (size_t)rows * D * e, (size_t)H * rows * D * e);
+}
+
+bool valid_desc(const sab_ring_desc* d) {
+  if (d == nullptr) return false;
+  if (d->num_layers < 1 || d->batch < 1 || d->heads < 1 || d->chunk_tokens < 1 || d->ring_slots < 1)
+    return false;
+  if (d->head_dim != 64 && d->head_dim != 128) return false;
+  if (d->has_sink != 0 && d->has_sink != 1) return false;
+  if (d->kv_dtype != SAB_KV_BF16 && d->kv_dtype != SAB_KV_FP8_E4M3) return false;
+  const long long rows = (long long)(d->has_sink + d->ring_slots) * d->chunk_tokens;
+  if (rows > (1LL << 30)) return false;
+  if ((long long)d->batch * d->heads * rows * d->head_dim > (1LL << 40)) return false;
+  return true;
+}
+
+struct Geometry {
+  long long rows;       // rows per (b, h)
+  size_t codes_bytes;   // one tensor (K or V) of one layer, aligned
+  size_t scale_bytes;   // one tensor's scales of one layer, aligned (FP8)
+  size_t layer_bytes;
+};
+
+Geometry geometry(const sab_ring_desc& d) {
+  Geometry g;
+  g.rows = (long long)(d.has_sink + d.ring_slots) * d.chunk_tokens;
+  const size_t esize = d.kv_dtype == SAB_KV_BF16 ? 2 : 1;
+  g.codes_bytes = align_up((size_t)d.batch * d.heads * g.rows * d.head_dim * esize, kAlign);
+  g.scale_bytes = d.kv_dtype == SAB_KV_FP8_E4M3
+                      ? align_up((size_t)d.batch * d.heads * (d.has_sink + d.ring_slots) * sizeof(float), kAlign)
+                      : 0;
+  g.layer_bytes = 2 * g.codes_bytes + 2 * g.scale_bytes;
+  return g;
+}
+
+// Query tiling shared by the workspace size and the launch.
+struct QTiling {
+  int n_qtiles, qt, n_qgroups, lq_pad;
+};
+QTiling qtiling(int Lq) {
+  QTiling t;
+  t.n_qtiles = (Lq + kTileM - 1) / kTileM;
+  t.qt = t.n_qtiles >= 2 ? 2 : 1;
+  t.n_qgroups = (t.n_qtiles + t.qt - 1) / t.qt;
+  t.lq_pad = t.n_qgroups * t.qt * kTileM;
+  return t;
+}
+
+struct WsLayout {
+  size_t count_off, o_off, lse_off, total;
+};
+WsLayout ws_layout(int BH, int Lq, int D, int splits) {
+  WsLayout w{0, 0, 0, 0};
+  if (splits <= 1) return w;
+  const QTiling t = qtiling(Lq);
+  w.count_off = 0;
+  w.o_off = align_up((size_t)BH * t.n_qgroups * sizeof(unsigned), kAlign);
+  w.lse_off = w.o_off + align_up((size_t)splits * BH * t.lq_pad * D * sizeof(float), kAlign);
+  w.total = w.lse_off + align_up((size_t)splits * BH * t.lq_pad * sizeof(float), kAlign);
+  return w;
+}
+
+constexpr int kMaxSplits = 256;
+
+}  // namespace
+
+struct sab_ring {
+  sab_ring_desc d;
+  uint8_t* mem;
+  Geometry g;
+  std::vector<long long> newest;
+  std::vector<int> held;
+  std::vector<int> sink_set;
+  std::vector<CUtensorMap> kmap, vmap;  // per layer, BF16 rings
+
+  uint8_t* layer_base(int l) const { return mem + (size_t)l * g.layer_bytes; }
+  void* k(int l) const { return layer_base(l); }
+  void* v(int l) const { return layer_base(l) + g.codes_bytes; }
+  float* ks(int l) const {
+    return g.scale_bytes ? reinterpret_cast<float*>(layer_base(l) + 2 * g.codes_bytes) : nullptr;
+  }
+  float* vs(int l) const {
+    return g.scale_bytes ? reinterpret_cast<float*>(layer_base(l) + 2 * g.codes_bytes + g.scale_bytes) : nullptr;
+  }
+};
+
+extern "C" {
+
+size_t sab_kv_ring_bytes(const sab_ring_desc* desc) {
+  if (!valid_desc(desc)) return 0;
+  return geometry(*desc).layer_bytes * (size_t)desc->num_layers;
+}
+
+sab_status sab_kv_ring_create(const sab_ring_desc* desc, void* dev_mem, size_t bytes, void* stream,
+                              sab_ring** out) {
+  if (out == nullptr || !valid_desc(desc) || dev_mem == nullptr) return SAB_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(dev_mem) % kAlign) != 0) return SAB_ERR_INVALID_ARG;
+  const size_t need = sab_kv_ring_bytes(desc);
+  if (bytes < need) return SAB_ERR_INVALID_ARG;
+  sab_ring* r = new (std::nothrow) sab_ring();
+  if (r == nullptr) return SAB_ERR_INVALID_ARG;
+  r->d = *desc;
+  r->mem = static_cast<uint8_t*>(dev_mem);
+  r->g = geometry(*desc);
+  r->newest.assign(desc->num_layers, -1);
+  r->held.assign(desc->num_layers, 0);
+  r->sink_set.assign(desc->num_layers, 0);
+  if (desc->kv_dtype == SAB_KV_BF16) {
+    r->kmap.resize(desc->num_layers);
+    r->vmap.resize(desc->num_layers);
+    for (int l = 0; l < desc->num_layers; ++l) {
+      if (!encode_head_major(&r->kmap[l], r->k(l), desc->batch, desc->heads, r->g.rows, desc->head_dim) ||
+          !encode_head_major(&r->vmap[l], r->v(l), desc->batch, desc->heads, r->g.rows, desc->head_dim)) {
+        delete r;
+        return SAB_ERR_CUDA;
+      }
+    }
+  }
+  if (cudaMemsetAsync(dev_mem, 0, need, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    delete r;
+    return SAB_ERR_CUDA;
+  }
+  *out = r;
+  return SAB_OK;
+}
+
+sab_status sab_kv_ring_destroy(sab_ring* ring) {
+  delete ring;
+  return SAB_OK;
+}
+
+sab_status sab_kv_ring_get_desc(const sab_ring* ring, sab_ring_desc* desc) {
+  if (ring == nullptr || desc == nullptr) return SAB_ERR_INVALID_ARG;
+  *desc = ring->d;
+  return SAB_OK;
+}
+
+sab_status sab_kv_ring_layer_ptrs(const sab_ring* ring, int layer, void** k, void** v, float** k_scale,
+                                  float** v_scale) {
+  if (ring == nullptr || layer < 0 || layer >= ring->d.num_layers) return SAB_ERR_INVALID_ARG;
+  if (k) *k = ring->k(layer);
+  if (v) *v = ring->v(layer);
+  if (k_scale) *k_scale = ring->ks(layer);
+  if (v_scale) *v_scale = ring->vs(layer);
+  return SAB_OK;
+}
+
+static sab_status write_chunk(sab_ring* r, int layer, int slot_row0, int scale_idx, const void* K, const void* V,
+                              void* stream) {
+  AppendParams p;
+  memset(&p, 0, sizeof(p));
+  p.src[0] = static_cast<const uint16_t*>(K);
+  p.src[1] = static_cast<const uint16_t*>(V);
+  p.dst[0] = r->k(layer);
+  p.dst[1] = r->v(layer);
+  p.scale[0] = r->ks(layer);
+  p.scale[1] = r->vs(layer);
+  p.B = r->d.batch;
+  p.H = r->d.heads;
+  p.D = r->d.head_dim;
+  p.Lc = r->d.chunk_tokens;
+  p.rows = (int)r->g.rows;
+  p.slot_row0 = slot_row0;
+  p.scale_idx = scale_idx;
+  p.scale_stride = r->d.has_sink + r->d.ring_slots;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = r->d.kv_dtype == SAB_KV_BF16 ? launch_append_bf16(p, s) : launch_append_fp8(p, s);
+  return e == cudaSuccess ? SAB_OK : SAB_ERR_CUDA;
+}
+
+sab_status sab_kv_ring_set_sink(sab_ring* ring, int layer, const void* K, const void* V, void* stream) {
+  if (ring == nullptr || layer < 0 || layer >= ring->d.num_layers) return SAB_ERR_INVALID_ARG;
+  if (K == nullptr || V == nullptr || !aligned16(K) || !aligned16(V)) return SAB_ERR_INVALID_ARG;
+  if (!ring->d.has_sink) return SAB_ERR_UNSUPPORTED;
+  const sab_status st = write_chunk(ring, layer, 0, 0, K, V, stream);
+  if (st == SAB_OK) ring->sink_set[layer] = 1;
+  return st;
+}
+
+sab_status sab_kv_ring_append(sab_ring* ring, int layer, long long chunk, const void* K, const void* V,
+                              void* stream) {
+  if (ring == nullptr || layer < 0 || layer >= ring->d.num_layers) return SAB_ERR_INVALID_ARG;
+  if (K == nullptr || V == nullptr || !aligned16(K) || !aligned16(V)) return SAB_ERR_INVALID_ARG;
+  if (chunk < 0) return SAB_ERR_OUT_OF_RANGE;
+  const long long newest = ring->newest[layer];
+  if (newest >= 0 && chunk != newest && chunk != newest + 1) return SAB_ERR_OUT_OF_RANGE;
+  const int R = ring->d.ring_slots;
+  const int slot = (int)(chunk % R);
+  const int row0 = (ring->d.has_sink + slot) * ring->d.chunk_tokens;
+  const sab_status st = write_chunk(ring, layer, row0, ring->d.has_sink + slot, K, V, stream);
+  if (st != SAB_OK) return st;
+  if (newest < 0) {
+    ring->held[layer] = 1;
+  } else if (chunk == newest + 1) {
+    ring->held[layer] = std::min(R, ring->held[layer] + 1);
+  }
+  ring->newest[layer] = chunk;
+  return SAB_OK;
+}
+
+sab_status sab_kv_ring_slot_of(const sab_ring* ring, int layer, long long chunk, int* slot) {
+  if (ring == nullptr || slot == nullptr || layer < 0 || layer >= ring->d.num_layers) return SAB_ERR_INVALID_ARG;
+  const long long newest = ring->newest[layer];
+  if (newest < 0 || chunk > newest || chunk <= newest - ring->held[layer]) return SAB_ERR_OUT_OF_RANGE;
+  *slot = (int)(chunk % ring->d.ring_slots);
+  return SAB_OK;
+}
+
+sab_status sab_kv_ring_get_state(const sab_ring* ring, long long* newest_chunk, int* held, int* sink_set) {
+  if (ring == nullptr) return SAB_ERR_INVALID_ARG;
+  for (int l = 0; l < ring->d.num_layers; ++l) {
+    if (newest_chunk) newest_chunk[l] = ring->newest[l];
+    if (held) held[l] = ring->held[l];
+    if (sink_set) sink_set[l] = ring->sink_set[l];
+  }
+  return SAB_OK;
+}
+
+sab_status sab_kv_ring_set_state(sab_ring* ring, const long long* newest_chunk, const int* held,
+                                 const int* sink_set) {
+  if (ring == nullptr || newest_chunk == nullptr || held == nullptr || sink_set == nullptr)
+    return SAB_ERR_INVALID_ARG;
+  for (int l = 0; l < ring->d.num_layers; ++l) {
+    const long long n = newest_chunk[l];
+    const int h = held[l];
+    if (n < -1 || h < 0 || h > ring->d.ring_slots || (long long)h > n + 1 || ((n == -1) != (h == 0)))
+      return SAB_ERR_INVALID_ARG;
+    if (sink_set[l] != 0 && sink_set[l] != 1) return SAB_ERR_INVALID_ARG;
+    if (sink_set[l] && !ring->d.has_sink) return SAB_ERR_INVALID_ARG;
+  }
+  for (int l = 0; l < ring->d.num_layers; ++l) {
+    ring->newest[l] = newest_chunk[l];
+    ring->held[l] = held[l];
+    ring->sink_set[l] = sink_set[l];
+  }
+  return SAB_OK;
+}
+
+size_t sab_chunk_attention_workspace(const sab_ring* ring, int num_splits) {
+  if (ring == nullptr || num_splits < 1 || num_splits > kMaxSplits) return 0;
+  return ws_layout(ring->d.batch * ring->d.heads, ring->d.chunk_tokens, ring->d.head_dim, num_splits).total;
+}
+
+static sab_status launch_attention(AttnParams& p, int Lq, int splits, void* workspace, size_t ws_bytes,
+                                   void* stream) {
+  const QTiling t = qtiling(Lq);
+  p.Lq = Lq;
+  p.n_qtiles = t.n_qtiles;
+  p.n_qgroups = t.n_qgroups;
+  p.lq_pad = t.lq_pad;
+  p.splits = splits;
+  if (splits > 1) {
+    const WsLayout w = ws_layout(p.B * p.H, Lq, p.D, splits);
+    if (workspace == nullptr || ws_bytes < w.total) return SAB_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0) return SAB_ERR_INVALID_ARG;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    p.ws_count = reinterpret_cast<unsigned*>(ws + w.count_off);
+    p.ws_o = reinterpret_cast<float*>(ws + w.o_off);
+    p.ws_lse = reinterpret_cast<float*>(ws + w.lse_off);
+  }
+  if ((long long)p.B * p.H > 65535) return SAB_ERR_UNSUPPORTED;
+  const cudaError_t e = launch_chunk_attention(p, t.qt, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SAB_OK : SAB_ERR_CUDA;
+}
+
+sab_status sab_chunk_attention(const sab_ring* ring, int layer, long long chunk, const void* Q, const void* K_cur,
+                               const void* V_cur, int window, int use_sink, int num_splits, float softmax_scale,
+                               void* O, float* LSE, void* workspace, size_t ws_bytes, void* stream) {
+  if (ring == nullptr || layer < 0 || layer >= ring->d.num_layers) return SAB_ERR_INVALID_ARG;
+  if (Q == nullptr || O == nullptr || !aligned16(Q) || !aligned16(O)) return SAB_ERR_INVALID_ARG;
+  if ((K_cur == nullptr) != (V_cur == nullptr)) return SAB_ERR_INVALID_ARG;
+  if (K_cur != nullptr && (!aligned16(K_cur) || !aligned16(V_cur))) return SAB_ERR_INVALID_ARG;
+  if (LSE != nullptr && (reinterpret_cast<uintptr_t>(LSE) & 3u) != 0) return SAB_ERR_INVALID_ARG;
+  if (window < 0 || num_splits < 1 || num_splits > kMaxSplits) return SAB_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.f) || !isfinite(softmax_scale)) return SAB_ERR_INVALID_ARG;
+  if (use_sink != 0 && use_sink != 1) return SAB_ERR_INVALID_ARG;
+  if (chunk < 0) return SAB_ERR_OUT_OF_RANGE;
+  const sab_ring_desc& d = ring->d;
+  if (use_sink && !d.has_sink) return SAB_ERR_INVALID_ARG;
+  if (use_sink && !ring->sink_set[layer]) return SAB_ERR_OUT_OF_RANGE;
+  if (d.kv_dtype != SAB_KV_BF16) return SAB_ERR_UNSUPPORTED;
+  const bool kcur = K_cur != nullptr;
+  const int R = d.ring_slots, Lc = d.chunk_tokens;
+
+  // ring chunks needed: [need_lo, need_hi]
+  const long long need_lo = std::max(0LL, chunk - window);
+  const long long need_hi = kcur ? chunk - 1 : chunk;
+  struct Run {
+    int row0, nrows;
+  };
+  std::vector<Run> runs;
+  if (use_sink) runs.push_back({0, Lc});
+  if (need_hi >= need_lo) {
+    const long long newest = ring->newest[layer];
+    const long long oldest = newest - ring->held[layer] + 1;
+    if (newest < 0 || need_hi > newest || need_lo < oldest) return SAB_ERR_OUT_OF_RANGE;
+    for (long long c = need_lo; c <= need_hi; ++c) {
+      const int row0 = (d.has_sink + (int)(c % R)) * Lc;
+      runs.push_back({row0, Lc});
+    }
+  }
+  // Softmax is invariant to key order: merge physically adjacent runs.
+  std::sort(runs.begin(), runs.end(), [](const Run& a, const Run& b) { return a.row0 < b.row0; });
+  std::vector<Run> merged;
+  for (const Run& r : runs) {
+    if (!merged.empty() && merged.back().row0 + merged.back().nrows == r.row0)
+      merged.back().nrows += r.nrows;
+    else
+      merged.push_back(r);
+  }
+
+  AttnParams p;
+  memset(&p, 0, sizeof(p));
+  p.mode = kModeStreaming;
+  p.B = d.batch;
+  p.H = d.heads;
+  p.D = d.head_dim;
+  p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  p.O = static_cast<uint16_t*>(O);
+  p.LSE = LSE;
+  int tiles = 0, nseg = 0;
+  for (const Run& r : merged) {
+    if (nseg >= kMaxSegments) return SAB_ERR_UNSUPPORTED;
+    p.seg[nseg] = KvSegment{0, r.row0, r.nrows, tiles};
+    tiles += (r.nrows + kTileN - 1) / kTileN;
+    ++nseg;
+  }
+  p.k_map[0] = ring->kmap[layer];
+  p.v_map[0] = ring->vmap[layer];
+  p.k_map[1] = ring->kmap[layer];
+  p.v_map[1] = ring->vmap[layer];
+  if (kcur) {
+    if (nseg >= kMaxSegments) return SAB_ERR_UNSUPPORTED;
+    p.seg[nseg] = KvSegment{1, 0, Lc, tiles};
+    tiles += (Lc + kTileN - 1) / kTileN;
+    ++nseg;
+    if (!encode_token_major(&p.k_map[1], K_cur, d.batch, Lc, d.heads, d.head_dim) ||
+        !encode_token_major(&p.v_map[1], V_cur, d.batch, Lc, d.heads, d.head_dim))
+      return SAB_ERR_CUDA;
+  }
+  p.nseg = nseg;
+  p.total_tiles = tiles;
+  if (!encode_token_major(&p.q_map, Q, d.batch, Lc, d.heads, d.head_dim)) return SAB_ERR_CUDA;
+  return launch_attention(p, Lc, num_splits, workspace, ws_bytes, stream);
+}
+
+size_t sab_block_causal_attention_workspace(int B, int L, int H, int D, int num_splits) {
+  if (B < 1 || L < 1 || H < 1 || (D != 64 && D != 128) || num_splits < 1 || num_splits > kMaxSplits) return 0;
+  return ws_layout(B * H, L, D, num_splits).total;
+}
+
+sab_status sab_block_causal_attention(const void* Q, const void* K, const void* V, int B, int L, int H, int D,
+                                      int chunk_tokens, int window, int num_splits, float softmax_scale, void* O,
+                                      float* LSE, void* workspace, size_t ws_bytes, void* stream) {
+  if (Q == nullptr || K == nullptr || V == nullptr || O == nullptr) return SAB_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return SAB_ERR_INVALID_ARG;
+  if (LSE != nullptr && (reinterpret_cast<uintptr_t>(LSE) & 3u) != 0) return SAB_ERR_INVALID_ARG;
+  if (B < 1 || L < 1 || H < 1 || (D != 64 && D != 128) || chunk_tokens < 1 || window < 0) return SAB_ERR_INVALID_ARG;
+  if (num_splits < 1 || num_splits > kMaxSplits) return SAB_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.f) || !isfinite(softmax_scale)) return SAB_ERR_INVALID_ARG;
+  if ((long long)L > (1LL << 30)) return SAB_ERR_INVALID_ARG;
+  AttnParams p;
+  memset(&p, 0, sizeof(p));
+  p.mode = kModeBlockCausal;
+  p.B = B;
+  p.H = H;
+  p.D = D;
+  p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  p.chunk_tokens = chunk_tokens;
+  p.window = window;
+  p.Lk = L;
+  p.O = static_cast<uint16_t*>(O);
+  p.LSE = LSE;
+  if (!encode_token_major(&p.q_map, Q, B, L, H, D) || !encode_token_major(&p.k_map[0], K, B, L, H, D) ||
+      !encode_token_major(&p.v_map[0], V, B, L, H, D))
+    return SAB_ERR_CUDA;
+  p.k_map[1] = p.k_map[0];
+  p.v_map[1] = p.v_map[0];
+  return launch_attention(p, L, num_splits, workspace, ws_bytes, stream);
+}
+
+sab_status sab_get_last_device_error(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return SAB_ERR_CUDA;
+  unsigned v = 0;
+  if (read_and_clear_device_error(&v) != cudaSuccess) return SAB_ERR_CUDA;
+  return v ? SAB_ERR_TIMEOUT : SAB_OK;
+}
+
+const char* sab_status_string(sab_status status) {
+  switch (status) {
+    case SAB_OK: return "SAB_OK";
+    case SAB_ERR_INVALID_ARG: return "SAB_ERR_INVALID_ARG";
+    case SAB_ERR_UNSUPPORTED: return "SAB_ERR_UNSUPPORTED";
+    case SAB_ERR_OUT_OF_RANGE: return "SAB_ERR_OUT_OF_RANGE";
+    case SAB_ERR_WORKSPACE: return "SAB_ERR_WORKSPACE";
+    case SAB_ERR_CUDA: return "SAB_ERR_CUDA";
+    case SAB_ERR_TIMEOUT: return "SAB_ERR_TIMEOUT";
+  }
+  return "SAB_ERR_UNKNOWN";
+}
+
+const char* sab_version(void) { return "sab 0.1.0 (sm_103a)"; }
+
+}  // extern "C"
