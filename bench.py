@@ -1,0 +1,365 @@
+"""Benchmark: streaming chunk attention at the Wan-1.3B shape on GB300.
+
+One step = one streamed chunk of the Wan-1.3B-shaped world model: 4 denoise
+steps x 30 layers of chunk attention (B=1, H=12, D=128, 1536 tokens per
+chunk, queries attend to their own chunk plus the 2 cached chunks of a 2-slot
+ring: 4608 keys in steady state), then the 30 ring appends of the chunk's KV.
+``value`` is chunks/s of the whole job (all ranks), inputs resident in HBM;
+``e2e`` repeats the measurement with the step's inputs copied from pinned host
+memory and its outputs copied back inside the timed region.
+
+``--impl reference`` times the CPU oracle (plain fp64 numpy) on the same
+metric, one sampled attention call per step, scaled to chunks/s.
+
+Multi-GPU: the path has no exchange step, so N ranks run N independent
+streams (weak scaling); value = chunks of all ranks / max-over-ranks time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+METRIC = "chunk-attention TFLOP/s & chunks/s at Wan-1.3B shape; % of roofline"
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                d = json.load(f)
+            return {k: float(d[k]) for k in FALLBACK_PEAKS if k in d}, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_ours(args):
+    import torch
+
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    import streaming_attention_block_gb300 as sab
+    from streaming_attention_block_gb300 import synth
+
+    sab.library()
+    w = synth.workload("wan13b")
+    L, S = w.layers, w.steps
+    B, H, D, Lc = w.B, w.H, w.D, w.Lc
+    stream = torch.cuda.current_stream()
+    # inputs for every (denoise step, layer), generated on the device (seeded)
+    g = synth.generator(w.seed + 7919 * rank, device=str(dev))
+    shape = (B, Lc, H, D)
+    Q = [[synth.randn_bf16(g, shape, str(dev), rms_norm=True) for _ in range(L)] for _ in range(S)]
+    Kc = [[synth.randn_bf16(g, shape, str(dev), rms_norm=True) for _ in range(L)] for _ in range(S)]
+    Vc = [[synth.randn_bf16(g, shape, str(dev)) for _ in range(L)] for _ in range(S)]
+    O = [[torch.empty(shape, dtype=torch.bfloat16, device=dev) for _ in range(L)] for _ in range(S)]
+    LSE = [[torch.empty((B, H, Lc), dtype=torch.float32, device=dev) for _ in range(L)] for _ in range(S)]
+    ring = sab.KVRing(L, B, H, D, Lc, w.R, device=dev)
+    save = max(0, S - 2)  # KV of the penultimate denoise step goes to the cache
+    launches = [0]
+
+    def chunk_step(c, ev=None):
+        for s in range(S):
+            for l in range(L):
+                if ev is not None:
+                    ev[0].append(torch.cuda.Event(enable_timing=True))
+                    ev[1].append(torch.cuda.Event(enable_timing=True))
+                    ev[0][-1].record(stream)
+                sab.chunk_attention(ring.handle, l, c, Q[s][l], Kc[s][l], Vc[s][l], w.W, False, 1, w.scale,
+                                    O[s][l], LSE[s][l], None, stream)
+                if ev is not None:
+                    ev[1][-1].record(stream)
+                launches[0] += 1
+        for l in range(L):
+            sab.kv_ring_append(ring.handle, l, c, Kc[save][l], Vc[save][l], stream)
+            launches[0] += 1
+
+    def barrier():
+        if pg is not None:
+            pg.barrier()
+        torch.cuda.synchronize()
+
+    chunk = 0
+    for _ in range(args.warmup):
+        chunk_step(chunk)
+        chunk += 1
+    assert chunk >= 2, "warm-up must reach the steady-state window (>= 2 chunks)"
+    barrier()
+    launches[0] = 0
+    ev = ([], [])
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        t0.record(stream)
+        for _ in range(args.steps):
+            chunk_step(chunk, ev)
+            chunk += 1
+        t1.record(stream)
+        barrier()
+    ms = t0.elapsed_time(t1)
+    gpu_launches = launches[0]
+    attn_ms = [a.elapsed_time(b) for a, b in zip(*ev)]
+    status = sab.get_last_device_error(stream)
+    if status != 0:
+        raise RuntimeError(f"device error {sab.status_string(status)}")
+
+    # ---------------- end to end: pinned host inputs in, outputs out, per step
+    hQ = [[Q[s][l].cpu().pin_memory() for l in range(L)] for s in range(S)]
+    hK = [[Kc[s][l].cpu().pin_memory() for l in range(L)] for s in range(S)]
+    hV = [[Vc[s][l].cpu().pin_memory() for l in range(L)] for s in range(S)]
+    hO = [[torch.empty(shape, dtype=torch.bfloat16).pin_memory() for _ in range(L)] for _ in range(S)]
+    hL = [[torch.empty((B, H, Lc), dtype=torch.float32).pin_memory() for _ in range(L)] for _ in range(S)]
+
+    def e2e_step(c):
+        for s in range(S):
+            for l in range(L):
+                Q[s][l].copy_(hQ[s][l], non_blocking=True)
+                Kc[s][l].copy_(hK[s][l], non_blocking=True)
+                Vc[s][l].copy_(hV[s][l], non_blocking=True)
+        chunk_step(c)
+        for s in range(S):
+            for l in range(L):
+                hO[s][l].copy_(O[s][l], non_blocking=True)
+                hL[s][l].copy_(LSE[s][l], non_blocking=True)
+
+    for _ in range(2):
+        e2e_step(chunk)
+        chunk += 1
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step(chunk)
+        chunk += 1
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1)
+    h2d = S * L * 3 * B * Lc * H * D * 2
+    d2h = S * L * (B * Lc * H * D * 2 + B * H * Lc * 4)
+
+    if pg is not None:
+        t = torch.tensor([ms, e2e_ms], device=dev, dtype=torch.float64)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms, e2e_ms = t.tolist()
+    nkeys = Lc * (w.W + 1)
+    flops_call = 4.0 * B * H * D * Lc * nkeys
+    calls = S * L * args.steps
+    chunks_total = args.steps * ws
+    value = chunks_total / (ms / 1e3)
+    tflops = flops_call * calls * ws / (ms / 1e3) / 1e12
+    attn_avg_s = statistics.mean(attn_ms) / 1e3
+    peaks, src = _peaks()
+    peak = peaks["bf16_tflops_sustained"]
+    achieved = flops_call / attn_avg_s / 1e12
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_sample(w, seconds_budget=args.cpu_seconds)
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "chunks/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "wan13b streaming: B1 H12 D128, 1536 tokens/chunk, ring 2 slots, window current+2 "
+                               "(4608 keys), 4 denoise steps x 30 layers per chunk + 30 ring appends",
+                   "global_batch": ws, "seq_len": Lc, "parallelism": f"replicas x{ws}",
+                   "l2": "inputs larger than L2 (30-layer ring 566 MB + 1.7 GB of per-call Q/K/V per step)"},
+        "tflops": round(tflops, 2), "attention_us_per_call": round(attn_avg_s * 1e6, 2),
+        "gpu_launches": gpu_launches,
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "peak_source": f"bf16 dense sustained, {src}"},
+        "e2e": {"value": round(chunks_total / (e2e_ms / 1e3), 3), "unit": "chunks/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "clocks": clk.summary(),
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+def cpu_baseline_sample(w, seconds_budget=20.0):
+    """Time the oracle on one steady-state attention call (all heads, all rows,
+    4608 keys) on the host cores; scale to chunks/s."""
+    import numpy as np
+
+    from oracle import attention as OA
+    from oracle.ring import ListRing
+    from streaming_attention_block_gb300 import synth
+
+    gen = synth.generator(w.seed)
+    ring = ListRing(w.R)
+    qs = None
+    t_calls = []
+    for c in range(3):
+        q, k, v = synth.chunk_qkv(w, gen)
+        qb, kb, vb = (np.transpose(x.float().numpy().astype(np.float64), (0, 2, 1, 3)) for x in (q, k, v))
+        if c == 2:
+            t = time.perf_counter()
+            OA.streaming_chunk_attention(qb, ring, c, kb, vb, w.W, False, w.scale)
+            t_calls.append(time.perf_counter() - t)
+        ring.append(c, kb, vb)
+    t_call = statistics.mean(t_calls)
+    per_chunk = t_call * w.steps * w.layers
+    return {"value": round(1.0 / per_chunk, 6), "unit": "chunks/s", "cores": _cpu_threads(), "kind": "oracle",
+            "sample": f"1 oracle call (chunk 2: 12 heads x 1536 queries x 4608 keys, fp64) took {t_call:.2f} s; "
+                      f"scaled x{w.steps * w.layers} calls per chunk"}
+
+
+def _cpu_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count()
+
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    import numpy as np
+
+    from oracle import attention as OA
+    from oracle.ring import ListRing
+    from streaming_attention_block_gb300 import synth
+
+    w = synth.workload("wan13b")
+    gen = synth.generator(w.seed)
+    ring = ListRing(w.R)
+    data = []
+    for c in range(3):
+        q, k, v = synth.chunk_qkv(w, gen)
+        data.append(tuple(np.transpose(x.float().numpy().astype(np.float64), (0, 2, 1, 3)) for x in (q, k, v)))
+    ring.append(0, data[0][1], data[0][2])
+    ring.append(1, data[1][1], data[1][2])
+    q, k, v = data[2]
+    # each step: a quarter of the query rows of one steady-state attention
+    # call (rows are independent), i.e. 1/480 of a chunk
+    rows = w.Lc // 4
+    sub = [q[:, :, i * rows:(i + 1) * rows] for i in range(4)]
+    for i in range(args.warmup):
+        OA.streaming_chunk_attention(sub[i % 4][:, :, :16], ring, 2, k, v, w.W, False, w.scale)
+    t = time.perf_counter()
+    for i in range(args.steps):
+        OA.streaming_chunk_attention(sub[i % 4], ring, 2, k, v, w.W, False, w.scale)
+    el = time.perf_counter() - t
+    per_step = el / args.steps
+    per_chunk = per_step * 4 * w.steps * w.layers
+    value = 1.0 / per_chunk
+    cpu = {"value": round(value, 6), "unit": "chunks/s", "cores": _cpu_threads(), "kind": "oracle",
+           "sample": f"{args.steps} steps of 384 query rows x 12 heads x 4608 keys (fp64), {per_step:.2f} s each; "
+                     f"scaled x{4 * w.steps * w.layers} to one chunk (4 steps x 30 layers x 1536 rows)"}
+    line = {"metric": METRIC, "value": round(value, 6), "unit": "chunks/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(per_step * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": "wan13b streaming: B1 H12 D128, 1536 tokens/chunk, ring 2 slots, window current+2 "
+                                   "(4608 keys); oracle sample per step, scaled to chunks/s",
+                       "global_batch": 1, "seq_len": w.Lc, "parallelism": "cpu"},
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(value, 6), "unit": "chunks/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

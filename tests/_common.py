@@ -123,7 +123,7 @@ def run_stream(w, ring, check_chunks, rows=None, layers=1, splits=None, device="
                                                                     w.scale)
                     torch.cuda.synchronize()
                     if on_check is not None:
-                        results.append((c, s, l) + on_check(O, LSE, o_ref, l_ref, rows, f"chunk {c} step {s} layer {l}"))
+                        results.append((c, s, l) + on_check(O, LSE, o_ref, l_ref, rows=rows, what=f"chunk {c} step {s} layer {l}"))
         if w.kcur_separate:
             for l in range(layers):
                 k, v, kd, vd = saved[l]
