@@ -137,6 +137,7 @@ def run_ours(args):
     O = [[torch.empty(shape, dtype=torch.bfloat16, device=dev) for _ in range(L)] for _ in range(S)]
     LSE = [[torch.empty((B, H, Lc), dtype=torch.float32, device=dev) for _ in range(L)] for _ in range(S)]
     ring = sab.KVRing(L, B, H, D, Lc, w.R, device=dev)
+    work = ring.workspace(args.splits) if args.splits != 1 else None
     save = max(0, S - 2)  # KV of the penultimate denoise step goes to the cache
     launches = [0]
 
@@ -147,8 +148,8 @@ def run_ours(args):
                     ev[0].append(torch.cuda.Event(enable_timing=True))
                     ev[1].append(torch.cuda.Event(enable_timing=True))
                     ev[0][-1].record(stream)
-                sab.chunk_attention(ring.handle, l, c, Q[s][l], Kc[s][l], Vc[s][l], w.W, False, 1, w.scale,
-                                    O[s][l], LSE[s][l], None, stream)
+                sab.chunk_attention(ring.handle, l, c, Q[s][l], Kc[s][l], Vc[s][l], w.W, False, args.splits,
+                                    w.scale, O[s][l], LSE[s][l], work, stream)
                 if ev is not None:
                     ev[1][-1].record(stream)
                 launches[0] += 1
@@ -262,6 +263,44 @@ def run_ours(args):
         pg.destroy_process_group()
 
 
+def run_attn_only(args):
+    """Small profiling case: one layer of the Wan-1.3B stream at chunk 2
+    (4608 keys), N back-to-back attention calls over 4 input sets."""
+    import torch
+
+    import streaming_attention_block_gb300 as sab
+    from streaming_attention_block_gb300 import synth
+
+    dev = torch.device("cuda", 0)
+    w = synth.workload("wan13b")
+    g = synth.generator(w.seed, device="cuda")
+    shape = (w.B, w.Lc, w.H, w.D)
+    sets = [tuple(synth.randn_bf16(g, shape, "cuda", rms_norm=(i < 2)) for i in range(3)) for _ in range(4)]
+    ring = sab.KVRing(1, w.B, w.H, w.D, w.Lc, w.R, device=dev)
+    ring.append(0, 0, sets[0][1], sets[0][2])
+    ring.append(0, 1, sets[1][1], sets[1][2])
+    ws = ring.workspace(args.splits) if args.splits != 1 else None
+    O = torch.empty(shape, dtype=torch.bfloat16, device=dev)
+    LSE = torch.empty((w.B, w.H, w.Lc), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    times = []
+    for i in range(args.attn_only):
+        q, k, v = sets[i % 4]
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        sab.chunk_attention(ring.handle, 0, 2, q, k, v, w.W, False, args.splits, w.scale, O, LSE, ws, stream)
+        b.record(stream)
+        times.append((a, b))
+    torch.cuda.synchronize()
+    us = [a.elapsed_time(b) * 1e3 for a, b in times]
+    flops = 4.0 * w.B * w.H * w.D * w.Lc * w.Lc * (w.W + 1)
+    tail = us[min(3, len(us) - 1):]
+    print(json.dumps({"attn_only_calls": len(us), "us_median": statistics.median(tail),
+                      "tflops_median": flops / (statistics.median(tail) * 1e-6) / 1e12, "splits": args.splits}))
+    assert sab.get_last_device_error(stream) == 0
+
+
 def cpu_baseline_sample(w, seconds_budget=20.0):
     """Time the oracle on one steady-state attention call (all heads, all rows,
     4608 keys) on the host cores; scale to chunks/s."""
@@ -352,7 +391,12 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--splits", type=int, default=0, help="KV splits per attention call (0: library's choice)")
+    ap.add_argument("--attn-only", type=int, default=0, metavar="N",
+                    help="profiling case: N steady-state attention calls on one layer, then exit")
     args = ap.parse_args()
+    if args.attn_only:
+        return run_attn_only(args)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":

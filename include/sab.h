@@ -165,7 +165,7 @@ sab_status sab_kv_ring_set_state(sab_ring* ring, const long long* newest_chunk, 
 
 /*
  * Workspace bytes sab_chunk_attention needs for `num_splits` KV partitions
- * (0 when num_splits == 1).  The workspace holds per-split partial outputs
+ * (0 when num_splits == 1; num_splits == 0 sizes it for any automatic choice).  The workspace holds per-split partial outputs
  * and LSEs plus one arrival counter per query tile; the counters must be zero
  * before the first call (zero-fill the workspace once after allocating it);
  * every successful call leaves them zero again.
@@ -184,7 +184,8 @@ size_t sab_chunk_attention_workspace(const sab_ring* ring, int num_splits);
  *   num_splits >= 1: KV partitions computed in parallel and merged by
  *          log-sum-exp inside the same kernel ("Matrix-Game 4.0", section
  *          "技术新颖性": the window is cut into intervals whose partial outputs
- *          are merged with log-sum-exp).
+ *          are merged with log-sum-exp); 0 lets the library choose (at most
+ *          16: enough partitions for one CTA per SM).
  *   softmax_scale  usually 1/sqrt(D).
  *   O      device, token-major [B, Lc, H, D] bf16 (output).
  *   LSE    device, [B, H, Lc] fp32, natural log of sum exp(s) (output; may be NULL).

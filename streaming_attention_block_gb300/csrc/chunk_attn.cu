@@ -48,7 +48,7 @@ namespace {
 
 using namespace ptx;
 
-constexpr uint32_t kWaitLimit = 1u << 23;  // ~2 s with the 256 ns back-off
+constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per pipeline wait
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows by > 2^8
@@ -81,18 +81,38 @@ struct Cfg {
   static constexpr uint32_t kTmemS = 0;          // S_t / P_t at column t * 128
   static constexpr uint32_t kTmemO = QT * 128;   // O_t at column kTmemO + t * D
   static constexpr uint32_t kTmemCols = (QT * 128 + QT * D <= 256) ? 256u : 512u;
+  // Cluster merge reuses the operand region (K, V, Q are dead by then):
+  // normalised partial rows of fp32, pitch D + 4 floats (bank-conflict free
+  // float4 access), then one LSE per row.
+  static constexpr uint32_t kMergePitch = D + 4;
+  static constexpr uint32_t kMergeOOff = kKOff;
+  static constexpr uint32_t kMergeLseOff = kMergeOOff + QT * 128 * kMergePitch * 4;
+  static_assert(kMergeLseOff + QT * 128 * 4 <= kBarOff, "merge buffer fits in the operand region");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded mbarrier wait.  try_wait already suspends the thread in hardware
+// until the phase completes (or a short system limit passes), so the loop
+// spins without sleeping -- a sleep would delay the wake-up of this
+// latency-critical pipeline.  Every 256 polls it checks the CTA abort flag and
+// the elapsed time; after kTimeoutNs it records the wait site, raises the
+// abort flag and gives up.
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                              unsigned site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
 #pragma unroll 1
-  for (uint32_t it = 0;; ++it) {
+  for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (it >= 64) {
+    if ((it & 255u) == 0) {
       if (*abort_flag) return false;
-      __nanosleep(it < 4096 ? 32 : 256);
-      if (it >= kWaitLimit) {
+      if (global_ns() - t0 > kTimeoutNs) {
         atomicOr(&g_sab_error_word, 1u << site);
         *abort_flag = 1;
         return false;
@@ -103,12 +123,14 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
 
 // Bounded wait used while draining after an abort (ignores the abort flag).
 __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = global_ns();
 #pragma unroll 1
-  for (uint32_t it = 0; it < kWaitLimit; ++it) {
-    if (mbar_try_wait(bar, parity)) return;
-    if (it >= 64) __nanosleep(256);
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_ns() - t0 > kTimeoutNs) {
+      atomicOr(&g_sab_error_word, 1u << 31);
+      return;
+    }
   }
-  atomicOr(&g_sab_error_word, 1u << 31);
 }
 
 struct Tile {
@@ -370,14 +392,7 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
         lo = klo - kr0;
         hi = khi - kr0;
       }
-      float mx = -INFINITY;
-      if (lo <= 0 && hi >= kTileN) {
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          mx = fmaxf(mx, fmaxf(__uint_as_float(s0[c]), __uint_as_float(s1[c])));
-          mx = fmaxf(mx, fmaxf(__uint_as_float(s2[c]), __uint_as_float(s3[c])));
-        }
-      } else {
+      if (!(lo <= 0 && hi >= kTileN)) {
         const uint32_t ninf = 0xff800000u;
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
@@ -385,10 +400,22 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
           s1[c] = (c + 32 >= lo && c + 32 < hi) ? s1[c] : ninf;
           s2[c] = (c + 64 >= lo && c + 64 < hi) ? s2[c] : ninf;
           s3[c] = (c + 96 >= lo && c + 96 < hi) ? s3[c] : ninf;
-          mx = fmaxf(mx, fmaxf(__uint_as_float(s0[c]), __uint_as_float(s1[c])));
-          mx = fmaxf(mx, fmaxf(__uint_as_float(s2[c]), __uint_as_float(s3[c])));
         }
       }
+      // row max as a tree: 8 independent partial maxima, then combine
+      float pm[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        pm[k] = fmaxf(fmaxf(__uint_as_float(s0[k]), __uint_as_float(s1[k])),
+                      fmaxf(__uint_as_float(s2[k]), __uint_as_float(s3[k])));
+#pragma unroll
+      for (int c = 8; c < 32; c += 8)
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          pm[k] = fmaxf(pm[k], fmaxf(fmaxf(__uint_as_float(s0[c + k]), __uint_as_float(s1[c + k])),
+                                     fmaxf(__uint_as_float(s2[c + k]), __uint_as_float(s3[c + k]))));
+      const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                             fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
       const float m_new = fmaxf(m_run, mx * sl);
       const bool need = m_new > m_run + kRescaleThreshold;
       float alpha = 1.f;
@@ -398,7 +425,7 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
         m_run = m_new;
       }
       const float mb = (m_run == -INFINITY) ? 0.f : m_run;
-      float sum = 0.f;
+      float ps[4] = {0.f, 0.f, 0.f, 0.f};
       // P (bf16 pairs) overwrites the first 64 columns of S: column k holds
       // keys 2k (low half) and 2k+1 (high half).
       {
@@ -409,7 +436,7 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
           const float a1 = ex2(fmaf(__uint_as_float(s0[2 * c + 1]), sl, -mb));
           const float b0 = ex2(fmaf(__uint_as_float(s1[2 * c]), sl, -mb));
           const float b1 = ex2(fmaf(__uint_as_float(s1[2 * c + 1]), sl, -mb));
-          sum += (a0 + a1) + (b0 + b1);
+          ps[c & 3] += (a0 + a1) + (b0 + b1);
           pk[c] = pack_bf16(a0, a1);
           pk[16 + c] = pack_bf16(b0, b1);
         }
@@ -423,13 +450,13 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
           const float a1 = ex2(fmaf(__uint_as_float(s2[2 * c + 1]), sl, -mb));
           const float b0 = ex2(fmaf(__uint_as_float(s3[2 * c]), sl, -mb));
           const float b1 = ex2(fmaf(__uint_as_float(s3[2 * c + 1]), sl, -mb));
-          sum += (a0 + a1) + (b0 + b1);
+          ps[c & 3] += (a0 + a1) + (b0 + b1);
           pk[c] = pack_bf16(a0, a1);
           pk[16 + c] = pack_bf16(b0, b1);
         }
         tmem_st32(tS + 32, pk);
       }
-      l_run += sum;
+      l_run += (ps[0] + ps[1]) + (ps[2] + ps[3]);
       if (j > 0 && __any_sync(0xffffffffu, need)) {
         // S_t(j) completion implies PV_t(j-1) completed (same-thread commit order)
 #pragma unroll
@@ -448,6 +475,9 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
     }
     if (ok) {
       ok = wait_bounded(bar(C::kBarOFinal + t), 0, abort_flag, 8 + t);
+      // the cluster merge overwrites operand smem: every MMA must be done
+      if (ok && QT == 2 && p.cluster_merge)
+        ok = wait_bounded(bar(C::kBarOFinal + (1 - t)), 0, abort_flag, 9 - t);
       ok = __all_sync(0xffffffffu, ok);
     }
     const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
@@ -481,6 +511,25 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
           }
         }
         if (row_valid && p.LSE != nullptr) p.LSE[(long long)bh * p.Lq + q_row] = lse;
+      } else if (p.cluster_merge) {
+        float* mrow = reinterpret_cast<float*>(base + C::kMergeOOff) + (t * 128 + row) * C::kMergePitch;
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t o[32];
+          if (n_tiles > 0) {
+            tmem_ld32(tO + c0, o);
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) o[c] = 0u;
+          }
+          float4* dst = reinterpret_cast<float4*>(mrow + c0);
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv_l, __uint_as_float(o[4 * v + 1]) * inv_l,
+                                 __uint_as_float(o[4 * v + 2]) * inv_l, __uint_as_float(o[4 * v + 3]) * inv_l);
+        }
+        reinterpret_cast<float*>(base + C::kMergeLseOff)[t * 128 + row] = lse;
       } else {
         const long long prow = ((long long)split * BH + bh) * p.lq_pad + (q_row);
         float* wrow = p.ws_o + prow * D;
@@ -503,8 +552,8 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
         p.ws_lse[prow] = lse;
       }
     }
-    if (p.splits > 1) {
-      // --------------------------------------- log-sum-exp merge of the splits
+    if (p.splits > 1 && !p.cluster_merge) {
+      // ------------------------- log-sum-exp merge of the splits through global memory
       __threadfence();
       named_bar_sync(1, 128 * QT);
       if (threadIdx.x == 128) {
@@ -565,6 +614,82 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
   }
 
   tc_fence_before();
+  if (p.cluster_merge) {
+    // ------------- log-sum-exp merge of the splits through distributed smem
+    // CTA `rank` of the cluster (= split index) merges rows
+    // [rank * rows_per, (rank + 1) * rows_per) of the query group, reading
+    // every split's normalised partial rows and LSEs from its peers' smem.
+    cluster_sync_all();
+    if (warp >= 4) {
+      const int S = p.splits;
+      const uint32_t rank = cluster_ctarank();
+      const int nthr = 128 * QT;
+      const int tid = threadIdx.x - 128;
+      const int rows_per = (QT * 128 + S - 1) / S;
+      int tpr = 1;  // threads per row: a power of two with tpr * rows_per <= nthr
+      while (tpr * 2 * rows_per <= nthr && tpr * 2 <= D / 4) tpr *= 2;
+      const int cpt = D / tpr;  // columns per thread (multiple of 4)
+      const int lr = tid / tpr;
+      const int r_cta = (int)rank * rows_per + lr;
+      const int q_row = q0 + r_cta;
+      if (lr < rows_per && r_cta < QT * 128 && q_row < p.Lq) {
+        const int col0 = (tid % tpr) * cpt;
+        const uint32_t lse_addr = base_u32 + C::kMergeLseOff + r_cta * 4;
+        const uint32_t o_addr = base_u32 + C::kMergeOOff + (r_cta * C::kMergePitch + col0) * 4;
+        float ls[8];
+        float M = -INFINITY;
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+          ls[s] = (s < S) ? ld_dsmem_f32(mapa(lse_addr, s)) : -INFINITY;
+          M = fmaxf(M, ls[s]);
+        }
+        float tot = 0.f;
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+          ls[s] = (M == -INFINITY || ls[s] == -INFINITY) ? 0.f : ex2((ls[s] - M) * kLog2e);
+          tot += ls[s];
+        }
+        const float inv_tot = tot > 0.f ? 1.f / tot : 0.f;
+        const float L = (M == -INFINITY) ? -INFINITY : M + __logf(tot);
+        uint16_t* orow = p.O + (((long long)b * p.Lq + q_row) * p.H + h) * D + col0;
+#pragma unroll 1
+        for (int c = 0; c < cpt; c += 16) {
+          float acc[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) acc[k] = 0.f;
+          float4 x[8][4];
+#pragma unroll
+          for (int s = 0; s < 8; ++s)
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              x[s][v] = (s < S && c + 4 * v < cpt) ? ld_dsmem_v4(mapa(o_addr + (c + 4 * v) * 4, s))
+                                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int s = 0; s < 8; ++s) {
+            const float wgt = ls[s] * inv_tot;
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              acc[4 * v] = fmaf(wgt, x[s][v].x, acc[4 * v]);
+              acc[4 * v + 1] = fmaf(wgt, x[s][v].y, acc[4 * v + 1]);
+              acc[4 * v + 2] = fmaf(wgt, x[s][v].z, acc[4 * v + 2]);
+              acc[4 * v + 3] = fmaf(wgt, x[s][v].w, acc[4 * v + 3]);
+            }
+          }
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            if (c + 4 * v < cpt) {
+              uint2 w2;
+              w2.x = pack_bf16(acc[4 * v], acc[4 * v + 1]);
+              w2.y = pack_bf16(acc[4 * v + 2], acc[4 * v + 3]);
+              *reinterpret_cast<uint2*>(orow + c + 4 * v) = w2;
+            }
+          }
+        }
+        if (col0 == 0 && p.LSE != nullptr) p.LSE[(long long)bh * p.Lq + q_row] = L;
+      }
+    }
+    cluster_sync_all();  // peers' smem stays valid until every CTA has read it
+  }
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
@@ -583,8 +708,23 @@ cudaError_t launch_impl(const AttnParams& p, cudaStream_t s) {
     attr_set = true;
   }
   dim3 grid(p.n_qgroups, p.B * p.H, p.splits);
-  chunk_attn_kernel<D, QT><<<grid, C::kThreads, C::kSmemBytes, s>>>(p);
-  return cudaGetLastError();
+  if (!p.cluster_merge) {
+    chunk_attn_kernel<D, QT><<<grid, C::kThreads, C::kSmemBytes, s>>>(p);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(C::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = (unsigned)p.splits;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, chunk_attn_kernel<D, QT>, p);
 }
 
 }  // namespace

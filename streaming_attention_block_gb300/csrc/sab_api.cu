@@ -126,6 +126,31 @@ WsLayout ws_layout(int BH, int Lq, int D, int splits) {
 }
 
 constexpr int kMaxSplits = 256;
+constexpr int kMaxAutoSplits = 8;
+constexpr int kMaxClusterSplits = 8;
+
+int device_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
+      n = v;
+    else
+      return 148;
+  }
+  return n;
+}
+
+// num_splits == 0: fill the GPU with one wave of CTAs (one CTA per SM fits):
+// the largest S with (query CTAs x S) <= SMs, at least 1, at most 16 and at
+// most half the KV tiles.
+int auto_splits(int base_ctas, int kv_tiles) {
+  int s = device_sms() / std::max(1, base_ctas);
+  s = std::min(s, kMaxAutoSplits);
+  s = std::min(s, std::max(1, kv_tiles / 2));
+  return std::max(1, s);
+}
 
 }  // namespace
 
@@ -302,13 +327,21 @@ sab_status sab_kv_ring_set_state(sab_ring* ring, const long long* newest_chunk, 
 }
 
 size_t sab_chunk_attention_workspace(const sab_ring* ring, int num_splits) {
-  if (ring == nullptr || num_splits < 1 || num_splits > kMaxSplits) return 0;
+  if (ring == nullptr || num_splits < 0 || num_splits > kMaxSplits) return 0;
+  if (num_splits == 0) num_splits = kMaxAutoSplits;
   return ws_layout(ring->d.batch * ring->d.heads, ring->d.chunk_tokens, ring->d.head_dim, num_splits).total;
 }
 
 static sab_status launch_attention(AttnParams& p, int Lq, int splits, void* workspace, size_t ws_bytes,
                                    void* stream) {
   const QTiling t = qtiling(Lq);
+  if (splits == 0) {
+    // block-causal: a CTA sees at most (window + 1) chunks plus one straddled tile
+    const int tiles = p.mode == kModeStreaming
+                          ? p.total_tiles
+                          : ((p.window + 1) * p.chunk_tokens + 2 * kTileN - 1) / kTileN;
+    splits = auto_splits(t.n_qgroups * p.B * p.H, tiles);
+  }
   p.Lq = Lq;
   p.n_qtiles = t.n_qtiles;
   p.n_qgroups = t.n_qgroups;
@@ -324,7 +357,15 @@ static sab_status launch_attention(AttnParams& p, int Lq, int splits, void* work
     p.ws_lse = reinterpret_cast<float*>(ws + w.lse_off);
   }
   if ((long long)p.B * p.H > 65535) return SAB_ERR_UNSUPPORTED;
-  const cudaError_t e = launch_chunk_attention(p, t.qt, static_cast<cudaStream_t>(stream));
+  // 2..8 splits of a query group merge inside a thread-block cluster; more
+  // splits (or a device refusing the cluster) merge through the workspace.
+  p.cluster_merge = (splits >= 2 && splits <= kMaxClusterSplits) ? 1 : 0;
+  cudaError_t e = launch_chunk_attention(p, t.qt, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess && p.cluster_merge) {
+    (void)cudaGetLastError();
+    p.cluster_merge = 0;
+    e = launch_chunk_attention(p, t.qt, static_cast<cudaStream_t>(stream));
+  }
   return e == cudaSuccess ? SAB_OK : SAB_ERR_CUDA;
 }
 
@@ -336,7 +377,7 @@ sab_status sab_chunk_attention(const sab_ring* ring, int layer, long long chunk,
   if ((K_cur == nullptr) != (V_cur == nullptr)) return SAB_ERR_INVALID_ARG;
   if (K_cur != nullptr && (!aligned16(K_cur) || !aligned16(V_cur))) return SAB_ERR_INVALID_ARG;
   if (LSE != nullptr && (reinterpret_cast<uintptr_t>(LSE) & 3u) != 0) return SAB_ERR_INVALID_ARG;
-  if (window < 0 || num_splits < 1 || num_splits > kMaxSplits) return SAB_ERR_INVALID_ARG;
+  if (window < 0 || num_splits < 0 || num_splits > kMaxSplits) return SAB_ERR_INVALID_ARG;
   if (!(softmax_scale > 0.f) || !isfinite(softmax_scale)) return SAB_ERR_INVALID_ARG;
   if (use_sink != 0 && use_sink != 1) return SAB_ERR_INVALID_ARG;
   if (chunk < 0) return SAB_ERR_OUT_OF_RANGE;
@@ -410,7 +451,8 @@ sab_status sab_chunk_attention(const sab_ring* ring, int layer, long long chunk,
 }
 
 size_t sab_block_causal_attention_workspace(int B, int L, int H, int D, int num_splits) {
-  if (B < 1 || L < 1 || H < 1 || (D != 64 && D != 128) || num_splits < 1 || num_splits > kMaxSplits) return 0;
+  if (B < 1 || L < 1 || H < 1 || (D != 64 && D != 128) || num_splits < 0 || num_splits > kMaxSplits) return 0;
+  if (num_splits == 0) num_splits = kMaxAutoSplits;
   return ws_layout(B * H, L, D, num_splits).total;
 }
 
@@ -421,7 +463,7 @@ sab_status sab_block_causal_attention(const void* Q, const void* K, const void* 
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return SAB_ERR_INVALID_ARG;
   if (LSE != nullptr && (reinterpret_cast<uintptr_t>(LSE) & 3u) != 0) return SAB_ERR_INVALID_ARG;
   if (B < 1 || L < 1 || H < 1 || (D != 64 && D != 128) || chunk_tokens < 1 || window < 0) return SAB_ERR_INVALID_ARG;
-  if (num_splits < 1 || num_splits > kMaxSplits) return SAB_ERR_INVALID_ARG;
+  if (num_splits < 0 || num_splits > kMaxSplits) return SAB_ERR_INVALID_ARG;
   if (!(softmax_scale > 0.f) || !isfinite(softmax_scale)) return SAB_ERR_INVALID_ARG;
   if ((long long)L > (1LL << 30)) return SAB_ERR_INVALID_ARG;
   AttnParams p;

@@ -35,6 +35,8 @@ struct AttnParams {
   int n_qgroups;          // CTAs along the query axis (q tiles per CTA: 1 or 2)
   int lq_pad;             // n_qgroups * tiles per CTA * 128 (workspace row pitch)
   int splits;
+  int cluster_merge;      // 1: the splits of a query tile form a thread-block
+                          // cluster and merge through distributed shared memory
   float scale_log2;       // softmax_scale * log2(e)
   // streaming
   int nseg;
