@@ -71,8 +71,8 @@ struct Cfg {
   static constexpr int kBarVFull = kBarKFull + kStages;
   static constexpr int kBarKVEmpty = kBarVFull + kStages;
   static constexpr int kBarSFull = kBarKVEmpty + kStages;  // [2]
-  static constexpr int kBarPFull = kBarSFull + 2;          // [2]
-  static constexpr int kBarOFinal = kBarPFull + 2;         // [2]
+  static constexpr int kBarPFull = kBarSFull + 2;          // [2 tiles][2 key halves]
+  static constexpr int kBarOFinal = kBarPFull + 4;         // [2]
   static constexpr int kBarDrain = kBarOFinal + 2;
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
@@ -81,13 +81,15 @@ struct Cfg {
   static constexpr uint32_t kTmemS = 0;          // S_t / P_t at column t * 128
   static constexpr uint32_t kTmemO = QT * 128;   // O_t at column kTmemO + t * D
   static constexpr uint32_t kTmemCols = (QT * 128 + QT * D <= 256) ? 256u : 512u;
-  // Cluster merge reuses the operand region (K, V, Q are dead by then):
-  // normalised partial rows of fp32, pitch D + 4 floats (bank-conflict free
-  // float4 access), then one LSE per row.
+  // Cluster merge reuses the operand region (K, V, Q are dead by then): the
+  // rows this CTA merges, one slot per split, fp32 with a pitch of D + 4
+  // floats (bank-conflict free float4 access), then one LSE per slot row.
+  // At most QT*128 + 7 slot rows (rows per CTA rounded up, 8 splits).
   static constexpr uint32_t kMergePitch = D + 4;
+  static constexpr uint32_t kMergeRows = QT * 128 + 8;
   static constexpr uint32_t kMergeOOff = kKOff;
-  static constexpr uint32_t kMergeLseOff = kMergeOOff + QT * 128 * kMergePitch * 4;
-  static_assert(kMergeLseOff + QT * 128 * 4 <= kBarOff, "merge buffer fits in the operand region");
+  static constexpr uint32_t kMergeLseOff = kMergeOOff + kMergeRows * kMergePitch * 4;
+  static_assert(kMergeLseOff + kMergeRows * 4 <= kBarOff, "merge buffer fits in the operand region");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
@@ -221,7 +223,8 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(C::kBarSFull + t), 1);
-      mbar_init(bar(C::kBarPFull + t), 128);
+      mbar_init(bar(C::kBarPFull + 2 * t), 128);
+      mbar_init(bar(C::kBarPFull + 2 * t + 1), 128);
       mbar_init(bar(C::kBarOFinal + t), 1);
     }
     mbar_init(bar(C::kBarDrain), 1);
@@ -244,6 +247,11 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
   tc_fence_after();
   const uint32_t tmem = misc[0];
 
+  // softmax-thread state handed to the cluster merge in the common tail
+  bool sm_ok = false;
+  float sm_inv_l = 0.f, sm_lse = -INFINITY;
+  uint32_t sm_tO = 0;
+  int sm_rcta = 0;
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -292,35 +300,52 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 1);
       bool ok = wait_bounded(bar(C::kBarQ), 0, abort_flag, 1);
       if (ok) tc_fence_after();
+      // Descriptors are built once: every operand tile of a kind shares the
+      // high word, and stepping K (or a stage) only adds a small constant to
+      // the 14-bit start-address field of the low word (no carry: shared
+      // addresses stay below 256 KB).
+      const uint64_t dq = smem_desc_sw128(sQ, 16, 1024);
+      const uint64_t dk = smem_desc_sw128(sK, 16, 1024);
+      const uint64_t dv = smem_desc_sw128(sV, C::kBoxBytes, 1024);
+      const uint32_t q_lo = (uint32_t)dq, k_lo = (uint32_t)dk, v_lo = (uint32_t)dv;
+      const uint32_t kq_hi = (uint32_t)(dq >> 32), v_hi = (uint32_t)(dv >> 32);
+      constexpr uint32_t kTileStep = C::kTileBytes >> 4;
       auto issue_s = [&](int t, int j) {
-        const int st = j % C::kStages;
+        const uint32_t st = (uint32_t)(j % C::kStages);
         const uint32_t d = tmem + C::kTmemS + t * 128;
+        const uint32_t a0 = q_lo + (uint32_t)t * kTileStep;
+        const uint32_t b0 = k_lo + st * kTileStep;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t koff = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
-          const uint64_t a = smem_desc_sw128(sQ + t * C::kTileBytes + koff, 16, 1024);
-          const uint64_t bd = smem_desc_sw128(sK + st * C::kTileBytes + koff, 16, 1024);
-          mma_ss(d, a, bd, idesc_qk, kk > 0 ? 1u : 0u);
+          const uint32_t koff = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
+          mma_ss(d, make_desc(a0 + koff, kq_hi), make_desc(b0 + koff, kq_hi), idesc_qk, kk > 0 ? 1u : 0u);
         }
       };
+      // O_t += P_t V in two halves of the key tile: the first half of P is
+      // published before the softmax computes the second one.
       auto issue_pv = [&](int t, int j) -> bool {
-        if (!wait_bounded(bar(C::kBarPFull + t), (uint32_t)j & 1u, abort_flag, 2 + t)) return false;
-        const int st = j % C::kStages;
-        if (!wait_bounded(bar(C::kBarVFull + st), (uint32_t)(j / C::kStages) & 1u, abort_flag, 4))
-          return false;
-        tc_fence_after();
+        const uint32_t st = (uint32_t)(j % C::kStages);
         const uint32_t d = tmem + C::kTmemO + t * D;
+        const uint32_t b0 = v_lo + st * kTileStep;
+        const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
-        for (int kk = 0; kk < kTileN / 16; ++kk) {
-          const uint32_t a_t = tmem + C::kTmemS + t * 128 + kk * 8;
-          const uint64_t bd = smem_desc_sw128(sV + st * C::kTileBytes + kk * 16 * 128, C::kBoxBytes, 1024);
-          mma_ts(d, a_t, bd, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+        for (int half = 0; half < 2; ++half) {
+          if (!wait_bounded(bar(C::kBarPFull + 2 * t + half), (uint32_t)j & 1u, abort_flag, 2 + t)) return false;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = half * 4; kk < half * 4 + 4; ++kk) {
+            const uint32_t a_t = tmem + C::kTmemS + t * 128 + kk * 8;
+            mma_ts(d, a_t, make_desc(b0 + ((kk * 16 * 128) >> 4), v_hi), idesc_pv, kk > 0 ? 1u : acc0);
+          }
         }
         return true;
       };
+      auto wait_v = [&](int j) -> bool {
+        return wait_bounded(bar(C::kBarVFull + j % C::kStages), (uint32_t)(j / C::kStages) & 1u, abort_flag, 4);
+      };
       for (int j = 0; ok && j < n_tiles; ++j) {
         const int st = j % C::kStages;
-        if (j > 0 && !(ok = issue_pv(0, j - 1))) break;
+        if (j > 0 && !(ok = wait_v(j - 1) && issue_pv(0, j - 1))) break;
         if (!(ok = wait_bounded(bar(C::kBarKFull + st), (uint32_t)(j / C::kStages) & 1u, abort_flag, 5)))
           break;
         tc_fence_after();
@@ -335,7 +360,7 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
       }
       if (ok) {
         if (n_tiles > 0) {
-          ok = issue_pv(0, n_tiles - 1);
+          ok = wait_v(n_tiles - 1) && issue_pv(0, n_tiles - 1);
           if (ok) mma_commit(bar(C::kBarOFinal + 0));
           if (ok && QT == 2) {
             ok = issue_pv(1, n_tiles - 1);
@@ -370,6 +395,13 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
       khi = min(p.Lk, (qc + 1) * p.chunk_tokens);
     }
     const float sl = p.scale_log2;
+    // streaming: the key runs in registers (the last tile of a run is partial)
+    int seg_tile0[kMaxSegments], seg_rows[kMaxSegments];
+#pragma unroll
+    for (int i = 0; i < kMaxSegments; ++i) {
+      seg_tile0[i] = (i < p.nseg) ? p.seg[i].tile0 : 0x7fffffff;
+      seg_rows[i] = p.seg[i].nrows;
+    }
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     for (int j = 0; j < n_tiles; ++j) {
@@ -382,16 +414,25 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
       tmem_ld32(tS + 32, s1);
       tmem_ld32(tS + 64, s2);
       tmem_ld32(tS + 96, s3);
-      tmem_wait_ld();
       int lo, hi;
+      const int g = first + j;
       if (p.mode == kModeStreaming) {
+        int sg = 0;
+#pragma unroll
+        for (int i = 1; i < kMaxSegments; ++i) sg = (g >= seg_tile0[i]) ? i : sg;
+        int t0 = seg_tile0[0], nr = seg_rows[0];
+#pragma unroll
+        for (int i = 1; i < kMaxSegments; ++i) {
+          t0 = (sg == i) ? seg_tile0[i] : t0;
+          nr = (sg == i) ? seg_rows[i] : nr;
+        }
         lo = 0;
-        hi = tile_at(p, first + j).valid;
+        hi = nr - (g - t0) * kTileN;
       } else {
-        const int kr0 = (first + j) * kTileN;
-        lo = klo - kr0;
-        hi = khi - kr0;
+        lo = klo - g * kTileN;
+        hi = khi - g * kTileN;
       }
+      tmem_wait_ld();
       if (!(lo <= 0 && hi >= kTileN)) {
         const uint32_t ninf = 0xff800000u;
 #pragma unroll
@@ -402,20 +443,20 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
           s3[c] = (c + 96 >= lo && c + 96 < hi) ? s3[c] : ninf;
         }
       }
-      // row max as a tree: 8 independent partial maxima, then combine
+      // row max: 8 independent chains of three-input maxima
       float pm[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k)
-        pm[k] = fmaxf(fmaxf(__uint_as_float(s0[k]), __uint_as_float(s1[k])),
-                      fmaxf(__uint_as_float(s2[k]), __uint_as_float(s3[k])));
-#pragma unroll
-      for (int c = 8; c < 32; c += 8)
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          pm[k] = fmaxf(pm[k], fmaxf(fmaxf(__uint_as_float(s0[c + k]), __uint_as_float(s1[c + k])),
-                                     fmaxf(__uint_as_float(s2[c + k]), __uint_as_float(s3[c + k]))));
-      const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
-                             fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+      for (int k = 0; k < 8; ++k) {
+        float m = fmax3(__uint_as_float(s0[k]), __uint_as_float(s0[k + 8]), __uint_as_float(s0[k + 16]));
+        m = fmax3(m, __uint_as_float(s0[k + 24]), __uint_as_float(s1[k]));
+        m = fmax3(m, __uint_as_float(s1[k + 8]), __uint_as_float(s1[k + 16]));
+        m = fmax3(m, __uint_as_float(s1[k + 24]), __uint_as_float(s2[k]));
+        m = fmax3(m, __uint_as_float(s2[k + 8]), __uint_as_float(s2[k + 16]));
+        m = fmax3(m, __uint_as_float(s2[k + 24]), __uint_as_float(s3[k]));
+        m = fmax3(m, __uint_as_float(s3[k + 8]), __uint_as_float(s3[k + 16]));
+        pm[k] = fmaxf(m, __uint_as_float(s3[k + 24]));
+      }
+      const float mx = fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7]));
       const float m_new = fmaxf(m_run, mx * sl);
       const bool need = m_new > m_run + kRescaleThreshold;
       float alpha = 1.f;
@@ -424,10 +465,24 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
         l_run *= alpha;
         m_run = m_new;
       }
+      if (j > 0 && __any_sync(0xffffffffu, need)) {
+        // S_t(j) completion implies PV_t(j-1) completed (same-thread commit
+        // order); the rescale lands before the first half of P is published.
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 16) {
+          uint32_t o[16];
+          tmem_ld16(tO + c0, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 16; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+          tmem_st16(tO + c0, o);
+        }
+      }
       const float mb = (m_run == -INFINITY) ? 0.f : m_run;
       float ps[4] = {0.f, 0.f, 0.f, 0.f};
       // P (bf16 pairs) overwrites the first 64 columns of S: column k holds
-      // keys 2k (low half) and 2k+1 (high half).
+      // keys 2k (low half) and 2k+1 (high half).  Keys 0..63 are published
+      // first so the PV MMA on them overlaps the exponentials of keys 64..127.
       {
         uint32_t pk[32];
 #pragma unroll
@@ -442,6 +497,9 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
         }
         tmem_st32(tS + 0, pk);
       }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(C::kBarPFull + 2 * t));
       {
         uint32_t pk[32];
 #pragma unroll
@@ -457,21 +515,9 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
         tmem_st32(tS + 32, pk);
       }
       l_run += (ps[0] + ps[1]) + (ps[2] + ps[3]);
-      if (j > 0 && __any_sync(0xffffffffu, need)) {
-        // S_t(j) completion implies PV_t(j-1) completed (same-thread commit order)
-#pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t o[32];
-          tmem_ld32(tO + c0, o);
-          tmem_wait_ld();
-#pragma unroll
-          for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-          tmem_st32(tO + c0, o);
-        }
-      }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar(C::kBarPFull + t));
+      mbar_arrive(bar(C::kBarPFull + 2 * t + 1));
     }
     if (ok) {
       ok = wait_bounded(bar(C::kBarOFinal + t), 0, abort_flag, 8 + t);
@@ -512,24 +558,13 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
         }
         if (row_valid && p.LSE != nullptr) p.LSE[(long long)bh * p.Lq + q_row] = lse;
       } else if (p.cluster_merge) {
-        float* mrow = reinterpret_cast<float*>(base + C::kMergeOOff) + (t * 128 + row) * C::kMergePitch;
-#pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t o[32];
-          if (n_tiles > 0) {
-            tmem_ld32(tO + c0, o);
-            tmem_wait_ld();
-          } else {
-#pragma unroll
-            for (int c = 0; c < 32; ++c) o[c] = 0u;
-          }
-          float4* dst = reinterpret_cast<float4*>(mrow + c0);
-#pragma unroll
-          for (int v = 0; v < 8; ++v)
-            dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv_l, __uint_as_float(o[4 * v + 1]) * inv_l,
-                                 __uint_as_float(o[4 * v + 2]) * inv_l, __uint_as_float(o[4 * v + 3]) * inv_l);
-        }
-        reinterpret_cast<float*>(base + C::kMergeLseOff)[t * 128 + row] = lse;
+        // the common tail pushes this row once every CTA of the cluster is
+        // done with its operand shared memory
+        sm_ok = true;
+        sm_inv_l = inv_l;
+        sm_lse = lse;
+        sm_tO = tO;
+        sm_rcta = t * 128 + row;
       } else {
         const long long prow = ((long long)split * BH + bh) * p.lq_pad + (q_row);
         float* wrow = p.ws_o + prow * D;
@@ -616,9 +651,37 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
   tc_fence_before();
   if (p.cluster_merge) {
     // ------------- log-sum-exp merge of the splits through distributed smem
-    // CTA `rank` of the cluster (= split index) merges rows
-    // [rank * rows_per, (rank + 1) * rows_per) of the query group, reading
-    // every split's normalised partial rows and LSEs from its peers' smem.
+    // CTA rank r of the cluster owns rows [r * rows_per, (r + 1) * rows_per)
+    // of the query group.  Barrier A: every CTA is done with its operand
+    // smem (all MMAs complete).  Each softmax thread then pushes its
+    // normalised partial row into the owner's smem with fire-and-forget
+    // distributed-shared-memory stores.  Barrier B: all pushes landed; each
+    // CTA merges its own rows from local smem.
+    cluster_sync_all();
+    if (warp >= 4 && sm_ok) {
+      tc_fence_after();
+      const int rows_per = (QT * 128 + p.splits - 1) / p.splits;
+      const uint32_t owner = (uint32_t)(sm_rcta / rows_per);
+      const int slot_row = split * rows_per + (sm_rcta - (int)owner * rows_per);
+      const uint32_t o_dst = mapa(base_u32 + C::kMergeOOff + slot_row * C::kMergePitch * 4, owner);
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t o[32];
+        if (n_tiles > 0) {
+          tmem_ld32(sm_tO + c0, o);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) o[c] = 0u;
+        }
+#pragma unroll
+        for (int v = 0; v < 8; ++v)
+          st_dsmem_v4(o_dst + (c0 + 4 * v) * 4, __uint_as_float(o[4 * v]) * sm_inv_l,
+                      __uint_as_float(o[4 * v + 1]) * sm_inv_l, __uint_as_float(o[4 * v + 2]) * sm_inv_l,
+                      __uint_as_float(o[4 * v + 3]) * sm_inv_l);
+      }
+      st_dsmem_f32(mapa(base_u32 + C::kMergeLseOff + slot_row * 4, owner), sm_lse);
+    }
     cluster_sync_all();
     if (warp >= 4) {
       const int S = p.splits;
@@ -634,13 +697,13 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
       const int q_row = q0 + r_cta;
       if (lr < rows_per && r_cta < QT * 128 && q_row < p.Lq) {
         const int col0 = (tid % tpr) * cpt;
-        const uint32_t lse_addr = base_u32 + C::kMergeLseOff + r_cta * 4;
-        const uint32_t o_addr = base_u32 + C::kMergeOOff + (r_cta * C::kMergePitch + col0) * 4;
+        const float* lse_buf = reinterpret_cast<const float*>(base + C::kMergeLseOff);
+        const float* o_buf = reinterpret_cast<const float*>(base + C::kMergeOOff);
         float ls[8];
         float M = -INFINITY;
 #pragma unroll
         for (int s = 0; s < 8; ++s) {
-          ls[s] = (s < S) ? ld_dsmem_f32(mapa(lse_addr, s)) : -INFINITY;
+          ls[s] = (s < S) ? lse_buf[s * rows_per + lr] : -INFINITY;
           M = fmaxf(M, ls[s]);
         }
         float tot = 0.f;
@@ -653,30 +716,29 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
         const float L = (M == -INFINITY) ? -INFINITY : M + __logf(tot);
         uint16_t* orow = p.O + (((long long)b * p.Lq + q_row) * p.H + h) * D + col0;
 #pragma unroll 1
-        for (int c = 0; c < cpt; c += 16) {
-          float acc[16];
+        for (int c = 0; c < cpt; c += 8) {
+          float acc[8];
 #pragma unroll
-          for (int k = 0; k < 16; ++k) acc[k] = 0.f;
-          float4 x[8][4];
-#pragma unroll
-          for (int s = 0; s < 8; ++s)
-#pragma unroll
-            for (int v = 0; v < 4; ++v)
-              x[s][v] = (s < S && c + 4 * v < cpt) ? ld_dsmem_v4(mapa(o_addr + (c + 4 * v) * 4, s))
-                                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int k = 0; k < 8; ++k) acc[k] = 0.f;
 #pragma unroll
           for (int s = 0; s < 8; ++s) {
-            const float wgt = ls[s] * inv_tot;
+            if (s < S) {
+              const float wgt = ls[s] * inv_tot;
+              const float* src = o_buf + (s * rows_per + lr) * C::kMergePitch + col0 + c;
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              acc[4 * v] = fmaf(wgt, x[s][v].x, acc[4 * v]);
-              acc[4 * v + 1] = fmaf(wgt, x[s][v].y, acc[4 * v + 1]);
-              acc[4 * v + 2] = fmaf(wgt, x[s][v].z, acc[4 * v + 2]);
-              acc[4 * v + 3] = fmaf(wgt, x[s][v].w, acc[4 * v + 3]);
+              for (int v = 0; v < 2; ++v) {
+                if (c + 4 * v < cpt) {
+                  const float4 x = *reinterpret_cast<const float4*>(src + 4 * v);
+                  acc[4 * v] = fmaf(wgt, x.x, acc[4 * v]);
+                  acc[4 * v + 1] = fmaf(wgt, x.y, acc[4 * v + 1]);
+                  acc[4 * v + 2] = fmaf(wgt, x.z, acc[4 * v + 2]);
+                  acc[4 * v + 3] = fmaf(wgt, x.w, acc[4 * v + 3]);
+                }
+              }
             }
           }
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
+          for (int v = 0; v < 2; ++v) {
             if (c + 4 * v < cpt) {
               uint2 w2;
               w2.x = pack_bf16(acc[4 * v], acc[4 * v + 1]);
@@ -688,7 +750,6 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
         if (col0 == 0 && p.LSE != nullptr) p.LSE[(long long)bh * p.Lq + q_row] = L;
       }
     }
-    cluster_sync_all();  // peers' smem stays valid until every CTA has read it
   }
   __syncthreads();
   if (warp == 1) {
