@@ -532,7 +532,9 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
     if (ok) {
       tc_fence_after();
       if (p.splits == 1) {
-        uint16_t* orow = p.O + (((long long)b * p.Lq + q_row) * p.H + h) * D;
+        // stage the bf16 row in this tile's (now dead) Q slot, in the
+        // 128-byte-swizzled layout of the output tensor map, for a TMA store
+        uint8_t* stage = base + C::kQOff + t * C::kTileBytes;
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t o[32];
@@ -543,17 +545,15 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
 #pragma unroll
             for (int c = 0; c < 32; ++c) o[c] = 0u;
           }
-          if (row_valid) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + c0);
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              uint4 w;
-              w.x = pack_bf16(__uint_as_float(o[8 * v + 0]) * inv_l, __uint_as_float(o[8 * v + 1]) * inv_l);
-              w.y = pack_bf16(__uint_as_float(o[8 * v + 2]) * inv_l, __uint_as_float(o[8 * v + 3]) * inv_l);
-              w.z = pack_bf16(__uint_as_float(o[8 * v + 4]) * inv_l, __uint_as_float(o[8 * v + 5]) * inv_l);
-              w.w = pack_bf16(__uint_as_float(o[8 * v + 6]) * inv_l, __uint_as_float(o[8 * v + 7]) * inv_l);
-              dst[v] = w;
-            }
+          for (int v = 0; v < 4; ++v) {
+            uint4 w;
+            w.x = pack_bf16(__uint_as_float(o[8 * v + 0]) * inv_l, __uint_as_float(o[8 * v + 1]) * inv_l);
+            w.y = pack_bf16(__uint_as_float(o[8 * v + 2]) * inv_l, __uint_as_float(o[8 * v + 3]) * inv_l);
+            w.z = pack_bf16(__uint_as_float(o[8 * v + 4]) * inv_l, __uint_as_float(o[8 * v + 5]) * inv_l);
+            w.w = pack_bf16(__uint_as_float(o[8 * v + 6]) * inv_l, __uint_as_float(o[8 * v + 7]) * inv_l);
+            const int k = (c0 >> 3) + v;  // 16-byte chunk of the row
+            *reinterpret_cast<uint4*>(stage + (k >> 3) * C::kBoxBytes + row * 128 + (((k & 7) ^ (row & 7)) << 4)) = w;
           }
         }
         if (row_valid && p.LSE != nullptr) p.LSE[(long long)bh * p.Lq + q_row] = lse;
@@ -585,6 +585,19 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
                                  __uint_as_float(o[4 * v + 2]) * inv_l, __uint_as_float(o[4 * v + 3]) * inv_l);
         }
         p.ws_lse[prow] = lse;
+      }
+    }
+    if (p.splits == 1) {
+      // every row of the tile is staged: one thread stores the tile with TMA
+      // (rows past the end of the sequence are clipped by the tensor map)
+      fence_proxy_async_smem();
+      named_bar_sync(2 + t, 128);
+      if (warp == 4 + 4 * t && lane == 0 && !*abort_flag && q0 + t * kTileM < p.Lq) {
+#pragma unroll
+        for (int bx = 0; bx < C::kBoxes; ++bx)
+          tma_store_4d(&p.o_map, base_u32 + C::kQOff + t * C::kTileBytes + bx * C::kBoxBytes, bx * 64,
+                       q0 + t * kTileM, h, b);
+        tma_store_commit_and_wait_read();
       }
     }
     if (p.splits > 1 && !p.cluster_merge) {
@@ -653,16 +666,24 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
     // ------------- log-sum-exp merge of the splits through distributed smem
     // CTA rank r of the cluster owns rows [r * rows_per, (r + 1) * rows_per)
     // of the query group.  Barrier A: every CTA is done with its operand
-    // smem (all MMAs complete).  Each softmax thread then pushes its
-    // normalised partial row into the owner's smem with fire-and-forget
-    // distributed-shared-memory stores.  Barrier B: all pushes landed; each
-    // CTA merges its own rows from local smem.
+    // smem (all MMAs complete).  Each softmax thread whose row another CTA
+    // owns pushes its normalised partial row and LSE into the owner's smem
+    // (slot = this split) with fire-and-forget distributed-shared-memory
+    // stores; rows this CTA owns stay in TMEM.  Barrier B: every push has
+    // landed; each owning thread merges its TMEM row with the received
+    // slots and writes the output row.  TMEM loads are warp-collective, so
+    // the branches are warp-uniform and only the stores are predicated per
+    // lane (a warp's rows may straddle two owners).
+    const int S = p.splits;
+    const int rows_per = (QT * 128 + S - 1) / S;
+    const uint32_t rank = cluster_ctarank();
+    const uint32_t owner = (uint32_t)(sm_rcta / rows_per);
+    const int lr = sm_rcta - (int)owner * rows_per;
+    const bool push = owner != rank;
     cluster_sync_all();
-    if (warp >= 4 && sm_ok) {
+    if (warp >= 4 && sm_ok && __any_sync(0xffffffffu, push)) {
       tc_fence_after();
-      const int rows_per = (QT * 128 + p.splits - 1) / p.splits;
-      const uint32_t owner = (uint32_t)(sm_rcta / rows_per);
-      const int slot_row = split * rows_per + (sm_rcta - (int)owner * rows_per);
+      const int slot_row = split * rows_per + lr;
       const uint32_t o_dst = mapa(base_u32 + C::kMergeOOff + slot_row * C::kMergePitch * 4, owner);
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
@@ -674,81 +695,85 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
 #pragma unroll
           for (int c = 0; c < 32; ++c) o[c] = 0u;
         }
+        if (push) {
 #pragma unroll
-        for (int v = 0; v < 8; ++v)
-          st_dsmem_v4(o_dst + (c0 + 4 * v) * 4, __uint_as_float(o[4 * v]) * sm_inv_l,
-                      __uint_as_float(o[4 * v + 1]) * sm_inv_l, __uint_as_float(o[4 * v + 2]) * sm_inv_l,
-                      __uint_as_float(o[4 * v + 3]) * sm_inv_l);
+          for (int v = 0; v < 8; ++v)
+            st_dsmem_v4(o_dst + (c0 + 4 * v) * 4, __uint_as_float(o[4 * v]) * sm_inv_l,
+                        __uint_as_float(o[4 * v + 1]) * sm_inv_l, __uint_as_float(o[4 * v + 2]) * sm_inv_l,
+                        __uint_as_float(o[4 * v + 3]) * sm_inv_l);
+        }
       }
-      st_dsmem_f32(mapa(base_u32 + C::kMergeLseOff + slot_row * 4, owner), sm_lse);
+      if (push) st_dsmem_f32(mapa(base_u32 + C::kMergeLseOff + slot_row * 4, owner), sm_lse);
     }
     cluster_sync_all();
-    if (warp >= 4) {
-      const int S = p.splits;
-      const uint32_t rank = cluster_ctarank();
-      const int nthr = 128 * QT;
-      const int tid = threadIdx.x - 128;
-      const int rows_per = (QT * 128 + S - 1) / S;
-      int tpr = 1;  // threads per row: a power of two with tpr * rows_per <= nthr
-      while (tpr * 2 * rows_per <= nthr && tpr * 2 <= D / 4) tpr *= 2;
-      const int cpt = D / tpr;  // columns per thread (multiple of 4)
-      const int lr = tid / tpr;
-      const int r_cta = (int)rank * rows_per + lr;
-      const int q_row = q0 + r_cta;
-      if (lr < rows_per && r_cta < QT * 128 && q_row < p.Lq) {
-        const int col0 = (tid % tpr) * cpt;
-        const float* lse_buf = reinterpret_cast<const float*>(base + C::kMergeLseOff);
-        const float* o_buf = reinterpret_cast<const float*>(base + C::kMergeOOff);
-        float ls[8];
-        float M = -INFINITY;
+    if (warp >= 4 && sm_ok && __any_sync(0xffffffffu, !push)) {
+      tc_fence_after();
+      const int q_row = q0 + sm_rcta;
+      const float* lse_buf = reinterpret_cast<const float*>(base + C::kMergeLseOff);
+      const float* o_buf = reinterpret_cast<const float*>(base + C::kMergeOOff);
+      float ls[8];
+      float M = -INFINITY;
 #pragma unroll
-        for (int s = 0; s < 8; ++s) {
-          ls[s] = (s < S) ? lse_buf[s * rows_per + lr] : -INFINITY;
-          M = fmaxf(M, ls[s]);
-        }
-        float tot = 0.f;
-#pragma unroll
-        for (int s = 0; s < 8; ++s) {
-          ls[s] = (M == -INFINITY || ls[s] == -INFINITY) ? 0.f : ex2((ls[s] - M) * kLog2e);
-          tot += ls[s];
-        }
-        const float inv_tot = tot > 0.f ? 1.f / tot : 0.f;
-        const float L = (M == -INFINITY) ? -INFINITY : M + __logf(tot);
-        uint16_t* orow = p.O + (((long long)b * p.Lq + q_row) * p.H + h) * D + col0;
-#pragma unroll 1
-        for (int c = 0; c < cpt; c += 8) {
-          float acc[8];
-#pragma unroll
-          for (int k = 0; k < 8; ++k) acc[k] = 0.f;
-#pragma unroll
-          for (int s = 0; s < 8; ++s) {
-            if (s < S) {
-              const float wgt = ls[s] * inv_tot;
-              const float* src = o_buf + (s * rows_per + lr) * C::kMergePitch + col0 + c;
-#pragma unroll
-              for (int v = 0; v < 2; ++v) {
-                if (c + 4 * v < cpt) {
-                  const float4 x = *reinterpret_cast<const float4*>(src + 4 * v);
-                  acc[4 * v] = fmaf(wgt, x.x, acc[4 * v]);
-                  acc[4 * v + 1] = fmaf(wgt, x.y, acc[4 * v + 1]);
-                  acc[4 * v + 2] = fmaf(wgt, x.z, acc[4 * v + 2]);
-                  acc[4 * v + 3] = fmaf(wgt, x.w, acc[4 * v + 3]);
-                }
-              }
-            }
-          }
-#pragma unroll
-          for (int v = 0; v < 2; ++v) {
-            if (c + 4 * v < cpt) {
-              uint2 w2;
-              w2.x = pack_bf16(acc[4 * v], acc[4 * v + 1]);
-              w2.y = pack_bf16(acc[4 * v + 2], acc[4 * v + 3]);
-              *reinterpret_cast<uint2*>(orow + c + 4 * v) = w2;
-            }
-          }
-        }
-        if (col0 == 0 && p.LSE != nullptr) p.LSE[(long long)bh * p.Lq + q_row] = L;
+      for (int s = 0; s < 8; ++s) {
+        ls[s] = (s >= S || push) ? -INFINITY : (s == (int)rank ? sm_lse : lse_buf[s * rows_per + lr]);
+        M = fmaxf(M, ls[s]);
       }
+      float tot = 0.f;
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        ls[s] = (M == -INFINITY || ls[s] == -INFINITY) ? 0.f : ex2((ls[s] - M) * kLog2e);
+        tot += ls[s];
+      }
+      const float inv_tot = tot > 0.f ? 1.f / tot : 0.f;
+      const float L = (M == -INFINITY) ? -INFINITY : M + __logf(tot);
+      const bool row_valid = !push && q_row < p.Lq;
+      uint16_t* orow = p.O + (((long long)b * p.Lq + q_row) * p.H + h) * D;
+      float l_own = 0.f;
+#pragma unroll
+      for (int s = 0; s < 8; ++s) l_own = (s == (int)rank) ? ls[s] : l_own;
+      const float w_own = l_own * inv_tot * sm_inv_l;
+#pragma unroll 1
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t o[32];
+        if (n_tiles > 0) {
+          tmem_ld32(sm_tO + c0, o);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) o[c] = 0u;
+        }
+        float acc[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) acc[c] = __uint_as_float(o[c]) * w_own;
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+          if (s < S && s != (int)rank && !push) {
+            const float wgt = ls[s] * inv_tot;
+            const float4* src = reinterpret_cast<const float4*>(o_buf + (s * rows_per + lr) * C::kMergePitch + c0);
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+              const float4 x = src[v];
+              acc[4 * v] = fmaf(wgt, x.x, acc[4 * v]);
+              acc[4 * v + 1] = fmaf(wgt, x.y, acc[4 * v + 1]);
+              acc[4 * v + 2] = fmaf(wgt, x.z, acc[4 * v + 2]);
+              acc[4 * v + 3] = fmaf(wgt, x.w, acc[4 * v + 3]);
+            }
+          }
+        }
+        if (row_valid) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint4 w;
+            w.x = pack_bf16(acc[8 * v + 0], acc[8 * v + 1]);
+            w.y = pack_bf16(acc[8 * v + 2], acc[8 * v + 3]);
+            w.z = pack_bf16(acc[8 * v + 4], acc[8 * v + 5]);
+            w.w = pack_bf16(acc[8 * v + 6], acc[8 * v + 7]);
+            dst[v] = w;
+          }
+        }
+      }
+      if (row_valid && p.LSE != nullptr) p.LSE[(long long)bh * p.Lq + q_row] = L;
     }
   }
   __syncthreads();

@@ -446,7 +446,9 @@ sab_status sab_chunk_attention(const sab_ring* ring, int layer, long long chunk,
   }
   p.nseg = nseg;
   p.total_tiles = tiles;
-  if (!encode_token_major(&p.q_map, Q, d.batch, Lc, d.heads, d.head_dim)) return SAB_ERR_CUDA;
+  if (!encode_token_major(&p.q_map, Q, d.batch, Lc, d.heads, d.head_dim) ||
+      !encode_token_major(&p.o_map, O, d.batch, Lc, d.heads, d.head_dim))
+    return SAB_ERR_CUDA;
   return launch_attention(p, Lc, num_splits, workspace, ws_bytes, stream);
 }
 
@@ -479,7 +481,7 @@ sab_status sab_block_causal_attention(const void* Q, const void* K, const void* 
   p.O = static_cast<uint16_t*>(O);
   p.LSE = LSE;
   if (!encode_token_major(&p.q_map, Q, B, L, H, D) || !encode_token_major(&p.k_map[0], K, B, L, H, D) ||
-      !encode_token_major(&p.v_map[0], V, B, L, H, D))
+      !encode_token_major(&p.v_map[0], V, B, L, H, D) || !encode_token_major(&p.o_map, O, B, L, H, D))
     return SAB_ERR_CUDA;
   p.k_map[1] = p.k_map[0];
   p.v_map[1] = p.v_map[0];

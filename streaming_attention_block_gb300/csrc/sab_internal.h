@@ -28,6 +28,7 @@ struct AttnParams {
   CUtensorMap q_map;      // dims (D, Lq, H, B), box (64, 128, 1, 1), SW128
   CUtensorMap k_map[2];   // per source, dims (D, rows, H, B)
   CUtensorMap v_map[2];
+  CUtensorMap o_map;      // output, dims (D, Lq, H, B), box (64, 128, 1, 1), SW128
   int mode;
   int B, H, D;
   int Lq;                 // query rows per (b, h)
