@@ -67,9 +67,8 @@ struct Cfg {
   static constexpr uint32_t kQOff = kVOff + kStages * kTileBytes;
   static constexpr uint32_t kBarOff = kQOff + QT * kTileBytes;
   static constexpr int kBarQ = 0;
-  static constexpr int kBarKFull = 1;
-  static constexpr int kBarVFull = kBarKFull + kStages;
-  static constexpr int kBarKVEmpty = kBarVFull + kStages;
+  static constexpr int kBarKFull = 1;                      // [kStages] K and V tile landed
+  static constexpr int kBarKVEmpty = kBarKFull + kStages;
   static constexpr int kBarSFull = kBarKVEmpty + kStages;  // [2]
   static constexpr int kBarPFull = kBarSFull + 2;          // [2 tiles][2 key halves]
   static constexpr int kBarOFinal = kBarPFull + 4;         // [2]
@@ -107,7 +106,7 @@ __device__ __forceinline__ uint64_t global_ns() {
 // abort flag and gives up.
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                              unsigned site) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_test_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
 #pragma unroll 1
   for (uint32_t it = 1;; ++it) {
@@ -218,7 +217,6 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
     mbar_init(bar(C::kBarQ), 1);
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(bar(C::kBarKFull + s), 1);
-      mbar_init(bar(C::kBarVFull + s), 1);
       mbar_init(bar(C::kBarKVEmpty + s), 1);
     }
     for (int t = 0; t < 2; ++t) {
@@ -270,16 +268,15 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
             !wait_bounded(bar(C::kBarKVEmpty + st), (round - 1u) & 1u, abort_flag, 0))
           break;
         const Tile ti = tile_at(p, first + j);
-        mbar_arrive_expect_tx(bar(C::kBarKFull + st), C::kTileBytes);
+        mbar_arrive_expect_tx(bar(C::kBarKFull + st), 2 * C::kTileBytes);
 #pragma unroll
         for (int bx = 0; bx < C::kBoxes; ++bx)
           tma_load_4d(sK + st * C::kTileBytes + bx * C::kBoxBytes, &p.k_map[ti.src],
                       bar(C::kBarKFull + st), bx * 64, ti.row, h, b);
-        mbar_arrive_expect_tx(bar(C::kBarVFull + st), C::kTileBytes);
 #pragma unroll
         for (int bx = 0; bx < C::kBoxes; ++bx)
           tma_load_4d(sV + st * C::kTileBytes + bx * C::kBoxBytes, &p.v_map[ti.src],
-                      bar(C::kBarVFull + st), bx * 64, ti.row, h, b);
+                      bar(C::kBarKFull + st), bx * 64, ti.row, h, b);
       }
       if (*abort_flag) {
         // let every copy this thread issued land before the CTA exits
@@ -288,7 +285,6 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
           const int st = jj % C::kStages;
           const uint32_t ph = (uint32_t)(jj / C::kStages) & 1u;
           wait_drain(bar(C::kBarKFull + st), ph);
-          wait_drain(bar(C::kBarVFull + st), ph);
         }
       }
     }
@@ -310,7 +306,15 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
       const uint32_t q_lo = (uint32_t)dq, k_lo = (uint32_t)dk, v_lo = (uint32_t)dv;
       const uint32_t kq_hi = (uint32_t)(dq >> 32), v_hi = (uint32_t)(dv >> 32);
       constexpr uint32_t kTileStep = C::kTileBytes >> 4;
-      auto issue_s = [&](int t, int j) {
+      // The issuing thread blocks on each MMA until the tensor pipe accepts
+      // it, so a barrier check between MMA groups leaves the pipe idle for
+      // its latency.  Barriers needed next are therefore probed without
+      // blocking in the middle of the preceding MMA group (the probe's latency
+      // hides behind the MMA issue stall); a later wait is skipped when its
+      // probe already saw the phase complete.  A probe can never observe a
+      // stale phase: each barrier's next phase depends on work this thread
+      // has not issued yet.
+      auto issue_s = [&](int t, int j, uint32_t pbar, uint32_t ppar, bool& pout) {
         const uint32_t st = (uint32_t)(j % C::kStages);
         const uint32_t d = tmem + C::kTmemS + t * 128;
         const uint32_t a0 = q_lo + (uint32_t)t * kTileStep;
@@ -319,51 +323,76 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
           mma_ss(d, make_desc(a0 + koff, kq_hi), make_desc(b0 + koff, kq_hi), idesc_qk, kk > 0 ? 1u : 0u);
+          if (kk == D / 32 && pbar != 0) pout = mbar_test_wait(pbar, ppar);
         }
       };
-      // O_t += P_t V in two halves of the key tile: the first half of P is
-      // published before the softmax computes the second one.
-      auto issue_pv = [&](int t, int j) -> bool {
+      // one half (64 keys) of O_t += P_t V
+      auto issue_pv_half = [&](int t, int j, int half, uint32_t pbar, uint32_t ppar, bool& pout) {
         const uint32_t st = (uint32_t)(j % C::kStages);
         const uint32_t d = tmem + C::kTmemO + t * D;
         const uint32_t b0 = v_lo + st * kTileStep;
         const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          if (!wait_bounded(bar(C::kBarPFull + 2 * t + half), (uint32_t)j & 1u, abort_flag, 2 + t)) return false;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = half * 4; kk < half * 4 + 4; ++kk) {
-            const uint32_t a_t = tmem + C::kTmemS + t * 128 + kk * 8;
-            mma_ts(d, a_t, make_desc(b0 + ((kk * 16 * 128) >> 4), v_hi), idesc_pv, kk > 0 ? 1u : acc0);
-          }
+        for (int kk = half * 4; kk < half * 4 + 4; ++kk) {
+          const uint32_t a_t = tmem + C::kTmemS + t * 128 + kk * 8;
+          mma_ts(d, a_t, make_desc(b0 + ((kk * 16 * 128) >> 4), v_hi), idesc_pv, kk > 0 ? 1u : acc0);
+          if (kk == half * 4 + 1 && pbar != 0) pout = mbar_test_wait(pbar, ppar);
         }
+      };
+      auto wait_probed = [&](uint32_t b, uint32_t par, bool probed, unsigned site) -> bool {
+        if (probed) return true;
+        return wait_bounded(b, par, abort_flag, site);
+      };
+      auto kbar = [&](int j) { return bar(C::kBarKFull + j % C::kStages); };
+      auto kpar = [&](int j) { return (uint32_t)(j / C::kStages) & 1u; };
+      auto pbar = [&](int t, int half) { return bar(C::kBarPFull + 2 * t + half); };
+      // PV_t(j): both halves, with the probes for what follows
+      // (V of tile j landed with K of tile j: one barrier covers both)
+      auto issue_pv = [&](int t, int j, bool pr_h0, uint32_t nbar, uint32_t npar, bool& nout) -> bool {
+        if (!wait_probed(pbar(t, 0), (uint32_t)j & 1u, pr_h0, 2 + t)) return false;
+        tc_fence_after();
+        bool pr_h1 = false;
+        issue_pv_half(t, j, 0, pbar(t, 1), (uint32_t)j & 1u, pr_h1);
+        if (!wait_probed(pbar(t, 1), (uint32_t)j & 1u, pr_h1, 2 + t)) return false;
+        tc_fence_after();
+        issue_pv_half(t, j, 1, nbar, npar, nout);
         return true;
       };
-      auto wait_v = [&](int j) -> bool {
-        return wait_bounded(bar(C::kBarVFull + j % C::kStages), (uint32_t)(j / C::kStages) & 1u, abort_flag, 4);
-      };
+      bool pr_p0 = false;  // probe for PV_0 of the previous tile
+      // A stage is released by a commit right after the last PV that reads
+      // it (before the next S is issued), so the release does not also wait
+      // for that S.
       for (int j = 0; ok && j < n_tiles; ++j) {
-        const int st = j % C::kStages;
-        if (j > 0 && !(ok = wait_v(j - 1) && issue_pv(0, j - 1))) break;
-        if (!(ok = wait_bounded(bar(C::kBarKFull + st), (uint32_t)(j / C::kStages) & 1u, abort_flag, 5)))
-          break;
+        bool pr_k = false;
+        if (j > 0 && !(ok = issue_pv(0, j - 1, pr_p0, kbar(j), kpar(j), pr_k))) break;
+        if (QT == 1 && j > 0) mma_commit(bar(C::kBarKVEmpty + (j - 1) % C::kStages));
+        if (!(ok = wait_probed(kbar(j), kpar(j), pr_k, 5))) break;
         tc_fence_after();
-        issue_s(0, j);
-        mma_commit(bar(C::kBarSFull + 0));
         if (QT == 2) {
-          if (j > 0 && !(ok = issue_pv(1, j - 1))) break;
-          issue_s(1, j);
+          bool pr_p1 = false;
+          issue_s(0, j, j > 0 ? pbar(1, 0) : 0u, (uint32_t)(j - 1) & 1u, pr_p1);
+          mma_commit(bar(C::kBarSFull + 0));
+          bool unused = false;
+          if (j > 0) {
+            if (!(ok = issue_pv(1, j - 1, pr_p1, 0u, 0u, unused))) break;
+            mma_commit(bar(C::kBarKVEmpty + (j - 1) % C::kStages));
+          }
+          issue_s(1, j, pbar(0, 0), (uint32_t)j & 1u, pr_p0);
           mma_commit(bar(C::kBarSFull + 1));
+        } else {
+          bool unused = false;
+          issue_s(0, j, 0u, 0u, unused);
+          mma_commit(bar(C::kBarSFull + 0));
+          pr_p0 = false;
         }
-        if (j > 0) mma_commit(bar(C::kBarKVEmpty + (j - 1) % C::kStages));
       }
       if (ok) {
         if (n_tiles > 0) {
-          ok = wait_v(n_tiles - 1) && issue_pv(0, n_tiles - 1);
+          bool unused = false;
+          ok = issue_pv(0, n_tiles - 1, pr_p0, 0u, 0u, unused);
           if (ok) mma_commit(bar(C::kBarOFinal + 0));
           if (ok && QT == 2) {
-            ok = issue_pv(1, n_tiles - 1);
+            ok = issue_pv(1, n_tiles - 1, false, 0u, 0u, unused);
             if (ok) mma_commit(bar(C::kBarOFinal + 1));
           }
           if (ok) mma_commit(bar(C::kBarKVEmpty + (n_tiles - 1) % C::kStages));
