@@ -191,7 +191,12 @@ size_t sab_chunk_attention_workspace(const sab_ring* ring, int num_splits);
  *   LSE    device, [B, H, Lc] fp32, natural log of sum exp(s) (output; may be NULL).
  *   workspace/ws_bytes  device scratch, >= sab_chunk_attention_workspace.
  * Every chunk in max(0, c-W) .. c-1 (and c itself when K_cur is NULL) must be
- * held by the ring: OUT_OF_RANGE otherwise.  Device-side pipeline waits are
+ * held by the ring: OUT_OF_RANGE otherwise.  With an FP8 ring the kernel
+ * expands the E4M3 codes times their per-(batch, head, chunk) scale to bf16
+ * on chip (exact) and applies the scales in fp32 (the K scale to the scores,
+ * the V scale to the probabilities); this path needs head_dim 128,
+ * chunk_tokens >= 128 and K_cur == V_cur == NULL (append the current chunk
+ * first): UNSUPPORTED otherwise.  Device-side pipeline waits are
  * bounded; a wait that gives up is reported by sab_get_last_device_error.
  */
 sab_status sab_chunk_attention(const sab_ring* ring, int layer, long long chunk, const void* Q,

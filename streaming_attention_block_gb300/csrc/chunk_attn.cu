@@ -53,9 +53,10 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows by > 2^8
 
-template <int D_, int QT_>
+template <int D_, int QT_, bool FP8_>
 struct Cfg {
   static constexpr int D = D_, QT = QT_;
+  static constexpr bool FP8 = FP8_;
   static constexpr int kBoxes = D / 64;                  // 64-column (128-byte) boxes per row
   static constexpr uint32_t kBoxBytes = 128u * 128u;     // 128 rows x 128 bytes
   static constexpr uint32_t kTileBytes = kBoxBytes * kBoxes;
@@ -73,7 +74,9 @@ struct Cfg {
   static constexpr int kBarPFull = kBarSFull + 2;          // [2 tiles][2 key halves]
   static constexpr int kBarOFinal = kBarPFull + 4;         // [2]
   static constexpr int kBarDrain = kBarOFinal + 2;
-  static constexpr int kNumBars = kBarDrain + 1;
+  static constexpr int kBarRawFull = kBarDrain + 1;          // [kStages] FP8 codes landed
+  static constexpr int kNumBars = kBarRawFull + kStages;
+  static constexpr int kConvThreads = 64;                    // warps 2-3 expand E4M3 tiles
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
   static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;  // + alignment slack
   static constexpr int kThreads = 128 + 128 * QT;
@@ -184,10 +187,11 @@ __device__ __forceinline__ void kv_range(const AttnParams& p, int q0, int qrows,
   count = (int)(e - a);
 }
 
-template <int D, int QT>
-__global__ void __launch_bounds__(Cfg<D, QT>::kThreads, 1)
+template <int D, int QT, bool FP8>
+__global__ void __launch_bounds__(Cfg<D, QT, FP8>::kThreads, 1)
 chunk_attn_kernel(const __grid_constant__ AttnParams p) {
-  using C = Cfg<D, QT>;
+  using C = Cfg<D, QT, FP8>;
+  static_assert(!FP8 || D == 128, "the FP8 cache path expands 128-byte code rows in place");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
   const uint32_t base_u32 = (raw_u32 + 1023u) & ~1023u;
@@ -216,7 +220,8 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
   if (threadIdx.x == 0) {
     mbar_init(bar(C::kBarQ), 1);
     for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(bar(C::kBarKFull + s), 1);
+      mbar_init(bar(C::kBarKFull + s), FP8 ? C::kConvThreads : 1);
+      mbar_init(bar(C::kBarRawFull + s), 1);
       mbar_init(bar(C::kBarKVEmpty + s), 1);
     }
     for (int t = 0; t < 2; ++t) {
@@ -268,15 +273,25 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
             !wait_bounded(bar(C::kBarKVEmpty + st), (round - 1u) & 1u, abort_flag, 0))
           break;
         const Tile ti = tile_at(p, first + j);
-        mbar_arrive_expect_tx(bar(C::kBarKFull + st), 2 * C::kTileBytes);
+        if (FP8) {
+          // E4M3 code rows (128 bytes each) land in the upper half of the bf16
+          // stage buffers; the converter warps expand them in place
+          mbar_arrive_expect_tx(bar(C::kBarRawFull + st), 2 * 128 * D);
+          tma_load_4d(sK + st * C::kTileBytes + C::kBoxBytes, &p.k_map[0], bar(C::kBarRawFull + st), 0, ti.row,
+                      h, b);
+          tma_load_4d(sV + st * C::kTileBytes + C::kBoxBytes, &p.v_map[0], bar(C::kBarRawFull + st), 0, ti.row,
+                      h, b);
+        } else {
+          mbar_arrive_expect_tx(bar(C::kBarKFull + st), 2 * C::kTileBytes);
 #pragma unroll
-        for (int bx = 0; bx < C::kBoxes; ++bx)
-          tma_load_4d(sK + st * C::kTileBytes + bx * C::kBoxBytes, &p.k_map[ti.src],
-                      bar(C::kBarKFull + st), bx * 64, ti.row, h, b);
+          for (int bx = 0; bx < C::kBoxes; ++bx)
+            tma_load_4d(sK + st * C::kTileBytes + bx * C::kBoxBytes, &p.k_map[ti.src],
+                        bar(C::kBarKFull + st), bx * 64, ti.row, h, b);
 #pragma unroll
-        for (int bx = 0; bx < C::kBoxes; ++bx)
-          tma_load_4d(sV + st * C::kTileBytes + bx * C::kBoxBytes, &p.v_map[ti.src],
-                      bar(C::kBarKFull + st), bx * 64, ti.row, h, b);
+          for (int bx = 0; bx < C::kBoxes; ++bx)
+            tma_load_4d(sV + st * C::kTileBytes + bx * C::kBoxBytes, &p.v_map[ti.src],
+                        bar(C::kBarKFull + st), bx * 64, ti.row, h, b);
+        }
       }
       if (*abort_flag) {
         // let every copy this thread issued land before the CTA exits
@@ -284,11 +299,58 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
         for (int jj = max(0, j - C::kStages); jj < j; ++jj) {
           const int st = jj % C::kStages;
           const uint32_t ph = (uint32_t)(jj / C::kStages) & 1u;
-          wait_drain(bar(C::kBarKFull + st), ph);
+          wait_drain(bar((FP8 ? C::kBarRawFull : C::kBarKFull) + st), ph);
         }
       }
     }
     __syncwarp();
+  } else if (FP8 && (warp == 2 || warp == 3)) {
+    // ------------------------------------------------ E4M3 -> bf16 expansion
+    // Each thread owns whole rows: it reads a row's 128 codes (which sit
+    // exactly where the row's upper bf16 half goes), then writes the 128
+    // code values as bf16 (exact) in the 128-byte-swizzled layout the MMA
+    // descriptors expect.  No other thread touches those bytes, so the
+    // in-place expansion needs no barrier.  The per-(batch, head, chunk)
+    // scales are applied in fp32 by the softmax: the K scale on the scores,
+    // the V scale on P.
+    const int ct = threadIdx.x - 64;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int st = j % C::kStages;
+      if (!wait_bounded(bar(C::kBarRawFull + st), (uint32_t)(j / C::kStages) & 1u, abort_flag, 12)) break;
+      const int row0 = tile_at(p, first + j).row;
+#pragma unroll 1
+      for (int job = ct; job < 2 * kTileN; job += C::kConvThreads) {
+        const int r = job & (kTileN - 1);
+        const bool isv = job >= kTileN;
+        uint8_t* tile = base + (isv ? C::kVOff : C::kKOff) + st * C::kTileBytes;
+        const uint4* src = reinterpret_cast<const uint4*>(tile + C::kBoxBytes + r * 128);
+        uint4 raw[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) raw[i] = src[i];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+          uint32_t out[8];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            float a0, a1, a2, a3;
+            e4m3x2_to_f32x2((uint16_t)(w[q] & 0xFFFFu), a0, a1);
+            e4m3x2_to_f32x2((uint16_t)(w[q] >> 16), a2, a3);
+            out[2 * q] = pack_bf16(a0, a1);  // exact: every E4M3 value is a bf16 value
+            out[2 * q + 1] = pack_bf16(a2, a3);
+          }
+          // codes 16i .. 16i+15 -> 16-byte chunks 2i, 2i+1 of the bf16 row
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int k = 2 * i + hh;
+            *reinterpret_cast<uint4*>(tile + (k >> 3) * C::kBoxBytes + r * 128 + (((k & 7) ^ (r & 7)) << 4)) =
+                make_uint4(out[4 * hh], out[4 * hh + 1], out[4 * hh + 2], out[4 * hh + 3]);
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(bar(C::kBarKFull + st));
+    }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
@@ -425,12 +487,14 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
     }
     const float sl = p.scale_log2;
     // streaming: the key runs in registers (the last tile of a run is partial)
-    int seg_tile0[kMaxSegments], seg_rows[kMaxSegments];
+    int seg_tile0[kMaxSegments], seg_rows[kMaxSegments], seg_row0[kMaxSegments];
 #pragma unroll
     for (int i = 0; i < kMaxSegments; ++i) {
       seg_tile0[i] = (i < p.nseg) ? p.seg[i].tile0 : 0x7fffffff;
       seg_rows[i] = p.seg[i].nrows;
+      seg_row0[i] = p.seg[i].row0;
     }
+    const long long srow = (long long)bh * p.scale_stride;  // FP8 scale row of this (b, h)
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     for (int j = 0; j < n_tiles; ++j) {
@@ -444,24 +508,56 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
       tmem_ld32(tS + 64, s2);
       tmem_ld32(tS + 96, s3);
       int lo, hi;
+      int tile_row0 = 0;
       const int g = first + j;
       if (p.mode == kModeStreaming) {
         int sg = 0;
 #pragma unroll
         for (int i = 1; i < kMaxSegments; ++i) sg = (g >= seg_tile0[i]) ? i : sg;
-        int t0 = seg_tile0[0], nr = seg_rows[0];
+        int t0 = seg_tile0[0], nr = seg_rows[0], r0 = seg_row0[0];
 #pragma unroll
         for (int i = 1; i < kMaxSegments; ++i) {
           t0 = (sg == i) ? seg_tile0[i] : t0;
           nr = (sg == i) ? seg_rows[i] : nr;
+          r0 = (sg == i) ? seg_row0[i] : r0;
         }
         lo = 0;
         hi = nr - (g - t0) * kTileN;
+        tile_row0 = r0 + (g - t0) * kTileN;
       } else {
         lo = klo - g * kTileN;
         hi = khi - g * kTileN;
       }
       tmem_wait_ld();
+      // FP8 cache: the keys of this tile belong to at most two chunks
+      // (chunk_tokens >= 128): columns [0, bnd) to the first, the rest to the
+      // next.  Score coefficient c = softmax_scale*log2(e)*k_scale; V scale
+      // folded into P (exponent offset d = log2 v_scale when uniform).
+      float c0 = sl, c1 = sl, d0 = 0.f, v0 = 1.f, v1 = 1.f, iv0 = 1.f;
+      int bnd = kTileN;
+      if constexpr (FP8) {
+        const int si0 = min(tile_row0 / p.chunk_tokens, p.scale_stride - 1);
+        const int si1 = min(si0 + 1, p.scale_stride - 1);
+        bnd = (si0 + 1) * p.chunk_tokens - tile_row0;
+        c0 = sl * __ldg(p.k_scale + srow + si0);
+        c1 = sl * __ldg(p.k_scale + srow + si1);
+        v0 = __ldg(p.v_scale + srow + si0);
+        v1 = __ldg(p.v_scale + srow + si1);
+        d0 = __log2f(v0);
+        iv0 = 1.f / v0;
+      }
+      const bool straddle = FP8 && bnd < kTileN;
+      if (straddle) {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          s0[c] = __float_as_uint(__uint_as_float(s0[c]) * (c < bnd ? c0 : c1));
+          s1[c] = __float_as_uint(__uint_as_float(s1[c]) * (c + 32 < bnd ? c0 : c1));
+          s2[c] = __float_as_uint(__uint_as_float(s2[c]) * (c + 64 < bnd ? c0 : c1));
+          s3[c] = __float_as_uint(__uint_as_float(s3[c]) * (c + 96 < bnd ? c0 : c1));
+        }
+      }
+      // mask after any per-column scaling (an unwritten FP8 slot has scale 0,
+      // and -inf * 0 would be NaN)
       if (!(lo <= 0 && hi >= kTileN)) {
         const uint32_t ninf = 0xff800000u;
 #pragma unroll
@@ -486,7 +582,7 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
         pm[k] = fmaxf(m, __uint_as_float(s3[k + 24]));
       }
       const float mx = fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7]));
-      const float m_new = fmaxf(m_run, mx * sl);
+      const float m_new = fmaxf(m_run, straddle ? mx : mx * c0);
       const bool need = m_new > m_run + kRescaleThreshold;
       float alpha = 1.f;
       if (need) {
@@ -512,38 +608,42 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
       // P (bf16 pairs) overwrites the first 64 columns of S: column k holds
       // keys 2k (low half) and 2k+1 (high half).  Keys 0..63 are published
       // first so the PV MMA on them overlaps the exponentials of keys 64..127.
-      {
+      // e = 2^(x) with x = s*c0 + d0 - m (bf16 cache: c0 = scale*log2(e),
+      // d0 = 0); a straddling FP8 tile has its scores pre-scaled per column
+      // and multiplies P by the column's V scale instead.
+      const float xa = straddle ? 1.f : c0;
+      const float xb = d0 - mb;
+      const float xs = straddle ? -mb : xb;
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
         uint32_t pk[32];
+        const uint32_t* sa = hf ? s2 : s0;
+        const uint32_t* sb = hf ? s3 : s1;
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-          const float a0 = ex2(fmaf(__uint_as_float(s0[2 * c]), sl, -mb));
-          const float a1 = ex2(fmaf(__uint_as_float(s0[2 * c + 1]), sl, -mb));
-          const float b0 = ex2(fmaf(__uint_as_float(s1[2 * c]), sl, -mb));
-          const float b1 = ex2(fmaf(__uint_as_float(s1[2 * c + 1]), sl, -mb));
+          float a0 = ex2(fmaf(__uint_as_float(sa[2 * c]), xa, xs));
+          float a1 = ex2(fmaf(__uint_as_float(sa[2 * c + 1]), xa, xs));
+          float b0 = ex2(fmaf(__uint_as_float(sb[2 * c]), xa, xs));
+          float b1 = ex2(fmaf(__uint_as_float(sb[2 * c + 1]), xa, xs));
           ps[c & 3] += (a0 + a1) + (b0 + b1);
+          if (straddle) {
+            const int k = hf * 64 + 2 * c;  // key index of a0
+            a0 *= (k < bnd ? v0 : v1);
+            a1 *= (k + 1 < bnd ? v0 : v1);
+            b0 *= (k + 32 < bnd ? v0 : v1);
+            b1 *= (k + 33 < bnd ? v0 : v1);
+          }
           pk[c] = pack_bf16(a0, a1);
           pk[16 + c] = pack_bf16(b0, b1);
         }
-        tmem_st32(tS + 0, pk);
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar(C::kBarPFull + 2 * t));
-      {
-        uint32_t pk[32];
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const float a0 = ex2(fmaf(__uint_as_float(s2[2 * c]), sl, -mb));
-          const float a1 = ex2(fmaf(__uint_as_float(s2[2 * c + 1]), sl, -mb));
-          const float b0 = ex2(fmaf(__uint_as_float(s3[2 * c]), sl, -mb));
-          const float b1 = ex2(fmaf(__uint_as_float(s3[2 * c + 1]), sl, -mb));
-          ps[c & 3] += (a0 + a1) + (b0 + b1);
-          pk[c] = pack_bf16(a0, a1);
-          pk[16 + c] = pack_bf16(b0, b1);
+        tmem_st32(tS + hf * 32, pk);
+        if (hf == 0) {
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(bar(C::kBarPFull + 2 * t));
         }
-        tmem_st32(tS + 32, pk);
       }
-      l_run += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+      l_run += ((ps[0] + ps[1]) + (ps[2] + ps[3])) * (straddle ? 1.f : iv0);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(C::kBarPFull + 2 * t + 1));
@@ -812,19 +912,19 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
   }
 }
 
-template <int D, int QT>
+template <int D, int QT, bool FP8>
 cudaError_t launch_impl(const AttnParams& p, cudaStream_t s) {
-  using C = Cfg<D, QT>;
+  using C = Cfg<D, QT, FP8>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(chunk_attn_kernel<D, QT>,
+    cudaError_t e = cudaFuncSetAttribute(chunk_attn_kernel<D, QT, FP8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   dim3 grid(p.n_qgroups, p.B * p.H, p.splits);
   if (!p.cluster_merge) {
-    chunk_attn_kernel<D, QT><<<grid, C::kThreads, C::kSmemBytes, s>>>(p);
+    chunk_attn_kernel<D, QT, FP8><<<grid, C::kThreads, C::kSmemBytes, s>>>(p);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
@@ -839,14 +939,18 @@ cudaError_t launch_impl(const AttnParams& p, cudaStream_t s) {
   attr[0].val.clusterDim.z = (unsigned)p.splits;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, chunk_attn_kernel<D, QT>, p);
+  return cudaLaunchKernelEx(&cfg, chunk_attn_kernel<D, QT, FP8>, p);
 }
 
 }  // namespace
 
 cudaError_t launch_chunk_attention(const AttnParams& p, int q_tiles_per_cta, cudaStream_t s) {
-  if (p.D == 128) return q_tiles_per_cta == 2 ? launch_impl<128, 2>(p, s) : launch_impl<128, 1>(p, s);
-  if (p.D == 64) return q_tiles_per_cta == 2 ? launch_impl<64, 2>(p, s) : launch_impl<64, 1>(p, s);
+  if (p.fp8) {
+    if (p.D != 128) return cudaErrorInvalidValue;
+    return q_tiles_per_cta == 2 ? launch_impl<128, 2, true>(p, s) : launch_impl<128, 1, true>(p, s);
+  }
+  if (p.D == 128) return q_tiles_per_cta == 2 ? launch_impl<128, 2, false>(p, s) : launch_impl<128, 1, false>(p, s);
+  if (p.D == 64) return q_tiles_per_cta == 2 ? launch_impl<64, 2, false>(p, s) : launch_impl<64, 1, false>(p, s);
   return cudaErrorInvalidValue;
 }
 

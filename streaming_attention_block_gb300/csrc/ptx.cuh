@@ -183,6 +183,14 @@ __device__ __forceinline__ float ex2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// two E4M3 codes (low byte = first) -> two fp32 values (exact)
+__device__ __forceinline__ void e4m3x2_to_f32x2(uint16_t codes, float& lo, float& hi) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(codes));
+  uint16_t a = (uint16_t)(h2 & 0xFFFFu), b = (uint16_t)(h2 >> 16);
+  asm("cvt.f32.f16 %0, %1;" : "=f"(lo) : "h"(a));
+  asm("cvt.f32.f16 %0, %1;" : "=f"(hi) : "h"(b));
+}
 // three-input maximum
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float r;

@@ -54,6 +54,20 @@ bool encode_map(CUtensorMap* m, const void* ptr, int D, long long rows, int H, i
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Head-major [B, H, rows, D] E4M3 codes: plain (unswizzled) 128-row boxes of
+// whole D-byte rows, expanded to bf16 inside the attention kernel.
+bool encode_head_major_u8(CUtensorMap* m, const void* ptr, int B, int H, long long rows, int D) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)rows, (cuuint64_t)H, (cuuint64_t)B};
+  const cuuint64_t strides[3] = {(cuuint64_t)D, (cuuint64_t)rows * D, (cuuint64_t)H * rows * D};
+  const cuuint32_t box[4] = {(cuuint32_t)D, (cuuint32_t)kTileN, 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Token-major [B, L, H, D] bf16.
 bool encode_token_major(CUtensorMap* m, const void* ptr, int B, int L, int H, int D) {
   const size_t e = 2;
@@ -195,15 +209,18 @@ sab_status sab_kv_ring_create(const sab_ring_desc* desc, void* dev_mem, size_t b
   r->newest.assign(desc->num_layers, -1);
   r->held.assign(desc->num_layers, 0);
   r->sink_set.assign(desc->num_layers, 0);
-  if (desc->kv_dtype == SAB_KV_BF16) {
-    r->kmap.resize(desc->num_layers);
-    r->vmap.resize(desc->num_layers);
-    for (int l = 0; l < desc->num_layers; ++l) {
-      if (!encode_head_major(&r->kmap[l], r->k(l), desc->batch, desc->heads, r->g.rows, desc->head_dim) ||
-          !encode_head_major(&r->vmap[l], r->v(l), desc->batch, desc->heads, r->g.rows, desc->head_dim)) {
-        delete r;
-        return SAB_ERR_CUDA;
-      }
+  r->kmap.resize(desc->num_layers);
+  r->vmap.resize(desc->num_layers);
+  const bool fp8 = desc->kv_dtype == SAB_KV_FP8_E4M3;
+  for (int l = 0; l < desc->num_layers; ++l) {
+    const int B = desc->batch, H = desc->heads, D = desc->head_dim;
+    const bool okm = fp8 ? (encode_head_major_u8(&r->kmap[l], r->k(l), B, H, r->g.rows, D) &&
+                            encode_head_major_u8(&r->vmap[l], r->v(l), B, H, r->g.rows, D))
+                         : (encode_head_major(&r->kmap[l], r->k(l), B, H, r->g.rows, D) &&
+                            encode_head_major(&r->vmap[l], r->v(l), B, H, r->g.rows, D));
+    if (!okm) {
+      delete r;
+      return SAB_ERR_CUDA;
     }
   }
   if (cudaMemsetAsync(dev_mem, 0, need, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
@@ -384,8 +401,12 @@ sab_status sab_chunk_attention(const sab_ring* ring, int layer, long long chunk,
   const sab_ring_desc& d = ring->d;
   if (use_sink && !d.has_sink) return SAB_ERR_INVALID_ARG;
   if (use_sink && !ring->sink_set[layer]) return SAB_ERR_OUT_OF_RANGE;
-  if (d.kv_dtype != SAB_KV_BF16) return SAB_ERR_UNSUPPORTED;
   const bool kcur = K_cur != nullptr;
+  const bool fp8 = d.kv_dtype == SAB_KV_FP8_E4M3;
+  // The FP8 cache path expands 128-byte code rows in place (D = 128), reads
+  // every key from the ring (the current chunk is appended first) and needs
+  // chunks of at least 128 tokens (a key tile spans at most two chunks).
+  if (fp8 && (kcur || d.head_dim != 128 || d.chunk_tokens < kTileN)) return SAB_ERR_UNSUPPORTED;
   const int R = d.ring_slots, Lc = d.chunk_tokens;
 
   // ring chunks needed: [need_lo, need_hi]
@@ -418,6 +439,11 @@ sab_status sab_chunk_attention(const sab_ring* ring, int layer, long long chunk,
   AttnParams p;
   memset(&p, 0, sizeof(p));
   p.mode = kModeStreaming;
+  p.fp8 = fp8 ? 1 : 0;
+  p.k_scale = ring->ks(layer);
+  p.v_scale = ring->vs(layer);
+  p.scale_stride = d.has_sink + d.ring_slots;
+  p.chunk_tokens = d.chunk_tokens;
   p.B = d.batch;
   p.H = d.heads;
   p.D = d.head_dim;

@@ -30,6 +30,10 @@ struct AttnParams {
   CUtensorMap v_map[2];
   CUtensorMap o_map;      // output, dims (D, Lq, H, B), box (64, 128, 1, 1), SW128
   int mode;
+  int fp8;                // 1: the ring holds E4M3 codes (k_map[0]/v_map[0] are uint8 maps)
+  const float* k_scale;   // FP8: [B*H][scale_stride] fp32 scales, index = ring row / chunk_tokens
+  const float* v_scale;
+  int scale_stride;
   int B, H, D;
   int Lq;                 // query rows per (b, h)
   int n_qtiles;           // ceil(Lq / 128)

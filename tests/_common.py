@@ -36,8 +36,13 @@ def bhld(t_blhd) -> np.ndarray:
 
 
 def compare(O_gpu: torch.Tensor, LSE_gpu: torch.Tensor, O_ref: np.ndarray, L_ref: np.ndarray, rows=None,
-            max_tol=BF16_MAX, mean_tol=BF16_MEAN, lse_tol=BF16_LSE, what=""):
-    """O_gpu token-major [B, L, H, D]; O_ref head-major [B, H, nrows, D] over `rows`."""
+            max_tol=BF16_MAX, mean_tol=BF16_MEAN, lse_tol=BF16_LSE, what="", rel_ulp=0.0):
+    """O_gpu token-major [B, L, H, D]; O_ref head-major [B, H, nrows, D] over `rows`.
+
+    ``rel_ulp`` widens the per-element bound to max_tol + rel_ulp * |O_ref|:
+    a bf16 output of magnitude >= 16 has an ulp of 0.125, so no absolute
+    bound below that can hold there (used for the outlier-heavy FP8 inputs).
+    """
     o = bhld(O_gpu)
     lse = f64(LSE_gpu)
     if rows is not None:
@@ -47,7 +52,7 @@ def compare(O_gpu: torch.Tensor, LSE_gpu: torch.Tensor, O_ref: np.ndarray, L_ref
     d = np.abs(o - O_ref)
     dl = np.abs(lse - L_ref)
     msg = f"{what}: max|dO|={d.max():.3e} mean|dO|={d.mean():.3e} max|dLSE|={dl.max():.3e}"
-    assert d.max() <= max_tol, msg
+    assert np.all(d <= max_tol + rel_ulp * np.abs(O_ref)), msg
     if mean_tol is not None:
         assert d.mean() <= mean_tol, msg
     assert dl.max() <= lse_tol, msg
