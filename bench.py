@@ -301,6 +301,83 @@ def run_attn_only(args):
     assert sab.get_last_device_error(stream) == 0
 
 
+def run_sweep(args):
+    """One JSON line per workload: device time per attention call (median
+    of CUDA-event-timed back-to-back calls after warm-up), algorithmic
+    TFLOP/s and the fraction of the bf16 peak.  Not the default bench line."""
+    import torch
+
+    import streaming_attention_block_gb300 as sab
+    from streaming_attention_block_gb300 import synth
+
+    peaks, src = _peaks()
+    stream = torch.cuda.current_stream()
+
+    def timed(fn, n):
+        for _ in range(3):
+            fn()
+        ev = []
+        for _ in range(n):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            ev.append((a, b))
+        torch.cuda.synchronize()
+        return statistics.median(x.elapsed_time(y) for x, y in ev) * 1e3
+
+    def report(name, us, flops, splits, extra=None):
+        line = {"sweep": name, "us_per_call": round(us, 2), "tflops": round(flops / (us * 1e-6) / 1e12, 1),
+                "frac_of_bf16_peak": round(flops / (us * 1e-6) / 1e12 / peaks["bf16_tflops"], 4),
+                "peak_source": f"bf16 dense burst, {src}", "splits": splits}
+        if extra:
+            line.update(extra)
+        print(json.dumps(line), flush=True)
+
+    for name in ("tiny", "wan13b", "long_sink", "fp8_kv"):
+        w = synth.workload(name)
+        g = synth.generator(w.seed, device="cuda")
+        ring = sab.KVRing(1, w.B, w.H, w.D, w.Lc, w.R, has_sink=w.sink,
+                          kv_dtype=sab.KV_FP8_E4M3 if w.kv_fp8 else sab.KV_BF16)
+        if w.sink:
+            sk, sv = synth.sink_kv(w, g, "cuda")
+            ring.set_sink(0, sk, sv)
+        steady = w.R if not w.kcur_separate else w.W  # first chunk with a full window
+        q = k = v = None
+        for c in range(steady + 1):
+            q, k, v = synth.chunk_qkv(w, g, "cuda")
+            if not w.kcur_separate or c < steady:
+                ring.append(0, c, k, v)
+        nkeys = w.Lc * (w.W + 1) + (w.Lc if w.sink else 0)
+        flops = 4.0 * w.B * w.H * w.D * w.Lc * nkeys
+        for splits in sorted({0, w.splits}):
+            work = ring.workspace(splits) if splits != 1 else None
+            O = torch.empty_like(q)
+            L = torch.empty((w.B, w.H, w.Lc), dtype=torch.float32, device="cuda")
+            kc, vc = (k, v) if w.kcur_separate else (None, None)
+
+            def call():
+                sab.chunk_attention(ring.handle, 0, steady, q, kc, vc, w.W, w.sink, splits, w.scale, O, L, work,
+                                    stream)
+
+            report(name, timed(call, 50), flops, splits, {"keys": nkeys})
+    w = synth.workload("block_causal")
+    g = synth.generator(w.seed, device="cuda")
+    q, k, v = synth.full_sequence_qkv(w, g, "cuda")
+    Lt = w.seq_chunks * w.Lc
+    O = torch.empty_like(q)
+    L = torch.empty((w.B, w.H, Lt), dtype=torch.float32, device="cuda")
+    pairs = sum(w.Lc * w.Lc * (min(c, w.W) + 1) for c in range(w.seq_chunks))
+    flops = 4.0 * w.B * w.H * w.D * pairs
+
+    def bc():
+        sab.block_causal_attention(q, k, v, w.Lc, w.W, 0, w.scale, O, L, None, stream)
+
+    report("block_causal", timed(bc, 10), flops, 0, {"tokens": Lt})
+    assert sab.get_last_device_error(stream) == 0
+
+
 def cpu_baseline_sample(w, seconds_budget=20.0):
     """Time the oracle on one steady-state attention call (all heads, all rows,
     4608 keys) on the host cores; scale to chunks/s."""
@@ -392,11 +469,14 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--splits", type=int, default=0, help="KV splits per attention call (0: library's choice)")
+    ap.add_argument("--sweep", action="store_true", help="time one attention call of every workload")
     ap.add_argument("--attn-only", type=int, default=0, metavar="N",
                     help="profiling case: N steady-state attention calls on one layer, then exit")
     args = ap.parse_args()
     if args.attn_only:
         return run_attn_only(args)
+    if args.sweep:
+        return run_sweep(args)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
