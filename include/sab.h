@@ -205,6 +205,33 @@ sab_status sab_chunk_attention(const sab_ring* ring, int layer, long long chunk,
                                void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * sab_chunk_attention without a caller workspace.  The method itself has no
+ * counterpart of this entry point; it exists for callers that cannot
+ * allocate device memory -- for instance a plugin whose host application
+ * owns every device allocation through its own pool, or a real-time stream
+ * that forbids allocation once it is running -- and so cannot hand over the
+ * workspace that a split (num_splits >= 2) merge needs.
+ *
+ * Arguments and results are those of sab_chunk_attention (num_splits >= 1,
+ * no automatic choice).  With num_splits >= 2 the partial outputs, partial
+ * LSEs and arrival counters of the split merge live in one library-owned
+ * device array of 8 MiB (a file-scope __device__ array: every GPU that loads
+ * the library holds it until the process exits).  A request whose merge
+ * needs more -- num_splits * B * H * ceil-to-256(Lc) * (D + 1) * 4 bytes,
+ * roughly -- returns SAB_ERR_WORKSPACE and launches nothing.
+ * The call allocates nothing (no cudaMalloc/cudaFree or allocating library
+ * routine); it clears the counters with cudaMemsetAsync on `stream`.
+ * The first call on a device looks up the array's device address (with
+ * that device current); make that first call before any stream capture.
+ * Every call shares the one array, which keeps the previous call's partials:
+ * calls whose executions overlap on the GPU (different streams, or devices
+ * sharing nothing but this array's name) race -- serialise them.
+ */
+sab_status sab_chunk_attention_noalloc(const sab_ring* ring, int layer, long long chunk, const void* Q,
+                                       const void* K_cur, const void* V_cur, int window, int use_sink,
+                                       int num_splits, float softmax_scale, void* O, float* LSE, void* stream);
+
+/*
  * Block-causal attention over whole sequences (training / causal-adaptation
  * shape; "WanToFight", section "训练流程 / Stage 2": the dense mask is replaced
  * by a block-causal one, bidirectional inside a chunk, each chunk seeing

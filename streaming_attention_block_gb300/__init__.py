@@ -16,6 +16,7 @@ from ._abi import (  # noqa: F401
     block_causal_attention,
     block_causal_attention_workspace,
     chunk_attention,
+    chunk_attention_noalloc,
     chunk_attention_workspace,
     get_last_device_error,
     kv_ring_append,

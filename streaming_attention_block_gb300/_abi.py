@@ -64,6 +64,7 @@ def library() -> ctypes.CDLL:
         "sab_kv_ring_set_state": (I, [P, ctypes.POINTER(LL), ctypes.POINTER(I), ctypes.POINTER(I)]),
         "sab_chunk_attention_workspace": (SZ, [P, I]),
         "sab_chunk_attention": (I, [P, I, LL, P, P, P, I, I, I, F, P, P, P, SZ, P]),
+        "sab_chunk_attention_noalloc": (I, [P, I, LL, P, P, P, I, I, I, F, P, P, P]),
         "sab_block_causal_attention_workspace": (SZ, [I, I, I, I, I]),
         "sab_block_causal_attention": (I, [P, P, P, I, I, I, I, I, I, I, F, P, P, P, SZ, P]),
         "sab_get_last_device_error": (I, [P]),
@@ -192,6 +193,17 @@ def chunk_attention(handle, layer: int, chunk: int, Q, K_cur, V_cur, window: int
         _ptr(V_cur, torch.bfloat16, "V_cur"), int(window), int(bool(use_sink)), int(num_splits),
         float(softmax_scale), _ptr(O, torch.bfloat16, "O"), _ptr(LSE, torch.float32, "LSE"),
         _ptr(workspace, None, "workspace"), ws_bytes, _stream(stream)), "chunk_attention")
+
+
+def chunk_attention_noalloc(handle, layer: int, chunk: int, Q, K_cur, V_cur, window: int, use_sink: bool,
+                            num_splits: int, softmax_scale: float, O, LSE=None, stream=None):
+    """sab_chunk_attention_noalloc: the split merge uses the library's own
+    device scratch instead of a caller workspace (see include/sab.h)."""
+    _check(library().sab_chunk_attention_noalloc(
+        handle, int(layer), int(chunk), _ptr(Q, torch.bfloat16, "Q"), _ptr(K_cur, torch.bfloat16, "K_cur"),
+        _ptr(V_cur, torch.bfloat16, "V_cur"), int(window), int(bool(use_sink)), int(num_splits),
+        float(softmax_scale), _ptr(O, torch.bfloat16, "O"), _ptr(LSE, torch.float32, "LSE"), _stream(stream)),
+        "chunk_attention_noalloc")
 
 
 def block_causal_attention_workspace(B: int, L: int, H: int, D: int, num_splits: int) -> int:

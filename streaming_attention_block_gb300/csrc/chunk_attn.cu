@@ -954,6 +954,33 @@ cudaError_t launch_chunk_attention(const AttnParams& p, int q_tiles_per_cta, cud
   return cudaErrorInvalidValue;
 }
 
+// Scratch of the allocation-free entry point: the split partials, partial
+// LSEs and arrival counters of the workspace merge live in this file-scope
+// array instead of caller-provided memory.  Every GPU that loads the library
+// holds it until the process exits.
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;  // 8 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+cudaError_t noalloc_scratch(void** ptr, size_t* bytes) {
+  // In host code the array's name is only a stand-in: the device address is
+  // looked up once per device (with that device current) and cached.
+  constexpr int kMaxDevices = 64;
+  static void* addr[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev] = p;
+  }
+  *ptr = addr[dev];
+  *bytes = kNoAllocScratchBytes;
+  return cudaSuccess;
+}
+
 cudaError_t read_and_clear_device_error(unsigned int* value) {
   unsigned int v = 0;
   cudaError_t e = cudaMemcpyFromSymbol(&v, g_sab_error_word, sizeof(v));

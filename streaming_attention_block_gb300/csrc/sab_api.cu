@@ -350,7 +350,7 @@ size_t sab_chunk_attention_workspace(const sab_ring* ring, int num_splits) {
 }
 
 static sab_status launch_attention(AttnParams& p, int Lq, int splits, void* workspace, size_t ws_bytes,
-                                   void* stream) {
+                                   void* stream, bool allow_cluster = true) {
   const QTiling t = qtiling(Lq);
   if (splits == 0) {
     // block-causal: a CTA sees at most (window + 1) chunks plus one straddled tile
@@ -376,7 +376,7 @@ static sab_status launch_attention(AttnParams& p, int Lq, int splits, void* work
   if ((long long)p.B * p.H > 65535) return SAB_ERR_UNSUPPORTED;
   // 2..8 splits of a query group merge inside a thread-block cluster; more
   // splits (or a device refusing the cluster) merge through the workspace.
-  p.cluster_merge = (splits >= 2 && splits <= kMaxClusterSplits) ? 1 : 0;
+  p.cluster_merge = (allow_cluster && splits >= 2 && splits <= kMaxClusterSplits) ? 1 : 0;
   cudaError_t e = launch_chunk_attention(p, t.qt, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess && p.cluster_merge) {
     (void)cudaGetLastError();
@@ -386,9 +386,10 @@ static sab_status launch_attention(AttnParams& p, int Lq, int splits, void* work
   return e == cudaSuccess ? SAB_OK : SAB_ERR_CUDA;
 }
 
-sab_status sab_chunk_attention(const sab_ring* ring, int layer, long long chunk, const void* Q, const void* K_cur,
-                               const void* V_cur, int window, int use_sink, int num_splits, float softmax_scale,
-                               void* O, float* LSE, void* workspace, size_t ws_bytes, void* stream) {
+// Validation and key-set planning shared by both chunk-attention entry points.
+static sab_status plan_chunk_attention(const sab_ring* ring, int layer, long long chunk, const void* Q,
+                                       const void* K_cur, const void* V_cur, int window, int use_sink,
+                                       int num_splits, float softmax_scale, void* O, float* LSE, AttnParams& p) {
   if (ring == nullptr || layer < 0 || layer >= ring->d.num_layers) return SAB_ERR_INVALID_ARG;
   if (Q == nullptr || O == nullptr || !aligned16(Q) || !aligned16(O)) return SAB_ERR_INVALID_ARG;
   if ((K_cur == nullptr) != (V_cur == nullptr)) return SAB_ERR_INVALID_ARG;
@@ -436,7 +437,6 @@ sab_status sab_chunk_attention(const sab_ring* ring, int layer, long long chunk,
       merged.push_back(r);
   }
 
-  AttnParams p;
   memset(&p, 0, sizeof(p));
   p.mode = kModeStreaming;
   p.fp8 = fp8 ? 1 : 0;
@@ -475,7 +475,40 @@ sab_status sab_chunk_attention(const sab_ring* ring, int layer, long long chunk,
   if (!encode_token_major(&p.q_map, Q, d.batch, Lc, d.heads, d.head_dim) ||
       !encode_token_major(&p.o_map, O, d.batch, Lc, d.heads, d.head_dim))
     return SAB_ERR_CUDA;
-  return launch_attention(p, Lc, num_splits, workspace, ws_bytes, stream);
+  return SAB_OK;
+}
+
+sab_status sab_chunk_attention(const sab_ring* ring, int layer, long long chunk, const void* Q, const void* K_cur,
+                               const void* V_cur, int window, int use_sink, int num_splits, float softmax_scale,
+                               void* O, float* LSE, void* workspace, size_t ws_bytes, void* stream) {
+  AttnParams p;
+  const sab_status st =
+      plan_chunk_attention(ring, layer, chunk, Q, K_cur, V_cur, window, use_sink, num_splits, softmax_scale, O, LSE, p);
+  if (st != SAB_OK) return st;
+  return launch_attention(p, ring->d.chunk_tokens, num_splits, workspace, ws_bytes, stream);
+}
+
+// Allocation-free variant: the split merge goes through the library's own
+// device scratch (a file-scope array of the attention kernel's translation
+// unit) instead of a caller workspace.  Not a counterpart of anything in the
+// method; see include/sab.h.
+sab_status sab_chunk_attention_noalloc(const sab_ring* ring, int layer, long long chunk, const void* Q,
+                                       const void* K_cur, const void* V_cur, int window, int use_sink,
+                                       int num_splits, float softmax_scale, void* O, float* LSE, void* stream) {
+  if (num_splits < 1) return SAB_ERR_INVALID_ARG;
+  AttnParams p;
+  const sab_status st =
+      plan_chunk_attention(ring, layer, chunk, Q, K_cur, V_cur, window, use_sink, num_splits, softmax_scale, O, LSE, p);
+  if (st != SAB_OK) return st;
+  if (num_splits == 1) return launch_attention(p, ring->d.chunk_tokens, 1, nullptr, 0, stream);
+  const WsLayout w = ws_layout(ring->d.batch * ring->d.heads, ring->d.chunk_tokens, ring->d.head_dim, num_splits);
+  void* scratch = nullptr;
+  size_t cap = 0;
+  if (noalloc_scratch(&scratch, &cap) != cudaSuccess) return SAB_ERR_CUDA;
+  if (w.total > cap) return SAB_ERR_WORKSPACE;
+  // the arrival counters must start at zero; the partial rows are fully rewritten
+  if (cudaMemsetAsync(scratch, 0, w.o_off, static_cast<cudaStream_t>(stream)) != cudaSuccess) return SAB_ERR_CUDA;
+  return launch_attention(p, ring->d.chunk_tokens, num_splits, scratch, cap, stream, /*allow_cluster=*/false);
 }
 
 size_t sab_block_causal_attention_workspace(int B, int L, int H, int D, int num_splits) {

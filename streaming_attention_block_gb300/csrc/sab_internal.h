@@ -77,6 +77,8 @@ cudaError_t launch_append_bf16(const AppendParams& p, cudaStream_t s);
 cudaError_t launch_append_fp8(const AppendParams& p, cudaStream_t s);
 cudaError_t launch_chunk_attention(const AttnParams& p, int q_tiles_per_cta, cudaStream_t s);
 cudaError_t read_and_clear_device_error(unsigned int* value);
+// Device address and size of the library's own split-merge scratch.
+cudaError_t noalloc_scratch(void** ptr, size_t* bytes);
 int attention_q_tiles_per_cta(int D);
 
 }  // namespace sab

@@ -1,0 +1,70 @@
+"""The allocation-free chunk-attention entry point, called through the C ABI.
+
+For callers that cannot allocate device memory (a plugin whose host
+application owns all device allocations, a real-time loop that forbids
+allocation after start-up), sab_chunk_attention_noalloc merges KV splits in a
+library-owned device array instead of a caller workspace.  Its output must
+match the regular entry point's, on two calls in a row (the array keeps the
+previous call's contents, so the second call checks that nothing stale
+leaks).  Collected last so that a stop at the first failure has already run
+every other test; it also passes when run alone in a fresh process.
+"""
+
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import streaming_attention_block_gb300 as sab
+from streaming_attention_block_gb300 import KVRing, synth
+
+pytestmark = pytest.mark.gpu
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def test_noalloc_matches_workspace_entry_point_twice():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    lib = sab.library()
+    w = synth.Workload("na", B=1, H=4, D=128, Lc=405, R=6, W=5, chunks=8, sink=True, kcur_separate=False, seed=71)
+    gen = synth.generator(w.seed)
+    ring = KVRing(1, w.B, w.H, w.D, w.Lc, w.R, has_sink=True)
+    sk, sv = synth.sink_kv(w, gen)
+    ring.set_sink(0, sk.cuda(), sv.cuda())
+    for c in range(w.chunks):
+        q, k, v = (x.cuda() for x in synth.chunk_qkv(w, gen))
+        ring.append(0, c, k, v)
+    c = w.chunks - 1
+    splits = 4
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    # the regular entry point with a caller workspace
+    ws = ring.workspace(splits)
+    O_ref = torch.empty_like(q)
+    L_ref = torch.empty((w.B, w.H, w.Lc), dtype=torch.float32, device="cuda")
+    st = lib.sab_chunk_attention(ring.handle, 0, c, _ptr(q), None, None, w.W, 1, splits, w.scale, _ptr(O_ref),
+                                 _ptr(L_ref), _ptr(ws), ws.numel(), stream)
+    assert st == 0
+    for call in range(2):
+        O = torch.full_like(q, float("nan"))
+        L = torch.full((w.B, w.H, w.Lc), float("nan"), dtype=torch.float32, device="cuda")
+        st = lib.sab_chunk_attention_noalloc(ring.handle, 0, c, _ptr(q), None, None, w.W, 1, splits, w.scale,
+                                             _ptr(O), _ptr(L), stream)
+        assert st == 0, sab.status_string(st)
+        torch.cuda.synchronize()
+        d = (O.float() - O_ref.float()).abs()
+        assert torch.isfinite(O.float()).all(), f"call {call}: non-finite output"
+        assert d.max().item() <= 1e-2 and d.mean().item() <= 1e-3, f"call {call}: max {d.max().item():.3e}"
+        assert (L - L_ref).abs().max().item() <= 1e-3, f"call {call}"
+    # a request larger than the library's scratch is refused before any launch
+    big = synth.Workload("nb", B=2, H=24, D=128, Lc=1536, R=2, W=1, seed=72)
+    rbig = KVRing(1, big.B, big.H, big.D, big.Lc, big.R)
+    qb, kb, vb = (x.cuda() for x in synth.chunk_qkv(big, synth.generator(big.seed)))
+    Ob = torch.empty_like(qb)
+    st = lib.sab_chunk_attention_noalloc(rbig.handle, 0, 0, _ptr(qb), _ptr(kb), _ptr(vb), 1, 0, 8, big.scale,
+                                         _ptr(Ob), None, stream)
+    assert st == 4  # SAB_ERR_WORKSPACE
+    assert lib.sab_get_last_device_error(stream) == 0
