@@ -142,17 +142,21 @@ def run_ours(args):
     launches = [0]
 
     def chunk_step(c, ev=None):
+        # ev: (start, end) event lists; one pair brackets the 30 back-to-back
+        # attention launches of each denoise step (per-launch events would
+        # themselves cost device time), so the attention kernel's average
+        # launch duration is measured live, on its own stream.
         for s in range(S):
+            if ev is not None:
+                ev[0].append(torch.cuda.Event(enable_timing=True))
+                ev[1].append(torch.cuda.Event(enable_timing=True))
+                ev[0][-1].record(stream)
             for l in range(L):
-                if ev is not None:
-                    ev[0].append(torch.cuda.Event(enable_timing=True))
-                    ev[1].append(torch.cuda.Event(enable_timing=True))
-                    ev[0][-1].record(stream)
                 sab.chunk_attention(ring.handle, l, c, Q[s][l], Kc[s][l], Vc[s][l], w.W, False, args.splits,
                                     w.scale, O[s][l], LSE[s][l], work, stream)
-                if ev is not None:
-                    ev[1][-1].record(stream)
                 launches[0] += 1
+            if ev is not None:
+                ev[1][-1].record(stream)
         for l in range(L):
             sab.kv_ring_append(ring.handle, l, c, Kc[save][l], Vc[save][l], stream)
             launches[0] += 1
@@ -181,7 +185,7 @@ def run_ours(args):
         barrier()
     ms = t0.elapsed_time(t1)
     gpu_launches = launches[0]
-    attn_ms = [a.elapsed_time(b) for a, b in zip(*ev)]
+    attn_ms = [a.elapsed_time(b) / L for a, b in zip(*ev)]  # per launch
     status = sab.get_last_device_error(stream)
     if status != 0:
         raise RuntimeError(f"device error {sab.status_string(status)}")

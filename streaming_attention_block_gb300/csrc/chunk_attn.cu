@@ -249,6 +249,11 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc[0];
+  // Everything above (barriers, TMEM, tensor-map prefetch) overlaps the tail
+  // of the previous kernel in the stream; no global memory is touched before
+  // the previous grid has completed.
+  griddep_launch_dependents();
+  griddep_wait();
 
   // softmax-thread state handed to the cluster merge in the common tail
   bool sm_ok = false;
@@ -922,23 +927,22 @@ cudaError_t launch_impl(const AttnParams& p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  dim3 grid(p.n_qgroups, p.B * p.H, p.splits);
-  if (!p.cluster_merge) {
-    chunk_attn_kernel<D, QT, FP8><<<grid, C::kThreads, C::kSmemBytes, s>>>(p);
-    return cudaGetLastError();
-  }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
+  cfg.gridDim = dim3(p.n_qgroups, p.B * p.H, p.splits);
   cfg.blockDim = dim3(C::kThreads, 1, 1);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 1;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = (unsigned)p.splits;
+  cudaLaunchAttribute attr[2];
+  // programmatic dependent launch: the kernel waits for its predecessor in
+  // griddepcontrol.wait, after its own set-up
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 1;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = (unsigned)p.splits;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = p.cluster_merge ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, chunk_attn_kernel<D, QT, FP8>, p);
 }
 

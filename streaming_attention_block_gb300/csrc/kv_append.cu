@@ -15,6 +15,7 @@
 // to nearest even with saturation ("Matrix-Game 4.0", section "技术新颖性":
 // 8-bit keys/values per window interval, only the changed interval is
 // re-quantised -- here the changed interval is the appended chunk).
+#include "ptx.cuh"
 #include "sab_internal.h"
 
 namespace sab {
@@ -24,6 +25,8 @@ constexpr int kAppendThreads = 256;
 
 __global__ void __launch_bounds__(kAppendThreads)
 append_bf16_kernel(const __grid_constant__ AppendParams p) {
+  ptx::griddep_launch_dependents();
+  ptx::griddep_wait();  // the slot may still be read by the previous kernel
   const int vec_per_row = p.D / 8;  // 16-byte vectors per row
   const long long per_tensor = (long long)p.B * p.H * p.Lc * vec_per_row;
   const long long total = 2 * per_tensor;
@@ -57,6 +60,8 @@ __device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
 
 __global__ void __launch_bounds__(kAppendThreads)
 append_fp8_kernel(const __grid_constant__ AppendParams p) {
+  ptx::griddep_launch_dependents();
+  ptx::griddep_wait();  // the slot may still be read by the previous kernel
   const int tensor = blockIdx.x;
   const int bh = blockIdx.y;
   const int b = bh / p.H, h = bh % p.H;
@@ -108,6 +113,22 @@ append_fp8_kernel(const __grid_constant__ AppendParams p) {
   }
 }
 
+// Launch with programmatic dependent launch allowed (the kernel itself waits
+// for its predecessor before touching global memory).
+cudaError_t launch_pdl(void (*kernel)(AppendParams), dim3 grid, const AppendParams& p, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kAppendThreads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
 int num_sms() {
   static int n = 0;
   if (n == 0) {
@@ -127,14 +148,11 @@ cudaError_t launch_append_bf16(const AppendParams& p, cudaStream_t s) {
   const long long cap = (long long)num_sms() * 8;  // grid-stride beyond 8 CTAs per SM
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  append_bf16_kernel<<<(unsigned)blocks, kAppendThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(append_bf16_kernel, dim3((unsigned)blocks), p, s);
 }
 
 cudaError_t launch_append_fp8(const AppendParams& p, cudaStream_t s) {
-  dim3 grid(2, p.B * p.H);
-  append_fp8_kernel<<<grid, kAppendThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(append_fp8_kernel, dim3(2, p.B * p.H), p, s);
 }
 
 }  // namespace sab
