@@ -141,24 +141,25 @@ def run_ours(args):
     save = max(0, S - 2)  # KV of the penultimate denoise step goes to the cache
     launches = [0]
 
-    def chunk_step(c, ev=None):
+    def chunk_step(c, ev=None, bufs=None):
         # ev: (start, end) event lists; one pair brackets the 30 back-to-back
         # attention launches of each denoise step (per-launch events would
         # themselves cost device time), so the attention kernel's average
         # launch duration is measured live, on its own stream.
+        q_, k_, v_, o_, l_ = bufs if bufs is not None else (Q, Kc, Vc, O, LSE)
         for s in range(S):
             if ev is not None:
                 ev[0].append(torch.cuda.Event(enable_timing=True))
                 ev[1].append(torch.cuda.Event(enable_timing=True))
                 ev[0][-1].record(stream)
             for l in range(L):
-                sab.chunk_attention(ring.handle, l, c, Q[s][l], Kc[s][l], Vc[s][l], w.W, False, args.splits,
-                                    w.scale, O[s][l], LSE[s][l], work, stream)
+                sab.chunk_attention(ring.handle, l, c, q_[s][l], k_[s][l], v_[s][l], w.W, False, args.splits,
+                                    w.scale, o_[s][l], l_[s][l], work, stream)
                 launches[0] += 1
             if ev is not None:
                 ev[1][-1].record(stream)
         for l in range(L):
-            sab.kv_ring_append(ring.handle, l, c, Kc[save][l], Vc[save][l], stream)
+            sab.kv_ring_append(ring.handle, l, c, k_[save][l], v_[save][l], stream)
             launches[0] += 1
 
     def barrier():
@@ -191,34 +192,68 @@ def run_ours(args):
         raise RuntimeError(f"device error {sab.status_string(status)}")
 
     # ---------------- end to end: pinned host inputs in, outputs out, per step
+    # Every step copies its inputs from pinned host memory and its outputs
+    # back.  The copies run on their own streams into double-buffered device
+    # sets, so step i+1's inputs upload and step i-1's outputs download while
+    # step i computes (the pages' asynchronous I/O); ordering is by events.
     hQ = [[Q[s][l].cpu().pin_memory() for l in range(L)] for s in range(S)]
     hK = [[Kc[s][l].cpu().pin_memory() for l in range(L)] for s in range(S)]
     hV = [[Vc[s][l].cpu().pin_memory() for l in range(L)] for s in range(S)]
     hO = [[torch.empty(shape, dtype=torch.bfloat16).pin_memory() for _ in range(L)] for _ in range(S)]
     hL = [[torch.empty((B, H, Lc), dtype=torch.float32).pin_memory() for _ in range(L)] for _ in range(S)]
 
-    def e2e_step(c):
-        for s in range(S):
-            for l in range(L):
-                Q[s][l].copy_(hQ[s][l], non_blocking=True)
-                Kc[s][l].copy_(hK[s][l], non_blocking=True)
-                Vc[s][l].copy_(hV[s][l], non_blocking=True)
-        chunk_step(c)
-        for s in range(S):
-            for l in range(L):
-                hO[s][l].copy_(O[s][l], non_blocking=True)
-                hL[s][l].copy_(LSE[s][l], non_blocking=True)
-
+    def dev_set():
+        return ([[torch.empty(shape, dtype=torch.bfloat16, device=dev) for _ in range(L)] for _ in range(S)]
+                for _ in range(3))
+    sets = []
     for _ in range(2):
-        e2e_step(chunk)
-        chunk += 1
+        qd, kd, vd = dev_set()
+        od = [[torch.empty(shape, dtype=torch.bfloat16, device=dev) for _ in range(L)] for _ in range(S)]
+        ld = [[torch.empty((B, H, Lc), dtype=torch.float32, device=dev) for _ in range(L)] for _ in range(S)]
+        sets.append((qd, kd, vd, od, ld))
+    up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+
+    def e2e_run(first_chunk, nsteps):
+        comp, d2h_done = [], []
+        for i in range(nsteps):
+            qd, kd, vd, od, ld = sets[i % 2]
+            if i >= 2:
+                up.wait_event(comp[i - 2])  # set i%2 inputs no longer read
+            with torch.cuda.stream(up):
+                for s in range(S):
+                    for l in range(L):
+                        qd[s][l].copy_(hQ[s][l], non_blocking=True)
+                        kd[s][l].copy_(hK[s][l], non_blocking=True)
+                        vd[s][l].copy_(hV[s][l], non_blocking=True)
+            h2d_ev = torch.cuda.Event()
+            h2d_ev.record(up)
+            stream.wait_event(h2d_ev)
+            if i >= 2:
+                stream.wait_event(d2h_done[i - 2])  # set i%2 outputs downloaded
+            chunk_step(first_chunk + i, bufs=sets[i % 2])
+            ce = torch.cuda.Event()
+            ce.record(stream)
+            comp.append(ce)
+            down.wait_event(ce)
+            with torch.cuda.stream(down):
+                for s in range(S):
+                    for l in range(L):
+                        hO[s][l].copy_(od[s][l], non_blocking=True)
+                        hL[s][l].copy_(ld[s][l], non_blocking=True)
+            de = torch.cuda.Event()
+            de.record(down)
+            d2h_done.append(de)
+        stream.wait_event(d2h_done[-1])
+
+    e2e_run(chunk, 2)
+    chunk += 2
     barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step(chunk)
-        chunk += 1
+    up.wait_event(e0)
+    e2e_run(chunk, args.steps)
+    chunk += args.steps
     e1.record(stream)
     barrier()
     e2e_ms = e0.elapsed_time(e1)

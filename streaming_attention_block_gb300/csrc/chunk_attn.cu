@@ -19,7 +19,7 @@
 // Design (one CTA = QT query tiles of 128 rows x one (b, h) x one KV split):
 //   warp 0      TMA producer: Q once, then K/V tiles through a smem ring of
 //               kStages stages (128-byte swizzle, 64-column boxes).
-//   warp 1      TMEM allocator and single-thread tcgen05 MMA issuer:
+//   warp 1      TMEM allocator and tcgen05 MMA issuer (one elected lane):
 //               S_t = Q_t K^T (M=128, N=128) into TMEM, then O_t += P_t V with
 //               P_t read from TMEM (it overwrites S_t in place, as bf16).
 //   warps 4..   one softmax warpgroup per query tile: thread = row = TMEM
@@ -358,10 +358,12 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the issue loop (its values stay warp-uniform);
+    // one elected lane issues each MMA and commit.
+    {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(128, kTileN, 0);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 1);
-      bool ok = wait_bounded(bar(C::kBarQ), 0, abort_flag, 1);
+      bool ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarQ), 0, abort_flag, 1));
       if (ok) tc_fence_after();
       // Descriptors are built once: every operand tile of a kind shares the
       // high word, and stepping K (or a stage) only adds a small constant to
@@ -389,7 +391,7 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
-          mma_ss(d, make_desc(a0 + koff, kq_hi), make_desc(b0 + koff, kq_hi), idesc_qk, kk > 0 ? 1u : 0u);
+          mma_ss_e(d, make_desc(a0 + koff, kq_hi), make_desc(b0 + koff, kq_hi), idesc_qk, kk > 0 ? 1u : 0u);
           if (kk == D / 32 && pbar != 0) pout = mbar_test_wait(pbar, ppar);
         }
       };
@@ -402,13 +404,13 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
 #pragma unroll
         for (int kk = half * 4; kk < half * 4 + 4; ++kk) {
           const uint32_t a_t = tmem + C::kTmemS + t * 128 + kk * 8;
-          mma_ts(d, a_t, make_desc(b0 + ((kk * 16 * 128) >> 4), v_hi), idesc_pv, kk > 0 ? 1u : acc0);
+          mma_ts_e(d, a_t, make_desc(b0 + ((kk * 16 * 128) >> 4), v_hi), idesc_pv, kk > 0 ? 1u : acc0);
           if (kk == half * 4 + 1 && pbar != 0) pout = mbar_test_wait(pbar, ppar);
         }
       };
       auto wait_probed = [&](uint32_t b, uint32_t par, bool probed, unsigned site) -> bool {
         if (probed) return true;
-        return wait_bounded(b, par, abort_flag, site);
+        return __all_sync(0xffffffffu, wait_bounded(b, par, abort_flag, site));
       };
       auto kbar = [&](int j) { return bar(C::kBarKFull + j % C::kStages); };
       auto kpar = [&](int j) { return (uint32_t)(j / C::kStages) & 1u; };
@@ -432,24 +434,24 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
       for (int j = 0; ok && j < n_tiles; ++j) {
         bool pr_k = false;
         if (j > 0 && !(ok = issue_pv(0, j - 1, pr_p0, kbar(j), kpar(j), pr_k))) break;
-        if (QT == 1 && j > 0) mma_commit(bar(C::kBarKVEmpty + (j - 1) % C::kStages));
+        if (QT == 1 && j > 0) mma_commit_e(bar(C::kBarKVEmpty + (j - 1) % C::kStages));
         if (!(ok = wait_probed(kbar(j), kpar(j), pr_k, 5))) break;
         tc_fence_after();
         if (QT == 2) {
           bool pr_p1 = false;
           issue_s(0, j, j > 0 ? pbar(1, 0) : 0u, (uint32_t)(j - 1) & 1u, pr_p1);
-          mma_commit(bar(C::kBarSFull + 0));
+          mma_commit_e(bar(C::kBarSFull + 0));
           bool unused = false;
           if (j > 0) {
             if (!(ok = issue_pv(1, j - 1, pr_p1, 0u, 0u, unused))) break;
-            mma_commit(bar(C::kBarKVEmpty + (j - 1) % C::kStages));
+            mma_commit_e(bar(C::kBarKVEmpty + (j - 1) % C::kStages));
           }
           issue_s(1, j, pbar(0, 0), (uint32_t)j & 1u, pr_p0);
-          mma_commit(bar(C::kBarSFull + 1));
+          mma_commit_e(bar(C::kBarSFull + 1));
         } else {
           bool unused = false;
           issue_s(0, j, 0u, 0u, unused);
-          mma_commit(bar(C::kBarSFull + 0));
+          mma_commit_e(bar(C::kBarSFull + 0));
           pr_p0 = false;
         }
       }
@@ -457,20 +459,20 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
         if (n_tiles > 0) {
           bool unused = false;
           ok = issue_pv(0, n_tiles - 1, pr_p0, 0u, 0u, unused);
-          if (ok) mma_commit(bar(C::kBarOFinal + 0));
+          if (ok) mma_commit_e(bar(C::kBarOFinal + 0));
           if (ok && QT == 2) {
             ok = issue_pv(1, n_tiles - 1, false, 0u, 0u, unused);
-            if (ok) mma_commit(bar(C::kBarOFinal + 1));
+            if (ok) mma_commit_e(bar(C::kBarOFinal + 1));
           }
-          if (ok) mma_commit(bar(C::kBarKVEmpty + (n_tiles - 1) % C::kStages));
+          if (ok) mma_commit_e(bar(C::kBarKVEmpty + (n_tiles - 1) % C::kStages));
         } else {
-          mma_commit(bar(C::kBarOFinal + 0));
-          if (QT == 2) mma_commit(bar(C::kBarOFinal + 1));
+          mma_commit_e(bar(C::kBarOFinal + 0));
+          if (QT == 2) mma_commit_e(bar(C::kBarOFinal + 1));
         }
       }
       if (!ok) {
-        mma_commit(bar(C::kBarDrain));
-        wait_drain(bar(C::kBarDrain), 0);
+        mma_commit_e(bar(C::kBarDrain));
+        if (lane == 0) wait_drain(bar(C::kBarDrain), 0);
       }
     }
     __syncwarp();
