@@ -56,7 +56,6 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max
 template <int D_, int QT_, bool FP8_>
 struct Cfg {
   static constexpr int D = D_, QT = QT_;
-  static constexpr bool FP8 = FP8_;
   static constexpr int kBoxes = D / 64;                  // 64-column (128-byte) boxes per row
   static constexpr uint32_t kBoxBytes = 128u * 128u;     // 128 rows x 128 bytes
   static constexpr uint32_t kTileBytes = kBoxBytes * kBoxes;
@@ -75,7 +74,10 @@ struct Cfg {
   static constexpr int kBarOFinal = kBarPFull + 4;         // [2]
   static constexpr int kBarDrain = kBarOFinal + 2;
   static constexpr int kBarRawFull = kBarDrain + 1;          // [kStages] FP8 codes landed
-  static constexpr int kNumBars = kBarRawFull + kStages;
+  static constexpr int kBarPairReady = kBarRawFull + kStages;  // pair merge: the peer can receive
+  static constexpr int kBarPairIn = kBarPairReady + 1;         // pair merge: the peer's rows landed
+  static constexpr int kBarPairDone = kBarPairIn + 1;          // pair merge: the peer has our rows
+  static constexpr int kNumBars = kBarPairDone + 1;
   static constexpr int kConvThreads = 64;                    // warps 2-3 expand E4M3 tiles
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
   static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;  // + alignment slack
@@ -92,6 +94,17 @@ struct Cfg {
   static constexpr uint32_t kMergeOOff = kKOff;
   static constexpr uint32_t kMergeLseOff = kMergeOOff + kMergeRows * kMergePitch * 4;
   static_assert(kMergeLseOff + kMergeRows * 4 <= kBarOff, "merge buffer fits in the operand region");
+  // Two-split pair merge (QT == 2), also in the dead operand region: the
+  // peer's normalised partial rows of the tile this CTA owns (128 rows of D
+  // fp32, 16-byte chunks XOR-swizzled by row, then 128 LSEs), the merged bf16
+  // tile in the output tensor map's layout, and this CTA's partial rows of
+  // the tile the peer owns (same layout as the received block).
+  static constexpr uint32_t kPairBytes = 128u * D * 4u + 128u * 4u;
+  static constexpr uint32_t kPairRecvOff = 0;
+  static constexpr uint32_t kPairOutOff = (kPairRecvOff + kPairBytes + 1023u) & ~1023u;
+  static constexpr uint32_t kPairSendOff = kPairOutOff + kTileBytes;
+  static_assert(QT != 2 || kPairSendOff + kPairBytes <= kBarOff, "pair merge buffers fit");
+  static_assert(kPairBytes % 16 == 0 && kPairSendOff % 16 == 0, "bulk copy alignment");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
@@ -107,13 +120,14 @@ __device__ __forceinline__ uint64_t global_ns() {
 // latency-critical pipeline.  Every 256 polls it checks the CTA abort flag and
 // the elapsed time; after kTimeoutNs it records the wait site, raises the
 // abort flag and gives up.
+template <bool kClusterScope = false>
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                              unsigned site) {
-  if (mbar_test_wait(bar, parity)) return true;
+  if (!kClusterScope && mbar_test_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
 #pragma unroll 1
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (kClusterScope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
     if ((it & 255u) == 0) {
       if (*abort_flag) return false;
       if (global_ns() - t0 > kTimeoutNs) {
@@ -231,6 +245,9 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
       mbar_init(bar(C::kBarOFinal + t), 1);
     }
     mbar_init(bar(C::kBarDrain), 1);
+    mbar_init(bar(C::kBarPairReady), 1);
+    mbar_init(bar(C::kBarPairIn), 1);
+    mbar_init(bar(C::kBarPairDone), 1);
     misc[1] = 0;
     misc[2] = 0;
     fence_mbar_init();
@@ -249,6 +266,8 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc[0];
+  const bool pair_merge = QT == 2 && p.cluster_merge == 2;
+  if (pair_merge) cluster_arrive_relaxed();  // barriers initialised (waited on before remote use)
   // Everything above (barriers, TMEM, tensor-map prefetch) overlaps the tail
   // of the previous kernel in the stream; no global memory is touched before
   // the previous grid has completed.
@@ -660,6 +679,7 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
       // the cluster merge overwrites operand smem: every MMA must be done
       if (ok && QT == 2 && p.cluster_merge)
         ok = wait_bounded(bar(C::kBarOFinal + (1 - t)), 0, abort_flag, 9 - t);
+      // (the pair merge also reuses operand smem: same condition)
       ok = __all_sync(0xffffffffu, ok);
     }
     const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
@@ -693,7 +713,7 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
           }
         }
         if (row_valid && p.LSE != nullptr) p.LSE[(long long)bh * p.Lq + q_row] = lse;
-      } else if (p.cluster_merge) {
+      } else if (p.cluster_merge == 1) {
         // the common tail pushes this row once every CTA of the cluster is
         // done with its operand shared memory
         sm_ok = true;
@@ -701,7 +721,7 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
         sm_lse = lse;
         sm_tO = tO;
         sm_rcta = t * 128 + row;
-      } else {
+      } else if (p.cluster_merge == 0) {
         const long long prow = ((long long)split * BH + bh) * p.lq_pad + (q_row);
         float* wrow = p.ws_o + prow * D;
 #pragma unroll
@@ -734,6 +754,97 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
           tma_store_4d(&p.o_map, base_u32 + C::kQOff + t * C::kTileBytes + bx * C::kBoxBytes, bx * 64,
                        q0 + t * kTileM, h, b);
         tma_store_commit_and_wait_read();
+      }
+    }
+    if (pair_merge) {
+      // ---------------- two-split log-sum-exp merge inside a CTA pair
+      // CTA rank r of the pair owns query tile r.  The warpgroup of the other
+      // tile normalises its partial rows into smem and sends them to the peer
+      // in one bulk copy, once the peer reports that its operand smem is free
+      // (all its MMAs done).  The owning warpgroup keeps its partial in TMEM,
+      // waits for the peer's rows, merges by log-sum-exp, and stores the bf16
+      // tile with TMA.  Three point-to-point mbarriers carry the handshake,
+      // each wait bounded; the sender keeps its source smem alive until the
+      // peer confirms receipt.
+      const uint32_t rank = cluster_ctarank();
+      const uint32_t peer = rank ^ 1u;
+      cluster_wait();  // the peer's barriers are initialised
+      tc_fence_after();
+      const bool leader = lane == 0 && quad == 0;
+      const uint32_t sw = (uint32_t)(row & 7);  // 16-byte chunk swizzle of this row
+      uint32_t o[D];
+      if (ok) {
+        if (n_tiles > 0) {
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) tmem_ld32(tO + c0, *reinterpret_cast<uint32_t(*)[32]>(o + c0));
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int c = 0; c < D; ++c) o[c] = 0u;
+        }
+      }
+      if (t != (int)rank) {
+        uint8_t* snd = base + C::kPairSendOff;
+        if (ok) {
+#pragma unroll
+          for (int k = 0; k < D / 4; ++k)
+            *reinterpret_cast<float4*>(snd + row * (D * 4) + ((k ^ sw) << 4)) =
+                make_float4(__uint_as_float(o[4 * k]) * inv_l, __uint_as_float(o[4 * k + 1]) * inv_l,
+                            __uint_as_float(o[4 * k + 2]) * inv_l, __uint_as_float(o[4 * k + 3]) * inv_l);
+          reinterpret_cast<float*>(snd + 128 * D * 4)[row] = lse;
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(2 + t, 128);
+        if (leader && ok && wait_bounded<true>(bar(C::kBarPairReady), 0, abort_flag, 10) && !*abort_flag) {
+          bulk_copy_to_cta(mapa(base_u32 + C::kPairRecvOff, peer), base_u32 + C::kPairSendOff, C::kPairBytes,
+                           mapa(bar(C::kBarPairIn), peer));
+          wait_bounded<true>(bar(C::kBarPairDone), 0, abort_flag, 10);
+        }
+      } else {
+        if (leader) {
+          mbar_arrive_expect_tx(bar(C::kBarPairIn), C::kPairBytes);
+          if (ok) mbar_arrive_remote(mapa(bar(C::kBarPairReady), peer));
+        }
+        const bool got = __all_sync(0xffffffffu, ok && wait_bounded(bar(C::kBarPairIn), 0, abort_flag, 11));
+        if (got && leader) mbar_arrive_remote(mapa(bar(C::kBarPairDone), peer));
+        if (got) {
+          const uint8_t* rcv = base + C::kPairRecvOff;
+          const float lse_p = reinterpret_cast<const float*>(rcv + 128 * D * 4)[row];
+          const float M = fmaxf(lse, lse_p);
+          float w_own = 0.f, w_peer = 0.f, L = -INFINITY;
+          if (M != -INFINITY) {
+            const float e_own = ex2((lse - M) * kLog2e), e_peer = ex2((lse_p - M) * kLog2e);
+            const float tot = e_own + e_peer;
+            w_own = e_own / tot * inv_l;
+            w_peer = e_peer / tot;
+            L = M + __logf(tot);
+          }
+          uint8_t* ost = base + C::kPairOutOff;
+#pragma unroll
+          for (int k = 0; k < D / 8; ++k) {  // 16-byte bf16 chunks of the output row
+            const float4 a = *reinterpret_cast<const float4*>(rcv + row * (D * 4) + (((2 * k) ^ sw) << 4));
+            const float4 c = *reinterpret_cast<const float4*>(rcv + row * (D * 4) + (((2 * k + 1) ^ sw) << 4));
+            uint4 w;
+            w.x = pack_bf16(fmaf(__uint_as_float(o[8 * k + 0]), w_own, a.x * w_peer),
+                            fmaf(__uint_as_float(o[8 * k + 1]), w_own, a.y * w_peer));
+            w.y = pack_bf16(fmaf(__uint_as_float(o[8 * k + 2]), w_own, a.z * w_peer),
+                            fmaf(__uint_as_float(o[8 * k + 3]), w_own, a.w * w_peer));
+            w.z = pack_bf16(fmaf(__uint_as_float(o[8 * k + 4]), w_own, c.x * w_peer),
+                            fmaf(__uint_as_float(o[8 * k + 5]), w_own, c.y * w_peer));
+            w.w = pack_bf16(fmaf(__uint_as_float(o[8 * k + 6]), w_own, c.z * w_peer),
+                            fmaf(__uint_as_float(o[8 * k + 7]), w_own, c.w * w_peer));
+            *reinterpret_cast<uint4*>(ost + (k >> 3) * C::kBoxBytes + row * 128 + (((k & 7) ^ sw) << 4)) = w;
+          }
+          if (row_valid && p.LSE != nullptr) p.LSE[(long long)bh * p.Lq + q_row] = L;
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(2 + t, 128);
+        if (leader && !*abort_flag && q0 + t * kTileM < p.Lq) {
+#pragma unroll
+          for (int bx = 0; bx < C::kBoxes; ++bx)
+            tma_store_4d(&p.o_map, base_u32 + C::kPairOutOff + bx * C::kBoxBytes, bx * 64, q0 + t * kTileM, h, b);
+          tma_store_commit_and_wait_read();
+        }
       }
     }
     if (p.splits > 1 && !p.cluster_merge) {
@@ -798,7 +909,8 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
   }
 
   tc_fence_before();
-  if (p.cluster_merge) {
+  if (pair_merge && warp < 4) cluster_wait();
+  if (p.cluster_merge == 1) {
     // ------------- log-sum-exp merge of the splits through distributed smem
     // CTA rank r of the cluster owns rows [r * rows_per, (r + 1) * rows_per)
     // of the query group.  Barrier A: every CTA is done with its operand

@@ -377,6 +377,7 @@ static sab_status launch_attention(AttnParams& p, int Lq, int splits, void* work
   // 2..8 splits of a query group merge inside a thread-block cluster; more
   // splits (or a device refusing the cluster) merge through the workspace.
   p.cluster_merge = (allow_cluster && splits >= 2 && splits <= kMaxClusterSplits) ? 1 : 0;
+  if (p.cluster_merge && splits == 2 && t.qt == 2) p.cluster_merge = 2;
   cudaError_t e = launch_chunk_attention(p, t.qt, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess && p.cluster_merge) {
     (void)cudaGetLastError();

@@ -40,8 +40,11 @@ struct AttnParams {
   int n_qgroups;          // CTAs along the query axis (q tiles per CTA: 1 or 2)
   int lq_pad;             // n_qgroups * tiles per CTA * 128 (workspace row pitch)
   int splits;
-  int cluster_merge;      // 1: the splits of a query tile form a thread-block
-                          // cluster and merge through distributed shared memory
+  int cluster_merge;      // 0: splits merge through the workspace; 1: the splits
+                          // of a query group form a thread-block cluster and
+                          // merge through distributed shared memory; 2: two
+                          // splits of a two-tile group merge as a CTA pair
+                          // (one bulk copy each way)
   float scale_log2;       // softmax_scale * log2(e)
   // streaming
   int nseg;
