@@ -1060,7 +1060,543 @@ cudaError_t launch_impl(const AttnParams& p, cudaStream_t s) {
   return cudaLaunchKernelEx(&cfg, chunk_attn_kernel<D, QT, FP8>, p);
 }
 
+// ===========================================================================
+// Key-half kernel: one CTA = one query tile of 128 rows x one (b, h), no KV
+// split.  Each 128-key tile's scores are processed by two softmax
+// warpgroups, one per 64-key half; each half keeps its own running max, row
+// sum and output accumulator O_h in TMEM (O_0 + O_1 combined by log-sum-exp
+// in the epilogue), so the halves never exchange data inside the loop.  S is
+// double-buffered in TMEM, so the MMA warp issues S(j+2) right after PV(j),
+// while the softmax of tile j+1 runs: the tensor pipe sees PV_0(j), PV_1(j),
+// S(j+2) per tile and the softmax has a whole tile period to finish.
+//   warp 0        TMA producer (Q once, K/V through kStages stages)
+//   warp 1        TMEM allocator, tcgen05 MMA issuer (one elected lane)
+//   warps 2-3     E4M3 -> bf16 expansion (FP8 cache only)
+//   8 warps       softmax: half h = keys [64h, 64h + 64) of every tile
+// TMEM: S/P buffers at columns 0 and 128 (P_h packed bf16 in the first 32
+// columns of its half), O_h at column 256 + h * D.
+template <int D_, bool FP8_>
+struct KhCfg {
+  static constexpr int D = D_;
+  static constexpr int kBoxes = D / 64;
+  static constexpr uint32_t kBoxBytes = 128u * 128u;
+  static constexpr uint32_t kTileBytes = kBoxBytes * kBoxes;
+  static constexpr int kStages = (D == 128) ? 3 : 4;
+  static constexpr uint32_t kKOff = 0;
+  static constexpr uint32_t kVOff = kKOff + kStages * kTileBytes;
+  static constexpr uint32_t kQOff = kVOff + kStages * kTileBytes;
+  static constexpr uint32_t kBarOff = kQOff + kTileBytes;
+  static constexpr int kBarQ = 0;
+  static constexpr int kBarKFull = 1;                         // [kStages]
+  static constexpr int kBarKVEmpty = kBarKFull + kStages;     // [kStages]
+  static constexpr int kBarRawFull = kBarKVEmpty + kStages;   // [kStages] FP8 codes landed
+  static constexpr int kBarSFull = kBarRawFull + kStages;     // [2 buffers]
+  static constexpr int kBarPFull = kBarSFull + 2;             // [2 buffers][2 halves]
+  static constexpr int kBarPVDone = kBarPFull + 4;            // [2 halves] one phase per tile
+  static constexpr int kBarOFinal = kBarPVDone + 2;           // every MMA complete
+  static constexpr int kBarDrain = kBarOFinal + 1;
+  static constexpr int kNumBars = kBarDrain + 1;
+  static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;
+  static constexpr int kConvThreads = 64;
+  static constexpr int kSoftmaxWarp0 = FP8_ ? 4 : 2;
+  static constexpr int kThreads = 32 * (kSoftmaxWarp0 + 8);
+  static constexpr uint32_t kTmemO = 256;
+  static constexpr uint32_t kTmemCols = 512;
+  // epilogue scratch in the dead operand region: (m, l) of every row and
+  // half, and the bf16 output tile (Q slot) for the TMA store
+  static constexpr uint32_t kXchOff = kKOff;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+template <int D, bool FP8>
+__global__ void __launch_bounds__(KhCfg<D, FP8>::kThreads, 1)
+chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
+  using C = KhCfg<D, FP8>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  const uint32_t base_u32 = (raw_u32 + 1023u) & ~1023u;
+  uint8_t* base = smem_raw + (base_u32 - raw_u32);
+  const uint32_t sQ = base_u32 + C::kQOff;
+  const uint32_t sK = base_u32 + C::kKOff;
+  const uint32_t sV = base_u32 + C::kVOff;
+  const uint32_t bars = base_u32 + C::kBarOff;
+  uint32_t* misc = reinterpret_cast<uint32_t*>(base + C::kMiscOff);  // [0] tmem, [1] abort
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
+  auto bar = [&](int i) -> uint32_t { return bars + 8u * (uint32_t)i; };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int bh = blockIdx.y;
+  const int b = bh / p.H;
+  const int h = bh - b * p.H;
+  const int q0 = blockIdx.x * kTileM;
+
+  int first = 0, n_tiles = 0;
+  kv_range(p, q0, kTileM, 0, first, n_tiles);
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(C::kBarQ), 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(bar(C::kBarKFull + s), FP8 ? C::kConvThreads : 1);
+      mbar_init(bar(C::kBarKVEmpty + s), 1);
+      mbar_init(bar(C::kBarRawFull + s), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(C::kBarSFull + i), 1);
+      mbar_init(bar(C::kBarPFull + 2 * i), 128);
+      mbar_init(bar(C::kBarPFull + 2 * i + 1), 128);
+      mbar_init(bar(C::kBarPVDone + i), 1);
+    }
+    mbar_init(bar(C::kBarOFinal), 1);
+    mbar_init(bar(C::kBarDrain), 1);
+    misc[1] = 0;
+    fence_mbar_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(misc), C::kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&p.q_map);
+    prefetch_tmap(&p.k_map[0]);
+    prefetch_tmap(&p.v_map[0]);
+    prefetch_tmap(&p.o_map);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+  griddep_launch_dependents();
+  griddep_wait();
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar(C::kBarQ), C::kTileBytes);
+#pragma unroll
+      for (int bx = 0; bx < C::kBoxes; ++bx)
+        tma_load_4d(sQ + bx * C::kBoxBytes, &p.q_map, bar(C::kBarQ), bx * 64, q0, h, b);
+      int j = 0;
+      for (; j < n_tiles; ++j) {
+        const int st = j % C::kStages;
+        if (j >= C::kStages &&
+            !wait_bounded(bar(C::kBarKVEmpty + st), (uint32_t)(j / C::kStages - 1) & 1u, abort_flag, 0))
+          break;
+        const Tile ti = tile_at(p, first + j);
+        if (FP8) {
+          mbar_arrive_expect_tx(bar(C::kBarRawFull + st), 2 * 128 * D);
+          tma_load_4d(sK + st * C::kTileBytes + C::kBoxBytes, &p.k_map[0], bar(C::kBarRawFull + st), 0, ti.row,
+                      h, b);
+          tma_load_4d(sV + st * C::kTileBytes + C::kBoxBytes, &p.v_map[0], bar(C::kBarRawFull + st), 0, ti.row,
+                      h, b);
+        } else {
+          mbar_arrive_expect_tx(bar(C::kBarKFull + st), 2 * C::kTileBytes);
+#pragma unroll
+          for (int bx = 0; bx < C::kBoxes; ++bx)
+            tma_load_4d(sK + st * C::kTileBytes + bx * C::kBoxBytes, &p.k_map[ti.src],
+                        bar(C::kBarKFull + st), bx * 64, ti.row, h, b);
+#pragma unroll
+          for (int bx = 0; bx < C::kBoxes; ++bx)
+            tma_load_4d(sV + st * C::kTileBytes + bx * C::kBoxBytes, &p.v_map[ti.src],
+                        bar(C::kBarKFull + st), bx * 64, ti.row, h, b);
+        }
+      }
+      if (*abort_flag) {
+        wait_drain(bar(C::kBarQ), 0);
+        for (int jj = max(0, j - C::kStages); jj < j; ++jj)
+          wait_drain(bar((FP8 ? C::kBarRawFull : C::kBarKFull) + jj % C::kStages),
+                     (uint32_t)(jj / C::kStages) & 1u);
+      }
+    }
+    __syncwarp();
+  } else if (FP8 && (warp == 2 || warp == 3)) {
+    // ------------------------------------------------ E4M3 -> bf16 expansion
+    // (same in-place row expansion as the two-tile kernel)
+    const int ct = threadIdx.x - 64;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int st = j % C::kStages;
+      if (!wait_bounded(bar(C::kBarRawFull + st), (uint32_t)(j / C::kStages) & 1u, abort_flag, 12)) break;
+#pragma unroll 1
+      for (int job = ct; job < 2 * kTileN; job += C::kConvThreads) {
+        const int r = job & (kTileN - 1);
+        const bool isv = job >= kTileN;
+        uint8_t* tile = base + (isv ? C::kVOff : C::kKOff) + st * C::kTileBytes;
+        const uint4* src = reinterpret_cast<const uint4*>(tile + C::kBoxBytes + r * 128);
+        uint4 raw[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) raw[i] = src[i];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+          uint32_t out[8];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            float a0, a1, a2, a3;
+            e4m3x2_to_f32x2((uint16_t)(w[q] & 0xFFFFu), a0, a1);
+            e4m3x2_to_f32x2((uint16_t)(w[q] >> 16), a2, a3);
+            out[2 * q] = pack_bf16(a0, a1);
+            out[2 * q + 1] = pack_bf16(a2, a3);
+          }
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int k = 2 * i + hh;
+            *reinterpret_cast<uint4*>(tile + (k >> 3) * C::kBoxBytes + r * 128 + (((k & 7) ^ (r & 7)) << 4)) =
+                make_uint4(out[4 * hh], out[4 * hh + 1], out[4 * hh + 2], out[4 * hh + 3]);
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(bar(C::kBarKFull + st));
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    constexpr uint32_t idesc_qk = idesc_bf16_f32(128, kTileN, 0);
+    constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 1);
+    bool ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarQ), 0, abort_flag, 1));
+    if (ok) tc_fence_after();
+    const uint64_t dq = smem_desc_sw128(sQ, 16, 1024);
+    const uint64_t dk = smem_desc_sw128(sK, 16, 1024);
+    const uint64_t dv = smem_desc_sw128(sV, C::kBoxBytes, 1024);
+    const uint32_t q_lo = (uint32_t)dq, k_lo = (uint32_t)dk, v_lo = (uint32_t)dv;
+    const uint32_t kq_hi = (uint32_t)(dq >> 32), v_hi = (uint32_t)(dv >> 32);
+    constexpr uint32_t kTileStep = C::kTileBytes >> 4;
+    // As in the two-tile kernel, the barrier needed next is probed without
+    // blocking in the middle of the preceding MMA group.
+    auto issue_s = [&](int j, uint32_t pb, uint32_t pp, bool& pout) {
+      const uint32_t d = tmem + (uint32_t)(j & 1) * 128u;
+      const uint32_t b0 = k_lo + (uint32_t)(j % C::kStages) * kTileStep;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t koff = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
+        mma_ss_e(d, make_desc(q_lo + koff, kq_hi), make_desc(b0 + koff, kq_hi), idesc_qk, kk > 0 ? 1u : 0u);
+        if (kk == D / 32 && pb != 0) pout = mbar_test_wait(pb, pp);
+      }
+    };
+    // O_hf += P_hf V[64 hf .. 64 hf + 63]
+    auto issue_pv = [&](int j, int hf, uint32_t pb, uint32_t pp, bool& pout) {
+      const uint32_t d = tmem + C::kTmemO + (uint32_t)hf * D;
+      const uint32_t b0 = v_lo + (uint32_t)(j % C::kStages) * kTileStep;
+      const uint32_t a0 = tmem + (uint32_t)(j & 1) * 128u + (uint32_t)hf * 64u;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const int kg = hf * 4 + kk;  // group of 16 keys
+        mma_ts_e(d, a0 + kk * 8, make_desc(b0 + ((kg * 16 * 128) >> 4), v_hi), idesc_pv,
+                 (kk > 0 || j > 0) ? 1u : 0u);
+        if (kk == 1 && pb != 0) pout = mbar_test_wait(pb, pp);
+      }
+    };
+    auto wait_probed = [&](uint32_t bb, uint32_t par, bool probed, unsigned site) -> bool {
+      if (probed) return true;
+      return __all_sync(0xffffffffu, wait_bounded(bb, par, abort_flag, site));
+    };
+    auto kbar = [&](int j) { return bar(C::kBarKFull + j % C::kStages); };
+    auto kpar = [&](int j) { return (uint32_t)(j / C::kStages) & 1u; };
+    auto pbar = [&](int j, int hf) { return bar(C::kBarPFull + 2 * (j & 1) + hf); };
+    auto ppar = [&](int j) { return (uint32_t)(j >> 1) & 1u; };
+    bool pr = false;
+    // prologue: S(0), S(1)
+    for (int j = 0; ok && j < 2 && j < n_tiles; ++j) {
+      if (!(ok = wait_probed(kbar(j), kpar(j), pr, 5))) break;
+      tc_fence_after();
+      pr = false;
+      if (j + 1 < 2 && j + 1 < n_tiles) issue_s(j, kbar(j + 1), kpar(j + 1), pr);
+      else issue_s(j, pbar(0, 0), ppar(0), pr);
+      mma_commit_e(bar(C::kBarSFull + (j & 1)));
+    }
+    for (int j = 0; ok && j < n_tiles; ++j) {
+      if (!(ok = wait_probed(pbar(j, 0), ppar(j), pr, 2))) break;
+      tc_fence_after();
+      pr = false;
+      issue_pv(j, 0, pbar(j, 1), ppar(j), pr);
+      mma_commit_e(bar(C::kBarPVDone + 0));
+      if (!(ok = wait_probed(pbar(j, 1), ppar(j), pr, 3))) break;
+      tc_fence_after();
+      pr = false;
+      if (j + 2 < n_tiles) issue_pv(j, 1, kbar(j + 2), kpar(j + 2), pr);
+      else issue_pv(j, 1, 0u, 0u, pr);
+      mma_commit_e(bar(C::kBarPVDone + 1));
+      mma_commit_e(bar(C::kBarKVEmpty + j % C::kStages));
+      if (j + 2 < n_tiles) {
+        if (!(ok = wait_probed(kbar(j + 2), kpar(j + 2), pr, 5))) break;
+        tc_fence_after();
+        pr = false;
+        issue_s(j + 2, pbar(j + 1, 0), ppar(j + 1), pr);
+        mma_commit_e(bar(C::kBarSFull + (j & 1)));
+      } else {
+        pr = false;
+      }
+    }
+    if (ok) mma_commit_e(bar(C::kBarOFinal));
+    if (!ok) {
+      mma_commit_e(bar(C::kBarDrain));
+      if (lane == 0) wait_drain(bar(C::kBarDrain), 0);
+    }
+    __syncwarp();
+  } else if (warp >= C::kSoftmaxWarp0) {
+    // ---------------------------------------------- softmax + epilogue
+    const int hf = (warp - C::kSoftmaxWarp0) >> 2;  // key half of every tile
+    const int quad = warp & 3;                        // TMEM lane quadrant of this warp
+    const int row = quad * 32 + lane;
+    const int q_row = q0 + row;
+    const bool row_valid = q_row < p.Lq;
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const uint32_t tSh = tmem + lane_off + (uint32_t)hf * 64u;  // + buffer * 128
+    const uint32_t tO = tmem + lane_off + C::kTmemO + (uint32_t)hf * D;
+    const int kofs = hf * 64;  // first key of this half inside a tile
+    int klo = 0, khi = 0;
+    if (p.mode == kModeBlockCausal && row_valid) {
+      const int qc = q_row / p.chunk_tokens;
+      klo = max(0, qc - p.window) * p.chunk_tokens;
+      khi = min(p.Lk, (qc + 1) * p.chunk_tokens);
+    }
+    const float sl = p.scale_log2;
+    int seg_tile0[kMaxSegments], seg_rows[kMaxSegments], seg_row0[kMaxSegments];
+#pragma unroll
+    for (int i = 0; i < kMaxSegments; ++i) {
+      seg_tile0[i] = (i < p.nseg) ? p.seg[i].tile0 : 0x7fffffff;
+      seg_rows[i] = p.seg[i].nrows;
+      seg_row0[i] = p.seg[i].row0;
+    }
+    const long long srow = (long long)bh * p.scale_stride;
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_tiles; ++j) {
+      ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarSFull + (j & 1)), (uint32_t)(j >> 1) & 1u,
+                                                abort_flag, 6 + hf));
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t tS = tSh + (uint32_t)(j & 1) * 128u;
+      uint32_t s0[32], s1[32];
+      tmem_ld32(tS + 0, s0);
+      tmem_ld32(tS + 32, s1);
+      int lo, hi;
+      int tile_row0 = 0;
+      const int g = first + j;
+      if (p.mode == kModeStreaming) {
+        int sg = 0;
+#pragma unroll
+        for (int i = 1; i < kMaxSegments; ++i) sg = (g >= seg_tile0[i]) ? i : sg;
+        int t0 = seg_tile0[0], nr = seg_rows[0], r0 = seg_row0[0];
+#pragma unroll
+        for (int i = 1; i < kMaxSegments; ++i) {
+          t0 = (sg == i) ? seg_tile0[i] : t0;
+          nr = (sg == i) ? seg_rows[i] : nr;
+          r0 = (sg == i) ? seg_row0[i] : r0;
+        }
+        lo = 0;
+        hi = nr - (g - t0) * kTileN;
+        tile_row0 = r0 + (g - t0) * kTileN;
+      } else {
+        lo = klo - g * kTileN;
+        hi = khi - g * kTileN;
+      }
+      lo -= kofs;
+      hi -= kofs;
+      tmem_wait_ld();
+      // FP8 cache: the tile's keys belong to at most two chunks; columns of
+      // this half before `bnd` to the first, the rest to the next
+      float c0 = sl, c1 = sl, d0 = 0.f, v0 = 1.f, v1 = 1.f, iv0 = 1.f;
+      int bnd = 64;
+      if constexpr (FP8) {
+        const int si0 = min(tile_row0 / p.chunk_tokens, p.scale_stride - 1);
+        const int si1 = min(si0 + 1, p.scale_stride - 1);
+        bnd = (si0 + 1) * p.chunk_tokens - tile_row0 - kofs;
+        float ks0 = __ldg(p.k_scale + srow + si0), ks1 = __ldg(p.k_scale + srow + si1);
+        float vs0 = __ldg(p.v_scale + srow + si0), vs1 = __ldg(p.v_scale + srow + si1);
+        if (bnd <= 0) {  // the whole half lies in the second chunk
+          ks0 = ks1;
+          vs0 = vs1;
+        }
+        // a zero scale marks a slot never written, whose keys are all masked:
+        // keep the coefficients finite and non-zero so that -inf stays -inf
+        c0 = ks0 > 0.f ? sl * ks0 : sl;
+        c1 = ks1 > 0.f ? sl * ks1 : sl;
+        v0 = vs0;
+        v1 = vs1;
+        d0 = vs0 > 0.f ? __log2f(vs0) : 0.f;
+        iv0 = vs0 > 0.f ? 1.f / vs0 : 0.f;
+      }
+      const bool straddle = FP8 && bnd > 0 && bnd < 64;
+      if (straddle) {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          s0[c] = __float_as_uint(__uint_as_float(s0[c]) * (c < bnd ? c0 : c1));
+          s1[c] = __float_as_uint(__uint_as_float(s1[c]) * (c + 32 < bnd ? c0 : c1));
+        }
+      }
+      if (!(lo <= 0 && hi >= 64)) {
+        const uint32_t ninf = 0xff800000u;
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          s0[c] = (c >= lo && c < hi) ? s0[c] : ninf;
+          s1[c] = (c + 32 >= lo && c + 32 < hi) ? s1[c] : ninf;
+        }
+      }
+      float pm[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        float m = fmax3(__uint_as_float(s0[k]), __uint_as_float(s0[k + 8]), __uint_as_float(s0[k + 16]));
+        m = fmax3(m, __uint_as_float(s0[k + 24]), __uint_as_float(s1[k]));
+        m = fmax3(m, __uint_as_float(s1[k + 8]), __uint_as_float(s1[k + 16]));
+        pm[k] = fmaxf(m, __uint_as_float(s1[k + 24]));
+      }
+      const float mx = fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7]));
+      const float m_new = fmaxf(m_run, straddle ? mx : mx * c0);
+      const bool need = m_new > m_run + kRescaleThreshold;
+      float alpha = 1.f;
+      if (need) {
+        alpha = ex2(m_run - m_new);
+        l_run *= alpha;
+        m_run = m_new;
+      }
+      if (j > 0 && __any_sync(0xffffffffu, need)) {
+        // O_hf holds PV_hf(j-1) only once that MMA group has completed
+        ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarPVDone + hf), (uint32_t)(j - 1) & 1u, abort_flag,
+                                                  8 + hf));
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int cc = 0; cc < D; cc += 16) {
+          uint32_t o[16];
+          tmem_ld16(tO + cc, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 16; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+          tmem_st16(tO + cc, o);
+        }
+      }
+      const float mb = (m_run == -INFINITY) ? 0.f : m_run;
+      const float xa = straddle ? 1.f : c0;
+      const float xs = straddle ? -mb : d0 - mb;
+      float ps[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t pk[32];
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        float a0 = ex2(fmaf(__uint_as_float(s0[2 * c]), xa, xs));
+        float a1 = ex2(fmaf(__uint_as_float(s0[2 * c + 1]), xa, xs));
+        float b0 = ex2(fmaf(__uint_as_float(s1[2 * c]), xa, xs));
+        float b1 = ex2(fmaf(__uint_as_float(s1[2 * c + 1]), xa, xs));
+        ps[c & 3] += (a0 + a1) + (b0 + b1);
+        if (straddle) {
+          const int k = 2 * c;
+          a0 *= (k < bnd ? v0 : v1);
+          a1 *= (k + 1 < bnd ? v0 : v1);
+          b0 *= (k + 32 < bnd ? v0 : v1);
+          b1 *= (k + 33 < bnd ? v0 : v1);
+        }
+        pk[c] = pack_bf16(a0, a1);
+        pk[16 + c] = pack_bf16(b0, b1);
+      }
+      tmem_st32(tS, pk);
+      l_run += ((ps[0] + ps[1]) + (ps[2] + ps[3])) * (straddle ? 1.f : iv0);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(C::kBarPFull + 2 * (j & 1) + hf));
+    }
+    // ------------------------------------------------------------ epilogue
+    // (the other half's softmax may still be a tile behind, so completion is
+    // read from the single-phase final barrier, not from the per-tile ones)
+    if (ok) ok = wait_bounded(bar(C::kBarOFinal), 0, abort_flag, 8);
+    ok = __all_sync(0xffffffffu, ok);
+    // every MMA is complete: the operand region is free.  Exchange (m, l) of
+    // the two halves of each row, then each half finishes D/2 columns.
+    float2* xch = reinterpret_cast<float2*>(base + C::kXchOff);
+    xch[hf * 128 + row] = make_float2(m_run, l_run);
+    named_bar_sync(1, 256);
+    const float2 other = xch[(1 - hf) * 128 + row];
+    const float m0 = hf == 0 ? m_run : other.x, l0 = hf == 0 ? l_run : other.y;
+    const float m1 = hf == 0 ? other.x : m_run, l1 = hf == 0 ? other.y : l_run;
+    const float M = fmaxf(m0, m1);
+    const float w0 = (M == -INFINITY) ? 0.f : ex2(m0 - M);
+    const float w1 = (M == -INFINITY) ? 0.f : ex2(m1 - M);
+    const float L = l0 * w0 + l1 * w1;
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    const float sc0 = w0 * inv, sc1 = w1 * inv;
+    constexpr int kHalfCols = D / 2;
+    uint8_t* stage = base + C::kQOff;
+    if (ok) {
+      tc_fence_after();
+      uint32_t oa[kHalfCols], ob[kHalfCols];
+      if (n_tiles > 0) {
+        const uint32_t tO0 = tmem + lane_off + C::kTmemO + (uint32_t)(hf * kHalfCols);
+#pragma unroll
+        for (int cc = 0; cc < kHalfCols; cc += 32) {
+          tmem_ld32(tO0 + cc, *reinterpret_cast<uint32_t(*)[32]>(oa + cc));
+          tmem_ld32(tO0 + D + cc, *reinterpret_cast<uint32_t(*)[32]>(ob + cc));
+        }
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int c = 0; c < kHalfCols; ++c) oa[c] = ob[c] = 0u;
+      }
+#pragma unroll
+      for (int i = 0; i < kHalfCols / 8; ++i) {
+        float v[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          v[c] = fmaf(__uint_as_float(oa[8 * i + c]), sc0, __uint_as_float(ob[8 * i + c]) * sc1);
+        uint4 w;
+        w.x = pack_bf16(v[0], v[1]);
+        w.y = pack_bf16(v[2], v[3]);
+        w.z = pack_bf16(v[4], v[5]);
+        w.w = pack_bf16(v[6], v[7]);
+        const int k = hf * (kHalfCols / 8) + i;  // 16-byte chunk of the output row
+        *reinterpret_cast<uint4*>(stage + (k >> 3) * C::kBoxBytes + row * 128 + (((k & 7) ^ (row & 7)) << 4)) = w;
+      }
+      if (hf == 0 && row_valid && p.LSE != nullptr)
+        p.LSE[(long long)bh * p.Lq + q_row] = L > 0.f ? (M + __log2f(L)) * kLn2 : -INFINITY;
+    }
+    fence_proxy_async_smem();
+    named_bar_sync(1, 256);
+    if (warp == C::kSoftmaxWarp0 && lane == 0 && !*abort_flag) {
+#pragma unroll
+      for (int bx = 0; bx < C::kBoxes; ++bx)
+        tma_store_4d(&p.o_map, base_u32 + C::kQOff + bx * C::kBoxBytes, bx * 64, q0, h, b);
+      tma_store_commit_and_wait_read();
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int D, bool FP8>
+cudaError_t launch_kh_impl(const AttnParams& p, cudaStream_t s) {
+  using C = KhCfg<D, FP8>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(chunk_attn_kh_kernel<D, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.n_qgroups, p.B * p.H, 1);
+  cfg.blockDim = dim3(C::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, chunk_attn_kh_kernel<D, FP8>, p);
+}
+
 }  // namespace
+
+cudaError_t launch_chunk_attention_kh(const AttnParams& p, cudaStream_t s) {
+  if (p.splits != 1) return cudaErrorInvalidValue;
+  if (p.fp8) return p.D == 128 ? launch_kh_impl<128, true>(p, s) : cudaErrorInvalidValue;
+  if (p.D == 128) return launch_kh_impl<128, false>(p, s);
+  if (p.D == 64) return launch_kh_impl<64, false>(p, s);
+  return cudaErrorInvalidValue;
+}
 
 cudaError_t launch_chunk_attention(const AttnParams& p, int q_tiles_per_cta, cudaStream_t s) {
   if (p.fp8) {

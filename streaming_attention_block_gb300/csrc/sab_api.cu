@@ -351,6 +351,20 @@ size_t sab_chunk_attention_workspace(const sab_ring* ring, int num_splits) {
 
 static sab_status launch_attention(AttnParams& p, int Lq, int splits, void* workspace, size_t ws_bytes,
                                    void* stream, bool allow_cluster = true) {
+  if ((long long)p.B * p.H > 65535) return SAB_ERR_UNSUPPORTED;
+  // One query tile per CTA without a KV split when that already fills the
+  // GPU (or the caller asks for one split): key-half kernel, no merge.
+  const int n_qtiles = (Lq + kTileM - 1) / kTileM;
+  if (splits == 1 || (splits == 0 && (long long)n_qtiles * p.B * p.H * 8 >= 7LL * device_sms())) {
+    p.Lq = Lq;
+    p.n_qtiles = n_qtiles;
+    p.n_qgroups = n_qtiles;
+    p.lq_pad = n_qtiles * kTileM;
+    p.splits = 1;
+    p.cluster_merge = 0;
+    return launch_chunk_attention_kh(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SAB_OK
+                                                                                          : SAB_ERR_CUDA;
+  }
   const QTiling t = qtiling(Lq);
   if (splits == 0) {
     // block-causal: a CTA sees at most (window + 1) chunks plus one straddled tile

@@ -79,6 +79,8 @@ struct AppendParams {
 cudaError_t launch_append_bf16(const AppendParams& p, cudaStream_t s);
 cudaError_t launch_append_fp8(const AppendParams& p, cudaStream_t s);
 cudaError_t launch_chunk_attention(const AttnParams& p, int q_tiles_per_cta, cudaStream_t s);
+// One query tile per CTA, key-half softmax warpgroups; unsplit KV only.
+cudaError_t launch_chunk_attention_kh(const AttnParams& p, cudaStream_t s);
 cudaError_t read_and_clear_device_error(unsigned int* value);
 // Device address and size of the library's own split-merge scratch.
 cudaError_t noalloc_scratch(void** ptr, size_t* bytes);
