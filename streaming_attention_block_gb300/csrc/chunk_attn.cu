@@ -1069,7 +1069,9 @@ cudaError_t launch_impl(const AttnParams& p, cudaStream_t s) {
 // double-buffered in TMEM, so the MMA warp issues S(j+2) right after PV(j),
 // while the softmax of tile j+1 runs: the tensor pipe sees PV_0(j), PV_1(j),
 // S(j+2) per tile and the softmax has a whole tile period to finish.
-//   warp 0        TMA producer (Q once, K/V through kStages stages)
+//   warp 0        TMA producer (Q once, then stage u holds K(u) and V(u-1):
+//                 a stage is released by PV(u-1), which the MMA warp issues
+//                 after S(u), and K(u) arrives two tile periods before S(u))
 //   warp 1        TMEM allocator, tcgen05 MMA issuer (one elected lane)
 //   warps 2-3     E4M3 -> bf16 expansion (FP8 cache only)
 //   8 warps       softmax: half h = keys [64h, 64h + 64) of every tile
@@ -1178,36 +1180,44 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
 #pragma unroll
       for (int bx = 0; bx < C::kBoxes; ++bx)
         tma_load_4d(sQ + bx * C::kBoxBytes, &p.q_map, bar(C::kBarQ), bx * 64, q0, h, b);
-      int j = 0;
-      for (; j < n_tiles; ++j) {
-        const int st = j % C::kStages;
-        if (j >= C::kStages &&
-            !wait_bounded(bar(C::kBarKVEmpty + st), (uint32_t)(j / C::kStages - 1) & 1u, abort_flag, 0))
+      int u = 0;
+      for (; u <= n_tiles && n_tiles > 0; ++u) {
+        const int st = u % C::kStages;
+        if (u >= C::kStages &&
+            !wait_bounded(bar(C::kBarKVEmpty + st), (uint32_t)(u / C::kStages - 1) & 1u, abort_flag, 0))
           break;
-        const Tile ti = tile_at(p, first + j);
+        const bool has_k = u < n_tiles, has_v = u > 0;
+        const Tile tk = tile_at(p, first + (has_k ? u : u - 1));
+        const Tile tv = tile_at(p, first + (has_v ? u - 1 : u));
         if (FP8) {
-          mbar_arrive_expect_tx(bar(C::kBarRawFull + st), 2 * 128 * D);
-          tma_load_4d(sK + st * C::kTileBytes + C::kBoxBytes, &p.k_map[0], bar(C::kBarRawFull + st), 0, ti.row,
-                      h, b);
-          tma_load_4d(sV + st * C::kTileBytes + C::kBoxBytes, &p.v_map[0], bar(C::kBarRawFull + st), 0, ti.row,
-                      h, b);
+          mbar_arrive_expect_tx(bar(C::kBarRawFull + st), (has_k ? 128 * D : 0) + (has_v ? 128 * D : 0));
+          if (has_k)
+            tma_load_4d(sK + st * C::kTileBytes + C::kBoxBytes, &p.k_map[0], bar(C::kBarRawFull + st), 0, tk.row,
+                        h, b);
+          if (has_v)
+            tma_load_4d(sV + st * C::kTileBytes + C::kBoxBytes, &p.v_map[0], bar(C::kBarRawFull + st), 0, tv.row,
+                        h, b);
         } else {
-          mbar_arrive_expect_tx(bar(C::kBarKFull + st), 2 * C::kTileBytes);
+          mbar_arrive_expect_tx(bar(C::kBarKFull + st), (has_k ? C::kTileBytes : 0) + (has_v ? C::kTileBytes : 0));
+          if (has_k) {
 #pragma unroll
-          for (int bx = 0; bx < C::kBoxes; ++bx)
-            tma_load_4d(sK + st * C::kTileBytes + bx * C::kBoxBytes, &p.k_map[ti.src],
-                        bar(C::kBarKFull + st), bx * 64, ti.row, h, b);
+            for (int bx = 0; bx < C::kBoxes; ++bx)
+              tma_load_4d(sK + st * C::kTileBytes + bx * C::kBoxBytes, &p.k_map[tk.src], bar(C::kBarKFull + st),
+                          bx * 64, tk.row, h, b);
+          }
+          if (has_v) {
 #pragma unroll
-          for (int bx = 0; bx < C::kBoxes; ++bx)
-            tma_load_4d(sV + st * C::kTileBytes + bx * C::kBoxBytes, &p.v_map[ti.src],
-                        bar(C::kBarKFull + st), bx * 64, ti.row, h, b);
+            for (int bx = 0; bx < C::kBoxes; ++bx)
+              tma_load_4d(sV + st * C::kTileBytes + bx * C::kBoxBytes, &p.v_map[tv.src], bar(C::kBarKFull + st),
+                          bx * 64, tv.row, h, b);
+          }
         }
       }
       if (*abort_flag) {
         wait_drain(bar(C::kBarQ), 0);
-        for (int jj = max(0, j - C::kStages); jj < j; ++jj)
-          wait_drain(bar((FP8 ? C::kBarRawFull : C::kBarKFull) + jj % C::kStages),
-                     (uint32_t)(jj / C::kStages) & 1u);
+        for (int uu = max(0, u - C::kStages); uu < u; ++uu)
+          wait_drain(bar((FP8 ? C::kBarRawFull : C::kBarKFull) + uu % C::kStages),
+                     (uint32_t)(uu / C::kStages) & 1u);
       }
     }
     __syncwarp();
@@ -1215,11 +1225,12 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
     // ------------------------------------------------ E4M3 -> bf16 expansion
     // (same in-place row expansion as the two-tile kernel)
     const int ct = threadIdx.x - 64;
-    for (int j = 0; j < n_tiles; ++j) {
-      const int st = j % C::kStages;
-      if (!wait_bounded(bar(C::kBarRawFull + st), (uint32_t)(j / C::kStages) & 1u, abort_flag, 12)) break;
+    for (int u = 0; u <= n_tiles && n_tiles > 0; ++u) {
+      const int st = u % C::kStages;
+      if (!wait_bounded(bar(C::kBarRawFull + st), (uint32_t)(u / C::kStages) & 1u, abort_flag, 12)) break;
+      const int job0 = u < n_tiles ? 0 : kTileN, job1 = u > 0 ? 2 * kTileN : kTileN;  // K rows, then V rows
 #pragma unroll 1
-      for (int job = ct; job < 2 * kTileN; job += C::kConvThreads) {
+      for (int job = job0 + ct; job < job1; job += C::kConvThreads) {
         const int r = job & (kTileN - 1);
         const bool isv = job >= kTileN;
         uint8_t* tile = base + (isv ? C::kVOff : C::kKOff) + st * C::kTileBytes;
@@ -1277,7 +1288,7 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
     // O_hf += P_hf V[64 hf .. 64 hf + 63]
     auto issue_pv = [&](int j, int hf, uint32_t pb, uint32_t pp, bool& pout) {
       const uint32_t d = tmem + C::kTmemO + (uint32_t)hf * D;
-      const uint32_t b0 = v_lo + (uint32_t)(j % C::kStages) * kTileStep;
+      const uint32_t b0 = v_lo + (uint32_t)((j + 1) % C::kStages) * kTileStep;
       const uint32_t a0 = tmem + (uint32_t)(j & 1) * 128u + (uint32_t)hf * 64u;
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
@@ -1304,8 +1315,12 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
       if (j + 1 < 2 && j + 1 < n_tiles) issue_s(j, kbar(j + 1), kpar(j + 1), pr);
       else issue_s(j, pbar(0, 0), ppar(0), pr);
       mma_commit_e(bar(C::kBarSFull + (j & 1)));
+      if (j == 0) mma_commit_e(bar(C::kBarKVEmpty + 0));  // stage 0 holds K(0) only
     }
     for (int j = 0; ok && j < n_tiles; ++j) {
+      // V(j) sits in stage j + 1 with K(j + 1): already waited for before
+      // S(j + 1), except after the last tile
+      if (j + 1 >= n_tiles && !(ok = wait_probed(kbar(j + 1), kpar(j + 1), false, 5))) break;
       if (!(ok = wait_probed(pbar(j, 0), ppar(j), pr, 2))) break;
       tc_fence_after();
       pr = false;
@@ -1317,7 +1332,9 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
       if (j + 2 < n_tiles) issue_pv(j, 1, kbar(j + 2), kpar(j + 2), pr);
       else issue_pv(j, 1, 0u, 0u, pr);
       mma_commit_e(bar(C::kBarPVDone + 1));
-      mma_commit_e(bar(C::kBarKVEmpty + j % C::kStages));
+      // stage j + 1 (K(j + 1), V(j)) is free once PV(j) completes: S(j + 1)
+      // was issued before it
+      mma_commit_e(bar(C::kBarKVEmpty + (j + 1) % C::kStages));
       if (j + 2 < n_tiles) {
         if (!(ok = wait_probed(kbar(j + 2), kpar(j + 2), pr, 5))) break;
         tc_fence_after();
@@ -1370,7 +1387,6 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
       const uint32_t tS = tSh + (uint32_t)(j & 1) * 128u;
       uint32_t s0[32], s1[32];
       tmem_ld32(tS + 0, s0);
-      tmem_ld32(tS + 32, s1);
       int lo, hi;
       int tile_row0 = 0;
       const int g = first + j;
@@ -1394,7 +1410,6 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
       }
       lo -= kofs;
       hi -= kofs;
-      tmem_wait_ld();
       // FP8 cache: the tile's keys belong to at most two chunks; columns of
       // this half before `bnd` to the first, the rest to the next
       float c0 = sl, c1 = sl, d0 = 0.f, v0 = 1.f, v1 = 1.f, iv0 = 1.f;
@@ -1419,78 +1434,96 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
         iv0 = vs0 > 0.f ? 1.f / vs0 : 0.f;
       }
       const bool straddle = FP8 && bnd > 0 && bnd < 64;
-      if (straddle) {
+      const bool masked = !(lo <= 0 && hi >= 64);
+      // per-column scaling (straddling FP8 tile) and masking of 32 columns
+      // starting at column cb of this half
+      auto prep = [&](uint32_t (&sv)[32], int cb) {
+        if (straddle) {
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          s0[c] = __float_as_uint(__uint_as_float(s0[c]) * (c < bnd ? c0 : c1));
-          s1[c] = __float_as_uint(__uint_as_float(s1[c]) * (c + 32 < bnd ? c0 : c1));
+          for (int c = 0; c < 32; ++c) sv[c] = __float_as_uint(__uint_as_float(sv[c]) * (cb + c < bnd ? c0 : c1));
         }
-      }
-      if (!(lo <= 0 && hi >= 64)) {
-        const uint32_t ninf = 0xff800000u;
+        if (masked) {
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          s0[c] = (c >= lo && c < hi) ? s0[c] : ninf;
-          s1[c] = (c + 32 >= lo && c + 32 < hi) ? s1[c] : ninf;
+          for (int c = 0; c < 32; ++c) sv[c] = (cb + c >= lo && cb + c < hi) ? sv[c] : 0xff800000u;
         }
-      }
-      float pm[8];
+      };
+      auto max32 = [&](const uint32_t (&sv)[32]) -> float {
+        float pm[4];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        float m = fmax3(__uint_as_float(s0[k]), __uint_as_float(s0[k + 8]), __uint_as_float(s0[k + 16]));
-        m = fmax3(m, __uint_as_float(s0[k + 24]), __uint_as_float(s1[k]));
-        m = fmax3(m, __uint_as_float(s1[k + 8]), __uint_as_float(s1[k + 16]));
-        pm[k] = fmaxf(m, __uint_as_float(s1[k + 24]));
-      }
-      const float mx = fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7]));
+        for (int k = 0; k < 4; ++k) {
+          float m = fmax3(__uint_as_float(sv[k]), __uint_as_float(sv[k + 4]), __uint_as_float(sv[k + 8]));
+          m = fmax3(m, __uint_as_float(sv[k + 12]), __uint_as_float(sv[k + 16]));
+          m = fmax3(m, __uint_as_float(sv[k + 20]), __uint_as_float(sv[k + 24]));
+          pm[k] = fmaxf(m, __uint_as_float(sv[k + 28]));
+        }
+        return fmax3(fmaxf(pm[0], pm[1]), pm[2], pm[3]);
+      };
+      // P of 32 columns: e = 2^(s*xa + xs); packed bf16 pairs into pko[0..15],
+      // row-sum terms into ps (before any per-column V scale)
+      auto exps32 = [&](const uint32_t (&sv)[32], int cb, float xa, float xs, uint32_t* pko, float2& ps) {
+        const float2 xa2 = make_float2(xa, xa), xs2 = make_float2(xs, xs);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const float2 x = __ffma2_rn(make_float2(__uint_as_float(sv[2 * c]), __uint_as_float(sv[2 * c + 1])), xa2, xs2);
+          float e0 = ex2(x.x), e1 = ex2(x.y);
+          ps = __fadd2_rn(ps, make_float2(e0, e1));
+          if (straddle) {
+            e0 *= (cb + 2 * c < bnd ? v0 : v1);
+            e1 *= (cb + 2 * c + 1 < bnd ? v0 : v1);
+          }
+          pko[c] = pack_bf16(e0, e1);
+        }
+      };
+      // Exponentials are taken against the running max m_run right away, in
+      // parallel with the row max; only when the max grows by more than the
+      // rescale threshold (always on a row's first visible tile) are they
+      // recomputed against the new max, with O and l rescaled.
+      const float mb0 = (m_run == -INFINITY) ? 0.f : m_run;
+      const float xa = straddle ? 1.f : c0;
+      uint32_t pk[32];
+      float2 psa = make_float2(0.f, 0.f), psb = make_float2(0.f, 0.f);
+      tmem_wait_ld();
+      tmem_ld32(tS + 32, s1);
+      prep(s0, 0);
+      const float mx0 = max32(s0);
+      exps32(s0, 0, xa, straddle ? -mb0 : d0 - mb0, pk, psa);
+      tmem_wait_ld();
+      prep(s1, 32);
+      const float mx1 = max32(s1);
+      exps32(s1, 32, xa, straddle ? -mb0 : d0 - mb0, pk + 16, psb);
+      const float mx = fmaxf(mx0, mx1);
       const float m_new = fmaxf(m_run, straddle ? mx : mx * c0);
       const bool need = m_new > m_run + kRescaleThreshold;
-      float alpha = 1.f;
-      if (need) {
-        alpha = ex2(m_run - m_new);
-        l_run *= alpha;
-        m_run = m_new;
-      }
-      if (j > 0 && __any_sync(0xffffffffu, need)) {
-        // O_hf holds PV_hf(j-1) only once that MMA group has completed
-        ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarPVDone + hf), (uint32_t)(j - 1) & 1u, abort_flag,
-                                                  8 + hf));
-        if (!ok) break;
-        tc_fence_after();
+      if (__any_sync(0xffffffffu, need)) {
+        float alpha = 1.f;
+        if (need) {
+          alpha = ex2(m_run - m_new);  // 0 when m_run is -inf
+          l_run *= alpha;
+          m_run = m_new;
+        }
+        if (j > 0) {
+          // O_hf holds PV_hf(j-1) only once that MMA group has completed
+          ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarPVDone + hf), (uint32_t)(j - 1) & 1u, abort_flag,
+                                                    8 + hf));
+          if (!ok) break;
+          tc_fence_after();
 #pragma unroll 1
-        for (int cc = 0; cc < D; cc += 16) {
-          uint32_t o[16];
-          tmem_ld16(tO + cc, o);
-          tmem_wait_ld();
+          for (int cc = 0; cc < D; cc += 16) {
+            uint32_t o[16];
+            tmem_ld16(tO + cc, o);
+            tmem_wait_ld();
 #pragma unroll
-          for (int c = 0; c < 16; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-          tmem_st16(tO + cc, o);
+            for (int c = 0; c < 16; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+            tmem_st16(tO + cc, o);
+          }
         }
-      }
-      const float mb = (m_run == -INFINITY) ? 0.f : m_run;
-      const float xa = straddle ? 1.f : c0;
-      const float xs = straddle ? -mb : d0 - mb;
-      float ps[4] = {0.f, 0.f, 0.f, 0.f};
-      uint32_t pk[32];
-#pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        float a0 = ex2(fmaf(__uint_as_float(s0[2 * c]), xa, xs));
-        float a1 = ex2(fmaf(__uint_as_float(s0[2 * c + 1]), xa, xs));
-        float b0 = ex2(fmaf(__uint_as_float(s1[2 * c]), xa, xs));
-        float b1 = ex2(fmaf(__uint_as_float(s1[2 * c + 1]), xa, xs));
-        ps[c & 3] += (a0 + a1) + (b0 + b1);
-        if (straddle) {
-          const int k = 2 * c;
-          a0 *= (k < bnd ? v0 : v1);
-          a1 *= (k + 1 < bnd ? v0 : v1);
-          b0 *= (k + 32 < bnd ? v0 : v1);
-          b1 *= (k + 33 < bnd ? v0 : v1);
-        }
-        pk[c] = pack_bf16(a0, a1);
-        pk[16 + c] = pack_bf16(b0, b1);
+        const float mb = (m_run == -INFINITY) ? 0.f : m_run;
+        psa = psb = make_float2(0.f, 0.f);
+        exps32(s0, 0, xa, straddle ? -mb : d0 - mb, pk, psa);
+        exps32(s1, 32, xa, straddle ? -mb : d0 - mb, pk + 16, psb);
       }
       tmem_st32(tS, pk);
-      l_run += ((ps[0] + ps[1]) + (ps[2] + ps[3])) * (straddle ? 1.f : iv0);
+      l_run += ((psa.x + psa.y) + (psb.x + psb.y)) * (straddle ? 1.f : iv0);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(C::kBarPFull + 2 * (j & 1) + hf));
