@@ -31,6 +31,10 @@ sys.path.insert(0, ROOT)
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 METRIC = "chunk-attention TFLOP/s & chunks/s at Wan-1.3B shape; % of roofline"
+# DRAM bytes (read + write) of one attention launch of this workload, from the
+# ncu capture summarised in profiles/chunk_attn_kh_wan13b_ncu.md; None once
+# the kernel has changed since that capture.
+ATTN_DRAM_BYTES_PER_LAUNCH = 33_093_376 + 512
 
 
 def _peaks():
@@ -288,7 +292,7 @@ def run_ours(args):
         "tflops": round(tflops, 2), "attention_us_per_call": round(attn_avg_s * 1e6, 2),
         "gpu_launches": gpu_launches,
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
-                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "frac": round(achieved / peak, 4), "traffic": ATTN_DRAM_BYTES_PER_LAUNCH,
                      "peak_source": f"bf16 dense sustained, {src}"},
         "e2e": {"value": round(chunks_total / (e2e_ms / 1e3), 3), "unit": "chunks/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -390,7 +394,7 @@ def run_sweep(args):
                 ring.append(0, c, k, v)
         nkeys = w.Lc * (w.W + 1) + (w.Lc if w.sink else 0)
         flops = 4.0 * w.B * w.H * w.D * w.Lc * nkeys
-        for splits in sorted({0, w.splits}):
+        for splits in sorted({0, 1, w.splits}):
             work = ring.workspace(splits) if splits != 1 else None
             O = torch.empty_like(q)
             L = torch.empty((w.B, w.H, w.Lc), dtype=torch.float32, device="cuda")

@@ -184,8 +184,10 @@ size_t sab_chunk_attention_workspace(const sab_ring* ring, int num_splits);
  *   num_splits >= 1: KV partitions computed in parallel and merged by
  *          log-sum-exp inside the same kernel ("Matrix-Game 4.0", section
  *          "技术新颖性": the window is cut into intervals whose partial outputs
- *          are merged with log-sum-exp); 0 lets the library choose (at most
- *          16: enough partitions for one CTA per SM).
+ *          are merged with log-sum-exp); 1 runs one 128-query tile per CTA
+ *          over the whole key set (no merge).  0 lets the library choose: no
+ *          split when the B * H * ceil(Lc / 128) query tiles cover at least a
+ *          quarter of the SMs, else up to 8 partitions.
  *   softmax_scale  usually 1/sqrt(D).
  *   O      device, token-major [B, Lc, H, D] bf16 (output).
  *   LSE    device, [B, H, Lc] fp32, natural log of sum exp(s) (output; may be NULL).

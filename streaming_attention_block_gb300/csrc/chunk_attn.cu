@@ -16,7 +16,10 @@
 // masked; in block-causal mode each row derives its key interval from its
 // chunk index.
 //
-// Design (one CTA = QT query tiles of 128 rows x one (b, h) x one KV split):
+// Two kernels.  chunk_attn_kh_kernel (further down) serves every unsplit
+// call: one query tile per CTA, key-half softmax warpgroups, double-buffered
+// S.  chunk_attn_kernel below serves split calls; its design (one CTA = QT
+// query tiles of 128 rows x one (b, h) x one KV split):
 //   warp 0      TMA producer: Q once, then K/V tiles through a smem ring of
 //               kStages stages (128-byte swizzle, 64-column boxes).
 //   warp 1      TMEM allocator and tcgen05 MMA issuer (one elected lane):
