@@ -200,50 +200,51 @@ def run_ours(args):
     # back.  The copies run on their own streams into double-buffered device
     # sets, so step i+1's inputs upload and step i-1's outputs download while
     # step i computes (the pages' asynchronous I/O); ordering is by events.
-    hQ = [[Q[s][l].cpu().pin_memory() for l in range(L)] for s in range(S)]
-    hK = [[Kc[s][l].cpu().pin_memory() for l in range(L)] for s in range(S)]
-    hV = [[Vc[s][l].cpu().pin_memory() for l in range(L)] for s in range(S)]
-    hO = [[torch.empty(shape, dtype=torch.bfloat16).pin_memory() for _ in range(L)] for _ in range(S)]
-    hL = [[torch.empty((B, H, Lc), dtype=torch.float32).pin_memory() for _ in range(L)] for _ in range(S)]
-
-    def dev_set():
-        return ([[torch.empty(shape, dtype=torch.bfloat16, device=dev) for _ in range(L)] for _ in range(S)]
-                for _ in range(3))
+    # One contiguous pinned block per direction and per device set, so each
+    # step moves its inputs in one host->device copy and its outputs in two
+    # device->host copies (fewer, larger copies keep the copy engines busy).
+    hQKV = torch.empty((S, L, 3) + shape, dtype=torch.bfloat16).pin_memory()
+    for s_ in range(S):
+        for l_ in range(L):
+            hQKV[s_, l_, 0].copy_(Q[s_][l_].cpu())
+            hQKV[s_, l_, 1].copy_(Kc[s_][l_].cpu())
+            hQKV[s_, l_, 2].copy_(Vc[s_][l_].cpu())
+    hO = torch.empty((S, L) + shape, dtype=torch.bfloat16).pin_memory()
+    hL = torch.empty((S, L, B, H, Lc), dtype=torch.float32).pin_memory()
     sets = []
     for _ in range(2):
-        qd, kd, vd = dev_set()
-        od = [[torch.empty(shape, dtype=torch.bfloat16, device=dev) for _ in range(L)] for _ in range(S)]
-        ld = [[torch.empty((B, H, Lc), dtype=torch.float32, device=dev) for _ in range(L)] for _ in range(S)]
-        sets.append((qd, kd, vd, od, ld))
+        qkv = torch.empty((S, L, 3) + shape, dtype=torch.bfloat16, device=dev)
+        od = torch.empty((S, L) + shape, dtype=torch.bfloat16, device=dev)
+        ld = torch.empty((S, L, B, H, Lc), dtype=torch.float32, device=dev)
+        views = ([[qkv[s_, l_, 0] for l_ in range(L)] for s_ in range(S)],
+                 [[qkv[s_, l_, 1] for l_ in range(L)] for s_ in range(S)],
+                 [[qkv[s_, l_, 2] for l_ in range(L)] for s_ in range(S)],
+                 [[od[s_, l_] for l_ in range(L)] for s_ in range(S)],
+                 [[ld[s_, l_] for l_ in range(L)] for s_ in range(S)])
+        sets.append((qkv, od, ld, views))
     up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
 
     def e2e_run(first_chunk, nsteps):
         comp, d2h_done = [], []
         for i in range(nsteps):
-            qd, kd, vd, od, ld = sets[i % 2]
+            qkv, od, ld, views = sets[i % 2]
             if i >= 2:
                 up.wait_event(comp[i - 2])  # set i%2 inputs no longer read
             with torch.cuda.stream(up):
-                for s in range(S):
-                    for l in range(L):
-                        qd[s][l].copy_(hQ[s][l], non_blocking=True)
-                        kd[s][l].copy_(hK[s][l], non_blocking=True)
-                        vd[s][l].copy_(hV[s][l], non_blocking=True)
+                qkv.copy_(hQKV, non_blocking=True)
             h2d_ev = torch.cuda.Event()
             h2d_ev.record(up)
             stream.wait_event(h2d_ev)
             if i >= 2:
                 stream.wait_event(d2h_done[i - 2])  # set i%2 outputs downloaded
-            chunk_step(first_chunk + i, bufs=sets[i % 2])
+            chunk_step(first_chunk + i, bufs=views)
             ce = torch.cuda.Event()
             ce.record(stream)
             comp.append(ce)
             down.wait_event(ce)
             with torch.cuda.stream(down):
-                for s in range(S):
-                    for l in range(L):
-                        hO[s][l].copy_(od[s][l], non_blocking=True)
-                        hL[s][l].copy_(ld[s][l], non_blocking=True)
+                hO.copy_(od, non_blocking=True)
+                hL.copy_(ld, non_blocking=True)
             de = torch.cuda.Event()
             de.record(down)
             d2h_done.append(de)
