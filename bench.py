@@ -379,11 +379,11 @@ def run_sweep(args):
             line.update(extra)
         print(json.dumps(line), flush=True)
 
-    for name in ("tiny", "wan13b", "long_sink", "fp8_kv"):
+    for name in ("tiny", "wan13b", "long_sink", "fp8_kv", "int8k_kv"):
         w = synth.workload(name)
         g = synth.generator(w.seed, device="cuda")
         ring = sab.KVRing(1, w.B, w.H, w.D, w.Lc, w.R, has_sink=w.sink,
-                          kv_dtype=sab.KV_FP8_E4M3 if w.kv_fp8 else sab.KV_BF16)
+                          kv_dtype=(sab.KV_INT8K_FP8V if w.kv_int8k else sab.KV_FP8_E4M3) if w.kv_fp8 else sab.KV_BF16)
         if w.sink:
             sk, sv = synth.sink_kv(w, g, "cuda")
             ring.set_sink(0, sk, sv)

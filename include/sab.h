@@ -66,7 +66,20 @@ typedef enum {
   SAB_ERR_TIMEOUT = 6        /* a device-side pipeline wait gave up (see sab_get_last_device_error) */
 } sab_status;
 
-typedef enum { SAB_KV_BF16 = 0, SAB_KV_FP8_E4M3 = 1 } sab_kv_dtype;
+/*
+ * KV cache element type.
+ *   SAB_KV_BF16        keys and values in bf16.
+ *   SAB_KV_FP8_E4M3    keys and values as E4M3 codes, one fp32 absmax scale
+ *                      (amax / 448) per (batch, head, chunk) and tensor.
+ *   SAB_KV_INT8K_FP8V  keys as INT8 codes with scale amax / 127 (symmetric,
+ *                      round half to even, clamped to +-127), values as E4M3
+ *                      codes with scale amax / 448 ("Matrix-Game 4.0", section
+ *                      "技术新颖性": each window interval caches INT8 keys and
+ *                      FP8 values; only the changed interval is re-quantised).
+ * Both 8-bit forms keep one byte per element in the ring and are expanded
+ * exactly to bf16 on chip; the scales are applied in fp32.
+ */
+typedef enum { SAB_KV_BF16 = 0, SAB_KV_FP8_E4M3 = 1, SAB_KV_INT8K_FP8V = 2 } sab_kv_dtype;
 
 /* Shape of one ring KV cache with `num_layers` independent per-layer rings. */
 typedef struct {
@@ -85,10 +98,10 @@ typedef struct sab_ring sab_ring; /* opaque host handle */
 /*
  * Device memory layout of a ring (informative; use sab_kv_ring_layer_ptrs):
  * per layer, 256-byte aligned regions
- *   K codes  [B][H][(has_sink + R) * Lc][D]   (bf16, or uint8 E4M3)
- *   V codes  same
- *   K scales [B][H][has_sink + R] fp32        (FP8 only)
- *   V scales same                             (FP8 only)
+ *   K codes  [B][H][(has_sink + R) * Lc][D]   (bf16, or one byte: E4M3 / INT8)
+ *   V codes  same                             (bf16, or one byte: E4M3)
+ *   K scales [B][H][has_sink + R] fp32        (8-bit forms only)
+ *   V scales same                             (8-bit forms only)
  * Rows [0, Lc) hold the sink when has_sink; slot r holds rows
  * [(has_sink + r) * Lc, (has_sink + r + 1) * Lc).
  */
@@ -139,7 +152,9 @@ sab_status sab_kv_ring_set_sink(sab_ring* ring, int layer, const void* K, const 
  * block of Lc x D values is quantised with amax = max |x|,
  * scale = amax / 448 (fp32, round-to-nearest division; 1 when amax = 0),
  * code = E4M3(x / scale) rounded to nearest even with saturation to +-448;
- * the scale is stored beside the slot.
+ * the scale is stored beside the slot.  An INT8K_FP8V ring quantises K the
+ * same way with scale = amax / 127 and code = round-half-even(x / scale)
+ * clamped to [-127, 127] (two's complement byte), and V as E4M3.
  * `chunk` must be >= 0 and, after the first append of that layer, equal to
  * the newest appended chunk (an in-place rewrite, e.g. the clean re-run of a
  * chunk) or one more.  Errors: INVALID_ARG, OUT_OF_RANGE (chunk order).
@@ -193,9 +208,10 @@ size_t sab_chunk_attention_workspace(const sab_ring* ring, int num_splits);
  *   LSE    device, [B, H, Lc] fp32, natural log of sum exp(s) (output; may be NULL).
  *   workspace/ws_bytes  device scratch, >= sab_chunk_attention_workspace.
  * Every chunk in max(0, c-W) .. c-1 (and c itself when K_cur is NULL) must be
- * held by the ring: OUT_OF_RANGE otherwise.  With an FP8 ring the kernel
- * expands the E4M3 codes times their per-(batch, head, chunk) scale to bf16
- * on chip (exact) and applies the scales in fp32 (the K scale to the scores,
+ * held by the ring: OUT_OF_RANGE otherwise.  With an 8-bit ring (FP8_E4M3
+ * or INT8K_FP8V) the kernel expands the codes to bf16 on chip (exact: every
+ * E4M3 value and every integer in [-127, 127] is a bf16 value) and applies
+ * the per-(batch, head, chunk) scales in fp32 (the K scale to the scores,
  * the V scale to the probabilities); this path needs head_dim 128,
  * chunk_tokens >= 128 and K_cur == V_cur == NULL (append the current chunk
  * first): UNSUPPORTED otherwise.  Device-side pipeline waits are

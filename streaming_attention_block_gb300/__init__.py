@@ -10,6 +10,7 @@ is missing.
 from ._abi import (  # noqa: F401
     KV_BF16,
     KV_FP8_E4M3,
+    KV_INT8K_FP8V,
     KVRing,
     RingDesc,
     SabError,

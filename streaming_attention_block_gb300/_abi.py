@@ -13,6 +13,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 KV_BF16 = 0
 KV_FP8_E4M3 = 1
+KV_INT8K_FP8V = 2
 
 _STATUS = {
     0: "SAB_OK", 1: "SAB_ERR_INVALID_ARG", 2: "SAB_ERR_UNSUPPORTED", 3: "SAB_ERR_OUT_OF_RANGE",
@@ -255,7 +256,7 @@ class KVRing:
         """(K, V, K_scale, V_scale) torch views of one layer's ring memory."""
         d = self.desc
         k, v, ks, vs = kv_ring_layer_ptrs(self.handle, layer)
-        fp8 = d.kv_dtype == KV_FP8_E4M3
+        fp8 = d.kv_dtype != KV_BF16  # one byte per element (E4M3, or INT8 keys)
         dt, es = (torch.uint8, 1) if fp8 else (torch.bfloat16, 2)
         shape = (d.batch, d.heads, self.rows, d.head_dim)
         n = d.batch * d.heads * self.rows * d.head_dim * es

@@ -204,6 +204,43 @@ __device__ __forceinline__ void kv_range(const AttnParams& p, int q0, int qrows,
   count = (int)(e - a);
 }
 
+// Expand one key/value row of 128 8-bit codes in place into 128 bf16 values.
+// The codes sit in the second 128-byte box of the row (where its upper bf16
+// half goes); all of them are read before any bf16 chunk is written, and the
+// bf16 row is written in the 128-byte-swizzled layout of the MMA operands.
+// E4M3 codes and INT8 codes (K8) both convert exactly.
+template <bool K8>
+__device__ __forceinline__ void expand_code_row(uint8_t* tile, int r, uint32_t box_bytes) {
+  const uint4* src = reinterpret_cast<const uint4*>(tile + box_bytes + r * 128);
+  uint4 raw[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) raw[i] = src[i];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+    uint32_t out[8];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if constexpr (K8) {
+        s8x4_to_bf16x4(w[q], out[2 * q], out[2 * q + 1]);
+      } else {
+        float a0, a1, a2, a3;
+        e4m3x2_to_f32x2((uint16_t)(w[q] & 0xFFFFu), a0, a1);
+        e4m3x2_to_f32x2((uint16_t)(w[q] >> 16), a2, a3);
+        out[2 * q] = pack_bf16(a0, a1);  // exact: every E4M3 value is a bf16 value
+        out[2 * q + 1] = pack_bf16(a2, a3);
+      }
+    }
+    // codes 16i .. 16i+15 -> 16-byte chunks 2i, 2i+1 of the bf16 row
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int k = 2 * i + hh;
+      *reinterpret_cast<uint4*>(tile + (k >> 3) * box_bytes + r * 128 + (((k & 7) ^ (r & 7)) << 4)) =
+          make_uint4(out[4 * hh], out[4 * hh + 1], out[4 * hh + 2], out[4 * hh + 3]);
+    }
+  }
+}
+
 template <int D, int QT, bool FP8>
 __global__ void __launch_bounds__(Cfg<D, QT, FP8>::kThreads, 1)
 chunk_attn_kernel(const __grid_constant__ AttnParams p) {
@@ -350,30 +387,8 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
         const int r = job & (kTileN - 1);
         const bool isv = job >= kTileN;
         uint8_t* tile = base + (isv ? C::kVOff : C::kKOff) + st * C::kTileBytes;
-        const uint4* src = reinterpret_cast<const uint4*>(tile + C::kBoxBytes + r * 128);
-        uint4 raw[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) raw[i] = src[i];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
-          uint32_t out[8];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            float a0, a1, a2, a3;
-            e4m3x2_to_f32x2((uint16_t)(w[q] & 0xFFFFu), a0, a1);
-            e4m3x2_to_f32x2((uint16_t)(w[q] >> 16), a2, a3);
-            out[2 * q] = pack_bf16(a0, a1);  // exact: every E4M3 value is a bf16 value
-            out[2 * q + 1] = pack_bf16(a2, a3);
-          }
-          // codes 16i .. 16i+15 -> 16-byte chunks 2i, 2i+1 of the bf16 row
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const int k = 2 * i + hh;
-            *reinterpret_cast<uint4*>(tile + (k >> 3) * C::kBoxBytes + r * 128 + (((k & 7) ^ (r & 7)) << 4)) =
-                make_uint4(out[4 * hh], out[4 * hh + 1], out[4 * hh + 2], out[4 * hh + 3]);
-          }
-        }
+        if (p.k_int8 && !isv) expand_code_row<true>(tile, r, C::kBoxBytes);  // INT8 keys
+        else expand_code_row<false>(tile, r, C::kBoxBytes);
       }
       fence_proxy_async_smem();
       mbar_arrive(bar(C::kBarKFull + st));
@@ -1237,29 +1252,8 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
         const int r = job & (kTileN - 1);
         const bool isv = job >= kTileN;
         uint8_t* tile = base + (isv ? C::kVOff : C::kKOff) + st * C::kTileBytes;
-        const uint4* src = reinterpret_cast<const uint4*>(tile + C::kBoxBytes + r * 128);
-        uint4 raw[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) raw[i] = src[i];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
-          uint32_t out[8];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            float a0, a1, a2, a3;
-            e4m3x2_to_f32x2((uint16_t)(w[q] & 0xFFFFu), a0, a1);
-            e4m3x2_to_f32x2((uint16_t)(w[q] >> 16), a2, a3);
-            out[2 * q] = pack_bf16(a0, a1);
-            out[2 * q + 1] = pack_bf16(a2, a3);
-          }
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const int k = 2 * i + hh;
-            *reinterpret_cast<uint4*>(tile + (k >> 3) * C::kBoxBytes + r * 128 + (((k & 7) ^ (r & 7)) << 4)) =
-                make_uint4(out[4 * hh], out[4 * hh + 1], out[4 * hh + 2], out[4 * hh + 3]);
-          }
-        }
+        if (p.k_int8 && !isv) expand_code_row<true>(tile, r, C::kBoxBytes);  // INT8 keys
+        else expand_code_row<false>(tile, r, C::kBoxBytes);
       }
       fence_proxy_async_smem();
       mbar_arrive(bar(C::kBarKFull + st));

@@ -14,7 +14,9 @@
 // scale = amax / 448 (IEEE round-to-nearest division) and E4M3 codes rounded
 // to nearest even with saturation ("Matrix-Game 4.0", section "技术新颖性":
 // 8-bit keys/values per window interval, only the changed interval is
-// re-quantised -- here the changed interval is the appended chunk).
+// re-quantised -- here the changed interval is the appended chunk).  An
+// INT8-key ring quantises K with scale = amax / 127 and codes rounded half to
+// even, clamped to [-127, 127] (the same section: INT8 keys, FP8 values).
 #include "ptx.cuh"
 #include "sab_internal.h"
 
@@ -58,11 +60,19 @@ __device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
   return r;
 }
 
+// One fp32 -> INT8 code: round half to even, clamp to the symmetric range.
+__device__ __forceinline__ uint32_t s8_code(float y) {
+  int q;
+  asm("cvt.rni.s32.f32 %0, %1;" : "=r"(q) : "f"(y));
+  return (uint32_t)(min(max(q, -127), 127)) & 0xFFu;
+}
+
 __global__ void __launch_bounds__(kAppendThreads)
 append_fp8_kernel(const __grid_constant__ AppendParams p) {
   ptx::griddep_launch_dependents();
   ptx::griddep_wait();  // the slot may still be read by the previous kernel
   const int tensor = blockIdx.x;
+  const bool int8 = p.k_int8 && tensor == 0;  // block-uniform
   const int bh = blockIdx.y;
   const int b = bh / p.H, h = bh % p.H;
   const int vec_per_row = p.D / 8;
@@ -90,7 +100,7 @@ append_fp8_kernel(const __grid_constant__ AppendParams p) {
   if (threadIdx.x == 0) {
     float m = 0.f;
     for (int w = 0; w < (int)(blockDim.x >> 5); ++w) m = fmaxf(m, red[w]);
-    const float sc = (m == 0.f) ? 1.0f : __fdiv_rn(m, 448.0f);
+    const float sc = (m == 0.f) ? 1.0f : __fdiv_rn(m, int8 ? 127.0f : 448.0f);
     s_scale = sc;
     p.scale[tensor][(long long)bh * p.scale_stride + p.scale_idx] = sc;
   }
@@ -102,11 +112,19 @@ append_fp8_kernel(const __grid_constant__ AppendParams p) {
     const uint4 x = src_vec(v);
     const uint32_t w[4] = {x.x, x.y, x.z, x.w};
     uint32_t out[2];
+    if (int8) {
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const uint16_t c0 = e4m3x2(__fdiv_rn(bf16_lo(w[2 * k]), sc), __fdiv_rn(bf16_hi(w[2 * k]), sc));
-      const uint16_t c1 = e4m3x2(__fdiv_rn(bf16_lo(w[2 * k + 1]), sc), __fdiv_rn(bf16_hi(w[2 * k + 1]), sc));
-      out[k] = (uint32_t)c0 | ((uint32_t)c1 << 16);
+      for (int k = 0; k < 2; ++k)
+        out[k] = s8_code(__fdiv_rn(bf16_lo(w[2 * k]), sc)) | (s8_code(__fdiv_rn(bf16_hi(w[2 * k]), sc)) << 8) |
+                 (s8_code(__fdiv_rn(bf16_lo(w[2 * k + 1]), sc)) << 16) |
+                 (s8_code(__fdiv_rn(bf16_hi(w[2 * k + 1]), sc)) << 24);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const uint16_t c0 = e4m3x2(__fdiv_rn(bf16_lo(w[2 * k]), sc), __fdiv_rn(bf16_hi(w[2 * k]), sc));
+        const uint16_t c1 = e4m3x2(__fdiv_rn(bf16_lo(w[2 * k + 1]), sc), __fdiv_rn(bf16_hi(w[2 * k + 1]), sc));
+        out[k] = (uint32_t)c0 | ((uint32_t)c1 << 16);
+      }
     }
     const int t = v / vec_per_row, c = v % vec_per_row;
     *reinterpret_cast<uint2*>(dst + (long long)t * p.D + c * 8) = make_uint2(out[0], out[1]);

@@ -233,6 +233,24 @@ __device__ __forceinline__ void e4m3x2_to_f32x2(uint16_t codes, float& lo, float
   asm("cvt.f32.f16 %0, %1;" : "=f"(lo) : "h"(a));
   asm("cvt.f32.f16 %0, %1;" : "=f"(hi) : "h"(b));
 }
+// Four INT8 codes (two's complement bytes, low byte first) -> four bf16
+// values, exactly: each byte, offset by 128, becomes the low mantissa bits of
+// 2^23 + (n + 128); subtracting 2^23 + 128 in fp32 leaves n exactly, and an
+// integer of magnitude <= 128 keeps all its bits in the upper half of its
+// fp32 pattern (the bf16).  `lo` holds codes 0, 1; `hi` codes 2, 3.
+__device__ __forceinline__ void s8x4_to_bf16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t t = w ^ 0x80808080u;
+  uint32_t x0, x1, x2, x3;
+  asm("prmt.b32 %0, %1, %2, 0x7650;" : "=r"(x0) : "r"(t), "r"(0x4B000000u));
+  asm("prmt.b32 %0, %1, %2, 0x7651;" : "=r"(x1) : "r"(t), "r"(0x4B000000u));
+  asm("prmt.b32 %0, %1, %2, 0x7652;" : "=r"(x2) : "r"(t), "r"(0x4B000000u));
+  asm("prmt.b32 %0, %1, %2, 0x7653;" : "=r"(x3) : "r"(t), "r"(0x4B000000u));
+  const float2 bias = make_float2(-8388736.0f, -8388736.0f);  // -(2^23 + 128)
+  const float2 f01 = __fadd2_rn(make_float2(__uint_as_float(x0), __uint_as_float(x1)), bias);
+  const float2 f23 = __fadd2_rn(make_float2(__uint_as_float(x2), __uint_as_float(x3)), bias);
+  asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(lo) : "r"(__float_as_uint(f01.x)), "r"(__float_as_uint(f01.y)));
+  asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(hi) : "r"(__float_as_uint(f23.x)), "r"(__float_as_uint(f23.y)));
+}
 // three-input maximum
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float r;

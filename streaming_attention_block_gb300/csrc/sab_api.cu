@@ -86,7 +86,8 @@ bool valid_desc(const sab_ring_desc* d) {
     return false;
   if (d->head_dim != 64 && d->head_dim != 128) return false;
   if (d->has_sink != 0 && d->has_sink != 1) return false;
-  if (d->kv_dtype != SAB_KV_BF16 && d->kv_dtype != SAB_KV_FP8_E4M3) return false;
+  if (d->kv_dtype != SAB_KV_BF16 && d->kv_dtype != SAB_KV_FP8_E4M3 && d->kv_dtype != SAB_KV_INT8K_FP8V)
+    return false;
   const long long rows = (long long)(d->has_sink + d->ring_slots) * d->chunk_tokens;
   if (rows > (1LL << 30)) return false;
   if ((long long)d->batch * d->heads * rows * d->head_dim > (1LL << 40)) return false;
@@ -105,7 +106,7 @@ Geometry geometry(const sab_ring_desc& d) {
   g.rows = (long long)(d.has_sink + d.ring_slots) * d.chunk_tokens;
   const size_t esize = d.kv_dtype == SAB_KV_BF16 ? 2 : 1;
   g.codes_bytes = align_up((size_t)d.batch * d.heads * g.rows * d.head_dim * esize, kAlign);
-  g.scale_bytes = d.kv_dtype == SAB_KV_FP8_E4M3
+  g.scale_bytes = d.kv_dtype != SAB_KV_BF16
                       ? align_up((size_t)d.batch * d.heads * (d.has_sink + d.ring_slots) * sizeof(float), kAlign)
                       : 0;
   g.layer_bytes = 2 * g.codes_bytes + 2 * g.scale_bytes;
@@ -211,7 +212,7 @@ sab_status sab_kv_ring_create(const sab_ring_desc* desc, void* dev_mem, size_t b
   r->sink_set.assign(desc->num_layers, 0);
   r->kmap.resize(desc->num_layers);
   r->vmap.resize(desc->num_layers);
-  const bool fp8 = desc->kv_dtype == SAB_KV_FP8_E4M3;
+  const bool fp8 = desc->kv_dtype != SAB_KV_BF16;  // one byte per element
   for (int l = 0; l < desc->num_layers; ++l) {
     const int B = desc->batch, H = desc->heads, D = desc->head_dim;
     const bool okm = fp8 ? (encode_head_major_u8(&r->kmap[l], r->k(l), B, H, r->g.rows, D) &&
@@ -270,6 +271,7 @@ static sab_status write_chunk(sab_ring* r, int layer, int slot_row0, int scale_i
   p.slot_row0 = slot_row0;
   p.scale_idx = scale_idx;
   p.scale_stride = r->d.has_sink + r->d.ring_slots;
+  p.k_int8 = r->d.kv_dtype == SAB_KV_INT8K_FP8V ? 1 : 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const cudaError_t e = r->d.kv_dtype == SAB_KV_BF16 ? launch_append_bf16(p, s) : launch_append_fp8(p, s);
   return e == cudaSuccess ? SAB_OK : SAB_ERR_CUDA;
@@ -420,8 +422,8 @@ static sab_status plan_chunk_attention(const sab_ring* ring, int layer, long lon
   if (use_sink && !d.has_sink) return SAB_ERR_INVALID_ARG;
   if (use_sink && !ring->sink_set[layer]) return SAB_ERR_OUT_OF_RANGE;
   const bool kcur = K_cur != nullptr;
-  const bool fp8 = d.kv_dtype == SAB_KV_FP8_E4M3;
-  // The FP8 cache path expands 128-byte code rows in place (D = 128), reads
+  const bool fp8 = d.kv_dtype != SAB_KV_BF16;
+  // The 8-bit cache path expands 128-byte code rows in place (D = 128), reads
   // every key from the ring (the current chunk is appended first) and needs
   // chunks of at least 128 tokens (a key tile spans at most two chunks).
   if (fp8 && (kcur || d.head_dim != 128 || d.chunk_tokens < kTileN)) return SAB_ERR_UNSUPPORTED;
@@ -457,6 +459,7 @@ static sab_status plan_chunk_attention(const sab_ring* ring, int layer, long lon
   memset(&p, 0, sizeof(p));
   p.mode = kModeStreaming;
   p.fp8 = fp8 ? 1 : 0;
+  p.k_int8 = d.kv_dtype == SAB_KV_INT8K_FP8V ? 1 : 0;
   p.k_scale = ring->ks(layer);
   p.v_scale = ring->vs(layer);
   p.scale_stride = d.has_sink + d.ring_slots;

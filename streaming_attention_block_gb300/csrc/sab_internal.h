@@ -30,7 +30,8 @@ struct AttnParams {
   CUtensorMap v_map[2];
   CUtensorMap o_map;      // output, dims (D, Lq, H, B), box (64, 128, 1, 1), SW128
   int mode;
-  int fp8;                // 1: the ring holds E4M3 codes (k_map[0]/v_map[0] are uint8 maps)
+  int fp8;                // 1: the ring holds 8-bit codes (k_map[0]/v_map[0] are uint8 maps)
+  int k_int8;             // with fp8: keys are INT8 codes (values stay E4M3)
   const float* k_scale;   // FP8: [B*H][scale_stride] fp32 scales, index = ring row / chunk_tokens
   const float* v_scale;
   int scale_stride;
@@ -73,6 +74,7 @@ struct AppendParams {
   int slot_row0;            // first row of the destination slot
   int scale_idx;            // (has_sink + slot) or 0 for the sink
   int scale_stride;         // has_sink + R
+  int k_int8;               // 8-bit ring: K as INT8 (amax / 127) instead of E4M3
 };
 
 // Launchers (return cudaError_t of the launch).

@@ -20,6 +20,8 @@ Workloads (shapes from the pages, values synthetic: no page publishes data):
   30720 tokens, H=12, D=128, window 2.
 * ``fp8_kv``: ``long_sink`` with an E4M3 KV cache; K/V drawn N(0,1) with 1% of
   entries multiplied by 8 (outliers).
+* ``int8k_kv``: ``fp8_kv`` with INT8 keys and E4M3 values ("Matrix-Game 4.0",
+  section "技术新颖性": INT8 keys, FP8 values per window interval).
 
 All values are N(0,1) fp32 draws rounded to bf16.  Draw order for a stream:
 for each chunk, for each denoise step, for each layer: Q, then K, then V.
@@ -47,7 +49,8 @@ class Workload:
     sink: bool = False
     kcur_separate: bool = True   # True: current chunk passed in; False: appended first
     splits: int = 1
-    kv_fp8: bool = False
+    kv_fp8: bool = False          # 8-bit cache (E4M3 keys and values, or INT8 keys with kv_int8k)
+    kv_int8k: bool = False
     rms_norm: bool = False
     outliers: bool = False
     seq_chunks: int = 0     # full-sequence mode: chunks per sequence
@@ -68,6 +71,8 @@ WORKLOADS = {
                              seed=1004),
     "fp8_kv": Workload("fp8_kv", B=1, H=24, D=128, Lc=405, R=20, W=19, chunks=60, sink=True,
                        kcur_separate=False, splits=8, kv_fp8=True, outliers=True, seed=1005),
+    "int8k_kv": Workload("int8k_kv", B=1, H=24, D=128, Lc=405, R=20, W=19, chunks=60, sink=True,
+                         kcur_separate=False, splits=8, kv_fp8=True, kv_int8k=True, outliers=True, seed=1006),
 }
 
 

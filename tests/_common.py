@@ -8,6 +8,7 @@ import torch
 
 from oracle import attention as OA
 from oracle import fp8 as OF
+from oracle import int8 as OI
 from oracle.ring import ListRing
 from streaming_attention_block_gb300 import synth
 
@@ -59,14 +60,19 @@ def compare(O_gpu: torch.Tensor, LSE_gpu: torch.Tensor, O_ref: np.ndarray, L_ref
     return d.max(), d.mean(), dl.max()
 
 
-def oracle_kv(k_blhd: torch.Tensor, v_blhd: torch.Tensor, fp8: bool):
-    """What the oracle caches for a chunk: bf16 values, or the dequantised E4M3
-    values of the per-(b, h) absmax quantiser."""
+def oracle_kv(k_blhd: torch.Tensor, v_blhd: torch.Tensor, fp8: bool, int8k: bool = False):
+    """What the oracle caches for a chunk: bf16 values, or the dequantised codes
+    of the per-(b, h) absmax quantisers (E4M3 keys, or INT8 keys with
+    ``int8k``; E4M3 values)."""
     if not fp8:
         return bhld(k_blhd), bhld(v_blhd)
-    kc, ks = OF.quantize_chunk_bhld(f64(k_blhd).astype(np.float32))
+    if int8k:
+        kc, ks = OI.quantize_chunk_bhld(f64(k_blhd).astype(np.float32))
+        kd = kc.astype(np.float64) * ks.astype(np.float64)[:, :, None, None]
+    else:
+        kc, ks = OF.quantize_chunk_bhld(f64(k_blhd).astype(np.float32))
+        kd = OF.e4m3_decode(kc) * ks.astype(np.float64)[:, :, None, None]
     vc, vs = OF.quantize_chunk_bhld(f64(v_blhd).astype(np.float32))
-    kd = OF.e4m3_decode(kc) * ks.astype(np.float64)[:, :, None, None]
     vd = OF.e4m3_decode(vc) * vs.astype(np.float64)[:, :, None, None]
     return kd, vd
 
@@ -84,6 +90,7 @@ def run_stream(w, ring, check_chunks, rows=None, layers=1, splits=None, device="
     (chunk, step, layer, max|dO|, mean|dO|, max|dLSE|).
     """
     fp8 = bool(w.kv_fp8)
+    i8 = bool(w.kv_int8k)
     splits = w.splits if splits is None else splits
     gen = synth.generator(w.seed)
     orings = [ListRing(w.R) for _ in range(layers)]
@@ -94,7 +101,7 @@ def run_stream(w, ring, check_chunks, rows=None, layers=1, splits=None, device="
         sk, sv = synth.sink_kv(w, gen)
         for l in range(layers):
             ring.set_sink(l, sk.to(device), sv.to(device))
-            orings[l].set_sink(*oracle_kv(sk, sv, fp8))
+            orings[l].set_sink(*oracle_kv(sk, sv, fp8, i8))
             orings_raw[l].set_sink(bhld(sk), bhld(sv))
     rsel = slice(None) if rows is None else rows
     save_step = max(0, w.steps - 2)
@@ -106,7 +113,7 @@ def run_stream(w, ring, check_chunks, rows=None, layers=1, splits=None, device="
                 qd, kd, vd = q.to(device), k.to(device), v.to(device)
                 if not w.kcur_separate:
                     ring.append(l, c, kd, vd)
-                    orings[l].append(c, *oracle_kv(k, v, fp8))
+                    orings[l].append(c, *oracle_kv(k, v, fp8, i8))
                     orings_raw[l].append(c, bhld(k), bhld(v))
                     O, LSE = ring.attention(l, c, qd, None, None, window=w.W, use_sink=w.sink,
                                             num_splits=splits, workspace=ws)
@@ -133,6 +140,6 @@ def run_stream(w, ring, check_chunks, rows=None, layers=1, splits=None, device="
             for l in range(layers):
                 k, v, kd, vd = saved[l]
                 ring.append(l, c, kd, vd)
-                orings[l].append(c, *oracle_kv(k, v, fp8))
+                orings[l].append(c, *oracle_kv(k, v, fp8, i8))
                 orings_raw[l].append(c, bhld(k), bhld(v))
     return results, orings

@@ -53,6 +53,8 @@ def test_ring_bytes(lib):
     codes_al = (codes + 255) // 256 * 256
     scales_al = (24 * 21 * 4 + 255) // 256 * 256
     assert sab.kv_ring_bytes(d8) == 2 * codes_al + 2 * scales_al
+    # INT8 keys / E4M3 values: the same byte layout
+    assert sab.kv_ring_bytes(dict(d8, kv_dtype=sab.KV_INT8K_FP8V)) == 2 * codes_al + 2 * scales_al
     for bad in (dict(d, head_dim=96), dict(d, ring_slots=0), dict(d, kv_dtype=7), dict(d, has_sink=2)):
         assert sab.kv_ring_bytes(bad) == 0
 
