@@ -265,6 +265,38 @@ def run_ours(args):
     h2d = S * L * 3 * B * Lc * H * D * 2
     d2h = S * L * (B * Lc * H * D * 2 + B * H * Lc * 4)
 
+    # ---------------- graph replay: one chunk step captured once with the
+    # device-indexed calls (chunk index in device memory), replayed per chunk
+    graph = None
+    if not args.no_graph:
+        d_chunk = torch.full((1,), chunk, dtype=torch.int64, device=dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            gs = torch.cuda.current_stream()
+            for s in range(S):
+                for l in range(L):
+                    sab.chunk_attention_dev(ring.handle, l, d_chunk, Q[s][l], Kc[s][l], Vc[s][l], w.W, False,
+                                            args.splits, w.scale, O[s][l], LSE[s][l], work, gs)
+            for l in range(L):
+                sab.kv_ring_append_dev(ring.handle, l, d_chunk, Kc[save][l], Vc[save][l], gs)
+            sab.chunk_counter_add(d_chunk, 1, gs)
+        for _ in range(max(3, args.warmup)):
+            g.replay()
+        barrier()
+        g0 = torch.cuda.Event(enable_timing=True)
+        g1 = torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(args.steps):
+            g.replay()
+        g1.record(stream)
+        barrier()
+        g_ms = g0.elapsed_time(g1)
+        status = sab.get_last_device_error(stream)
+        if status != 0:
+            raise RuntimeError(f"device error {sab.status_string(status)}")
+        graph = {"value": round(args.steps * ws / (g_ms / 1e3), 3), "unit": "chunks/s",
+                 "ms_per_step": round(g_ms / args.steps, 4), "kernels_per_replay": S * L + L + 1}
+
     if pg is not None:
         t = torch.tensor([ms, e2e_ms], device=dev, dtype=torch.float64)
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
@@ -299,6 +331,8 @@ def run_ours(args):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "clocks": clk.summary(),
     }
+    if graph is not None:
+        line["graph_replay"] = graph
     if cpu is not None:
         line["cpu_baseline"] = cpu
     if rank == 0:
@@ -512,6 +546,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--no-graph", action="store_true", help="skip the graph-replay measurement")
     ap.add_argument("--splits", type=int, default=0, help="KV splits per attention call (0: library's choice)")
     ap.add_argument("--sweep", action="store_true", help="time one attention call of every workload")
     ap.add_argument("--attn-only", type=int, default=0, metavar="N",

@@ -223,6 +223,42 @@ sab_status sab_chunk_attention(const sab_ring* ring, int layer, long long chunk,
                                void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * Graph-capturable streaming ("Matrix-Game 4.0", section "前置知识 / FP8 量化
+ * 与 CUDA Graph": a whole chunk's GPU work is recorded once as a graph and
+ * replayed with one launch per chunk, removing the per-kernel CPU launch
+ * cost).  The three calls below read the chunk index from `d_chunk`, one
+ * int64 in device memory, when their kernels run -- not when they are
+ * launched -- so a chunk step (every layer's and denoise step's attention,
+ * the ring appends and one sab_chunk_counter_add) captured once with
+ * cudaStreamBeginCapture on `stream` replays correctly for every later chunk.
+ *
+ * sab_chunk_attention_dev: as sab_chunk_attention for chunk *d_chunk.  The
+ *   key set is planned on the device by the same rule; the caller guarantees
+ *   the stream discipline the host check enforces for sab_chunk_attention
+ *   (every chunk the window needs was appended, in order, through
+ *   sab_kv_ring_append_dev; *d_chunk >= 0).  Checked at the call: everything
+ *   independent of the chunk, and that the window fits the ring (window <= R
+ *   with K_cur, <= R - 1 without).  A chunk index that breaks the discipline
+ *   gives wrong results but no out-of-range access: every key row read lies
+ *   inside the layer's ring.  num_splits 0 sizes the automatic choice for a
+ *   full window.
+ * sab_kv_ring_append_dev: as sab_kv_ring_append into slot (*d_chunk mod R).
+ *   The host handle's chunk bookkeeping (sab_kv_ring_get_state, the order
+ *   check of sab_kv_ring_append) is not updated: drive a ring either through
+ *   the _dev calls or through the host-indexed calls, not both.
+ * sab_chunk_counter_add: *d_chunk += delta, as a kernel on `stream` (ordered
+ *   after the work before it on the stream).
+ * d_chunk: device pointer, 8-byte aligned; INVALID_ARG otherwise.
+ */
+sab_status sab_chunk_attention_dev(const sab_ring* ring, int layer, const long long* d_chunk, const void* Q,
+                                   const void* K_cur, const void* V_cur, int window, int use_sink, int num_splits,
+                                   float softmax_scale, void* O, float* LSE, void* workspace, size_t ws_bytes,
+                                   void* stream);
+sab_status sab_kv_ring_append_dev(sab_ring* ring, int layer, const long long* d_chunk, const void* K,
+                                  const void* V, void* stream);
+sab_status sab_chunk_counter_add(long long* d_chunk, long long delta, void* stream);
+
+/*
  * sab_chunk_attention without a caller workspace.  The method itself has no
  * counterpart of this entry point; it exists for callers that cannot
  * allocate device memory -- for instance a plugin whose host application

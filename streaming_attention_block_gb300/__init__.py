@@ -17,10 +17,13 @@ from ._abi import (  # noqa: F401
     block_causal_attention,
     block_causal_attention_workspace,
     chunk_attention,
+    chunk_attention_dev,
     chunk_attention_noalloc,
+    chunk_counter_add,
     chunk_attention_workspace,
     get_last_device_error,
     kv_ring_append,
+    kv_ring_append_dev,
     kv_ring_bytes,
     kv_ring_create,
     kv_ring_destroy,

@@ -66,6 +66,9 @@ def library() -> ctypes.CDLL:
         "sab_chunk_attention_workspace": (SZ, [P, I]),
         "sab_chunk_attention": (I, [P, I, LL, P, P, P, I, I, I, F, P, P, P, SZ, P]),
         "sab_chunk_attention_noalloc": (I, [P, I, LL, P, P, P, I, I, I, F, P, P, P]),
+        "sab_chunk_attention_dev": (I, [P, I, P, P, P, P, I, I, I, F, P, P, P, SZ, P]),
+        "sab_kv_ring_append_dev": (I, [P, I, P, P, P, P]),
+        "sab_chunk_counter_add": (I, [P, LL, P]),
         "sab_block_causal_attention_workspace": (SZ, [I, I, I, I, I]),
         "sab_block_causal_attention": (I, [P, P, P, I, I, I, I, I, I, I, F, P, P, P, SZ, P]),
         "sab_get_last_device_error": (I, [P]),
@@ -205,6 +208,33 @@ def chunk_attention_noalloc(handle, layer: int, chunk: int, Q, K_cur, V_cur, win
         _ptr(V_cur, torch.bfloat16, "V_cur"), int(window), int(bool(use_sink)), int(num_splits),
         float(softmax_scale), _ptr(O, torch.bfloat16, "O"), _ptr(LSE, torch.float32, "LSE"), _stream(stream)),
         "chunk_attention_noalloc")
+
+
+def chunk_attention_dev(handle, layer: int, d_chunk, Q, K_cur, V_cur, window: int, use_sink: bool,
+                        num_splits: int, softmax_scale: float, O, LSE=None, workspace=None, stream=None):
+    """sab_chunk_attention_dev: the chunk index is read from ``d_chunk`` (a
+    device int64 tensor) when the kernel runs, so the call can be captured
+    once in a CUDA graph and replayed for every chunk (see include/sab.h)."""
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(library().sab_chunk_attention_dev(
+        handle, int(layer), _ptr(d_chunk, torch.int64, "d_chunk"), _ptr(Q, torch.bfloat16, "Q"),
+        _ptr(K_cur, torch.bfloat16, "K_cur"), _ptr(V_cur, torch.bfloat16, "V_cur"), int(window),
+        int(bool(use_sink)), int(num_splits), float(softmax_scale), _ptr(O, torch.bfloat16, "O"),
+        _ptr(LSE, torch.float32, "LSE"), _ptr(workspace, None, "workspace"), ws_bytes, _stream(stream)),
+        "chunk_attention_dev")
+
+
+def kv_ring_append_dev(handle, layer: int, d_chunk, K, V, stream=None):
+    """sab_kv_ring_append_dev: append into slot (*d_chunk mod R), chunk read on the device."""
+    _check(library().sab_kv_ring_append_dev(handle, int(layer), _ptr(d_chunk, torch.int64, "d_chunk"),
+                                            _ptr(K, torch.bfloat16, "K"), _ptr(V, torch.bfloat16, "V"),
+                                            _stream(stream)), "kv_ring_append_dev")
+
+
+def chunk_counter_add(d_chunk, delta: int = 1, stream=None):
+    """sab_chunk_counter_add: *d_chunk += delta on the stream."""
+    _check(library().sab_chunk_counter_add(_ptr(d_chunk, torch.int64, "d_chunk"), int(delta), _stream(stream)),
+           "chunk_counter_add")
 
 
 def block_causal_attention_workspace(B: int, L: int, H: int, D: int, num_splits: int) -> int:

@@ -160,21 +160,21 @@ struct Tile {
   int valid;  // keys of the run inside this tile (streaming); 128 otherwise
 };
 
-__device__ __forceinline__ Tile stream_tile(const AttnParams& p, int g) {
+__device__ __forceinline__ Tile stream_tile(const KeyPlan& kp, int g) {
   int s = 0;
 #pragma unroll
   for (int i = 1; i < kMaxSegments; ++i)
-    if (i < p.nseg && g >= p.seg[i].tile0) s = i;
-  const int t = g - p.seg[s].tile0;
+    if (i < kp.nseg && g >= kp.seg[i].tile0) s = i;
+  const int t = g - kp.seg[s].tile0;
   Tile ti;
-  ti.src = p.seg[s].src;
-  ti.row = p.seg[s].row0 + t * kTileN;
-  ti.valid = min(kTileN, p.seg[s].nrows - t * kTileN);
+  ti.src = kp.seg[s].src;
+  ti.row = kp.seg[s].row0 + t * kTileN;
+  ti.valid = min(kTileN, kp.seg[s].nrows - t * kTileN);
   return ti;
 }
 
-__device__ __forceinline__ Tile tile_at(const AttnParams& p, int g) {
-  if (p.mode == kModeStreaming) return stream_tile(p, g);
+__device__ __forceinline__ Tile tile_at(const AttnParams& p, const KeyPlan& kp, int g) {
+  if (p.mode == kModeStreaming) return stream_tile(kp, g);
   Tile ti;
   ti.src = 0;
   ti.row = g * kTileN;
@@ -183,11 +183,11 @@ __device__ __forceinline__ Tile tile_at(const AttnParams& p, int g) {
 }
 
 // KV tiles of this CTA: [first, first + count).
-__device__ __forceinline__ void kv_range(const AttnParams& p, int q0, int qrows, int split,
+__device__ __forceinline__ void kv_range(const AttnParams& p, const KeyPlan& kp, int q0, int qrows, int split,
                                          int& first, int& count) {
   int total = 0, base = 0;
   if (p.mode == kModeStreaming) {
-    total = p.total_tiles;
+    total = kp.total_tiles;
   } else {
     const int q_last = min(p.Lq, q0 + qrows) - 1;
     if (q_last >= q0) {
@@ -268,8 +268,6 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
   const int h = bh - b * p.H;
   const int q0 = qg * QT * kTileM;
 
-  int first = 0, n_tiles = 0;
-  kv_range(p, q0, QT * kTileM, split, first, n_tiles);
 
   if (threadIdx.x == 0) {
     mbar_init(bar(C::kBarQ), 1);
@@ -313,6 +311,15 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
   // the previous grid has completed.
   griddep_launch_dependents();
   griddep_wait();
+  // key runs: planned on the host, or (graph mode) by every thread from the
+  // chunk index in device memory, read only after the previous grid completed
+  KeyPlan kp;
+  if (p.mode == kModeStreaming && p.d_chunk != nullptr)
+    plan_key_runs(*p.d_chunk, p.window, p.ring_slots, p.chunk_tokens, p.has_sink, p.use_sink, p.kcur, kp);
+  else
+    kp = p.plan;
+  int first = 0, n_tiles = 0;
+  kv_range(p, kp, q0, QT * kTileM, split, first, n_tiles);
 
   // softmax-thread state handed to the cluster merge in the common tail
   bool sm_ok = false;
@@ -336,7 +343,7 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
         if (j >= C::kStages &&
             !wait_bounded(bar(C::kBarKVEmpty + st), (round - 1u) & 1u, abort_flag, 0))
           break;
-        const Tile ti = tile_at(p, first + j);
+        const Tile ti = tile_at(p, kp, first + j);
         if (FP8) {
           // E4M3 code rows (128 bytes each) land in the upper half of the bf16
           // stage buffers; the converter warps expand them in place
@@ -381,7 +388,7 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
     for (int j = 0; j < n_tiles; ++j) {
       const int st = j % C::kStages;
       if (!wait_bounded(bar(C::kBarRawFull + st), (uint32_t)(j / C::kStages) & 1u, abort_flag, 12)) break;
-      const int row0 = tile_at(p, first + j).row;
+      const int row0 = tile_at(p, kp, first + j).row;
 #pragma unroll 1
       for (int job = ct; job < 2 * kTileN; job += C::kConvThreads) {
         const int r = job & (kTileN - 1);
@@ -534,9 +541,9 @@ chunk_attn_kernel(const __grid_constant__ AttnParams p) {
     int seg_tile0[kMaxSegments], seg_rows[kMaxSegments], seg_row0[kMaxSegments];
 #pragma unroll
     for (int i = 0; i < kMaxSegments; ++i) {
-      seg_tile0[i] = (i < p.nseg) ? p.seg[i].tile0 : 0x7fffffff;
-      seg_rows[i] = p.seg[i].nrows;
-      seg_row0[i] = p.seg[i].row0;
+      seg_tile0[i] = (i < kp.nseg) ? kp.seg[i].tile0 : 0x7fffffff;
+      seg_rows[i] = kp.seg[i].nrows;
+      seg_row0[i] = kp.seg[i].row0;
     }
     const long long srow = (long long)bh * p.scale_stride;  // FP8 scale row of this (b, h)
     float m_run = -INFINITY, l_run = 0.f;
@@ -1152,8 +1159,6 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
   const int h = bh - b * p.H;
   const int q0 = blockIdx.x * kTileM;
 
-  int first = 0, n_tiles = 0;
-  kv_range(p, q0, kTileM, 0, first, n_tiles);
 
   if (threadIdx.x == 0) {
     mbar_init(bar(C::kBarQ), 1);
@@ -1190,6 +1195,15 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
   const uint32_t tmem = misc[0];
   griddep_launch_dependents();
   griddep_wait();
+  // key runs: planned on the host, or (graph mode) by every thread from the
+  // chunk index in device memory, read only after the previous grid completed
+  KeyPlan kp;
+  if (p.mode == kModeStreaming && p.d_chunk != nullptr)
+    plan_key_runs(*p.d_chunk, p.window, p.ring_slots, p.chunk_tokens, p.has_sink, p.use_sink, p.kcur, kp);
+  else
+    kp = p.plan;
+  int first = 0, n_tiles = 0;
+  kv_range(p, kp, q0, kTileM, 0, first, n_tiles);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -1205,8 +1219,8 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
             !wait_bounded(bar(C::kBarKVEmpty + st), (uint32_t)(u / C::kStages - 1) & 1u, abort_flag, 0))
           break;
         const bool has_k = u < n_tiles, has_v = u > 0;
-        const Tile tk = tile_at(p, first + (has_k ? u : u - 1));
-        const Tile tv = tile_at(p, first + (has_v ? u - 1 : u));
+        const Tile tk = tile_at(p, kp, first + (has_k ? u : u - 1));
+        const Tile tv = tile_at(p, kp, first + (has_v ? u - 1 : u));
         if (FP8) {
           mbar_arrive_expect_tx(bar(C::kBarRawFull + st), (has_k ? 128 * D : 0) + (has_v ? 128 * D : 0));
           if (has_k)
@@ -1369,9 +1383,9 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
     int seg_tile0[kMaxSegments], seg_rows[kMaxSegments], seg_row0[kMaxSegments];
 #pragma unroll
     for (int i = 0; i < kMaxSegments; ++i) {
-      seg_tile0[i] = (i < p.nseg) ? p.seg[i].tile0 : 0x7fffffff;
-      seg_rows[i] = p.seg[i].nrows;
-      seg_row0[i] = p.seg[i].row0;
+      seg_tile0[i] = (i < kp.nseg) ? kp.seg[i].tile0 : 0x7fffffff;
+      seg_rows[i] = kp.seg[i].nrows;
+      seg_row0[i] = kp.seg[i].row0;
     }
     const long long srow = (long long)bh * p.scale_stride;
     float m_run = -INFINITY, l_run = 0.f;

@@ -29,6 +29,11 @@ __global__ void __launch_bounds__(kAppendThreads)
 append_bf16_kernel(const __grid_constant__ AppendParams p) {
   ptx::griddep_launch_dependents();
   ptx::griddep_wait();  // the slot may still be read by the previous kernel
+  int slot_row0 = p.slot_row0;
+  if (p.d_chunk != nullptr) {  // graph mode: the chunk index lives on the device
+    const long long c = *p.d_chunk;
+    slot_row0 = (p.has_sink + (int)((c < 0 ? 0 : c) % p.ring_slots)) * p.Lc;
+  }
   const int vec_per_row = p.D / 8;  // 16-byte vectors per row
   const long long per_tensor = (long long)p.B * p.H * p.Lc * vec_per_row;
   const long long total = 2 * per_tensor;
@@ -45,7 +50,7 @@ append_bf16_kernel(const __grid_constant__ AppendParams p) {
         p.src[tensor] + (((long long)b * p.Lc + t) * p.H + h) * p.D) + vec;
     uint4* dst = reinterpret_cast<uint4*>(
         static_cast<uint16_t*>(p.dst[tensor]) +
-        (((long long)b * p.H + h) * p.rows + p.slot_row0 + t) * p.D) + vec;
+        (((long long)b * p.H + h) * p.rows + slot_row0 + t) * p.D) + vec;
     *dst = __ldg(src);
   }
 }
@@ -73,6 +78,13 @@ append_fp8_kernel(const __grid_constant__ AppendParams p) {
   ptx::griddep_wait();  // the slot may still be read by the previous kernel
   const int tensor = blockIdx.x;
   const bool int8 = p.k_int8 && tensor == 0;  // block-uniform
+  int slot_row0 = p.slot_row0, scale_idx = p.scale_idx;
+  if (p.d_chunk != nullptr) {  // graph mode: the chunk index lives on the device
+    const long long c = *p.d_chunk;
+    const int slot = (int)((c < 0 ? 0 : c) % p.ring_slots);
+    slot_row0 = (p.has_sink + slot) * p.Lc;
+    scale_idx = p.has_sink + slot;
+  }
   const int bh = blockIdx.y;
   const int b = bh / p.H, h = bh % p.H;
   const int vec_per_row = p.D / 8;
@@ -102,12 +114,12 @@ append_fp8_kernel(const __grid_constant__ AppendParams p) {
     for (int w = 0; w < (int)(blockDim.x >> 5); ++w) m = fmaxf(m, red[w]);
     const float sc = (m == 0.f) ? 1.0f : __fdiv_rn(m, int8 ? 127.0f : 448.0f);
     s_scale = sc;
-    p.scale[tensor][(long long)bh * p.scale_stride + p.scale_idx] = sc;
+    p.scale[tensor][(long long)bh * p.scale_stride + scale_idx] = sc;
   }
   __syncthreads();
   const float sc = s_scale;
   // pass 2: quantise (the block is re-read from L2)
-  uint8_t* dst = static_cast<uint8_t*>(p.dst[tensor]) + ((long long)bh * p.rows + p.slot_row0) * p.D;
+  uint8_t* dst = static_cast<uint8_t*>(p.dst[tensor]) + ((long long)bh * p.rows + slot_row0) * p.D;
   for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
     const uint4 x = src_vec(v);
     const uint32_t w[4] = {x.x, x.y, x.z, x.w};
@@ -147,6 +159,12 @@ cudaError_t launch_pdl(void (*kernel)(AppendParams), dim3 grid, const AppendPara
   return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
+// Graph mode: advance the device-side chunk index at the end of a chunk step.
+__global__ void counter_add_kernel(long long* counter, long long delta) {
+  ptx::griddep_wait();
+  *counter += delta;
+}
+
 int num_sms() {
   static int n = 0;
   if (n == 0) {
@@ -171,6 +189,11 @@ cudaError_t launch_append_bf16(const AppendParams& p, cudaStream_t s) {
 
 cudaError_t launch_append_fp8(const AppendParams& p, cudaStream_t s) {
   return launch_pdl(append_fp8_kernel, dim3(2, p.B * p.H), p, s);
+}
+
+cudaError_t launch_counter_add(long long* counter, long long delta, cudaStream_t s) {
+  counter_add_kernel<<<1, 1, 0, s>>>(counter, delta);
+  return cudaGetLastError();
 }
 
 }  // namespace sab

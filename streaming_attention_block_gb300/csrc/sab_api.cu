@@ -254,7 +254,7 @@ sab_status sab_kv_ring_layer_ptrs(const sab_ring* ring, int layer, void** k, voi
 }
 
 static sab_status write_chunk(sab_ring* r, int layer, int slot_row0, int scale_idx, const void* K, const void* V,
-                              void* stream) {
+                              void* stream, const long long* d_chunk = nullptr) {
   AppendParams p;
   memset(&p, 0, sizeof(p));
   p.src[0] = static_cast<const uint16_t*>(K);
@@ -272,6 +272,9 @@ static sab_status write_chunk(sab_ring* r, int layer, int slot_row0, int scale_i
   p.scale_idx = scale_idx;
   p.scale_stride = r->d.has_sink + r->d.ring_slots;
   p.k_int8 = r->d.kv_dtype == SAB_KV_INT8K_FP8V ? 1 : 0;
+  p.d_chunk = d_chunk;
+  p.ring_slots = r->d.ring_slots;
+  p.has_sink = r->d.has_sink;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const cudaError_t e = r->d.kv_dtype == SAB_KV_BF16 ? launch_append_bf16(p, s) : launch_append_fp8(p, s);
   return e == cudaSuccess ? SAB_OK : SAB_ERR_CUDA;
@@ -373,7 +376,7 @@ static sab_status launch_attention(AttnParams& p, int Lq, int splits, void* work
   if (splits == 0) {
     // block-causal: a CTA sees at most (window + 1) chunks plus one straddled tile
     const int tiles = p.mode == kModeStreaming
-                          ? p.total_tiles
+                          ? p.plan.total_tiles
                           : ((p.window + 1) * p.chunk_tokens + 2 * kTileN - 1) / kTileN;
     splits = auto_splits(t.n_qgroups * p.B * p.H, tiles);
   }
@@ -406,9 +409,11 @@ static sab_status launch_attention(AttnParams& p, int Lq, int splits, void* work
 }
 
 // Validation and key-set planning shared by both chunk-attention entry points.
-static sab_status plan_chunk_attention(const sab_ring* ring, int layer, long long chunk, const void* Q,
-                                       const void* K_cur, const void* V_cur, int window, int use_sink,
-                                       int num_splits, float softmax_scale, void* O, float* LSE, AttnParams& p) {
+// Validation and parameters common to host-planned and graph-mode calls
+// (everything but the chunk index).
+static sab_status plan_common(const sab_ring* ring, int layer, const void* Q, const void* K_cur, const void* V_cur,
+                              int window, int use_sink, int num_splits, float softmax_scale, void* O, float* LSE,
+                              AttnParams& p) {
   if (ring == nullptr || layer < 0 || layer >= ring->d.num_layers) return SAB_ERR_INVALID_ARG;
   if (Q == nullptr || O == nullptr || !aligned16(Q) || !aligned16(O)) return SAB_ERR_INVALID_ARG;
   if ((K_cur == nullptr) != (V_cur == nullptr)) return SAB_ERR_INVALID_ARG;
@@ -417,7 +422,6 @@ static sab_status plan_chunk_attention(const sab_ring* ring, int layer, long lon
   if (window < 0 || num_splits < 0 || num_splits > kMaxSplits) return SAB_ERR_INVALID_ARG;
   if (!(softmax_scale > 0.f) || !isfinite(softmax_scale)) return SAB_ERR_INVALID_ARG;
   if (use_sink != 0 && use_sink != 1) return SAB_ERR_INVALID_ARG;
-  if (chunk < 0) return SAB_ERR_OUT_OF_RANGE;
   const sab_ring_desc& d = ring->d;
   if (use_sink && !d.has_sink) return SAB_ERR_INVALID_ARG;
   if (use_sink && !ring->sink_set[layer]) return SAB_ERR_OUT_OF_RANGE;
@@ -427,35 +431,7 @@ static sab_status plan_chunk_attention(const sab_ring* ring, int layer, long lon
   // every key from the ring (the current chunk is appended first) and needs
   // chunks of at least 128 tokens (a key tile spans at most two chunks).
   if (fp8 && (kcur || d.head_dim != 128 || d.chunk_tokens < kTileN)) return SAB_ERR_UNSUPPORTED;
-  const int R = d.ring_slots, Lc = d.chunk_tokens;
-
-  // ring chunks needed: [need_lo, need_hi]
-  const long long need_lo = std::max(0LL, chunk - window);
-  const long long need_hi = kcur ? chunk - 1 : chunk;
-  struct Run {
-    int row0, nrows;
-  };
-  std::vector<Run> runs;
-  if (use_sink) runs.push_back({0, Lc});
-  if (need_hi >= need_lo) {
-    const long long newest = ring->newest[layer];
-    const long long oldest = newest - ring->held[layer] + 1;
-    if (newest < 0 || need_hi > newest || need_lo < oldest) return SAB_ERR_OUT_OF_RANGE;
-    for (long long c = need_lo; c <= need_hi; ++c) {
-      const int row0 = (d.has_sink + (int)(c % R)) * Lc;
-      runs.push_back({row0, Lc});
-    }
-  }
-  // Softmax is invariant to key order: merge physically adjacent runs.
-  std::sort(runs.begin(), runs.end(), [](const Run& a, const Run& b) { return a.row0 < b.row0; });
-  std::vector<Run> merged;
-  for (const Run& r : runs) {
-    if (!merged.empty() && merged.back().row0 + merged.back().nrows == r.row0)
-      merged.back().nrows += r.nrows;
-    else
-      merged.push_back(r);
-  }
-
+  const int Lc = d.chunk_tokens;
   memset(&p, 0, sizeof(p));
   p.mode = kModeStreaming;
   p.fp8 = fp8 ? 1 : 0;
@@ -470,31 +446,43 @@ static sab_status plan_chunk_attention(const sab_ring* ring, int layer, long lon
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
   p.O = static_cast<uint16_t*>(O);
   p.LSE = LSE;
-  int tiles = 0, nseg = 0;
-  for (const Run& r : merged) {
-    if (nseg >= kMaxSegments) return SAB_ERR_UNSUPPORTED;
-    p.seg[nseg] = KvSegment{0, r.row0, r.nrows, tiles};
-    tiles += (r.nrows + kTileN - 1) / kTileN;
-    ++nseg;
-  }
+  p.window = window;
+  p.ring_slots = d.ring_slots;
+  p.has_sink = d.has_sink;
+  p.use_sink = use_sink;
+  p.kcur = kcur ? 1 : 0;
   p.k_map[0] = ring->kmap[layer];
   p.v_map[0] = ring->vmap[layer];
   p.k_map[1] = ring->kmap[layer];
   p.v_map[1] = ring->vmap[layer];
   if (kcur) {
-    if (nseg >= kMaxSegments) return SAB_ERR_UNSUPPORTED;
-    p.seg[nseg] = KvSegment{1, 0, Lc, tiles};
-    tiles += (Lc + kTileN - 1) / kTileN;
-    ++nseg;
     if (!encode_token_major(&p.k_map[1], K_cur, d.batch, Lc, d.heads, d.head_dim) ||
         !encode_token_major(&p.v_map[1], V_cur, d.batch, Lc, d.heads, d.head_dim))
       return SAB_ERR_CUDA;
   }
-  p.nseg = nseg;
-  p.total_tiles = tiles;
   if (!encode_token_major(&p.q_map, Q, d.batch, Lc, d.heads, d.head_dim) ||
       !encode_token_major(&p.o_map, O, d.batch, Lc, d.heads, d.head_dim))
     return SAB_ERR_CUDA;
+  return SAB_OK;
+}
+
+// Validation and key-set planning of a host-planned call (chunk known here).
+static sab_status plan_chunk_attention(const sab_ring* ring, int layer, long long chunk, const void* Q,
+                                       const void* K_cur, const void* V_cur, int window, int use_sink,
+                                       int num_splits, float softmax_scale, void* O, float* LSE, AttnParams& p) {
+  const sab_status st =
+      plan_common(ring, layer, Q, K_cur, V_cur, window, use_sink, num_splits, softmax_scale, O, LSE, p);
+  if (st != SAB_OK) return st;
+  if (chunk < 0) return SAB_ERR_OUT_OF_RANGE;
+  // ring chunks needed: [need_lo, need_hi], all held by the ring
+  const long long need_lo = std::max(0LL, chunk - window);
+  const long long need_hi = p.kcur ? chunk - 1 : chunk;
+  if (need_hi >= need_lo) {
+    const long long newest = ring->newest[layer];
+    const long long oldest = newest - ring->held[layer] + 1;
+    if (newest < 0 || need_hi > newest || need_lo < oldest) return SAB_ERR_OUT_OF_RANGE;
+  }
+  plan_key_runs(chunk, window, p.ring_slots, p.chunk_tokens, p.has_sink, use_sink, p.kcur, p.plan);
   return SAB_OK;
 }
 
@@ -506,6 +494,39 @@ sab_status sab_chunk_attention(const sab_ring* ring, int layer, long long chunk,
       plan_chunk_attention(ring, layer, chunk, Q, K_cur, V_cur, window, use_sink, num_splits, softmax_scale, O, LSE, p);
   if (st != SAB_OK) return st;
   return launch_attention(p, ring->d.chunk_tokens, num_splits, workspace, ws_bytes, stream);
+}
+
+sab_status sab_chunk_attention_dev(const sab_ring* ring, int layer, const long long* d_chunk, const void* Q,
+                                   const void* K_cur, const void* V_cur, int window, int use_sink, int num_splits,
+                                   float softmax_scale, void* O, float* LSE, void* workspace, size_t ws_bytes,
+                                   void* stream) {
+  if (d_chunk == nullptr || (reinterpret_cast<uintptr_t>(d_chunk) & 7u) != 0) return SAB_ERR_INVALID_ARG;
+  AttnParams p;
+  const sab_status st =
+      plan_common(ring, layer, Q, K_cur, V_cur, window, use_sink, num_splits, softmax_scale, O, LSE, p);
+  if (st != SAB_OK) return st;
+  // every window the stream can ask for must fit in the ring
+  if (window > (p.kcur ? p.ring_slots : p.ring_slots - 1)) return SAB_ERR_OUT_OF_RANGE;
+  p.d_chunk = d_chunk;
+  // the host plan of a full window sizes the split choice; the kernels plan
+  // the actual chunk on the device
+  plan_key_runs((long long)window + p.ring_slots, window, p.ring_slots, p.chunk_tokens, p.has_sink, use_sink,
+                p.kcur, p.plan);
+  return launch_attention(p, ring->d.chunk_tokens, num_splits, workspace, ws_bytes, stream);
+}
+
+sab_status sab_kv_ring_append_dev(sab_ring* ring, int layer, const long long* d_chunk, const void* K,
+                                  const void* V, void* stream) {
+  if (ring == nullptr || layer < 0 || layer >= ring->d.num_layers) return SAB_ERR_INVALID_ARG;
+  if (K == nullptr || V == nullptr || !aligned16(K) || !aligned16(V)) return SAB_ERR_INVALID_ARG;
+  if (d_chunk == nullptr || (reinterpret_cast<uintptr_t>(d_chunk) & 7u) != 0) return SAB_ERR_INVALID_ARG;
+  return write_chunk(ring, layer, 0, 0, K, V, stream, d_chunk);
+}
+
+sab_status sab_chunk_counter_add(long long* d_chunk, long long delta, void* stream) {
+  if (d_chunk == nullptr || (reinterpret_cast<uintptr_t>(d_chunk) & 7u) != 0) return SAB_ERR_INVALID_ARG;
+  return launch_counter_add(d_chunk, delta, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SAB_OK
+                                                                                            : SAB_ERR_CUDA;
 }
 
 // Allocation-free variant: the split merge goes through the library's own

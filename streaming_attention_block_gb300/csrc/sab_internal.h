@@ -24,6 +24,72 @@ struct KvSegment {
 
 enum AttnMode : int { kModeStreaming = 0, kModeBlockCausal = 1 };
 
+// Key runs of one streaming call, in physical row order.
+struct KeyPlan {
+  int nseg;
+  int total_tiles;
+  KvSegment seg[kMaxSegments];
+};
+
+// Key set of chunk c ("WanToFight", table "模型组件", row "Rolling KV Cache";
+// "Matrix-Game 4.0", section "前置知识 / 因果自回归与 KV 缓存"): the sink rows
+// [0, Lc) when used, the ring chunks max(0, c - W) .. c - 1 (and c itself when
+// the current chunk was appended first, kcur == 0) at rows
+// (has_sink + chunk mod R) * Lc, physically adjacent runs merged (softmax does
+// not depend on key order), then the current chunk's own tensor (kcur == 1).
+// The host planner and the graph-mode kernels (chunk index read on the
+// device) share this function.  At most R ring chunks are taken.
+__host__ __device__ inline void plan_key_runs(long long c, int W, int R, int Lc, int has_sink, int use_sink,
+                                              int kcur, KeyPlan& kp) {
+  int r0[3], nr[3], n = 0;
+  if (use_sink) {
+    r0[n] = 0;
+    nr[n] = Lc;
+    ++n;
+  }
+  if (c < 0) c = 0;
+  const long long lo = c - W > 0 ? c - W : 0;
+  const long long hi = kcur ? c - 1 : c;
+  if (hi >= lo && R > 0) {
+    long long cnt = hi - lo + 1;
+    if (cnt > R) cnt = R;
+    const int s_lo = (int)(lo % R), s_end = s_lo + (int)cnt;
+    const int base = has_sink * Lc;
+    if (s_end <= R) {
+      r0[n] = base + s_lo * Lc;
+      nr[n] = (int)cnt * Lc;
+      ++n;
+    } else {  // wraps: the low slots come first in row order
+      r0[n] = base;
+      nr[n] = (s_end - R) * Lc;
+      ++n;
+      r0[n] = base + s_lo * Lc;
+      nr[n] = (R - s_lo) * Lc;
+      ++n;
+    }
+  }
+  int tiles = 0, m = 0;
+  for (int i = 0; i < n; ++i) {
+    if (m > 0 && kp.seg[m - 1].row0 + kp.seg[m - 1].nrows == r0[i]) {
+      tiles -= (kp.seg[m - 1].nrows + kTileN - 1) / kTileN;
+      kp.seg[m - 1].nrows += nr[i];
+      tiles += (kp.seg[m - 1].nrows + kTileN - 1) / kTileN;
+    } else {
+      kp.seg[m] = KvSegment{0, r0[i], nr[i], tiles};
+      tiles += (nr[i] + kTileN - 1) / kTileN;
+      ++m;
+    }
+  }
+  if (kcur) {
+    kp.seg[m] = KvSegment{1, 0, Lc, tiles};
+    tiles += (Lc + kTileN - 1) / kTileN;
+    ++m;
+  }
+  for (int i = m; i < kMaxSegments; ++i) kp.seg[i] = KvSegment{0, 0, 0, 0x7fffffff};
+  kp.nseg = m;
+  kp.total_tiles = tiles;
+}
+
 struct AttnParams {
   CUtensorMap q_map;      // dims (D, Lq, H, B), box (64, 128, 1, 1), SW128
   CUtensorMap k_map[2];   // per source, dims (D, rows, H, B)
@@ -47,10 +113,11 @@ struct AttnParams {
                           // splits of a two-tile group merge as a CTA pair
                           // (one bulk copy each way)
   float scale_log2;       // softmax_scale * log2(e)
-  // streaming
-  int nseg;
-  int total_tiles;
-  KvSegment seg[kMaxSegments];
+  // streaming: key runs planned on the host, or (d_chunk != null: graph mode)
+  // planned by every CTA from the chunk index in device memory
+  KeyPlan plan;
+  const long long* d_chunk;
+  int ring_slots, has_sink, use_sink, kcur;
   // block-causal
   int chunk_tokens;
   int window;
@@ -75,11 +142,15 @@ struct AppendParams {
   int scale_idx;            // (has_sink + slot) or 0 for the sink
   int scale_stride;         // has_sink + R
   int k_int8;               // 8-bit ring: K as INT8 (amax / 127) instead of E4M3
+  // graph mode: the slot is chunk mod R with the chunk read on the device
+  const long long* d_chunk;
+  int ring_slots, has_sink;
 };
 
 // Launchers (return cudaError_t of the launch).
 cudaError_t launch_append_bf16(const AppendParams& p, cudaStream_t s);
 cudaError_t launch_append_fp8(const AppendParams& p, cudaStream_t s);
+cudaError_t launch_counter_add(long long* counter, long long delta, cudaStream_t s);
 cudaError_t launch_chunk_attention(const AttnParams& p, int q_tiles_per_cta, cudaStream_t s);
 // One query tile per CTA, key-half softmax warpgroups; unsplit KV only.
 cudaError_t launch_chunk_attention_kh(const AttnParams& p, cudaStream_t s);

@@ -83,4 +83,11 @@ def test_validation_before_any_cuda_call(lib):
     p = ctypes.c_void_p(4096)
     assert lib.sab_block_causal_attention(p, p, p, 1, 128, 1, 96, 64, 1, 1, 0.1, p, None, None, 0, None) == 1
     assert lib.sab_block_causal_attention(p, p, p, 1, 128, 1, 64, 64, -1, 1, 0.1, p, None, None, 0, None) == 1
+    # graph-mode entry points: null / misaligned device chunk index, no ring
+    assert lib.sab_chunk_attention_dev(None, 0, None, p, None, None, 2, 0, 1, 0.1, p, None, None, 0, None) == 1
+    assert lib.sab_chunk_attention_dev(None, 0, ctypes.c_void_p(4100), p, None, None, 2, 0, 1, 0.1, p, None, None,
+                                       0, None) == 1
+    assert lib.sab_kv_ring_append_dev(None, 0, p, p, p, None) == 1
+    assert lib.sab_chunk_counter_add(None, 1, None) == 1
+    assert lib.sab_chunk_counter_add(ctypes.c_void_p(4100), 1, None) == 1
     assert lib.sab_kv_ring_destroy(None) == 0
