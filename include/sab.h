@@ -309,6 +309,18 @@ sab_status sab_block_causal_attention(const void* Q, const void* K, const void* 
  */
 sab_status sab_get_last_device_error(void* stream);
 
+/*
+ * Self-test of the device-side failure detection (no counterpart in the
+ * method): launches one CTA on `stream` whose pipeline wait -- the same
+ * bounded mbarrier wait every kernel of the library uses -- waits on a
+ * barrier that nothing ever completes.  After timeout_ns (1 ms .. 2 s;
+ * INVALID_ARG otherwise) the wait gives up, records its site and the kernel
+ * returns; a following sab_get_last_device_error reports SAB_ERR_TIMEOUT and
+ * clears the record.  Nothing faults, traps or hangs, and the context stays
+ * usable.
+ */
+sab_status sab_selftest_bounded_wait(unsigned long long timeout_ns, void* stream);
+
 /* Static, human-readable name of a status code. */
 const char* sab_status_string(sab_status status);
 

@@ -35,6 +35,7 @@ from ._abi import (  # noqa: F401
     kv_ring_slot_of,
     library,
     library_path,
+    selftest_bounded_wait,
     status_string,
     version,
 )

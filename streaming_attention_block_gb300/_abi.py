@@ -72,6 +72,7 @@ def library() -> ctypes.CDLL:
         "sab_block_causal_attention_workspace": (SZ, [I, I, I, I, I]),
         "sab_block_causal_attention": (I, [P, P, P, I, I, I, I, I, I, I, F, P, P, P, SZ, P]),
         "sab_get_last_device_error": (I, [P]),
+        "sab_selftest_bounded_wait": (I, [ctypes.c_ulonglong, P]),
         "sab_status_string": (ctypes.c_char_p, [I]),
         "sab_version": (ctypes.c_char_p, []),
     }
@@ -254,6 +255,12 @@ def block_causal_attention(Q, K, V, chunk_tokens: int, window: int, num_splits: 
 
 def get_last_device_error(stream=None) -> int:
     return int(library().sab_get_last_device_error(_stream(stream)))
+
+
+def selftest_bounded_wait(timeout_ns: int, stream=None):
+    """sab_selftest_bounded_wait: a device wait that nothing completes gives up
+    after timeout_ns; read the result with get_last_device_error."""
+    _check(library().sab_selftest_bounded_wait(int(timeout_ns), _stream(stream)), "selftest_bounded_wait")
 
 
 class KVRing:

@@ -125,7 +125,7 @@ __device__ __forceinline__ uint64_t global_ns() {
 // abort flag and gives up.
 template <bool kClusterScope = false>
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                             unsigned site) {
+                                             unsigned site, uint64_t timeout_ns = kTimeoutNs) {
   if (!kClusterScope && mbar_test_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
 #pragma unroll 1
@@ -133,7 +133,7 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
     if (kClusterScope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
     if ((it & 255u) == 0) {
       if (*abort_flag) return false;
-      if (global_ns() - t0 > kTimeoutNs) {
+      if (global_ns() - t0 > timeout_ns) {
         atomicOr(&g_sab_error_word, 1u << site);
         *abort_flag = 1;
         return false;
@@ -1632,7 +1632,30 @@ cudaError_t launch_kh_impl(const AttnParams& p, cudaStream_t s) {
   return cudaLaunchKernelEx(&cfg, chunk_attn_kh_kernel<D, FP8>, p);
 }
 
+// Self-test of the failure detection: one CTA waits, with the pipeline's own
+// bounded wait, on an mbarrier that nothing ever completes.  The wait gives
+// up after timeout_ns, records its site (bit 30) in the device error word and
+// the kernel returns: no fault, no hang.
+__global__ void wait_timeout_probe_kernel(uint64_t timeout_ns) {
+  __shared__ __align__(8) uint64_t bar_;
+  __shared__ int abort_;
+  const uint32_t bar = smem_u32(&bar_);
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    abort_ = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) (void)wait_bounded(bar, 0, reinterpret_cast<volatile int*>(&abort_), 30, timeout_ns);
+  __syncthreads();
+}
+
 }  // namespace
+
+cudaError_t launch_wait_timeout_probe(unsigned long long timeout_ns, cudaStream_t s) {
+  wait_timeout_probe_kernel<<<1, 32, 0, s>>>(timeout_ns);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_chunk_attention_kh(const AttnParams& p, cudaStream_t s) {
   if (p.splits != 1) return cudaErrorInvalidValue;

@@ -588,6 +588,12 @@ sab_status sab_block_causal_attention(const void* Q, const void* K, const void* 
   return launch_attention(p, L, num_splits, workspace, ws_bytes, stream);
 }
 
+sab_status sab_selftest_bounded_wait(unsigned long long timeout_ns, void* stream) {
+  if (timeout_ns < 1000000ull || timeout_ns > 2000000000ull) return SAB_ERR_INVALID_ARG;
+  return launch_wait_timeout_probe(timeout_ns, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SAB_OK
+                                                                                                : SAB_ERR_CUDA;
+}
+
 sab_status sab_get_last_device_error(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return SAB_ERR_CUDA;
   unsigned v = 0;

@@ -151,6 +151,7 @@ struct AppendParams {
 cudaError_t launch_append_bf16(const AppendParams& p, cudaStream_t s);
 cudaError_t launch_append_fp8(const AppendParams& p, cudaStream_t s);
 cudaError_t launch_counter_add(long long* counter, long long delta, cudaStream_t s);
+cudaError_t launch_wait_timeout_probe(unsigned long long timeout_ns, cudaStream_t s);
 cudaError_t launch_chunk_attention(const AttnParams& p, int q_tiles_per_cta, cudaStream_t s);
 // One query tile per CTA, key-half softmax warpgroups; unsplit KV only.
 cudaError_t launch_chunk_attention_kh(const AttnParams& p, cudaStream_t s);

@@ -90,4 +90,5 @@ def test_validation_before_any_cuda_call(lib):
     assert lib.sab_kv_ring_append_dev(None, 0, p, p, p, None) == 1
     assert lib.sab_chunk_counter_add(None, 1, None) == 1
     assert lib.sab_chunk_counter_add(ctypes.c_void_p(4100), 1, None) == 1
+    assert lib.sab_selftest_bounded_wait(10, None) == 1  # limit outside 1 ms .. 2 s
     assert lib.sab_kv_ring_destroy(None) == 0
