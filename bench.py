@@ -440,6 +440,42 @@ def run_sweep(args):
                                     stream)
 
             report(name, timed(call, 50), flops, splits, {"keys": nkeys})
+    # fused Q/K RMSNorm + rotary embedding + BF16 ring append at the Wan-1.3B
+    # chunk shape (latent grid 2 x 24 x 32, rotary bands 44/42/42); 16 input
+    # sets rotate so that every call reads from HBM (16 x 18.9 MB > L2)
+    w = synth.workload("wan13b")
+    g = synth.generator(w.seed, device="cuda")
+    shape = (w.B, w.Lc, w.H, w.D)
+    nsets = 16
+    sets = [tuple(synth.randn_bf16(g, shape, "cuda") for _ in range(3)) for _ in range(nsets)]
+    qouts = [torch.empty(shape, dtype=torch.bfloat16, device="cuda") for _ in range(nsets)]
+    ring = sab.KVRing(1, w.B, w.H, w.D, w.Lc, w.R)
+    rope = sab.RopeDesc(2, 24, 32, 44, 42, 42, 10000.0, 1e-6)
+    state = {"i": 0, "c": 0}
+
+    def producer():
+        i = state["i"] % nsets
+        q, k, v = sets[i]
+        sab.qk_norm_rope(ring.handle, 0, state["c"], q, k, v, rope, qouts[i], append=True, stream=stream)
+        state["i"] += 1
+        state["c"] += 1
+
+    for _ in range(8):
+        producer()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(64):  # back to back, like the attention calls of a denoise step
+        producer()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / 64
+    nbytes = 6 * w.B * w.Lc * w.H * w.D * 2  # read q, k, v; write q', ring k', ring v
+    gbs = nbytes / (us * 1e-6) / 1e9
+    print(json.dumps({"sweep": "qk_norm_rope_append", "us_per_call": round(us, 2), "GB_per_s": round(gbs, 1),
+                      "frac_of_hbm_peak": round(gbs / peaks["hbm_gbs"], 4), "peak_source": f"hbm copy, {src}",
+                      "bytes_per_call": nbytes}), flush=True)
+
     w = synth.workload("block_causal")
     g = synth.generator(w.seed, device="cuda")
     q, k, v = synth.full_sequence_qkv(w, g, "cuda")

@@ -223,6 +223,45 @@ sab_status sab_chunk_attention(const sab_ring* ring, int layer, long long chunk,
                                void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * Fused Q/K normalisation and rotary embedding of one chunk, with the K/V
+ * append ("WorldPlay2: Extending Real-Time Interactive World Models in
+ * Control and Horizon", section 方法步骤详情: QKRoPE and QKV fusion;
+ * "Matrix-Game 4.0", section 实验结果: a fused RoPE kernel).  The pages give
+ * no formulas; the plain ones of a Wan-style video DiT are used:
+ *   q' = RoPE(RMSNorm_q(q)), k' = RoPE(RMSNorm_k(k)), v' = v, where
+ *   RMSNorm(x) = x / sqrt(mean(x^2) + eps) * gamma over each token's H*D
+ *   values (gamma NULL: 1), and RoPE rotates the interleaved pairs
+ *   (2i, 2i+1) of every head by pos * base^(-2i / band): the head dimension
+ *   is split into bands (band_t, band_h, band_w) rotated by the token's
+ *   frame, row and column in the chunk's latent grid (frames x height x
+ *   width = chunk_tokens; token t of chunk c is at frame
+ *   c * frames + t / (height * width)).  band_h = band_w = 0 with
+ *   height = width = 1 is the one-dimensional embedding over the token index.
+ * Q, K, V  device, token-major [B, Lc, H, D] bf16 (the QKV projection's
+ *          output; shape from the ring).  gamma_q, gamma_k: device [H*D] fp32
+ *          or NULL.  Q_out: device [B, Lc, H, D] bf16.  K_out, V_out: device
+ *          [B, Lc, H, D] bf16 or NULL (k' and a copy of v).
+ * append   1: also store k', v into slot chunk mod R of `layer`, with the
+ *          rules and chunk-order check of sab_kv_ring_append -- fused into
+ *          the same kernel for a BF16 ring; an 8-bit ring needs K_out and
+ *          V_out and runs its quantiser on them.  0: no ring write (the
+ *          chunk index still sets the positions).
+ * Computed in fp32, rounded to bf16 once.  Errors: INVALID_ARG (pointers,
+ * bands not even or not summing to head_dim, grid not matching chunk_tokens,
+ * base <= 1, eps <= 0), OUT_OF_RANGE (chunk order when appending).
+ */
+typedef struct {
+  int frames, height, width;    /* latent grid of one chunk                     */
+  int band_t, band_h, band_w;   /* rotary bands of head_dim (even, sum = D)     */
+  float base;                   /* rotary base, e.g. 10000                      */
+  float eps;                    /* RMSNorm epsilon, e.g. 1e-6                   */
+} sab_rope_desc;
+
+sab_status sab_qk_norm_rope(sab_ring* ring, int layer, long long chunk, const void* Q, const void* K, const void* V,
+                            const float* gamma_q, const float* gamma_k, const sab_rope_desc* rope, void* Q_out,
+                            void* K_out, void* V_out, int append, void* stream);
+
+/*
  * Graph-capturable streaming ("Matrix-Game 4.0", section "前置知识 / FP8 量化
  * 与 CUDA Graph": a whole chunk's GPU work is recorded once as a graph and
  * replayed with one launch per chunk, removing the per-kernel CPU launch

@@ -13,6 +13,7 @@ from ._abi import (  # noqa: F401
     KV_INT8K_FP8V,
     KVRing,
     RingDesc,
+    RopeDesc,
     SabError,
     block_causal_attention,
     block_causal_attention_workspace,
@@ -35,6 +36,7 @@ from ._abi import (  # noqa: F401
     kv_ring_slot_of,
     library,
     library_path,
+    qk_norm_rope,
     selftest_bounded_wait,
     status_string,
     version,

@@ -73,6 +73,7 @@ def library() -> ctypes.CDLL:
         "sab_block_causal_attention": (I, [P, P, P, I, I, I, I, I, I, I, F, P, P, P, SZ, P]),
         "sab_get_last_device_error": (I, [P]),
         "sab_selftest_bounded_wait": (I, [ctypes.c_ulonglong, P]),
+        "sab_qk_norm_rope": (I, [P, I, LL, P, P, P, P, P, P, P, P, P, I, P]),
         "sab_status_string": (ctypes.c_char_p, [I]),
         "sab_version": (ctypes.c_char_p, []),
     }
@@ -261,6 +262,22 @@ def selftest_bounded_wait(timeout_ns: int, stream=None):
     """sab_selftest_bounded_wait: a device wait that nothing completes gives up
     after timeout_ns; read the result with get_last_device_error."""
     _check(library().sab_selftest_bounded_wait(int(timeout_ns), _stream(stream)), "selftest_bounded_wait")
+
+
+class RopeDesc(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in ("frames", "height", "width", "band_t", "band_h", "band_w")] + [
+        ("base", ctypes.c_float), ("eps", ctypes.c_float)]
+
+
+def qk_norm_rope(handle, layer: int, chunk: int, Q, K, V, rope: RopeDesc, Q_out, K_out=None, V_out=None,
+                 gamma_q=None, gamma_k=None, append: bool = False, stream=None):
+    """sab_qk_norm_rope: q' = RoPE(RMSNorm(q)), k' = RoPE(RMSNorm(k)) of one
+    chunk, optionally appending k', v into the ring slot (see include/sab.h)."""
+    _check(library().sab_qk_norm_rope(
+        handle, int(layer), int(chunk), _ptr(Q, torch.bfloat16, "Q"), _ptr(K, torch.bfloat16, "K"),
+        _ptr(V, torch.bfloat16, "V"), _ptr(gamma_q, torch.float32, "gamma_q"), _ptr(gamma_k, torch.float32, "gamma_k"),
+        ctypes.byref(rope), _ptr(Q_out, torch.bfloat16, "Q_out"), _ptr(K_out, torch.bfloat16, "K_out"),
+        _ptr(V_out, torch.bfloat16, "V_out"), int(bool(append)), _stream(stream)), "qk_norm_rope")
 
 
 class KVRing:

@@ -18,7 +18,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libsab.so")
-SOURCES = ["sab_api.cu", "chunk_attn.cu", "kv_append.cu"]
+SOURCES = ["sab_api.cu", "chunk_attn.cu", "kv_append.cu", "qk_rope.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -515,6 +515,78 @@ sab_status sab_chunk_attention_dev(const sab_ring* ring, int layer, const long l
   return launch_attention(p, ring->d.chunk_tokens, num_splits, workspace, ws_bytes, stream);
 }
 
+sab_status sab_qk_norm_rope(sab_ring* ring, int layer, long long chunk, const void* Q, const void* K, const void* V,
+                            const float* gamma_q, const float* gamma_k, const sab_rope_desc* rope, void* Q_out,
+                            void* K_out, void* V_out, int append, void* stream) {
+  if (ring == nullptr || layer < 0 || layer >= ring->d.num_layers || rope == nullptr) return SAB_ERR_INVALID_ARG;
+  const sab_ring_desc& d = ring->d;
+  if (Q == nullptr || K == nullptr || V == nullptr || Q_out == nullptr) return SAB_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(Q_out)) return SAB_ERR_INVALID_ARG;
+  if ((K_out && !aligned16(K_out)) || (V_out && !aligned16(V_out))) return SAB_ERR_INVALID_ARG;
+  if ((gamma_q && (reinterpret_cast<uintptr_t>(gamma_q) & 3u)) || (gamma_k && (reinterpret_cast<uintptr_t>(gamma_k) & 3u)))
+    return SAB_ERR_INVALID_ARG;
+  if (append != 0 && append != 1) return SAB_ERR_INVALID_ARG;
+  if (rope->frames < 1 || rope->height < 1 || rope->width < 1 ||
+      (long long)rope->frames * rope->height * rope->width != d.chunk_tokens)
+    return SAB_ERR_INVALID_ARG;
+  if (rope->band_t < 0 || rope->band_h < 0 || rope->band_w < 0 || (rope->band_t | rope->band_h | rope->band_w) & 1 ||
+      rope->band_t + rope->band_h + rope->band_w != d.head_dim)
+    return SAB_ERR_INVALID_ARG;
+  if (!(rope->base > 1.f) || !isfinite(rope->base) || !(rope->eps > 0.f) || !isfinite(rope->eps))
+    return SAB_ERR_INVALID_ARG;
+  if (chunk < 0) return SAB_ERR_OUT_OF_RANGE;
+  const bool bf16_ring = d.kv_dtype == SAB_KV_BF16;
+  // an 8-bit ring quantises per (batch, head) block: K', V go through K_out,
+  // V_out and the ring's own quantiser
+  if (append && !bf16_ring && (K_out == nullptr || V_out == nullptr)) return SAB_ERR_INVALID_ARG;
+  const long long newest = ring->newest[layer];
+  if (append && newest >= 0 && chunk != newest && chunk != newest + 1) return SAB_ERR_OUT_OF_RANGE;
+  const int R = d.ring_slots, slot = (int)(chunk % R);
+  RopeParams rp;
+  memset(&rp, 0, sizeof(rp));
+  rp.q_in = static_cast<const uint16_t*>(Q);
+  rp.k_in = static_cast<const uint16_t*>(K);
+  rp.v_in = static_cast<const uint16_t*>(V);
+  rp.gamma_q = gamma_q;
+  rp.gamma_k = gamma_k;
+  rp.q_out = static_cast<uint16_t*>(Q_out);
+  rp.k_out = static_cast<uint16_t*>(K_out);
+  rp.v_out = static_cast<uint16_t*>(V_out);
+  if (append && bf16_ring) {
+    rp.ring_k = static_cast<uint16_t*>(ring->k(layer));
+    rp.ring_v = static_cast<uint16_t*>(ring->v(layer));
+  }
+  rp.B = d.batch;
+  rp.H = d.heads;
+  rp.D = d.head_dim;
+  rp.Lc = d.chunk_tokens;
+  rp.rows = (int)ring->g.rows;
+  rp.slot_row0 = (d.has_sink + slot) * d.chunk_tokens;
+  rp.chunk = chunk;
+  rp.F = rope->frames;
+  rp.Hp = rope->height;
+  rp.Wp = rope->width;
+  rp.bt = rope->band_t;
+  rp.bh = rope->band_h;
+  rp.bw = rope->band_w;
+  rp.log2_base = log2f(rope->base);
+  rp.eps = rope->eps;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (launch_qk_rope(rp, s) != cudaSuccess) return SAB_ERR_CUDA;
+  if (!append) return SAB_OK;
+  if (!bf16_ring) {
+    const sab_status st = write_chunk(ring, layer, rp.slot_row0, d.has_sink + slot, K_out, V_out, stream);
+    if (st != SAB_OK) return st;
+  }
+  if (newest < 0) {
+    ring->held[layer] = 1;
+  } else if (chunk == newest + 1) {
+    ring->held[layer] = std::min(R, ring->held[layer] + 1);
+  }
+  ring->newest[layer] = chunk;
+  return SAB_OK;
+}
+
 sab_status sab_kv_ring_append_dev(sab_ring* ring, int layer, const long long* d_chunk, const void* K,
                                   const void* V, void* stream) {
   if (ring == nullptr || layer < 0 || layer >= ring->d.num_layers) return SAB_ERR_INVALID_ARG;

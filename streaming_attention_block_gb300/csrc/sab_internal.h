@@ -147,10 +147,33 @@ struct AppendParams {
   int ring_slots, has_sink;
 };
 
+// Fused Q/K RMSNorm + rotary embedding of one chunk (token-major [B, Lc, H, D]).
+struct RopeParams {
+  const uint16_t* q_in;
+  const uint16_t* k_in;
+  const uint16_t* v_in;
+  const float* gamma_q;     // [H*D] or null (1)
+  const float* gamma_k;
+  uint16_t* q_out;
+  uint16_t* k_out;          // token-major K', or null
+  uint16_t* v_out;          // token-major V copy, or null
+  uint16_t* ring_k;         // BF16 ring K/V region of the layer, or null (no append)
+  uint16_t* ring_v;
+  int B, H, D, Lc;
+  int rows;                 // ring rows per (b, h)
+  int slot_row0;            // first ring row of the chunk's slot
+  long long chunk;
+  int F, Hp, Wp;            // latent grid of a chunk: Lc = F * Hp * Wp
+  int bt, bh, bw;           // rotary bands of the head dimension (even, sum D)
+  float log2_base;          // log2(rotary base)
+  float eps;
+};
+
 // Launchers (return cudaError_t of the launch).
 cudaError_t launch_append_bf16(const AppendParams& p, cudaStream_t s);
 cudaError_t launch_append_fp8(const AppendParams& p, cudaStream_t s);
 cudaError_t launch_counter_add(long long* counter, long long delta, cudaStream_t s);
+cudaError_t launch_qk_rope(const RopeParams& p, cudaStream_t s);
 cudaError_t launch_wait_timeout_probe(unsigned long long timeout_ns, cudaStream_t s);
 cudaError_t launch_chunk_attention(const AttnParams& p, int q_tiles_per_cta, cudaStream_t s);
 // One query tile per CTA, key-half softmax warpgroups; unsplit KV only.
