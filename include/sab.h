@@ -223,6 +223,27 @@ sab_status sab_chunk_attention(const sab_ring* ring, int layer, long long chunk,
                                void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * Gradients of block-causal attention (training / causal adaptation:
+ * "WanToFight", section 训练流程 / Stage 2; the same mask as
+ * sab_block_causal_attention).  For a loss with gradient dO with respect to
+ * O = softmax(scale Q K^T + mask) V, with P recomputed from the forward's LSE
+ * and delta_i = sum_d dO_id O_id:
+ *   dV = P^T dO,  dS = P * (dO V^T - delta),  dQ = scale dS K,  dK = scale dS^T Q.
+ * Q, K, V, O, dO  device, token-major [B, L, H, D] bf16 (O and LSE as the
+ *          forward produced them).  LSE: device [B, H, L] fp32.
+ * dQ, dK, dV  device, token-major [B, L, H, D] bf16 (outputs).
+ * workspace  device scratch of sab_block_causal_attention_backward_workspace
+ *          bytes (delta), 256-byte aligned; no zero-fill needed.
+ * D must be 64 or 128.  Errors: INVALID_ARG, WORKSPACE, CUDA.
+ */
+size_t sab_block_causal_attention_backward_workspace(int B, int L, int H);
+sab_status sab_block_causal_attention_backward(const void* Q, const void* K, const void* V, const void* O,
+                                               const void* dO, const float* LSE, int B, int L, int H, int D,
+                                               int chunk_tokens, int window, float softmax_scale, void* dQ,
+                                               void* dK, void* dV, void* workspace, size_t ws_bytes,
+                                               void* stream);
+
+/*
  * Fused Q/K normalisation and rotary embedding of one chunk, with the K/V
  * append ("WorldPlay2: Extending Real-Time Interactive World Models in
  * Control and Horizon", section 方法步骤详情: QKRoPE and QKV fusion;

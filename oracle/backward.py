@@ -19,9 +19,11 @@ gradient with respect to O is dO:
 
 computed in float64 with the explicit token mask (query i sees key j iff
 0 <= chunk(i) - chunk(j) <= window).  ``abs_bounds`` also returns, for every
-output element, the sum of the absolute values of the products it adds up --
-the scale of the rounding error of any finite-precision evaluation of that
-sum.
+output element, the scale of the rounding error of a finite-precision
+evaluation: the sum of the absolute values of the products it adds up, plus
+(dQ, dK) the sensitivity to an error in delta of relative size 1 --
+scale * sum_j P_ij * (sum_d |dO_id O_id|) * |K_jd| (dQ) and likewise with Q
+(dK) -- since delta is itself a sum of products.
 """
 
 from __future__ import annotations
@@ -64,7 +66,9 @@ def block_causal_attention_backward(q_blhd, k_blhd, v_blhd, do_blhd, chunk_token
             dq, dk, dv, p, ds = _head(qh, kh, vh, doh, mask, scale)
             out[0][b, :, h], out[1][b, :, h], out[2][b, :, h] = dq, dk, dv
             if abs_bounds:
-                bnd[0][b, :, h] = scale * (np.abs(ds) @ np.abs(kh))
-                bnd[1][b, :, h] = scale * (np.abs(ds).T @ np.abs(qh))
+                o = p @ vh
+                dabs = np.sum(np.abs(doh * o), axis=1, keepdims=True)  # scale of delta's rounding
+                bnd[0][b, :, h] = scale * (np.abs(ds) @ np.abs(kh) + dabs * (p @ np.abs(kh)))
+                bnd[1][b, :, h] = scale * (np.abs(ds).T @ np.abs(qh) + p.T @ (dabs * np.abs(qh)))
                 bnd[2][b, :, h] = np.abs(p).T @ np.abs(doh)
     return (tuple(out), tuple(bnd)) if abs_bounds else tuple(out)

@@ -16,6 +16,7 @@ from ._abi import (  # noqa: F401
     RopeDesc,
     SabError,
     block_causal_attention,
+    block_causal_attention_backward,
     block_causal_attention_workspace,
     chunk_attention,
     chunk_attention_dev,

@@ -74,6 +74,8 @@ def library() -> ctypes.CDLL:
         "sab_get_last_device_error": (I, [P]),
         "sab_selftest_bounded_wait": (I, [ctypes.c_ulonglong, P]),
         "sab_qk_norm_rope": (I, [P, I, LL, P, P, P, P, P, P, P, P, P, I, P]),
+        "sab_block_causal_attention_backward_workspace": (SZ, [I, I, I]),
+        "sab_block_causal_attention_backward": (I, [P, P, P, P, P, P, I, I, I, I, I, I, F, P, P, P, P, SZ, P]),
         "sab_status_string": (ctypes.c_char_p, [I]),
         "sab_version": (ctypes.c_char_p, []),
     }
@@ -237,6 +239,23 @@ def chunk_counter_add(d_chunk, delta: int = 1, stream=None):
     """sab_chunk_counter_add: *d_chunk += delta on the stream."""
     _check(library().sab_chunk_counter_add(_ptr(d_chunk, torch.int64, "d_chunk"), int(delta), _stream(stream)),
            "chunk_counter_add")
+
+
+def block_causal_attention_backward(Q, K, V, O, dO, LSE, chunk_tokens: int, window: int, softmax_scale: float,
+                                    dQ, dK, dV, workspace=None, stream=None):
+    """sab_block_causal_attention_backward: (dQ, dK, dV) of block-causal
+    attention from the forward's O and LSE (see include/sab.h)."""
+    B, L, H, D = Q.shape
+    if workspace is None:
+        n = int(library().sab_block_causal_attention_backward_workspace(B, L, H))
+        workspace = torch.empty(n, dtype=torch.uint8, device=Q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(library().sab_block_causal_attention_backward(
+        _ptr(Q, torch.bfloat16, "Q"), _ptr(K, torch.bfloat16, "K"), _ptr(V, torch.bfloat16, "V"),
+        _ptr(O, torch.bfloat16, "O"), _ptr(dO, torch.bfloat16, "dO"), _ptr(LSE, torch.float32, "LSE"),
+        B, L, H, D, int(chunk_tokens), int(window), float(softmax_scale), _ptr(dQ, torch.bfloat16, "dQ"),
+        _ptr(dK, torch.bfloat16, "dK"), _ptr(dV, torch.bfloat16, "dV"), _ptr(workspace, None, "workspace"),
+        ws_bytes, _stream(stream)), "block_causal_attention_backward")
 
 
 def block_causal_attention_workspace(B: int, L: int, H: int, D: int, num_splits: int) -> int:

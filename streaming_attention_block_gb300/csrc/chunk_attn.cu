@@ -1632,6 +1632,392 @@ cudaError_t launch_kh_impl(const AttnParams& p, cudaStream_t s) {
   return cudaLaunchKernelEx(&cfg, chunk_attn_kh_kernel<D, FP8>, p);
 }
 
+// ===========================================================================
+// Backward of block-causal attention ("WanToFight", section 训练流程 / Stage 2:
+// training with the block-causal mask).  With P = softmax(scale * Q K^T) over
+// the visible keys (recomputed from the forward's LSE), delta_i = sum_d dO O:
+//   dV = P^T dO,  dP = dO V^T,  dS = P * (dP - delta),
+//   dK = scale * dS^T Q,  dQ = scale * dS K.
+// Two kernels with the pipeline of the forward: the key-tile kernel keeps K,
+// V of 128 keys resident and streams the visible query tiles (S^T = K Q^T and
+// dP^T = V dO^T into TMEM; the softmax warps write P^T and dS^T back as bf16;
+// dV += P^T dO and dK += dS^T Q read them from TMEM); the query-tile kernel
+// keeps Q, dO resident and streams the visible key tiles (S, dP; dS back to
+// TMEM; dQ += dS K).  Every MMA operand layout is one the forward uses.
+template <int D_>
+struct BwdCfg {
+  static constexpr int D = D_;
+  static constexpr int kBoxes = D / 64;
+  static constexpr uint32_t kBoxBytes = 128u * 128u;
+  static constexpr uint32_t kTileBytes = kBoxBytes * kBoxes;
+  static constexpr int kStages = 2;
+  static constexpr uint32_t kR0Off = 0;                   // resident tile 0 (K, or Q)
+  static constexpr uint32_t kR1Off = kTileBytes;          // resident tile 1 (V, or dO)
+  static constexpr uint32_t kStageOff = 2 * kTileBytes;
+  // stage: streamed tile 0 (Q_j, or K_j), streamed tile 1 (dO_j, or V_j), then
+  // 128 fp32 lse * log2(e) and 128 fp32 delta of the stage's queries
+  static constexpr uint32_t kStageBytes = 2 * kTileBytes + 1024;
+  static constexpr uint32_t kBarOff = kStageOff + kStages * kStageBytes;
+  static constexpr int kBarRes = 0;
+  static constexpr int kBarFull = 1;                      // [kStages]
+  static constexpr int kBarEmpty = kBarFull + kStages;    // [kStages]
+  static constexpr int kBarSFull = kBarEmpty + kStages;
+  static constexpr int kBarPFull = kBarSFull + 1;         // [2 halves]
+  static constexpr int kBarFinal = kBarPFull + 2;
+  static constexpr int kBarDrain = kBarFinal + 1;
+  static constexpr int kNumBars = kBarDrain + 1;
+  static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;
+  static constexpr int kThreads = 320;                    // producer, MMA, 8 softmax warps
+  static constexpr uint32_t kTmemCols = 512;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+// delta = rowsum(dO * O) per (b, h, token): one warp per token, D / 8 lanes per head
+__global__ void __launch_bounds__(256) bwd_delta_kernel(const __grid_constant__ BwdParams p) {
+  griddep_launch_dependents();
+  griddep_wait();
+  const int lane = threadIdx.x & 31;
+  const long long tok = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (tok >= (long long)p.B * p.L) return;
+  const int b = (int)(tok / p.L), t = (int)(tok % p.L);
+  const int HD = p.H * p.D, lph = p.D / 8;  // lanes per head
+  const uint4* o4 = reinterpret_cast<const uint4*>(p.O + tok * HD);
+  const uint4* d4 = reinterpret_cast<const uint4*>(p.dO + tok * HD);
+  for (int v0 = 0; v0 < HD / 8; v0 += 32) {
+    const int v = v0 + lane;
+    float acc = 0.f;
+    if (v < HD / 8) {
+      const uint4 a = o4[v], c = d4[v];
+      const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wc[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        acc = fmaf(__uint_as_float(wa[j] << 16), __uint_as_float(wc[j] << 16),
+                   fmaf(__uint_as_float(wa[j] & 0xFFFF0000u), __uint_as_float(wc[j] & 0xFFFF0000u), acc));
+    }
+    for (int o = lph >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    const int h = (v * 8) / p.D;
+    if (v < HD / 8 && (lane % lph) == 0) p.delta[((long long)b * p.H + h) * p.L + t] = acc;
+  }
+}
+
+// Visible query rows of a key tile / key rows of a query tile (block-causal):
+// query i sees key j iff 0 <= chunk(i) - chunk(j) <= window.
+__device__ __forceinline__ void bwd_q_range(const BwdParams& p, int k0, int& qt0, int& nqt) {
+  const int k_last = min(p.L, k0 + kTileN) - 1;
+  const int c_lo = k0 / p.chunk_tokens, c_hi = k_last / p.chunk_tokens;
+  const int qlo = c_lo * p.chunk_tokens;
+  const int qhi = min(p.L, (c_hi + p.window + 1) * p.chunk_tokens);
+  qt0 = qlo / kTileM;
+  nqt = (qhi + kTileM - 1) / kTileM - qt0;
+}
+__device__ __forceinline__ void bwd_k_range(const BwdParams& p, int q0, int& kt0, int& nkt) {
+  const int q_last = min(p.L, q0 + kTileM) - 1;
+  const int c_lo = q0 / p.chunk_tokens, c_hi = q_last / p.chunk_tokens;
+  const int klo = max(0, c_lo - p.window) * p.chunk_tokens;
+  const int khi = min(p.L, (c_hi + 1) * p.chunk_tokens);
+  kt0 = klo / kTileN;
+  nkt = (khi + kTileN - 1) / kTileN - kt0;
+}
+
+// KQ == true: key-tile kernel (dK, dV); false: query-tile kernel (dQ).
+template <int D, bool KQ>
+__global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
+attn_bwd_kernel(const __grid_constant__ BwdParams p) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  const uint32_t base_u32 = (raw_u32 + 1023u) & ~1023u;
+  uint8_t* base = smem_raw + (base_u32 - raw_u32);
+  const uint32_t bars = base_u32 + C::kBarOff;
+  uint32_t* misc = reinterpret_cast<uint32_t*>(base + C::kMiscOff);  // [0] tmem, [1] abort
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
+  auto bar = [&](int i) -> uint32_t { return bars + 8u * (uint32_t)i; };
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bh = blockIdx.y, b = bh / p.H, h = bh - b * p.H;
+  const int r0 = blockIdx.x * 128;  // first row of the resident tile (keys, or queries)
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(C::kBarRes), 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(bar(C::kBarFull + s), 1);
+      mbar_init(bar(C::kBarEmpty + s), 1);
+    }
+    mbar_init(bar(C::kBarSFull), 1);
+    mbar_init(bar(C::kBarPFull + 0), 128);
+    mbar_init(bar(C::kBarPFull + 1), 128);
+    mbar_init(bar(C::kBarFinal), 1);
+    mbar_init(bar(C::kBarDrain), 1);
+    misc[1] = 0;
+    fence_mbar_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(misc), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+  griddep_launch_dependents();
+  griddep_wait();
+  int t0 = 0, nt = 0;  // streamed tiles
+  if (KQ) bwd_q_range(p, r0, t0, nt);
+  else bwd_k_range(p, r0, t0, nt);
+  // resident: K, V (key-tile kernel) or Q, dO (query-tile kernel);
+  // streamed: Q_j, dO_j or K_j, V_j
+  const CUtensorMap* res0 = KQ ? &p.k_map : &p.q_map;
+  const CUtensorMap* res1 = KQ ? &p.v_map : &p.do_map;
+  const CUtensorMap* str0 = KQ ? &p.q_map : &p.k_map;
+  const CUtensorMap* str1 = KQ ? &p.do_map : &p.v_map;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar(C::kBarRes), 2 * C::kTileBytes);
+#pragma unroll
+      for (int bx = 0; bx < C::kBoxes; ++bx) {
+        tma_load_4d(base_u32 + C::kR0Off + bx * C::kBoxBytes, res0, bar(C::kBarRes), bx * 64, r0, h, b);
+        tma_load_4d(base_u32 + C::kR1Off + bx * C::kBoxBytes, res1, bar(C::kBarRes), bx * 64, r0, h, b);
+      }
+    }
+    int j = 0;
+    for (; j < nt; ++j) {
+      const int st = j % C::kStages;
+      bool ok = true;
+      if (j >= C::kStages)
+        ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarEmpty + st), (uint32_t)(j / C::kStages - 1) & 1u,
+                                                  abort_flag, 0));
+      if (!ok) break;
+      const uint32_t so = C::kStageOff + st * C::kStageBytes;
+      const int row = (t0 + j) * 128;
+      if (KQ) {  // lse * log2(e) and delta of the stage's 128 queries (plain loads, whole warp)
+        float* ls = reinterpret_cast<float*>(base + so + 2 * C::kTileBytes);
+        float* dl = ls + 128;
+        for (int i = lane; i < 128; i += 32) {
+          const int q = row + i;
+          const bool in = q < p.L;
+          ls[i] = in ? __ldg(p.LSE + (long long)bh * p.L + q) * kLog2e : INFINITY;
+          dl[i] = in ? __ldg(p.delta + (long long)bh * p.L + q) : 0.f;
+        }
+        __syncwarp();
+      }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar(C::kBarFull + st), 2 * C::kTileBytes);
+#pragma unroll
+        for (int bx = 0; bx < C::kBoxes; ++bx) {
+          tma_load_4d(base_u32 + so + bx * C::kBoxBytes, str0, bar(C::kBarFull + st), bx * 64, row, h, b);
+          tma_load_4d(base_u32 + so + C::kTileBytes + bx * C::kBoxBytes, str1, bar(C::kBarFull + st), bx * 64,
+                      row, h, b);
+        }
+      }
+      __syncwarp();
+    }
+    if (lane == 0 && *abort_flag) {
+      wait_drain(bar(C::kBarRes), 0);
+      for (int jj = max(0, j - C::kStages); jj < j; ++jj)
+        wait_drain(bar(C::kBarFull + jj % C::kStages), (uint32_t)(jj / C::kStages) & 1u);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0);  // scores: N = 128 rows of the streamed tile
+    constexpr uint32_t idesc_acc = idesc_bf16_f32(128, D, 1);  // accumulators: B MN-major, N = D
+    constexpr uint32_t kStageStep = C::kStageBytes >> 4;
+    bool ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarRes), 0, abort_flag, 1));
+    if (ok) tc_fence_after();
+    const uint64_t dr0 = smem_desc_sw128(base_u32 + C::kR0Off, 16, 1024);
+    const uint64_t dr1 = smem_desc_sw128(base_u32 + C::kR1Off, 16, 1024);
+    const uint64_t ds0 = smem_desc_sw128(base_u32 + C::kStageOff, 16, 1024);
+    const uint64_t ds1 = smem_desc_sw128(base_u32 + C::kStageOff + C::kTileBytes, 16, 1024);
+    const uint64_t dm0 = smem_desc_sw128(base_u32 + C::kStageOff, C::kBoxBytes, 1024);  // streamed tile 0, MN-major
+    const uint64_t dm1 = smem_desc_sw128(base_u32 + C::kStageOff + C::kTileBytes, C::kBoxBytes, 1024);
+    const uint32_t hi_k = (uint32_t)(dr0 >> 32), hi_mn = (uint32_t)(dm0 >> 32);
+    // scores of the resident tile against a streamed tile: d = A_res . B_str^T
+    auto scores = [&](uint32_t d, uint64_t a, uint64_t bdesc, uint32_t st) {
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t koff = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
+        mma_ss_e(d, make_desc((uint32_t)a + koff, hi_k), make_desc((uint32_t)bdesc + st * kStageStep + koff, hi_k),
+                 idesc_s, kk > 0 ? 1u : 0u);
+      }
+    };
+    // acc += X . streamed tile (X: bf16 rows of 128 written to TMEM at column
+    // a_col, half h in columns [64h, 64h + 32); the streamed tile as the
+    // MN-major B operand, K = its 128 rows)
+    auto accum = [&](uint32_t d, uint32_t a_col, uint64_t bmn, uint32_t st, bool first) {
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t ac = a_col + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
+        mma_ts_e(d, tmem + ac, make_desc((uint32_t)bmn + st * kStageStep + ((kk * 16 * 128) >> 4), hi_mn),
+                 idesc_acc, (first && kk == 0) ? 0u : 1u);
+      }
+    };
+    for (int j = 0; ok && j < nt; ++j) {
+      const uint32_t st = (uint32_t)(j % C::kStages);
+      if (!(ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarFull + st), (uint32_t)(j / C::kStages) & 1u,
+                                                      abort_flag, 5))))
+        break;
+      tc_fence_after();
+      scores(tmem + 0, dr0, ds0, st);    // S^T = K Q^T  (or S = Q K^T)
+      scores(tmem + 128, dr1, ds1, st);  // dP^T = V dO^T (or dP = dO V^T)
+      mma_commit_e(bar(C::kBarSFull));
+      if (!(ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarPFull + 0), (uint32_t)j & 1u, abort_flag, 2))))
+        break;
+      if (!(ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarPFull + 1), (uint32_t)j & 1u, abort_flag, 3))))
+        break;
+      tc_fence_after();
+      if (KQ) {
+        accum(tmem + 256, 0, dm1, st, j == 0);      // dV += P^T dO
+        accum(tmem + 256 + D, 128, dm0, st, j == 0);  // dK += dS^T Q
+      } else {
+        accum(tmem + 256, 0, dm0, st, j == 0);      // dQ += dS K
+      }
+      mma_commit_e(bar(C::kBarEmpty + st));
+    }
+    if (ok) mma_commit_e(bar(C::kBarFinal));
+    if (!ok) {
+      mma_commit_e(bar(C::kBarDrain));
+      if (lane == 0) wait_drain(bar(C::kBarDrain), 0);
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------- probabilities + epilogue
+    const int hf = (warp - 2) >> 2;  // half of the streamed tile's 128 rows
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;  // row of the resident tile
+    const int r = r0 + row;
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const uint32_t tS = tmem + lane_off + hf * 64, tdP = tmem + lane_off + 128 + hf * 64;
+    // visible interval of the streamed rows for this resident row
+    int vlo = 0, vhi = 0;
+    float lse2 = 0.f, dlt = 0.f;
+    if (r < p.L) {
+      const int c = r / p.chunk_tokens;
+      if (KQ) {  // key r: queries of chunks c .. c + W
+        vlo = c * p.chunk_tokens;
+        vhi = min(p.L, (c + p.window + 1) * p.chunk_tokens);
+      } else {   // query r: keys of chunks c - W .. c
+        vlo = max(0, c - p.window) * p.chunk_tokens;
+        vhi = min(p.L, (c + 1) * p.chunk_tokens);
+        lse2 = __ldg(p.LSE + (long long)bh * p.L + r) * kLog2e;
+        dlt = __ldg(p.delta + (long long)bh * p.L + r);
+      }
+    }
+    const float sc = p.scale_log2;
+    bool ok = true;
+    for (int j = 0; j < nt; ++j) {
+      ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarSFull), (uint32_t)j & 1u, abort_flag, 6 + hf));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t s0[32], s1[32], d0[32], d1[32];
+      tmem_ld32(tS, s0);
+      tmem_ld32(tS + 32, s1);
+      tmem_ld32(tdP, d0);
+      tmem_ld32(tdP + 32, d1);
+      const int c0 = (t0 + j) * 128 + hf * 64;  // first streamed row of this half
+      const int lo = vlo - c0, hi = vhi - c0;
+      const float* ls = reinterpret_cast<const float*>(base + C::kStageOff + (j % C::kStages) * C::kStageBytes +
+                                                       2 * C::kTileBytes) + hf * 64;
+      const float* dl = ls + 128;
+      tmem_wait_ld();
+      uint32_t pk[32], dk[32];
+      auto one = [&](uint32_t s, uint32_t dpv, int c, float& pv, float& dsv) {
+        const bool vis = c >= lo && c < hi;
+        const float l2 = KQ ? ls[c] : lse2;
+        const float de = KQ ? dl[c] : dlt;
+        pv = vis ? ex2(fmaf(__uint_as_float(s), sc, -l2)) : 0.f;
+        dsv = pv * (__uint_as_float(dpv) - de);
+      };
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        float pa, pb, da, db;
+        one(s0[2 * c], d0[2 * c], 2 * c, pa, da);
+        one(s0[2 * c + 1], d0[2 * c + 1], 2 * c + 1, pb, db);
+        pk[c] = pack_bf16(pa, pb);
+        dk[c] = pack_bf16(da, db);
+        one(s1[2 * c], d1[2 * c], 32 + 2 * c, pa, da);
+        one(s1[2 * c + 1], d1[2 * c + 1], 33 + 2 * c, pb, db);
+        pk[16 + c] = pack_bf16(pa, pb);
+        dk[16 + c] = pack_bf16(da, db);
+      }
+      if (KQ) {
+        tmem_st32(tS, pk);   // P^T over S^T
+        tmem_st32(tdP, dk);  // dS^T over dP^T
+      } else {
+        tmem_st32(tS, dk);   // dS over S
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(C::kBarPFull + hf));
+    }
+    // ------------------------------------------------------------ epilogue
+    if (ok) ok = wait_bounded(bar(C::kBarFinal), 0, abort_flag, 8);
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) {  // warp-uniform: tcgen05.ld is warp-collective, rows past L only skip the store
+      tc_fence_after();
+      // key-tile kernel: half 0 writes the dV row, half 1 the dK row;
+      // query-tile kernel: half h writes columns [h D/2, (h + 1) D/2) of dQ
+      constexpr int kCols = KQ ? D : D / 2;
+      const uint32_t src = tmem + lane_off + 256 + (KQ ? hf * D : hf * (D / 2));
+      uint16_t* dst = (KQ ? (hf == 0 ? p.dV : p.dK) : p.dQ) + (((long long)b * p.L + r) * p.H + h) * D +
+                      (KQ ? 0 : hf * (D / 2));
+      const float mul = (KQ && hf == 0) ? 1.f : p.scale;  // dK, dQ carry the softmax scale
+#pragma unroll
+      for (int cc = 0; cc < kCols; cc += 32) {
+        uint32_t o[32];
+        if (nt > 0) {
+          tmem_ld32(src + cc, o);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) o[c] = 0u;
+        }
+        if (r >= p.L) continue;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          uint4 w;
+          w.x = pack_bf16(__uint_as_float(o[8 * v + 0]) * mul, __uint_as_float(o[8 * v + 1]) * mul);
+          w.y = pack_bf16(__uint_as_float(o[8 * v + 2]) * mul, __uint_as_float(o[8 * v + 3]) * mul);
+          w.z = pack_bf16(__uint_as_float(o[8 * v + 4]) * mul, __uint_as_float(o[8 * v + 5]) * mul);
+          w.w = pack_bf16(__uint_as_float(o[8 * v + 6]) * mul, __uint_as_float(o[8 * v + 7]) * mul);
+          reinterpret_cast<uint4*>(dst + cc)[v] = w;
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int D, bool KQ>
+cudaError_t launch_bwd_impl(const BwdParams& p, cudaStream_t s) {
+  using C = BwdCfg<D>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<D, KQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((p.L + 127) / 128, p.B * p.H, 1);
+  cfg.blockDim = dim3(C::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attn_bwd_kernel<D, KQ>, p);
+}
+
 // Self-test of the failure detection: one CTA waits, with the pipeline's own
 // bounded wait, on an mbarrier that nothing ever completes.  The wait gives
 // up after timeout_ns, records its site (bit 30) in the device error word and
@@ -1651,6 +2037,30 @@ __global__ void wait_timeout_probe_kernel(uint64_t timeout_ns) {
 }
 
 }  // namespace
+
+cudaError_t launch_attention_backward(const BwdParams& p, cudaStream_t s) {
+  const long long tokens = (long long)p.B * p.L;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((tokens + 7) / 8), 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, bwd_delta_kernel, p);
+  if (e != cudaSuccess) return e;
+  if (p.D == 128) {
+    e = launch_bwd_impl<128, true>(p, s);
+    return e != cudaSuccess ? e : launch_bwd_impl<128, false>(p, s);
+  }
+  if (p.D == 64) {
+    e = launch_bwd_impl<64, true>(p, s);
+    return e != cudaSuccess ? e : launch_bwd_impl<64, false>(p, s);
+  }
+  return cudaErrorInvalidValue;
+}
 
 cudaError_t launch_wait_timeout_probe(unsigned long long timeout_ns, cudaStream_t s) {
   wait_timeout_probe_kernel<<<1, 32, 0, s>>>(timeout_ns);

@@ -660,6 +660,49 @@ sab_status sab_block_causal_attention(const void* Q, const void* K, const void* 
   return launch_attention(p, L, num_splits, workspace, ws_bytes, stream);
 }
 
+size_t sab_block_causal_attention_backward_workspace(int B, int L, int H) {
+  if (B < 1 || L < 1 || H < 1) return 0;
+  return align_up((size_t)B * H * L * sizeof(float), kAlign);
+}
+
+sab_status sab_block_causal_attention_backward(const void* Q, const void* K, const void* V, const void* O,
+                                               const void* dO, const float* LSE, int B, int L, int H, int D,
+                                               int chunk_tokens, int window, float softmax_scale, void* dQ,
+                                               void* dK, void* dV, void* workspace, size_t ws_bytes,
+                                               void* stream) {
+  const void* ins[] = {Q, K, V, O, dO, dQ, dK, dV};
+  for (const void* x : ins)
+    if (x == nullptr || !aligned16(x)) return SAB_ERR_INVALID_ARG;
+  if (LSE == nullptr || (reinterpret_cast<uintptr_t>(LSE) & 3u) != 0) return SAB_ERR_INVALID_ARG;
+  if (B < 1 || L < 1 || H < 1 || (D != 64 && D != 128) || chunk_tokens < 1 || window < 0) return SAB_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.f) || !isfinite(softmax_scale)) return SAB_ERR_INVALID_ARG;
+  if ((long long)L > (1LL << 30) || (long long)B * H > 65535) return SAB_ERR_INVALID_ARG;
+  if (workspace == nullptr || ws_bytes < sab_block_causal_attention_backward_workspace(B, L, H) ||
+      (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0)
+    return SAB_ERR_WORKSPACE;
+  BwdParams p;
+  memset(&p, 0, sizeof(p));
+  p.O = static_cast<const uint16_t*>(O);
+  p.dO = static_cast<const uint16_t*>(dO);
+  p.LSE = LSE;
+  p.delta = static_cast<float*>(workspace);
+  p.dQ = static_cast<uint16_t*>(dQ);
+  p.dK = static_cast<uint16_t*>(dK);
+  p.dV = static_cast<uint16_t*>(dV);
+  p.B = B;
+  p.H = H;
+  p.D = D;
+  p.L = L;
+  p.chunk_tokens = chunk_tokens;
+  p.window = window;
+  p.scale = softmax_scale;
+  p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  if (!encode_token_major(&p.q_map, Q, B, L, H, D) || !encode_token_major(&p.k_map, K, B, L, H, D) ||
+      !encode_token_major(&p.v_map, V, B, L, H, D) || !encode_token_major(&p.do_map, dO, B, L, H, D))
+    return SAB_ERR_CUDA;
+  return launch_attention_backward(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SAB_OK : SAB_ERR_CUDA;
+}
+
 sab_status sab_selftest_bounded_wait(unsigned long long timeout_ns, void* stream) {
   if (timeout_ns < 1000000ull || timeout_ns > 2000000000ull) return SAB_ERR_INVALID_ARG;
   return launch_wait_timeout_probe(timeout_ns, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SAB_OK

@@ -169,11 +169,28 @@ struct RopeParams {
   float eps;
 };
 
+// Backward of block-causal attention (token-major [B, L, H, D] tensors).
+struct BwdParams {
+  CUtensorMap q_map, k_map, v_map, do_map;  // dims (D, L, H, B), box (64, 128, 1, 1), SW128
+  const uint16_t* O;      // forward output
+  const uint16_t* dO;
+  const float* LSE;       // [B, H, L] natural-log LSE of the forward
+  float* delta;           // [B, H, L] workspace: sum_d dO * O
+  uint16_t* dQ;
+  uint16_t* dK;
+  uint16_t* dV;
+  int B, H, D, L;
+  int chunk_tokens, window;
+  float scale;            // softmax scale
+  float scale_log2;       // scale * log2(e)
+};
+
 // Launchers (return cudaError_t of the launch).
 cudaError_t launch_append_bf16(const AppendParams& p, cudaStream_t s);
 cudaError_t launch_append_fp8(const AppendParams& p, cudaStream_t s);
 cudaError_t launch_counter_add(long long* counter, long long delta, cudaStream_t s);
 cudaError_t launch_qk_rope(const RopeParams& p, cudaStream_t s);
+cudaError_t launch_attention_backward(const BwdParams& p, cudaStream_t s);
 cudaError_t launch_wait_timeout_probe(unsigned long long timeout_ns, cudaStream_t s);
 cudaError_t launch_chunk_attention(const AttnParams& p, int q_tiles_per_cta, cudaStream_t s);
 // One query tile per CTA, key-half softmax warpgroups; unsplit KV only.

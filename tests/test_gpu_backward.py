@@ -1,0 +1,62 @@
+"""GPU parity of the block-causal attention backward against the fp64
+gradient oracle (``oracle/backward.py``), on the same bf16 inputs.
+
+The GPU path runs the GPU forward for O and LSE, then the backward.  Error
+budget per output element (derived from the arithmetic): P and dS are
+rounded to bf16 before the gradient MMAs (2^-9 relative each), delta uses
+the bf16 forward output, the MMAs accumulate exact bf16 products in fp32,
+and the result is rounded to bf16 once -- so |gpu - ref| <= 2^-6 * bound +
+2^-8 * |ref| + 1e-5, with the oracle's per-element error scale ``bound``
+(an 8x margin over the first-order estimate 2^-9 * bound)."""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import backward as OB
+from streaming_attention_block_gb300 import synth
+import streaming_attention_block_gb300 as sab
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    sab.library()
+
+
+CASES = [
+    # (B, L, H, D, chunk_tokens, window)
+    ("aligned", 1, 640, 2, 128, 128, 1),
+    ("ragged_d64", 2, 500, 2, 64, 100, 2),
+    ("long_chunks", 1, 3 * 1536, 2, 128, 1536, 2),
+]
+
+
+@pytest.mark.parametrize("name,B,L,H,D,Lc,W", CASES, ids=[c[0] for c in CASES])
+def test_backward_matches_oracle(name, B, L, H, D, Lc, W):
+    gen = torch.Generator().manual_seed(4242 + L)
+    q, k, v, do = (synth.randn_bf16(gen, (B, L, H, D), "cpu") for _ in range(4))
+    scale = D ** -0.5
+    qd, kd, vd, dod = (x.cuda() for x in (q, k, v, do))
+    O = torch.empty_like(qd)
+    LSE = torch.empty((B, H, L), dtype=torch.float32, device="cuda")
+    sab.block_causal_attention(qd, kd, vd, Lc, W, 1, scale, O, LSE)
+    dQ, dK, dV = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    sab.block_causal_attention_backward(qd, kd, vd, O, dod, LSE, Lc, W, scale, dQ, dK, dV)
+    torch.cuda.synchronize()
+    assert sab.get_last_device_error() == 0
+    f64 = lambda t: t.float().numpy().astype(np.float64)
+    refs, bounds = OB.block_causal_attention_backward(f64(q), f64(k), f64(v), f64(do), Lc, W, scale,
+                                                      abs_bounds=True)
+    for nm, got, ref, bnd in zip(("dQ", "dK", "dV"), (dQ, dK, dV), refs, bounds):
+        g = f64(got.cpu())
+        err = np.abs(g - ref)
+        tol = 2.0 ** -6 * bnd + 2.0 ** -8 * np.abs(ref) + 1e-5
+        bad = np.argwhere(err > tol)
+        assert bad.size == 0, (f"{name} {nm}: {len(bad)} elements out of tolerance; max err {err.max():.3e}, "
+                               f"worst ratio {np.max(err / tol):.2f}, first {bad[:3]}")
+        # and the bulk is far tighter than the bound
+        assert np.mean(err) <= 2.0 ** -8 * np.mean(np.abs(ref)) + 1e-5, f"{name} {nm}: mean error too large"
