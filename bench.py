@@ -489,6 +489,16 @@ def run_sweep(args):
         sab.block_causal_attention(q, k, v, w.Lc, w.W, 0, w.scale, O, L, None, stream)
 
     report("block_causal", timed(bc, 10), flops, 0, {"tokens": Lt})
+    # backward of the same shape: algorithmic 10 D flops per visible pair
+    # (S recompute, dP, dV, dK, dQ); the kernels recompute S and dP once more
+    do = synth.randn_bf16(g, tuple(q.shape), "cuda")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    bws = torch.empty(sab.block_causal_attention_backward_workspace(w.B, Lt, w.H), dtype=torch.uint8, device="cuda")
+
+    def bwd():
+        sab.block_causal_attention_backward(q, k, v, O, do, L, w.Lc, w.W, w.scale, dq, dk, dv, bws, stream)
+
+    report("block_causal_backward", timed(bwd, 10), 2.5 * flops, 0, {"tokens": Lt})
     assert sab.get_last_device_error(stream) == 0
 
 

@@ -72,3 +72,46 @@ def block_causal_attention_backward(q_blhd, k_blhd, v_blhd, do_blhd, chunk_token
                 bnd[1][b, :, h] = scale * (np.abs(ds).T @ np.abs(qh) + p.T @ (dabs * np.abs(qh)))
                 bnd[2][b, :, h] = np.abs(p).T @ np.abs(doh)
     return (tuple(out), tuple(bnd)) if abs_bounds else tuple(out)
+
+
+def block_causal_attention_backward_rows(q_blhd, k_blhd, v_blhd, do_blhd, chunk_tokens: int, window: int,
+                                         scale: float, b: int, h: int, q_rows, k_rows):
+    """The same gradients for one (batch, head), only at sampled rows: dQ at
+    ``q_rows`` and dK, dV at ``k_rows`` (float64 [n, D] each, plus the error
+    scales of ``block_causal_attention_backward``).  Every query that sees a
+    sampled key contributes its full softmax row, computed chunk by chunk
+    over the keys that chunk sees; no other reordering."""
+    q, k, v, do = (np.asarray(x[b, :, h], dtype=np.float64) for x in (q_blhd, k_blhd, v_blhd, do_blhd))
+    L, D = q.shape
+    Lc, W = int(chunk_tokens), int(window)
+    q_rows, k_rows = np.asarray(q_rows), np.asarray(k_rows)
+    nchunks = (L + Lc - 1) // Lc
+    need = set((q_rows // Lc).tolist())
+    for c in set((k_rows // Lc).tolist()):
+        need.update(range(c, min(nchunks, c + W + 1)))
+    dq, bq = np.zeros((len(q_rows), D)), np.zeros((len(q_rows), D))
+    dk, bk = np.zeros((len(k_rows), D)), np.zeros((len(k_rows), D))
+    dv, bv = np.zeros((len(k_rows), D)), np.zeros((len(k_rows), D))
+    for c in sorted(need):
+        qs = np.arange(c * Lc, min(L, (c + 1) * Lc))
+        ks = np.arange(max(0, c - W) * Lc, min(L, (c + 1) * Lc))  # keys of chunks c - W .. c
+        s = scale * (q[qs] @ k[ks].T)
+        e = np.exp(s - s.max(axis=1, keepdims=True))
+        p = e / e.sum(axis=1, keepdims=True)
+        o = p @ v[ks]
+        delta = np.sum(do[qs] * o, axis=1, keepdims=True)
+        ds = p * (do[qs] @ v[ks].T - delta)
+        dabs = np.sum(np.abs(do[qs] * o), axis=1, keepdims=True)
+        sel = np.nonzero((q_rows // Lc) == c)[0]
+        if sel.size:
+            li = q_rows[sel] - c * Lc
+            dq[sel] = scale * (ds[li] @ k[ks])
+            bq[sel] = scale * (np.abs(ds[li]) @ np.abs(k[ks]) + dabs[li] * (p[li] @ np.abs(k[ks])))
+        kin = np.nonzero((k_rows >= ks[0]) & (k_rows <= ks[-1]))[0]
+        if kin.size:
+            lj = k_rows[kin] - ks[0]
+            dv[kin] += p[:, lj].T @ do[qs]
+            bv[kin] += p[:, lj].T @ np.abs(do[qs])
+            dk[kin] += scale * (ds[:, lj].T @ q[qs])
+            bk[kin] += scale * (np.abs(ds[:, lj]).T @ np.abs(q[qs]) + p[:, lj].T @ (dabs * np.abs(q[qs])))
+    return (dq, dk, dv), (bq, bk, bv)

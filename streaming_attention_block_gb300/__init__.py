@@ -17,6 +17,7 @@ from ._abi import (  # noqa: F401
     SabError,
     block_causal_attention,
     block_causal_attention_backward,
+    block_causal_attention_backward_workspace,
     block_causal_attention_workspace,
     chunk_attention,
     chunk_attention_dev,

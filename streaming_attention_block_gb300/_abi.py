@@ -241,6 +241,10 @@ def chunk_counter_add(d_chunk, delta: int = 1, stream=None):
            "chunk_counter_add")
 
 
+def block_causal_attention_backward_workspace(B: int, L: int, H: int) -> int:
+    return int(library().sab_block_causal_attention_backward_workspace(B, L, H))
+
+
 def block_causal_attention_backward(Q, K, V, O, dO, LSE, chunk_tokens: int, window: int, softmax_scale: float,
                                     dQ, dK, dV, workspace=None, stream=None):
     """sab_block_causal_attention_backward: (dQ, dK, dV) of block-causal

@@ -68,3 +68,21 @@ def test_structure_and_bounds():
     # every query's probabilities sum to 1, so the value gradients of all keys
     # sum to the sum of the output gradients
     assert np.allclose(dv.sum(axis=1), do.sum(axis=1))
+
+
+def test_sampled_rows_equal_full():
+    """The row-restricted form returns the full form's rows (ragged last
+    chunk, window 2, rows at chunk edges and inside)."""
+    B, L, H, D, Lc, W = 2, 340, 2, 16, 64, 2
+    q, k, v, do = _inputs(B, L, H, D, 11)
+    (fq, fk, fv), (gq, gk, gv) = OB.block_causal_attention_backward(q, k, v, do, Lc, W, 0.3, abs_bounds=True)
+    qr = np.array([0, 63, 64, 200, 339])
+    kr = np.array([1, 64, 127, 128, 300, 339])
+    for b, h in ((0, 1), (1, 0)):
+        (dq, dk, dv), (bq, bk, bv) = OB.block_causal_attention_backward_rows(q, k, v, do, Lc, W, 0.3, b, h, qr, kr)
+        np.testing.assert_allclose(dq, fq[b, qr, h], rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(dk, fk[b, kr, h], rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(dv, fv[b, kr, h], rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(bq, gq[b, qr, h], rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(bk, gk[b, kr, h], rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(bv, gv[b, kr, h], rtol=1e-12, atol=1e-13)
