@@ -244,6 +244,41 @@ sab_status sab_block_causal_attention_backward(const void* Q, const void* K, con
                                                void* stream);
 
 /*
+ * Block-causal attention behind a variable-length memory prefix (training
+ * with compressed memory: "WorldPlay2: Extending Real-Time Interactive World
+ * Models in Control and Horizon", Figure 3 and section 方法步骤详情, training
+ * stage 3, where the padded variable-length memory is attended with a mask).
+ * Each sample's L tokens are mem_pad memory positions, of which the first
+ * mem_len[b] are real and the rest padding, then target tokens in chunks of
+ * chunk_tokens (target token t is in chunk (t - mem_pad) / chunk_tokens).
+ * A real memory query sees the real memory; a target query of chunk c sees
+ * the real memory and the target chunks c - window .. c; padding sees nothing
+ * and is seen by nothing, so padded rows get O = 0 and LSE = -inf (and zero
+ * gradients).
+ * Q, K, V, O  device, token-major [B, L, H, D] bf16, 16-byte aligned.
+ * mem_len     device int32 [B], 4-byte aligned; values are clamped to
+ *             [0, mem_pad] on the device.  May be NULL when mem_pad == 0
+ *             (then this is sab_block_causal_attention with one split).
+ * LSE         device [B, H, L] fp32 or NULL.  No workspace; one query tile
+ *             of 128 rows per CTA.  D must be 64 or 128.
+ * Errors: INVALID_ARG (pointers, sizes, mem_pad outside [0, L]), CUDA.
+ */
+sab_status sab_memory_prefix_attention(const void* Q, const void* K, const void* V, int B, int L, int H, int D,
+                                       int mem_pad, const int* mem_len, int chunk_tokens, int window,
+                                       float softmax_scale, void* O, float* LSE, void* stream);
+
+/*
+ * Gradients of sab_memory_prefix_attention (same formulas and arguments as
+ * sab_block_causal_attention_backward, plus mem_pad and mem_len as above;
+ * the workspace size is sab_block_causal_attention_backward_workspace).
+ */
+sab_status sab_memory_prefix_attention_backward(const void* Q, const void* K, const void* V, const void* O,
+                                                const void* dO, const float* LSE, int B, int L, int H, int D,
+                                                int mem_pad, const int* mem_len, int chunk_tokens, int window,
+                                                float softmax_scale, void* dQ, void* dK, void* dV, void* workspace,
+                                                size_t ws_bytes, void* stream);
+
+/*
  * Fused Q/K normalisation and rotary embedding of one chunk, with the K/V
  * append ("WorldPlay2: Extending Real-Time Interactive World Models in
  * Control and Horizon", section 方法步骤详情: QKRoPE and QKV fusion;

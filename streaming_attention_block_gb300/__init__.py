@@ -38,6 +38,8 @@ from ._abi import (  # noqa: F401
     kv_ring_slot_of,
     library,
     library_path,
+    memory_prefix_attention,
+    memory_prefix_attention_backward,
     qk_norm_rope,
     selftest_bounded_wait,
     status_string,

@@ -76,6 +76,9 @@ def library() -> ctypes.CDLL:
         "sab_qk_norm_rope": (I, [P, I, LL, P, P, P, P, P, P, P, P, P, I, P]),
         "sab_block_causal_attention_backward_workspace": (SZ, [I, I, I]),
         "sab_block_causal_attention_backward": (I, [P, P, P, P, P, P, I, I, I, I, I, I, F, P, P, P, P, SZ, P]),
+        "sab_memory_prefix_attention": (I, [P, P, P, I, I, I, I, I, P, I, I, F, P, P, P]),
+        "sab_memory_prefix_attention_backward": (I, [P, P, P, P, P, P, I, I, I, I, I, P, I, I, F, P, P, P, P, SZ,
+                                                     P]),
         "sab_status_string": (ctypes.c_char_p, [I]),
         "sab_version": (ctypes.c_char_p, []),
     }
@@ -260,6 +263,37 @@ def block_causal_attention_backward(Q, K, V, O, dO, LSE, chunk_tokens: int, wind
         B, L, H, D, int(chunk_tokens), int(window), float(softmax_scale), _ptr(dQ, torch.bfloat16, "dQ"),
         _ptr(dK, torch.bfloat16, "dK"), _ptr(dV, torch.bfloat16, "dV"), _ptr(workspace, None, "workspace"),
         ws_bytes, _stream(stream)), "block_causal_attention_backward")
+
+
+def memory_prefix_attention(Q, K, V, mem_pad: int, mem_len, chunk_tokens: int, window: int, softmax_scale: float,
+                            O, LSE=None, stream=None):
+    """sab_memory_prefix_attention: block-causal target chunks behind a
+    per-sample memory prefix of mem_pad positions, mem_len (device int32 [B])
+    of them real (see include/sab.h)."""
+    B, L, H, D = Q.shape
+    _check(library().sab_memory_prefix_attention(
+        _ptr(Q, torch.bfloat16, "Q"), _ptr(K, torch.bfloat16, "K"), _ptr(V, torch.bfloat16, "V"),
+        B, L, H, D, int(mem_pad), _ptr(mem_len, torch.int32, "mem_len"), int(chunk_tokens), int(window),
+        float(softmax_scale), _ptr(O, torch.bfloat16, "O"), _ptr(LSE, torch.float32, "LSE"), _stream(stream)),
+        "memory_prefix_attention")
+
+
+def memory_prefix_attention_backward(Q, K, V, O, dO, LSE, mem_pad: int, mem_len, chunk_tokens: int, window: int,
+                                     softmax_scale: float, dQ, dK, dV, workspace=None, stream=None):
+    """sab_memory_prefix_attention_backward: (dQ, dK, dV) of
+    memory_prefix_attention from its O and LSE (see include/sab.h)."""
+    B, L, H, D = Q.shape
+    if workspace is None:
+        n = int(library().sab_block_causal_attention_backward_workspace(B, L, H))
+        workspace = torch.empty(n, dtype=torch.uint8, device=Q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(library().sab_memory_prefix_attention_backward(
+        _ptr(Q, torch.bfloat16, "Q"), _ptr(K, torch.bfloat16, "K"), _ptr(V, torch.bfloat16, "V"),
+        _ptr(O, torch.bfloat16, "O"), _ptr(dO, torch.bfloat16, "dO"), _ptr(LSE, torch.float32, "LSE"),
+        B, L, H, D, int(mem_pad), _ptr(mem_len, torch.int32, "mem_len"), int(chunk_tokens), int(window),
+        float(softmax_scale), _ptr(dQ, torch.bfloat16, "dQ"), _ptr(dK, torch.bfloat16, "dK"),
+        _ptr(dV, torch.bfloat16, "dV"), _ptr(workspace, None, "workspace"), ws_bytes, _stream(stream)),
+        "memory_prefix_attention_backward")
 
 
 def block_causal_attention_workspace(B: int, L: int, H: int, D: int, num_splits: int) -> int:

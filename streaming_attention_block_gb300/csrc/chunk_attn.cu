@@ -174,7 +174,7 @@ __device__ __forceinline__ Tile stream_tile(const KeyPlan& kp, int g) {
 }
 
 __device__ __forceinline__ Tile tile_at(const AttnParams& p, const KeyPlan& kp, int g) {
-  if (p.mode == kModeStreaming) return stream_tile(kp, g);
+  if (p.mode != kModeBlockCausal) return stream_tile(kp, g);
   Tile ti;
   ti.src = 0;
   ti.row = g * kTileN;
@@ -186,7 +186,7 @@ __device__ __forceinline__ Tile tile_at(const AttnParams& p, const KeyPlan& kp, 
 __device__ __forceinline__ void kv_range(const AttnParams& p, const KeyPlan& kp, int q0, int qrows, int split,
                                          int& first, int& count) {
   int total = 0, base = 0;
-  if (p.mode == kModeStreaming) {
+  if (p.mode != kModeBlockCausal) {
     total = kp.total_tiles;
   } else {
     const int q_last = min(p.Lq, q0 + qrows) - 1;
@@ -202,6 +202,33 @@ __device__ __forceinline__ void kv_range(const AttnParams& p, const KeyPlan& kp,
   const long long e = (long long)total * (split + 1) / p.splits;
   first = base + (int)a;
   count = (int)(e - a);
+}
+
+// Key runs of the query rows [q0, q0 + qrows) behind a memory prefix
+// ("WorldPlay2", Figure 3 and section 方法步骤详情, training stage 3): the
+// first P = mem_len[b] positions are real memory that every real query sees;
+// target chunk c (tokens from mem_pad on) also sees target chunks c - W .. c.
+// Run 0: the real memory [0, P), when any row of the tile sees it; run 1:
+// the union of the target rows' chunk windows.  Padding is in neither.
+__device__ __forceinline__ void plan_prefix_runs(const AttnParams& p, int b, int q0, int qrows, KeyPlan& kp) {
+  const int M = p.mem_pad;
+  const int P = min(max(__ldg(p.mem_len + b), 0), M);
+  const int q_last = min(p.Lq, q0 + qrows) - 1;
+  const bool any_target = q_last >= M;
+  const int nmem = (q0 < P || any_target) ? P : 0;
+  int klo = M, khi = M;
+  if (any_target) {
+    const int c_lo = (max(q0, M) - M) / p.chunk_tokens, c_hi = (q_last - M) / p.chunk_tokens;
+    klo = M + max(0, c_lo - p.window) * p.chunk_tokens;
+    khi = min(p.Lk, M + (c_hi + 1) * p.chunk_tokens);
+  }
+  const int t1 = (nmem + kTileN - 1) / kTileN;
+  kp.nseg = 2;
+  kp.seg[0] = KvSegment{0, 0, nmem, 0};
+  kp.seg[1] = KvSegment{0, klo, khi - klo, t1};
+#pragma unroll
+  for (int i = 2; i < kMaxSegments; ++i) kp.seg[i] = KvSegment{0, 0, 0, 0x7fffffff};
+  kp.total_tiles = t1 + (khi - klo + kTileN - 1) / kTileN;
 }
 
 // Expand one key/value row of 128 8-bit codes in place into 128 bf16 values.
@@ -1200,6 +1227,8 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
   KeyPlan kp;
   if (p.mode == kModeStreaming && p.d_chunk != nullptr)
     plan_key_runs(*p.d_chunk, p.window, p.ring_slots, p.chunk_tokens, p.has_sink, p.use_sink, p.kcur, kp);
+  else if (p.mode == kModeMemPrefix)
+    plan_prefix_runs(p, b, q0, kTileM, kp);
   else
     kp = p.plan;
   int first = 0, n_tiles = 0;
@@ -1373,11 +1402,17 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
     const uint32_t tSh = tmem + lane_off + (uint32_t)hf * 64u;  // + buffer * 128
     const uint32_t tO = tmem + lane_off + C::kTmemO + (uint32_t)hf * D;
     const int kofs = hf * 64;  // first key of this half inside a tile
-    int klo = 0, khi = 0;
-    if (p.mode == kModeBlockCausal && row_valid) {
-      const int qc = q_row / p.chunk_tokens;
-      klo = max(0, qc - p.window) * p.chunk_tokens;
-      khi = min(p.Lk, (qc + 1) * p.chunk_tokens);
+    // visible keys of this row: block-causal window [klo, khi); behind a
+    // memory prefix also the memory run [0, mhi)
+    int klo = 0, khi = 0, mhi = 0;
+    if (p.mode != kModeStreaming && row_valid) {
+      const int tq = q_row - p.mem_pad;  // position among the target tokens
+      if (tq >= 0) {
+        const int qc = tq / p.chunk_tokens;
+        klo = p.mem_pad + max(0, qc - p.window) * p.chunk_tokens;
+        khi = min(p.Lk, p.mem_pad + (qc + 1) * p.chunk_tokens);
+      }
+      if (p.mode == kModeMemPrefix) mhi = (tq >= 0 || q_row < kp.seg[0].nrows) ? kp.seg[0].nrows : 0;
     }
     const float sl = p.scale_log2;
     int seg_tile0[kMaxSegments], seg_rows[kMaxSegments], seg_row0[kMaxSegments];
@@ -1401,7 +1436,7 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
       int lo, hi;
       int tile_row0 = 0;
       const int g = first + j;
-      if (p.mode == kModeStreaming) {
+      if (p.mode != kModeBlockCausal) {
         int sg = 0;
 #pragma unroll
         for (int i = 1; i < kMaxSegments; ++i) sg = (g >= seg_tile0[i]) ? i : sg;
@@ -1412,9 +1447,14 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
           nr = (sg == i) ? seg_rows[i] : nr;
           r0 = (sg == i) ? seg_row0[i] : r0;
         }
-        lo = 0;
-        hi = nr - (g - t0) * kTileN;
         tile_row0 = r0 + (g - t0) * kTileN;
+        if (p.mode == kModeStreaming) {
+          lo = 0;
+          hi = nr - (g - t0) * kTileN;
+        } else {  // memory run, then the chunk window
+          lo = (sg == 0 ? 0 : klo) - tile_row0;
+          hi = (sg == 0 ? mhi : khi) - tile_row0;
+        }
       } else {
         lo = klo - g * kTileN;
         hi = khi - g * kTileN;
@@ -1701,23 +1741,41 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const __grid_constant__ 
   }
 }
 
-// Visible query rows of a key tile / key rows of a query tile (block-causal):
-// query i sees key j iff 0 <= chunk(i) - chunk(j) <= window.
-__device__ __forceinline__ void bwd_q_range(const BwdParams& p, int k0, int& qt0, int& nqt) {
-  const int k_last = min(p.L, k0 + kTileN) - 1;
-  const int c_lo = k0 / p.chunk_tokens, c_hi = k_last / p.chunk_tokens;
-  const int qlo = c_lo * p.chunk_tokens;
-  const int qhi = min(p.L, (c_hi + p.window + 1) * p.chunk_tokens);
-  qt0 = qlo / kTileM;
-  nqt = (qhi + kTileM - 1) / kTileM - qt0;
-}
-__device__ __forceinline__ void bwd_k_range(const BwdParams& p, int q0, int& kt0, int& nkt) {
-  const int q_last = min(p.L, q0 + kTileM) - 1;
-  const int c_lo = q0 / p.chunk_tokens, c_hi = q_last / p.chunk_tokens;
-  const int klo = max(0, c_lo - p.window) * p.chunk_tokens;
-  const int khi = min(p.L, (c_hi + 1) * p.chunk_tokens);
-  kt0 = klo / kTileN;
-  nkt = (khi + kTileN - 1) / kTileN - kt0;
+// Streamed tiles of a resident tile of rows [r0, r0 + 128): run 0 = n0
+// tiles from row 0 (the real memory [0, P) behind a memory prefix), run 1 =
+// n1 tiles from row1.  Query i sees key j iff both are real memory, or i is
+// a target token and j real memory, or both are target tokens with
+// 0 <= chunk(i) - chunk(j) <= window (target chunks counted from mem_pad;
+// mem_pad = P = 0 is plain block-causal attention).
+struct BwdRuns {
+  int n0, row1, n1;
+};
+template <bool KQ>
+__device__ __forceinline__ BwdRuns bwd_runs(const BwdParams& p, int P, int r0) {
+  const int M = p.mem_pad, Lc = p.chunk_tokens;
+  const int r_last = min(p.L, r0 + kTileM) - 1;
+  const bool any_target = r_last >= M;
+  const int c_lo = (max(r0, M) - M) / Lc, c_hi = (r_last - M) / Lc;  // target chunks of the tile
+  BwdRuns u{0, M, 0};
+  int lo = M, hi = M;
+  if (KQ) {  // keys: the queries that see them
+    if (r0 < P) {
+      u.n0 = (P + kTileM - 1) / kTileM;
+      hi = p.L;  // every target query sees the real memory
+    } else if (any_target) {
+      lo = M + c_lo * Lc;
+      hi = min(p.L, M + (c_hi + p.window + 1) * Lc);
+    }
+  } else {   // queries: the keys they see
+    if (r0 < P || any_target) u.n0 = (P + kTileN - 1) / kTileN;
+    if (any_target) {
+      lo = M + max(0, c_lo - p.window) * Lc;
+      hi = min(p.L, M + (c_hi + 1) * Lc);
+    }
+  }
+  u.row1 = lo;
+  u.n1 = (hi - lo + kTileN - 1) / kTileN;
+  return u;
 }
 
 // KQ == true: key-tile kernel (dK, dV); false: query-tile kernel (dQ).
@@ -1762,9 +1820,10 @@ attn_bwd_kernel(const __grid_constant__ BwdParams p) {
   const uint32_t tmem = misc[0];
   griddep_launch_dependents();
   griddep_wait();
-  int t0 = 0, nt = 0;  // streamed tiles
-  if (KQ) bwd_q_range(p, r0, t0, nt);
-  else bwd_k_range(p, r0, t0, nt);
+  const int P = p.mem_pad > 0 ? min(max(__ldg(p.mem_len + b), 0), p.mem_pad) : 0;  // real memory
+  const BwdRuns u = bwd_runs<KQ>(p, P, r0);
+  const int nt = u.n0 + u.n1;  // streamed tiles
+  auto tile_row = [&](int j) { return j < u.n0 ? j * 128 : u.row1 + (j - u.n0) * 128; };
   // resident: K, V (key-tile kernel) or Q, dO (query-tile kernel);
   // streamed: Q_j, dO_j or K_j, V_j
   const CUtensorMap* res0 = KQ ? &p.k_map : &p.q_map;
@@ -1791,7 +1850,7 @@ attn_bwd_kernel(const __grid_constant__ BwdParams p) {
                                                   abort_flag, 0));
       if (!ok) break;
       const uint32_t so = C::kStageOff + st * C::kStageBytes;
-      const int row = (t0 + j) * 128;
+      const int row = tile_row(j);
       if (KQ) {  // lse * log2(e) and delta of the stage's 128 queries (plain loads, whole warp)
         float* ls = reinterpret_cast<float*>(base + so + 2 * C::kTileBytes);
         float* dl = ls + 128;
@@ -1890,17 +1949,29 @@ attn_bwd_kernel(const __grid_constant__ BwdParams p) {
     const int r = r0 + row;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const uint32_t tS = tmem + lane_off + hf * 64, tdP = tmem + lane_off + 128 + hf * 64;
-    // visible interval of the streamed rows for this resident row
-    int vlo = 0, vhi = 0;
+    // visible streamed rows of this resident row: [lo0, hi0) in run 0 (real
+    // memory) and [lo1, hi1) in run 1
+    int hi0 = 0, lo1 = 0, hi1 = 0;
     float lse2 = 0.f, dlt = 0.f;
     if (r < p.L) {
-      const int c = r / p.chunk_tokens;
-      if (KQ) {  // key r: queries of chunks c .. c + W
-        vlo = c * p.chunk_tokens;
-        vhi = min(p.L, (c + p.window + 1) * p.chunk_tokens);
-      } else {   // query r: keys of chunks c - W .. c
-        vlo = max(0, c - p.window) * p.chunk_tokens;
-        vhi = min(p.L, (c + 1) * p.chunk_tokens);
+      const int M = p.mem_pad, Lc = p.chunk_tokens, t = r - M;
+      if (KQ) {
+        if (r < P) {           // real memory key: real memory and every target query
+          hi0 = P;
+          lo1 = M;
+          hi1 = p.L;
+        } else if (t >= 0) {   // target key of chunk c: queries of chunks c .. c + W
+          const int c = t / Lc;
+          lo1 = M + c * Lc;
+          hi1 = min(p.L, M + (c + p.window + 1) * Lc);
+        }
+      } else {
+        if (r < P || t >= 0) hi0 = P;  // real queries see the real memory
+        if (t >= 0) {                  // target query of chunk c: keys of chunks c - W .. c
+          const int c = t / Lc;
+          lo1 = M + max(0, c - p.window) * Lc;
+          hi1 = min(p.L, M + (c + 1) * Lc);
+        }
         lse2 = __ldg(p.LSE + (long long)bh * p.L + r) * kLog2e;
         dlt = __ldg(p.delta + (long long)bh * p.L + r);
       }
@@ -1916,8 +1987,8 @@ attn_bwd_kernel(const __grid_constant__ BwdParams p) {
       tmem_ld32(tS + 32, s1);
       tmem_ld32(tdP, d0);
       tmem_ld32(tdP + 32, d1);
-      const int c0 = (t0 + j) * 128 + hf * 64;  // first streamed row of this half
-      const int lo = vlo - c0, hi = vhi - c0;
+      const int c0 = tile_row(j) + hf * 64;  // first streamed row of this half
+      const int lo = (j < u.n0 ? 0 : lo1) - c0, hi = (j < u.n0 ? hi0 : hi1) - c0;
       const float* ls = reinterpret_cast<const float*>(base + C::kStageOff + (j % C::kStages) * C::kStageBytes +
                                                        2 * C::kTileBytes) + hf * 64;
       const float* dl = ls + 128;

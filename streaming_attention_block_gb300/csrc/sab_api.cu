@@ -660,21 +660,58 @@ sab_status sab_block_causal_attention(const void* Q, const void* K, const void* 
   return launch_attention(p, L, num_splits, workspace, ws_bytes, stream);
 }
 
+sab_status sab_memory_prefix_attention(const void* Q, const void* K, const void* V, int B, int L, int H, int D,
+                                       int mem_pad, const int* mem_len, int chunk_tokens, int window,
+                                       float softmax_scale, void* O, float* LSE, void* stream) {
+  if (Q == nullptr || K == nullptr || V == nullptr || O == nullptr) return SAB_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return SAB_ERR_INVALID_ARG;
+  if (LSE != nullptr && (reinterpret_cast<uintptr_t>(LSE) & 3u) != 0) return SAB_ERR_INVALID_ARG;
+  if (B < 1 || L < 1 || H < 1 || (D != 64 && D != 128) || chunk_tokens < 1 || window < 0) return SAB_ERR_INVALID_ARG;
+  if (mem_pad < 0 || mem_pad > L) return SAB_ERR_INVALID_ARG;
+  if (mem_pad > 0 && (mem_len == nullptr || (reinterpret_cast<uintptr_t>(mem_len) & 3u) != 0))
+    return SAB_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.f) || !isfinite(softmax_scale)) return SAB_ERR_INVALID_ARG;
+  if ((long long)L > (1LL << 30)) return SAB_ERR_INVALID_ARG;
+  AttnParams p;
+  memset(&p, 0, sizeof(p));
+  p.mode = mem_pad > 0 ? kModeMemPrefix : kModeBlockCausal;
+  p.B = B;
+  p.H = H;
+  p.D = D;
+  p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  p.chunk_tokens = chunk_tokens;
+  p.window = window;
+  p.Lk = L;
+  p.mem_pad = mem_pad;
+  p.mem_len = mem_len;
+  p.O = static_cast<uint16_t*>(O);
+  p.LSE = LSE;
+  if (!encode_token_major(&p.q_map, Q, B, L, H, D) || !encode_token_major(&p.k_map[0], K, B, L, H, D) ||
+      !encode_token_major(&p.v_map[0], V, B, L, H, D) || !encode_token_major(&p.o_map, O, B, L, H, D))
+    return SAB_ERR_CUDA;
+  p.k_map[1] = p.k_map[0];
+  p.v_map[1] = p.v_map[0];
+  // one query tile per CTA, unsplit: the key runs are planned per CTA
+  return launch_attention(p, L, 1, nullptr, 0, stream);
+}
+
 size_t sab_block_causal_attention_backward_workspace(int B, int L, int H) {
   if (B < 1 || L < 1 || H < 1) return 0;
   return align_up((size_t)B * H * L * sizeof(float), kAlign);
 }
 
-sab_status sab_block_causal_attention_backward(const void* Q, const void* K, const void* V, const void* O,
-                                               const void* dO, const float* LSE, int B, int L, int H, int D,
-                                               int chunk_tokens, int window, float softmax_scale, void* dQ,
-                                               void* dK, void* dV, void* workspace, size_t ws_bytes,
-                                               void* stream) {
+static sab_status attention_backward(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                                     const float* LSE, int B, int L, int H, int D, int mem_pad, const int* mem_len,
+                                     int chunk_tokens, int window, float softmax_scale, void* dQ, void* dK, void* dV,
+                                     void* workspace, size_t ws_bytes, void* stream) {
   const void* ins[] = {Q, K, V, O, dO, dQ, dK, dV};
   for (const void* x : ins)
     if (x == nullptr || !aligned16(x)) return SAB_ERR_INVALID_ARG;
   if (LSE == nullptr || (reinterpret_cast<uintptr_t>(LSE) & 3u) != 0) return SAB_ERR_INVALID_ARG;
   if (B < 1 || L < 1 || H < 1 || (D != 64 && D != 128) || chunk_tokens < 1 || window < 0) return SAB_ERR_INVALID_ARG;
+  if (mem_pad < 0 || mem_pad > L) return SAB_ERR_INVALID_ARG;
+  if (mem_pad > 0 && (mem_len == nullptr || (reinterpret_cast<uintptr_t>(mem_len) & 3u) != 0))
+    return SAB_ERR_INVALID_ARG;
   if (!(softmax_scale > 0.f) || !isfinite(softmax_scale)) return SAB_ERR_INVALID_ARG;
   if ((long long)L > (1LL << 30) || (long long)B * H > 65535) return SAB_ERR_INVALID_ARG;
   if (workspace == nullptr || ws_bytes < sab_block_causal_attention_backward_workspace(B, L, H) ||
@@ -695,12 +732,32 @@ sab_status sab_block_causal_attention_backward(const void* Q, const void* K, con
   p.L = L;
   p.chunk_tokens = chunk_tokens;
   p.window = window;
+  p.mem_pad = mem_pad;
+  p.mem_len = mem_pad > 0 ? mem_len : nullptr;
   p.scale = softmax_scale;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
   if (!encode_token_major(&p.q_map, Q, B, L, H, D) || !encode_token_major(&p.k_map, K, B, L, H, D) ||
       !encode_token_major(&p.v_map, V, B, L, H, D) || !encode_token_major(&p.do_map, dO, B, L, H, D))
     return SAB_ERR_CUDA;
   return launch_attention_backward(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SAB_OK : SAB_ERR_CUDA;
+}
+
+sab_status sab_block_causal_attention_backward(const void* Q, const void* K, const void* V, const void* O,
+                                               const void* dO, const float* LSE, int B, int L, int H, int D,
+                                               int chunk_tokens, int window, float softmax_scale, void* dQ,
+                                               void* dK, void* dV, void* workspace, size_t ws_bytes,
+                                               void* stream) {
+  return attention_backward(Q, K, V, O, dO, LSE, B, L, H, D, 0, nullptr, chunk_tokens, window, softmax_scale, dQ, dK,
+                            dV, workspace, ws_bytes, stream);
+}
+
+sab_status sab_memory_prefix_attention_backward(const void* Q, const void* K, const void* V, const void* O,
+                                                const void* dO, const float* LSE, int B, int L, int H, int D,
+                                                int mem_pad, const int* mem_len, int chunk_tokens, int window,
+                                                float softmax_scale, void* dQ, void* dK, void* dV, void* workspace,
+                                                size_t ws_bytes, void* stream) {
+  return attention_backward(Q, K, V, O, dO, LSE, B, L, H, D, mem_pad, mem_len, chunk_tokens, window, softmax_scale,
+                            dQ, dK, dV, workspace, ws_bytes, stream);
 }
 
 sab_status sab_selftest_bounded_wait(unsigned long long timeout_ns, void* stream) {

@@ -22,7 +22,11 @@ struct KvSegment {
   int tile0;   // global index of the run's first 128-key tile
 };
 
-enum AttnMode : int { kModeStreaming = 0, kModeBlockCausal = 1 };
+// kModeMemPrefix: block-causal target chunks behind a per-sample memory
+// prefix of mem_pad positions, the first mem_len[b] of them real; the key
+// runs of a query tile (memory, then the chunk window) are planned by each
+// CTA on the device.
+enum AttnMode : int { kModeStreaming = 0, kModeBlockCausal = 1, kModeMemPrefix = 2 };
 
 // Key runs of one streaming call, in physical row order.
 struct KeyPlan {
@@ -118,10 +122,12 @@ struct AttnParams {
   KeyPlan plan;
   const long long* d_chunk;
   int ring_slots, has_sink, use_sink, kcur;
-  // block-causal
+  // block-causal (and memory prefix)
   int chunk_tokens;
   int window;
   int Lk;
+  int mem_pad;            // memory positions ahead of the first target chunk
+  const int* mem_len;     // device [B]: real memory positions per sample
   // outputs
   uint16_t* O;            // bf16 [B, Lq, H, D]
   float* LSE;             // [B, H, Lq] or null
@@ -181,6 +187,8 @@ struct BwdParams {
   uint16_t* dV;
   int B, H, D, L;
   int chunk_tokens, window;
+  int mem_pad;            // memory prefix (0: plain block-causal), as in AttnParams
+  const int* mem_len;     // device [B] (read only when mem_pad > 0)
   float scale;            // softmax scale
   float scale_log2;       // scale * log2(e)
 };

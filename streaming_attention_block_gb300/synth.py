@@ -54,6 +54,8 @@ class Workload:
     rms_norm: bool = False
     outliers: bool = False
     seq_chunks: int = 0     # full-sequence mode: chunks per sequence
+    mem_pad: int = 0        # full-sequence mode: memory positions ahead of the target chunks
+    mem_lens: tuple = ()    # real memory positions per sample (the rest is padding)
     seed: int = 1000
 
     @property
@@ -69,6 +71,10 @@ WORKLOADS = {
                           sink=True, kcur_separate=False, splits=8, seed=1003),
     "block_causal": Workload("block_causal", B=2, H=12, D=128, Lc=1536, W=2, seq_chunks=20,
                              seed=1004),
+    # compressed-memory training: 4 target chunks behind a padded memory of
+    # two chunks' length, one sample's memory full and one's partly padding
+    "memory_prefix": Workload("memory_prefix", B=2, H=12, D=128, Lc=1536, W=3, seq_chunks=4, mem_pad=3072,
+                              mem_lens=(3072, 1900), seed=1007),
     "fp8_kv": Workload("fp8_kv", B=1, H=24, D=128, Lc=405, R=20, W=19, chunks=60, sink=True,
                        kcur_separate=False, splits=8, kv_fp8=True, outliers=True, seed=1005),
     "int8k_kv": Workload("int8k_kv", B=1, H=24, D=128, Lc=405, R=20, W=19, chunks=60, sink=True,
@@ -123,7 +129,7 @@ def sink_kv(w: Workload, gen: torch.Generator, device: str = "cpu"):
 
 
 def full_sequence_qkv(w: Workload, gen: torch.Generator, device: str = "cpu", seq_chunks: int | None = None):
-    """Full-sequence Q, K, V ``[B, L, H, D]`` bf16 with L = seq_chunks * Lc."""
+    """Full-sequence Q, K, V ``[B, L, H, D]`` bf16 with L = mem_pad + seq_chunks * Lc."""
     n = w.seq_chunks if seq_chunks is None else seq_chunks
-    shape = (w.B, n * w.Lc, w.H, w.D)
+    shape = (w.B, w.mem_pad + n * w.Lc, w.H, w.D)
     return tuple(randn_bf16(gen, shape, device) for _ in range(3))

@@ -92,3 +92,15 @@ def test_validation_before_any_cuda_call(lib):
     assert lib.sab_chunk_counter_add(ctypes.c_void_p(4100), 1, None) == 1
     assert lib.sab_selftest_bounded_wait(10, None) == 1  # limit outside 1 ms .. 2 s
     assert lib.sab_kv_ring_destroy(None) == 0
+
+
+def test_memory_prefix_validation_before_any_cuda_call(lib):
+    p = ctypes.c_void_p(256)  # aligned dummy: validation fails before it is used
+    args = lambda M, ml: (p, p, p, 2, 512, 2, 128, M, ml, 128, 2, 0.1, p, None, None)
+    assert lib.sab_memory_prefix_attention(*args(513, p)) == 1    # mem_pad > L
+    assert lib.sab_memory_prefix_attention(*args(-1, p)) == 1     # negative
+    assert lib.sab_memory_prefix_attention(*args(64, None)) == 1  # lengths missing
+    assert lib.sab_memory_prefix_attention(*args(64, ctypes.c_void_p(258))) == 1  # misaligned lengths
+    bw = lambda M, ml: (p, p, p, p, p, p, 2, 512, 2, 128, M, ml, 128, 2, 0.1, p, p, p, p, 1 << 20, None)
+    assert lib.sab_memory_prefix_attention_backward(*bw(600, p)) == 1
+    assert lib.sab_memory_prefix_attention_backward(*bw(64, None)) == 1
