@@ -34,7 +34,7 @@ METRIC = "chunk-attention TFLOP/s & chunks/s at Wan-1.3B shape; % of roofline"
 # DRAM bytes (read + write) of one attention launch of this workload, from the
 # ncu capture summarised in profiles/chunk_attn_kh_wan13b_ncu.md; None once
 # the kernel has changed since that capture.
-ATTN_DRAM_BYTES_PER_LAUNCH = 33_093_376 + 512
+ATTN_DRAM_BYTES_PER_LAUNCH = 33_098_240 + 1_536
 
 
 def _peaks():
@@ -50,34 +50,51 @@ def _peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling during the timed region."""
+    """nvidia-smi clock / throttle sampling during the timed region.
+
+    nvidia-smi starts before the warm-up and is waited for until its first
+    sample arrives; it then polls every ``period_ms``.  Each sample is stamped
+    with the host time it arrived, and only samples inside [begin(), end()]
+    (end() is called after the closing synchronize) are summarised."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, period_ms: int = 20):
         self.idx = gpu_index
+        self.period_ms = period_ms
         self.proc = None
-        self.lines = []
+        self.lines = []  # (host time, csv line)
+        self.t_begin = self.t_end = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", str(self.period_ms)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            deadline = time.monotonic() + 5.0
+            while not self.lines and time.monotonic() < deadline and self.proc.poll() is None:
+                time.sleep(0.01)
         except Exception:
             self.proc = None
         return self
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.monotonic(), line.strip()))
+
+    def begin(self):
+        self.t_begin = time.monotonic()
+
+    def end(self):
+        self.t_end = time.monotonic()
 
     def __exit__(self, *a):
         if self.proc is not None:
+            time.sleep(2.5 * self.period_ms / 1000.0)  # let the sample in flight arrive
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
@@ -87,7 +104,11 @@ class ClockSampler:
     def summary(self):
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        lo = self.t_begin if self.t_begin is not None else -1e30
+        hi = (self.t_end if self.t_end is not None else 1e30) + 1.5 * self.period_ms / 1000.0
+        for t, ln in list(self.lines):
+            if not (lo <= t <= hi):
+                continue
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 8:
                 continue
@@ -102,7 +123,7 @@ class ClockSampler:
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "period_ms": self.period_ms}
 
 
 def _dist():
@@ -172,22 +193,24 @@ def run_ours(args):
         torch.cuda.synchronize()
 
     chunk = 0
-    for _ in range(args.warmup):
-        chunk_step(chunk)
-        chunk += 1
-    assert chunk >= 2, "warm-up must reach the steady-state window (>= 2 chunks)"
-    barrier()
-    launches[0] = 0
-    ev = ([], [])
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
+        for _ in range(args.warmup):
+            chunk_step(chunk)
+            chunk += 1
+        assert chunk >= 2, "warm-up must reach the steady-state window (>= 2 chunks)"
+        barrier()
+        launches[0] = 0
+        ev = ([], [])
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        clk.begin()
         t0.record(stream)
         for _ in range(args.steps):
             chunk_step(chunk, ev)
             chunk += 1
         t1.record(stream)
         barrier()
+        clk.end()
     ms = t0.elapsed_time(t1)
     gpu_launches = launches[0]
     attn_ms = [a.elapsed_time(b) / L for a, b in zip(*ev)]  # per launch
@@ -499,6 +522,33 @@ def run_sweep(args):
         sab.block_causal_attention_backward(q, k, v, O, do, L, w.Lc, w.W, w.scale, dq, dk, dv, bws, stream)
 
     report("block_causal_backward", timed(bwd, 10), 2.5 * flops, 0, {"tokens": Lt})
+    del q, k, v, O, L, do, dq, dk, dv
+    # memory prefix (compressed-memory training shape): visible pairs counted
+    # per sample -- real memory x real memory, and each target chunk against
+    # the real memory plus its window of target chunks
+    w = synth.workload("memory_prefix")
+    q, k, v = synth.full_sequence_qkv(w, g, "cuda")
+    Lt = q.shape[1]
+    ml = torch.tensor(w.mem_lens, dtype=torch.int32, device="cuda")
+    O = torch.empty_like(q)
+    L = torch.empty((w.B, w.H, Lt), dtype=torch.float32, device="cuda")
+    pairs = sum(P * P + sum(w.Lc * (P + w.Lc * (min(c, w.W) + 1)) for c in range(w.seq_chunks))
+                for P in w.mem_lens)
+    flops = 4.0 * w.H * w.D * pairs
+
+    def mp():
+        sab.memory_prefix_attention(q, k, v, w.mem_pad, ml, w.Lc, w.W, w.scale, O, L, stream)
+
+    report("memory_prefix", timed(mp, 10), flops, 1, {"tokens": Lt, "mem_pad": w.mem_pad})
+    do = synth.randn_bf16(g, tuple(q.shape), "cuda")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    bws = torch.empty(sab.block_causal_attention_backward_workspace(w.B, Lt, w.H), dtype=torch.uint8, device="cuda")
+
+    def mpb():
+        sab.memory_prefix_attention_backward(q, k, v, O, do, L, w.mem_pad, ml, w.Lc, w.W, w.scale, dq, dk, dv, bws,
+                                             stream)
+
+    report("memory_prefix_backward", timed(mpb, 10), 2.5 * flops, 0, {"tokens": Lt, "mem_pad": w.mem_pad})
     assert sab.get_last_device_error(stream) == 0
 
 
