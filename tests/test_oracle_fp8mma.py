@@ -1,0 +1,131 @@
+"""Pins of the E4M3-product attention oracle (``oracle/fp8mma.py``): the
+per-row Q quantiser against torch's float8_e4m3fn rounding, the exact part
+against the plain attention oracle on the same quantised operands, and the
+P-rounding bound against a brute-force replay of the rounding (torch's E4M3
+cast, running-max offsets, relative V scales down to 1/40), which a bound
+that forgot the V-scale factor fails."""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention as OA
+from oracle import fp8mma as OF
+
+
+def _e4m3_round(x):
+    """Round float32 values to E4M3 with torch (independent of oracle.fp8)."""
+    return torch.from_numpy(np.asarray(x, dtype=np.float32)).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def test_row_quantiser_matches_torch_cast():
+    rng = np.random.default_rng(1)
+    q = (rng.standard_normal((64, 128)) * rng.uniform(0.01, 30, (64, 1))).astype(np.float32)
+    q[3] = 0.0
+    q_hat, sc = OF.quantize_rows(q)
+    for i in range(q.shape[0]):
+        amax = np.float32(np.max(np.abs(q[i])))
+        s = np.float32(1.0) if amax == 0 else np.float32(amax / np.float32(448.0))
+        assert sc[i] == s
+        ref = _e4m3_round((q[i] / s).astype(np.float32)) * np.float64(s)
+        np.testing.assert_array_equal(q_hat[i], ref)
+    # every row's largest magnitude lands on the top code 448
+    big = np.argmax(np.abs(q[0]))
+    assert abs(q_hat[0, big]) == 448.0 * np.float64(sc[0])
+
+
+def test_exact_part_is_plain_attention_on_quantised_operands():
+    rng = np.random.default_rng(2)
+    q = rng.standard_normal((40, 32)).astype(np.float32)
+    k, v = rng.standard_normal((2, 90, 32))
+    mask = rng.random((40, 90)) < 0.6
+    mask[:, 0] = True
+    o, lse, _ = OF.head_attention(q, k, v, mask, 0.2, np.ones(90))
+    q_hat, _ = OF.quantize_rows(q)
+    o2, l2 = OA.masked_attention(q_hat, k, v, mask, 0.2)
+    np.testing.assert_allclose(o, o2, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse, l2, rtol=0, atol=1e-13)
+
+
+def _replay(q, k, v, mask, scale, vs, delta, bound_fn=None, gain=OF.P_GAIN_LOG2):
+    """Round P the way the product sees it: P * r * 2^(gain + delta) to E4M3
+    and back."""
+    o, lse, bound = OF.head_attention(q, k, v, mask, scale, vs, gain)
+    q_hat, _ = OF.quantize_rows(q)
+    s = np.where(mask, scale * (q_hat @ k.T), -np.inf)
+    p = np.where(mask, np.exp(s - s.max(axis=1, keepdims=True)), 0.0)
+    vs_ref = vs[mask.any(axis=0)].max()
+    r = vs / vs_ref
+    f = r[None, :] * 2.0 ** (gain + delta)
+    assert np.all(p * f <= 448.0)
+    p_q = _e4m3_round(p * f) / f
+    o_sim = (p_q @ v) / p.sum(axis=1, keepdims=True)
+    if bound_fn is not None:
+        e = np.where(mask, bound_fn(p, r), 0.0)
+        bound = (e @ np.abs(v)) / p.sum(axis=1, keepdims=True)
+    return np.abs(o_sim - o), bound
+
+
+@pytest.mark.parametrize("peak", [0.3, 3.0, 12.0])
+@pytest.mark.parametrize("delta", [0, 1, 2])
+def test_bound_holds_under_brute_force_rounding(peak, delta):
+    rng = np.random.default_rng(int(peak * 10) + delta)
+    Nk, D = 600, 64
+    q = (rng.standard_normal((48, D)) * peak).astype(np.float32)
+    k = rng.standard_normal((Nk, D))
+    v = rng.standard_normal((Nk, D))
+    # three chunks with very different V scales; one with 8x outliers
+    vs = np.repeat([0.05, 0.9, 2.0], Nk // 3)
+    v[400:] *= 1.0
+    v[rng.random((Nk, D)) < 0.01] *= 8.0
+    mask = np.ones((48, Nk), dtype=bool)
+    mask[::3, 450:] = False
+    err, bound = _replay(q, k, v, mask, 1.0 / np.sqrt(D), vs, delta)
+    assert np.all(err <= bound + 1e-12), float(np.max(err - bound))
+    assert np.mean(bound) < 2.0 ** -3 * np.mean(np.abs(v))  # not vacuous (the leading term is 2^-4)
+
+
+def test_bound_without_the_scale_factor_fails():
+    """One dominant key (r = 1) and 390 keys of equal score whose V scale is
+    1/40 of it, with no gain: P r = 1.49 * 2^-9 rounds down by 0.49 subnormal
+    steps for all of them at once (coherent error).  The bound holds; a bound
+    that forgot the relative V scale r is violated."""
+    D, Nk = 32, 400
+    p0 = 1.49 * 2.0 ** -9 * 40.0
+    q = np.zeros((4, D), dtype=np.float32)
+    q[:, 0] = 1.0
+    k = np.zeros((Nk, D))
+    k[0, 0] = 2.0
+    k[1:391, 0] = 2.0 + np.log(p0)
+    k[391:, 0] = -3.0
+    v = np.ones((Nk, D))
+    vs = np.ones(Nk)
+    vs[1:391] = 0.025
+    mask = np.ones((4, Nk), dtype=bool)
+    wrong = lambda p, r: np.where(p >= 2.0 ** -6, 2.0 ** -4 * p, np.minimum(p, 2.0 ** -10))
+    err, bad_bound = _replay(q, k, v, mask, 1.0, vs, 0, bound_fn=wrong, gain=0)
+    assert np.all(err > 4 * bad_bound)
+    err, bound = _replay(q, k, v, mask, 1.0, vs, 0, gain=0)
+    assert np.all(err <= bound + 1e-12)
+    assert np.all(err >= 0.9 * bound)  # and it is tight here
+
+
+def test_gain_shrinks_the_subnormal_term():
+    """With the kernel's gain the same coherent case is 64x tighter and still
+    covered."""
+    D, Nk = 32, 400
+    p0 = 1.49 * 2.0 ** -9 * 40.0 / 64.0  # P r 2^6 = 1.49 * 2^-9
+    q = np.zeros((4, D), dtype=np.float32)
+    q[:, 0] = 1.0
+    k = np.zeros((Nk, D))
+    k[0, 0] = 2.0
+    k[1:391, 0] = 2.0 + np.log(p0)
+    k[391:, 0] = -3.0
+    v = np.ones((Nk, D))
+    vs = np.ones(Nk)
+    vs[1:391] = 0.025
+    mask = np.ones((4, Nk), dtype=bool)
+    err, bound = _replay(q, k, v, mask, 1.0, vs, 0)
+    assert np.all(err <= bound + 1e-12)
+    err0, bound0 = _replay(q, k, v, mask, 1.0, vs, 0, gain=0)
+    assert np.all(bound < bound0)
