@@ -463,6 +463,21 @@ def run_sweep(args):
                                     stream)
 
             report(name, timed(call, 50), flops, splits, {"keys": nkeys})
+        if w.kv_fp8 and not w.kv_int8k:
+            # E4M3 tensor-core products (Q and P rounded to E4M3): the peak is
+            # the bf16 one x 2, the nominal fp8 / bf16 dense ratio
+            O = torch.empty_like(q)
+            L = torch.empty((w.B, w.H, w.Lc), dtype=torch.float32, device="cuda")
+
+            def call_f8():
+                sab.chunk_attention_fp8mma(ring.handle, 0, steady, q, w.W, w.sink, w.scale, O, L, stream)
+
+            us = timed(call_f8, 50)
+            tf = flops / (us * 1e-6) / 1e12
+            print(json.dumps({"sweep": name + "_e4m3_mma", "us_per_call": round(us, 2), "tflops": round(tf, 1),
+                              "frac_of_fp8_peak": round(tf / (2 * peaks["bf16_tflops"]), 4),
+                              "peak_source": f"2 x bf16 dense burst, {src}", "splits": 1, "keys": nkeys}),
+                  flush=True)
     # fused Q/K RMSNorm + rotary embedding + BF16 ring append at the Wan-1.3B
     # chunk shape (latent grid 2 x 24 x 32, rotary bands 44/42/42); 16 input
     # sets rotate so that every call reads from HBM (16 x 18.9 MB > L2)

@@ -25,8 +25,8 @@ P'_j = P_j * r_j * 2^(g + delta), where P_j = exp(s_j - max) <= 1,
 r_j = vs_j / vs_ref <= 1 is the key's V scale relative to the largest V scale
 of the visible keys (the V scales are applied before the rounding so that the
 product uses the codes as stored), g is a fixed gain that lifts the values
-out of the subnormal range (the kernel uses g = 6 with a running-max slack
-of at most 2^2, so P' <= 2^8 < 448), and delta >= 0 accounts for a running
+out of the subnormal range (the kernel uses g = 4 with a running-max slack
+of at most 2^4, so P' <= 2^8 < 448), and delta >= 0 accounts for a running
 maximum that has not yet caught up (the values are then larger, never
 smaller).  E4M3 rounding to nearest changes a value by at most 2^-4 of itself
 when it is normal (>= 2^-6) and by at most 2^-10 (half the subnormal spacing
@@ -39,6 +39,13 @@ that.  In units of P_j:
 and O_i = sum_j P_ij v_j / l_i (l_i = sum_j P_ij, kept in fp32 from the
 unrounded values) moves by at most  bound_i = sum_j e_ij |v_j| / l_i  per
 output column.
+
+The typical size.  Modelling each rounding error as uniform over one E4M3
+spacing u_j of P'_j (spacing 2^(floor(log2 P') - 3) when normal, 2^-9 below
+2^-6; in units of P divided by r_j 2^g) and independent across keys, the
+error of O_id has standard deviation
+sigma_id = sqrt(sum_j (u_j^2 / 12) v_jd^2) / l_i, and its mean magnitude is
+about sqrt(2 / pi) sigma_id.
 """
 
 from __future__ import annotations
@@ -61,7 +68,7 @@ def quantize_rows(q: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
     return out, sc
 
 
-P_GAIN_LOG2 = 6  # g of the module docstring
+P_GAIN_LOG2 = 4  # g of the module docstring
 
 
 def p_rounding_error(p: np.ndarray, r: np.ndarray, gain_log2: int = P_GAIN_LOG2) -> np.ndarray:
@@ -71,6 +78,34 @@ def p_rounding_error(p: np.ndarray, r: np.ndarray, gain_log2: int = P_GAIN_LOG2)
     rg = np.asarray(r, dtype=np.float64)[None, :] * 2.0 ** gain_log2
     normal = p * rg >= 2.0 ** -6
     return np.where(normal, 2.0 ** -4 * p, np.minimum(p, 2.0 ** -10 / rg))
+
+
+def p_rounding_spacing(p: np.ndarray, r: np.ndarray, gain_log2: int = P_GAIN_LOG2) -> np.ndarray:
+    """u_j of the module docstring (E4M3 spacing at P' = P r 2^g, in units of
+    P) for probabilities ``p [n, Nk]`` and relative V scales ``r [Nk]``."""
+    p = np.asarray(p, dtype=np.float64)
+    rg = np.asarray(r, dtype=np.float64)[None, :] * 2.0 ** gain_log2
+    x = p * rg
+    e = np.floor(np.log2(np.maximum(x, 2.0 ** -6)))
+    return 2.0 ** (e - 3) / rg
+
+
+def rounding_sigma(q: np.ndarray, k_hat: np.ndarray, v_hat: np.ndarray, mask: np.ndarray, scale: float,
+                   v_scale_key: np.ndarray, gain_log2: int = P_GAIN_LOG2) -> np.ndarray:
+    """sigma ``[Lq, D]`` of the module docstring for the inputs of
+    ``head_attention``."""
+    q_hat, _ = quantize_rows(q)
+    k = np.asarray(k_hat, dtype=np.float64)
+    v = np.asarray(v_hat, dtype=np.float64)
+    mask = np.asarray(mask, dtype=bool)
+    vs = np.asarray(v_scale_key, dtype=np.float64)
+    s = np.where(mask, float(scale) * (q_hat @ k.T), -np.inf)
+    p = np.where(mask, np.exp(s - np.max(s, axis=1, keepdims=True)), 0.0)
+    l = p.sum(axis=1, keepdims=True)
+    vs_ref = np.max(np.where(mask.any(axis=0), vs, 0.0))
+    r = np.where(vs > 0, vs / vs_ref, 1.0)
+    u = np.where(mask, p_rounding_spacing(p, r, gain_log2), 0.0)
+    return np.sqrt((u * u / 12.0) @ (v * v)) / l
 
 
 def head_attention(q: np.ndarray, k_hat: np.ndarray, v_hat: np.ndarray, mask: np.ndarray, scale: float,

@@ -21,6 +21,7 @@ from ._abi import (  # noqa: F401
     block_causal_attention_workspace,
     chunk_attention,
     chunk_attention_dev,
+    chunk_attention_fp8mma,
     chunk_attention_noalloc,
     chunk_counter_add,
     chunk_attention_workspace,

@@ -77,6 +77,7 @@ def library() -> ctypes.CDLL:
         "sab_block_causal_attention_backward_workspace": (SZ, [I, I, I]),
         "sab_block_causal_attention_backward": (I, [P, P, P, P, P, P, I, I, I, I, I, I, F, P, P, P, P, SZ, P]),
         "sab_memory_prefix_attention": (I, [P, P, P, I, I, I, I, I, P, I, I, F, P, P, P]),
+        "sab_chunk_attention_fp8mma": (I, [P, I, LL, P, I, I, F, P, P, P]),
         "sab_memory_prefix_attention_backward": (I, [P, P, P, P, P, P, I, I, I, I, I, P, I, I, F, P, P, P, P, SZ,
                                                      P]),
         "sab_status_string": (ctypes.c_char_p, [I]),
@@ -263,6 +264,16 @@ def block_causal_attention_backward(Q, K, V, O, dO, LSE, chunk_tokens: int, wind
         B, L, H, D, int(chunk_tokens), int(window), float(softmax_scale), _ptr(dQ, torch.bfloat16, "dQ"),
         _ptr(dK, torch.bfloat16, "dK"), _ptr(dV, torch.bfloat16, "dV"), _ptr(workspace, None, "workspace"),
         ws_bytes, _stream(stream)), "block_causal_attention_backward")
+
+
+def chunk_attention_fp8mma(handle, layer: int, chunk: int, Q, window: int, use_sink: bool, softmax_scale: float,
+                           O, LSE=None, stream=None):
+    """sab_chunk_attention_fp8mma: chunk attention over an E4M3 ring with Q and
+    P rounded to E4M3 for the tensor-core products (see include/sab.h)."""
+    _check(library().sab_chunk_attention_fp8mma(
+        handle, int(layer), int(chunk), _ptr(Q, torch.bfloat16, "Q"), int(window), 1 if use_sink else 0,
+        float(softmax_scale), _ptr(O, torch.bfloat16, "O"), _ptr(LSE, torch.float32, "LSE"), _stream(stream)),
+        "chunk_attention_fp8mma")
 
 
 def memory_prefix_attention(Q, K, V, mem_pad: int, mem_len, chunk_tokens: int, window: int, softmax_scale: float,

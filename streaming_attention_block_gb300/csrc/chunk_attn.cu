@@ -55,6 +55,7 @@ constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per pipeline wait
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows by > 2^8
+constexpr float kRescaleThresholdF8 = 4.0f;  // E4M3 P: by > 2^4 (P' = P * 2^4 * vs / vs_ref <= 2^8)
 
 template <int D_, int QT_, bool FP8_>
 struct Cfg {
@@ -1129,17 +1130,23 @@ cudaError_t launch_impl(const AttnParams& p, cudaStream_t s) {
 //   8 warps       softmax: half h = keys [64h, 64h + 64) of every tile
 // TMEM: S/P buffers at columns 0 and 128 (P_h packed bf16 in the first 32
 // columns of its half), O_h at column 256 + h * D.
-template <int D_, bool FP8_>
+template <int D_, bool FP8_, bool F8MMA_ = false>
 struct KhCfg {
   static constexpr int D = D_;
+  // F8MMA: E4M3 K/V tiles go to the tensor core as stored (no expansion);
+  // Q is quantised per row on chip and P is rounded to E4M3
+  static constexpr bool kConv = FP8_ && !F8MMA_;  // E4M3 -> bf16 expansion warps
   static constexpr int kBoxes = D / 64;
   static constexpr uint32_t kBoxBytes = 128u * 128u;
-  static constexpr uint32_t kTileBytes = kBoxBytes * kBoxes;
-  static constexpr int kStages = (D == 128) ? 3 : 4;
+  static constexpr uint32_t kTileBytes = kBoxBytes * kBoxes;                  // bf16 tile of 128 rows
+  static constexpr uint32_t kKVTileBytes = F8MMA_ ? 128u * D : kTileBytes;   // one K or V stage tile
+  static constexpr int kStages = F8MMA_ ? 5 : ((D == 128) ? 3 : 4);
   static constexpr uint32_t kKOff = 0;
-  static constexpr uint32_t kVOff = kKOff + kStages * kTileBytes;
-  static constexpr uint32_t kQOff = kVOff + kStages * kTileBytes;
-  static constexpr uint32_t kBarOff = kQOff + kTileBytes;
+  static constexpr uint32_t kVOff = kKOff + kStages * kKVTileBytes;
+  static constexpr uint32_t kQOff = kVOff + kStages * kKVTileBytes;
+  static constexpr uint32_t kQ8Off = kQOff + kTileBytes;                        // E4M3 Q (F8MMA)
+  static constexpr uint32_t kQmaxOff = kQ8Off + (F8MMA_ ? 128u * D : 0u);       // 2 x 128 row maxima
+  static constexpr uint32_t kBarOff = kQmaxOff + (F8MMA_ ? 1024u : 0u);
   static constexpr int kBarQ = 0;
   static constexpr int kBarKFull = 1;                         // [kStages]
   static constexpr int kBarKVEmpty = kBarKFull + kStages;     // [kStages]
@@ -1149,11 +1156,12 @@ struct KhCfg {
   static constexpr int kBarPVDone = kBarPFull + 4;            // [2 halves] one phase per tile
   static constexpr int kBarOFinal = kBarPVDone + 2;           // every MMA complete
   static constexpr int kBarDrain = kBarOFinal + 1;
-  static constexpr int kNumBars = kBarDrain + 1;
+  static constexpr int kBarQ8 = kBarDrain + 1;                // F8MMA: E4M3 Q written
+  static constexpr int kNumBars = kBarQ8 + 1;
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
   static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;
   static constexpr int kConvThreads = 64;
-  static constexpr int kSoftmaxWarp0 = FP8_ ? 4 : 2;
+  static constexpr int kSoftmaxWarp0 = kConv ? 4 : 2;
   static constexpr int kThreads = 32 * (kSoftmaxWarp0 + 8);
   static constexpr uint32_t kTmemO = 256;
   static constexpr uint32_t kTmemCols = 512;
@@ -1163,10 +1171,11 @@ struct KhCfg {
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
-template <int D, bool FP8>
-__global__ void __launch_bounds__(KhCfg<D, FP8>::kThreads, 1)
+template <int D, bool FP8, bool F8MMA>
+__global__ void __launch_bounds__(KhCfg<D, FP8, F8MMA>::kThreads, 1)
 chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
-  using C = KhCfg<D, FP8>;
+  using C = KhCfg<D, FP8, F8MMA>;
+  static_assert(!F8MMA || (FP8 && D == 128), "E4M3 products: 8-bit cache, D = 128");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
   const uint32_t base_u32 = (raw_u32 + 1023u) & ~1023u;
@@ -1190,7 +1199,7 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
   if (threadIdx.x == 0) {
     mbar_init(bar(C::kBarQ), 1);
     for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(bar(C::kBarKFull + s), FP8 ? C::kConvThreads : 1);
+      mbar_init(bar(C::kBarKFull + s), C::kConv ? C::kConvThreads : 1);
       mbar_init(bar(C::kBarKVEmpty + s), 1);
       mbar_init(bar(C::kBarRawFull + s), 1);
     }
@@ -1202,6 +1211,7 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
     }
     mbar_init(bar(C::kBarOFinal), 1);
     mbar_init(bar(C::kBarDrain), 1);
+    mbar_init(bar(C::kBarQ8), 256);
     misc[1] = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
@@ -1250,7 +1260,14 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
         const bool has_k = u < n_tiles, has_v = u > 0;
         const Tile tk = tile_at(p, kp, first + (has_k ? u : u - 1));
         const Tile tv = tile_at(p, kp, first + (has_v ? u - 1 : u));
-        if (FP8) {
+        if constexpr (F8MMA) {  // E4M3 code tiles, used by the MMA as stored
+          mbar_arrive_expect_tx(bar(C::kBarKFull + st),
+                                (has_k ? C::kKVTileBytes : 0u) + (has_v ? C::kKVTileBytes : 0u));
+          if (has_k)
+            tma_load_4d(sK + st * C::kKVTileBytes, &p.k_map[0], bar(C::kBarKFull + st), 0, tk.row, h, b);
+          if (has_v)
+            tma_load_4d(sV + st * C::kKVTileBytes, &p.v_map[0], bar(C::kBarKFull + st), 0, tv.row, h, b);
+        } else if (FP8) {
           mbar_arrive_expect_tx(bar(C::kBarRawFull + st), (has_k ? 128 * D : 0) + (has_v ? 128 * D : 0));
           if (has_k)
             tma_load_4d(sK + st * C::kTileBytes + C::kBoxBytes, &p.k_map[0], bar(C::kBarRawFull + st), 0, tk.row,
@@ -1277,12 +1294,12 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
       if (*abort_flag) {
         wait_drain(bar(C::kBarQ), 0);
         for (int uu = max(0, u - C::kStages); uu < u; ++uu)
-          wait_drain(bar((FP8 ? C::kBarRawFull : C::kBarKFull) + uu % C::kStages),
+          wait_drain(bar((C::kConv ? C::kBarRawFull : C::kBarKFull) + uu % C::kStages),
                      (uint32_t)(uu / C::kStages) & 1u);
       }
     }
     __syncwarp();
-  } else if (FP8 && (warp == 2 || warp == 3)) {
+  } else if (C::kConv && (warp == 2 || warp == 3)) {
     // ------------------------------------------------ E4M3 -> bf16 expansion
     // (same in-place row expansion as the two-tile kernel)
     const int ct = threadIdx.x - 64;
@@ -1303,26 +1320,36 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    constexpr uint32_t idesc_qk = idesc_bf16_f32(128, kTileN, 0);
-    constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 1);
-    bool ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarQ), 0, abort_flag, 1));
+    constexpr uint32_t idesc_qk = F8MMA ? idesc_e4m3_f32(128, kTileN, 0) : idesc_bf16_f32(128, kTileN, 0);
+    constexpr uint32_t idesc_pv = F8MMA ? idesc_e4m3_f32(128, D, 1) : idesc_bf16_f32(128, D, 1);
+    // F8MMA: the A operand is the E4M3 Q the softmax warps write
+    bool ok = __all_sync(0xffffffffu, wait_bounded(bar(F8MMA ? C::kBarQ8 : C::kBarQ), 0, abort_flag, 1));
     if (ok) tc_fence_after();
-    const uint64_t dq = smem_desc_sw128(sQ, 16, 1024);
+    const uint64_t dq = smem_desc_sw128(F8MMA ? base_u32 + C::kQ8Off : sQ, 16, 1024);
     const uint64_t dk = smem_desc_sw128(sK, 16, 1024);
     const uint64_t dv = smem_desc_sw128(sV, C::kBoxBytes, 1024);
     const uint32_t q_lo = (uint32_t)dq, k_lo = (uint32_t)dk, v_lo = (uint32_t)dv;
     const uint32_t kq_hi = (uint32_t)(dq >> 32), v_hi = (uint32_t)(dv >> 32);
-    constexpr uint32_t kTileStep = C::kTileBytes >> 4;
+    constexpr uint32_t kTileStep = C::kKVTileBytes >> 4;
     // As in the two-tile kernel, the barrier needed next is probed without
     // blocking in the middle of the preceding MMA group.
     auto issue_s = [&](int j, uint32_t pb, uint32_t pp, bool& pout) {
       const uint32_t d = tmem + (uint32_t)(j & 1) * 128u;
       const uint32_t b0 = k_lo + (uint32_t)(j % C::kStages) * kTileStep;
+      if constexpr (F8MMA) {  // 128-byte code rows: K = 32 codes (32 bytes) a step
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t koff = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
-        mma_ss_e(d, make_desc(q_lo + koff, kq_hi), make_desc(b0 + koff, kq_hi), idesc_qk, kk > 0 ? 1u : 0u);
-        if (kk == D / 32 && pb != 0) pout = mbar_test_wait(pb, pp);
+        for (int kk = 0; kk < D / 32; ++kk) {
+          const uint32_t koff = (uint32_t)(kk * 32) >> 4;
+          mma_ss_f8_e(d, make_desc(q_lo + koff, kq_hi), make_desc(b0 + koff, kq_hi), idesc_qk, kk > 0 ? 1u : 0u);
+          if (kk == D / 64 && pb != 0) pout = mbar_test_wait(pb, pp);
+        }
+      } else {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t koff = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
+          mma_ss_e(d, make_desc(q_lo + koff, kq_hi), make_desc(b0 + koff, kq_hi), idesc_qk, kk > 0 ? 1u : 0u);
+          if (kk == D / 32 && pb != 0) pout = mbar_test_wait(pb, pp);
+        }
       }
     };
     // O_hf += P_hf V[64 hf .. 64 hf + 63]
@@ -1330,12 +1357,22 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
       const uint32_t d = tmem + C::kTmemO + (uint32_t)hf * D;
       const uint32_t b0 = v_lo + (uint32_t)((j + 1) % C::kStages) * kTileStep;
       const uint32_t a0 = tmem + (uint32_t)(j & 1) * 128u + (uint32_t)hf * 64u;
+      if constexpr (F8MMA) {  // P_hf: 64 E4M3 keys in 16 columns, 32 keys (8 columns) a step
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const int kg = hf * 4 + kk;  // group of 16 keys
-        mma_ts_e(d, a0 + kk * 8, make_desc(b0 + ((kg * 16 * 128) >> 4), v_hi), idesc_pv,
-                 (kk > 0 || j > 0) ? 1u : 0u);
-        if (kk == 1 && pb != 0) pout = mbar_test_wait(pb, pp);
+        for (int kk = 0; kk < 2; ++kk) {
+          const int kr = hf * 64 + kk * 32;  // first key row of the step
+          mma_ts_f8_e(d, a0 + kk * 8, make_desc(b0 + ((kr * 128) >> 4), v_hi), idesc_pv,
+                      (kk > 0 || j > 0) ? 1u : 0u);
+          if (kk == 0 && pb != 0) pout = mbar_test_wait(pb, pp);
+        }
+      } else {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const int kg = hf * 4 + kk;  // group of 16 keys
+          mma_ts_e(d, a0 + kk * 8, make_desc(b0 + ((kg * 16 * 128) >> 4), v_hi), idesc_pv,
+                   (kk > 0 || j > 0) ? 1u : 0u);
+          if (kk == 1 && pb != 0) pout = mbar_test_wait(pb, pp);
+        }
       }
     };
     auto wait_probed = [&](uint32_t bb, uint32_t par, bool probed, unsigned site) -> bool {
@@ -1425,7 +1462,67 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
     const long long srow = (long long)bh * p.scale_stride;
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
-    for (int j = 0; j < n_tiles; ++j) {
+    // E4M3 products: this thread quantises its half of the row's Q (one
+    // absmax scale per row, as the cache's quantiser does per chunk; the
+    // division in fp32), and P is formed as P * (vs / vs_ref) * 2^4 so that
+    // the codes of V are used as stored and P stays out of the subnormals
+    // (the running max lags by at most 2^4, so P' <= 2^8 < 448).
+    float slq = sl, vgain = 1.f, ofac = 1.f;
+    if constexpr (F8MMA) {
+      ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarQ), 0, abort_flag, 10));
+      float* qmax = reinterpret_cast<float*>(base + C::kQmaxOff);
+      const uint8_t* qrow = base + C::kQOff + hf * C::kBoxBytes + row * 128;  // bf16 columns 64hf ..
+      uint4 qv[8];
+      float amax = 0.f;
+      if (ok) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          qv[c] = *reinterpret_cast<const uint4*>(qrow + ((c ^ (row & 7)) << 4));
+          const uint32_t w[4] = {qv[c].x, qv[c].y, qv[c].z, qv[c].w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[k] << 16)), fabsf(__uint_as_float(w[k] & 0xFFFF0000u))));
+        }
+      }
+      qmax[hf * 128 + row] = amax;
+      named_bar_sync(1, 256);
+      amax = fmaxf(amax, qmax[(1 - hf) * 128 + row]);
+      const float qs = amax == 0.f ? 1.f : __fdiv_rn(amax, 448.f);
+      if (ok) {
+        uint8_t* q8row = base + C::kQ8Off + row * 128;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {  // 16 codes: bf16 chunks 2i, 2i + 1 of this half
+          uint32_t o[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint4 src = qv[2 * i + (k >> 1)];
+            const uint32_t wa = (k & 1) ? src.z : src.x, wb = (k & 1) ? src.w : src.y;
+            o[k] = pack_e4m3x2(__fdiv_rn(__uint_as_float(wa << 16), qs),
+                               __fdiv_rn(__uint_as_float(wa & 0xFFFF0000u), qs)) |
+                   (pack_e4m3x2(__fdiv_rn(__uint_as_float(wb << 16), qs),
+                                __fdiv_rn(__uint_as_float(wb & 0xFFFF0000u), qs))
+                    << 16);
+          }
+          *reinterpret_cast<uint4*>(q8row + (((4 * hf + i) ^ (row & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(bar(C::kBarQ8));
+      slq = sl * qs;
+      // largest V scale over the chunks of the key runs
+      float vmax = 0.f;
+#pragma unroll 1
+      for (int i = 0; i < kp.nseg; ++i) {
+        if (kp.seg[i].nrows <= 0) continue;
+        const int c_hi = min((kp.seg[i].row0 + kp.seg[i].nrows - 1) / p.chunk_tokens, p.scale_stride - 1);
+#pragma unroll 1
+        for (int c = kp.seg[i].row0 / p.chunk_tokens; c <= c_hi; ++c) vmax = fmaxf(vmax, __ldg(p.v_scale + srow + c));
+      }
+      const float vref = vmax > 0.f ? vmax : 1.f;
+      vgain = __fdiv_rn(16.f, vref);
+      ofac = vref * (1.f / 16.f);
+    }
+    for (int j = 0; ok && j < n_tiles; ++j) {
       ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarSFull + (j & 1)), (uint32_t)(j >> 1) & 1u,
                                                 abort_flag, 6 + hf));
       if (!ok) break;
@@ -1463,7 +1560,7 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
       hi -= kofs;
       // FP8 cache: the tile's keys belong to at most two chunks; columns of
       // this half before `bnd` to the first, the rest to the next
-      float c0 = sl, c1 = sl, d0 = 0.f, v0 = 1.f, v1 = 1.f, iv0 = 1.f;
+      float c0 = slq, c1 = slq, d0 = 0.f, v0 = 1.f, v1 = 1.f, iv0 = 1.f;
       int bnd = 64;
       if constexpr (FP8) {
         const int si0 = min(tile_row0 / p.chunk_tokens, p.scale_stride - 1);
@@ -1477,12 +1574,12 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
         }
         // a zero scale marks a slot never written, whose keys are all masked:
         // keep the coefficients finite and non-zero so that -inf stays -inf
-        c0 = ks0 > 0.f ? sl * ks0 : sl;
-        c1 = ks1 > 0.f ? sl * ks1 : sl;
-        v0 = vs0;
-        v1 = vs1;
-        d0 = vs0 > 0.f ? __log2f(vs0) : 0.f;
-        iv0 = vs0 > 0.f ? 1.f / vs0 : 0.f;
+        c0 = ks0 > 0.f ? slq * ks0 : slq;
+        c1 = ks1 > 0.f ? slq * ks1 : slq;
+        v0 = vs0 * vgain;  // vgain = 1 unless the product is E4M3
+        v1 = vs1 * vgain;
+        d0 = vs0 > 0.f ? __log2f(v0) : 0.f;
+        iv0 = vs0 > 0.f ? 1.f / v0 : 0.f;
       }
       const bool straddle = FP8 && bnd > 0 && bnd < 64;
       const bool masked = !(lo <= 0 && hi >= 64);
@@ -1509,10 +1606,12 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
         }
         return fmax3(fmaxf(pm[0], pm[1]), pm[2], pm[3]);
       };
-      // P of 32 columns: e = 2^(s*xa + xs); packed bf16 pairs into pko[0..15],
-      // row-sum terms into ps (before any per-column V scale)
+      // P of 32 columns: e = 2^(s*xa + xs); packed bf16 pairs into pko[0..15]
+      // (E4M3 products: four codes a word into pko[0..7]), row-sum terms into
+      // ps (before any per-column V scale)
       auto exps32 = [&](const uint32_t (&sv)[32], int cb, float xa, float xs, uint32_t* pko, float2& ps) {
         const float2 xa2 = make_float2(xa, xa), xs2 = make_float2(xs, xs);
+        uint32_t lo16 = 0;
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
           const float2 x = __ffma2_rn(make_float2(__uint_as_float(sv[2 * c]), __uint_as_float(sv[2 * c + 1])), xa2, xs2);
@@ -1522,7 +1621,13 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
             e0 *= (cb + 2 * c < bnd ? v0 : v1);
             e1 *= (cb + 2 * c + 1 < bnd ? v0 : v1);
           }
-          pko[c] = pack_bf16(e0, e1);
+          if constexpr (F8MMA) {
+            const uint32_t h2 = pack_e4m3x2(e0, e1);
+            if (c & 1) pko[c >> 1] = lo16 | (h2 << 16);
+            else lo16 = h2;
+          } else {
+            pko[c] = pack_bf16(e0, e1);
+          }
         }
       };
       // Exponentials are taken against the running max m_run right away, in
@@ -1541,10 +1646,10 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
       tmem_wait_ld();
       prep(s1, 32);
       const float mx1 = max32(s1);
-      exps32(s1, 32, xa, straddle ? -mb0 : d0 - mb0, pk + 16, psb);
+      exps32(s1, 32, xa, straddle ? -mb0 : d0 - mb0, pk + (F8MMA ? 8 : 16), psb);
       const float mx = fmaxf(mx0, mx1);
       const float m_new = fmaxf(m_run, straddle ? mx : mx * c0);
-      const bool need = m_new > m_run + kRescaleThreshold;
+      const bool need = m_new > m_run + (F8MMA ? kRescaleThresholdF8 : kRescaleThreshold);
       if (__any_sync(0xffffffffu, need)) {
         float alpha = 1.f;
         if (need) {
@@ -1571,9 +1676,10 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
         const float mb = (m_run == -INFINITY) ? 0.f : m_run;
         psa = psb = make_float2(0.f, 0.f);
         exps32(s0, 0, xa, straddle ? -mb : d0 - mb, pk, psa);
-        exps32(s1, 32, xa, straddle ? -mb : d0 - mb, pk + 16, psb);
+        exps32(s1, 32, xa, straddle ? -mb : d0 - mb, pk + (F8MMA ? 8 : 16), psb);
       }
-      tmem_st32(tS, pk);
+      if constexpr (F8MMA) tmem_st16(tS, *reinterpret_cast<const uint32_t(*)[16]>(pk));
+      else tmem_st32(tS, pk);
       l_run += ((psa.x + psa.y) + (psb.x + psb.y)) * (straddle ? 1.f : iv0);
       tmem_wait_st();
       tc_fence_before();
@@ -1597,7 +1703,7 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
     const float w1 = (M == -INFINITY) ? 0.f : ex2(m1 - M);
     const float L = l0 * w0 + l1 * w1;
     const float inv = L > 0.f ? 1.f / L : 0.f;
-    const float sc0 = w0 * inv, sc1 = w1 * inv;
+    const float sc0 = w0 * inv * ofac, sc1 = w1 * inv * ofac;  // ofac undoes the E4M3 P gain
     constexpr int kHalfCols = D / 2;
     uint8_t* stage = base + C::kQOff;
     if (ok) {
@@ -1649,13 +1755,13 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
   }
 }
 
-template <int D, bool FP8>
+template <int D, bool FP8, bool F8MMA = false>
 cudaError_t launch_kh_impl(const AttnParams& p, cudaStream_t s) {
-  using C = KhCfg<D, FP8>;
+  using C = KhCfg<D, FP8, F8MMA>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(chunk_attn_kh_kernel<D, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)C::kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(chunk_attn_kh_kernel<D, FP8, F8MMA>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
@@ -1669,7 +1775,7 @@ cudaError_t launch_kh_impl(const AttnParams& p, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, chunk_attn_kh_kernel<D, FP8>, p);
+  return cudaLaunchKernelEx(&cfg, chunk_attn_kh_kernel<D, FP8, F8MMA>, p);
 }
 
 // ===========================================================================
@@ -2140,6 +2246,7 @@ cudaError_t launch_wait_timeout_probe(unsigned long long timeout_ns, cudaStream_
 
 cudaError_t launch_chunk_attention_kh(const AttnParams& p, cudaStream_t s) {
   if (p.splits != 1) return cudaErrorInvalidValue;
+  if (p.f8mma) return (p.fp8 && !p.k_int8 && p.D == 128) ? launch_kh_impl<128, true, true>(p, s) : cudaErrorInvalidValue;
   if (p.fp8) return p.D == 128 ? launch_kh_impl<128, true>(p, s) : cudaErrorInvalidValue;
   if (p.D == 128) return launch_kh_impl<128, false>(p, s);
   if (p.D == 64) return launch_kh_impl<64, false>(p, s);

@@ -56,7 +56,8 @@ bool encode_map(CUtensorMap* m, const void* ptr, int D, long long rows, int H, i
 
 // Head-major [B, H, rows, D] E4M3 codes: plain (unswizzled) 128-row boxes of
 // whole D-byte rows, expanded to bf16 inside the attention kernel.
-bool encode_head_major_u8(CUtensorMap* m, const void* ptr, int B, int H, long long rows, int D) {
+bool encode_head_major_u8(CUtensorMap* m, const void* ptr, int B, int H, long long rows, int D,
+                          bool swizzle128 = false) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
   const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)rows, (cuuint64_t)H, (cuuint64_t)B};
@@ -64,8 +65,8 @@ bool encode_head_major_u8(CUtensorMap* m, const void* ptr, int B, int H, long lo
   const cuuint32_t box[4] = {(cuuint32_t)D, (cuuint32_t)kTileN, 1, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(ptr), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Token-major [B, L, H, D] bf16.
@@ -494,6 +495,24 @@ sab_status sab_chunk_attention(const sab_ring* ring, int layer, long long chunk,
       plan_chunk_attention(ring, layer, chunk, Q, K_cur, V_cur, window, use_sink, num_splits, softmax_scale, O, LSE, p);
   if (st != SAB_OK) return st;
   return launch_attention(p, ring->d.chunk_tokens, num_splits, workspace, ws_bytes, stream);
+}
+
+sab_status sab_chunk_attention_fp8mma(const sab_ring* ring, int layer, long long chunk, const void* Q, int window,
+                                      int use_sink, float softmax_scale, void* O, float* LSE, void* stream) {
+  if (ring == nullptr) return SAB_ERR_INVALID_ARG;
+  if (ring->d.kv_dtype != SAB_KV_FP8_E4M3) return SAB_ERR_UNSUPPORTED;
+  AttnParams p;
+  const sab_status st =
+      plan_chunk_attention(ring, layer, chunk, Q, nullptr, nullptr, window, use_sink, 1, softmax_scale, O, LSE, p);
+  if (st != SAB_OK) return st;
+  p.f8mma = 1;
+  // the tensor cores read the code tiles as K-major / MN-major operands in
+  // the 128-byte-swizzled layout (D = 128 codes = one swizzle row)
+  const sab_ring_desc& d = ring->d;
+  if (!encode_head_major_u8(&p.k_map[0], ring->k(layer), d.batch, d.heads, ring->g.rows, d.head_dim, true) ||
+      !encode_head_major_u8(&p.v_map[0], ring->v(layer), d.batch, d.heads, ring->g.rows, d.head_dim, true))
+    return SAB_ERR_CUDA;
+  return launch_attention(p, ring->d.chunk_tokens, 1, nullptr, 0, stream);
 }
 
 sab_status sab_chunk_attention_dev(const sab_ring* ring, int layer, const long long* d_chunk, const void* Q,

@@ -102,6 +102,7 @@ struct AttnParams {
   int mode;
   int fp8;                // 1: the ring holds 8-bit codes (k_map[0]/v_map[0] are uint8 maps)
   int k_int8;             // with fp8: keys are INT8 codes (values stay E4M3)
+  int f8mma;              // with fp8 (E4M3 keys and values): Q and P in E4M3, kind::f8f6f4 products
   const float* k_scale;   // FP8: [B*H][scale_stride] fp32 scales, index = ring row / chunk_tokens
   const float* v_scale;
   int scale_stride;

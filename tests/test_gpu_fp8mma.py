@@ -1,0 +1,118 @@
+"""GPU parity of chunk attention with E4M3 tensor-core products
+(``sab_chunk_attention_fp8mma``) against the oracle of ``oracle/fp8mma.py``.
+
+The oracle quantises each query row exactly as the kernel does (the same
+fp32 decisions), uses the cache's dequantised keys and values, and returns
+the exact result with a per-element bound on what rounding P to E4M3 can
+change.  Tolerance per element: that bound, plus one bf16 ulp of the result
+(2^-8 |O|) and 1e-3 for the fp32 accumulations and the approximate
+exponential; LSE within 2e-3 (P is not rounded in the row sums, so LSE only
+sees the fp32 score accumulation of exact E4M3 products).  The bulk is held
+to the oracle's statistical model of the rounding: over each checked call,
+mean |error| <= 1.5 x mean(sqrt(2/pi) sigma) + 2^-10 mean |O| + 1e-4, with
+sigma the standard deviation of uniform rounding of every P to E4M3 and the
+second term the bf16 rounding of the output."""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention as OA
+from oracle import fp8 as O8
+from oracle import fp8mma as OF
+from oracle.ring import ListRing
+from streaming_attention_block_gb300 import synth
+import streaming_attention_block_gb300 as sab
+
+from ._common import bhld, f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    sab.library()
+
+
+def _quantised(x_blhd):
+    codes, scales = O8.quantize_chunk_bhld(x_blhd.float().numpy())
+    deq = np.empty(codes.shape, dtype=np.float64)
+    for b in range(codes.shape[0]):
+        for h in range(codes.shape[1]):
+            deq[b, h] = O8.dequantize_block(codes[b, h], scales[b, h])
+    return deq, scales
+
+
+def _stream(w, check_chunks, rows=None):
+    """Append-first stream over an E4M3 ring; at ``check_chunks`` compare every
+    (b, h) on ``rows``.  Returns the worst error / tolerance ratio and, per
+    checked chunk, the mean error and the predicted mean rounding error."""
+    gen = synth.generator(w.seed)
+    ring = sab.KVRing(1, w.B, w.H, w.D, w.Lc, w.R, has_sink=w.sink, kv_dtype=sab.KV_FP8_E4M3)
+    oring = ListRing(w.R)
+    vscale = {}  # chunk id -> V scales [B, H]
+    if w.sink:
+        sk, sv = synth.sink_kv(w, gen)
+        ring.set_sink(0, sk.cuda(), sv.cuda())
+        (kq, _), (vq, vsc) = _quantised(sk), _quantised(sv)
+        oring.set_sink(kq, vq)
+        vscale[OA.SINK_CHUNK] = vsc
+    worst, stats = 0.0, []
+    rsel = slice(None) if rows is None else rows
+    for c in range(w.chunks):
+        q, k, v = synth.chunk_qkv(w, gen)
+        ring.append(0, c, k.cuda(), v.cuda())
+        (kq, _), (vq, vsc) = _quantised(k), _quantised(v)
+        oring.append(c, kq, vq)
+        vscale[c] = vsc
+        O = torch.empty((w.B, w.Lc, w.H, w.D), dtype=torch.bfloat16, device="cuda")
+        LSE = torch.empty((w.B, w.H, w.Lc), dtype=torch.float32, device="cuda")
+        sab.chunk_attention_fp8mma(ring.handle, 0, c, q.cuda(), w.W, w.sink, w.scale, O, LSE)
+        if c not in check_chunks:
+            continue
+        torch.cuda.synchronize()
+        assert sab.get_last_device_error() == 0
+        K, V, kid, ksink = OA.streaming_key_set(oring, c, None, None, w.W, w.sink)
+        qq = bhld(q)[:, :, rsel]
+        mask = OA.chunk_visibility(np.full(qq.shape[2], c), kid, w.W, ksink)
+        o_gpu = bhld(O)[:, :, rsel]
+        l_gpu = f64(LSE)[:, :, rsel]
+        e_sum = p_sum = o_sum = 0.0
+        for b in range(w.B):
+            for h in range(w.H):
+                vs_key = np.array([vscale[int(i)][b, h] for i in kid], dtype=np.float64)
+                o, lse, bound = OF.head_attention(qq[b, h].astype(np.float32), K[b, h], V[b, h], mask, w.scale,
+                                                  vs_key)
+                err = np.abs(o_gpu[b, h] - o)
+                tol = bound + 2.0 ** -8 * np.abs(o) + 1e-3
+                worst = max(worst, float(np.max(err / tol)))
+                sigma = OF.rounding_sigma(qq[b, h].astype(np.float32), K[b, h], V[b, h], mask, w.scale, vs_key)
+                e_sum += float(np.mean(err))
+                p_sum += float(np.mean(np.sqrt(2.0 / np.pi) * sigma))
+                o_sum += float(np.mean(np.abs(o)))
+                assert np.all(err <= tol), (f"chunk {c} b{b} h{h}: max err {err.max():.3e}, worst ratio "
+                                            f"{np.max(err / tol):.2f}")
+                assert np.max(np.abs(l_gpu[b, h] - lse)) <= 2e-3, f"chunk {c} b{b} h{h}: LSE"
+        n = w.B * w.H
+        stats.append((c, e_sum / n, p_sum / n))
+        assert e_sum <= 1.5 * p_sum + 2.0 ** -10 * o_sum + 1e-4 * n, (c, e_sum / n, p_sum / n)
+    return worst, stats
+
+
+def test_fp8mma_small_elementwise():
+    """Sink + 3-slot ring, 200-token chunks (key tiles straddle chunks),
+    window 2, 1% x8 outliers; every row of chunks 0, 1, 3 and 5."""
+    w = synth.Workload("f8s", B=1, H=2, D=128, Lc=200, R=3, W=2, chunks=6, sink=True, kcur_separate=False,
+                       kv_fp8=True, outliers=True, seed=41)
+    _stream(w, {0, 1, 3, 5})
+
+
+def test_fp8mma_full_size_sampled_rows():
+    """Long-window FP8 workload (H24, 405-token chunks, sink + 20-slot ring,
+    window 19, 60 chunks so the ring wraps 3 times): sampled rows of chunks
+    around the wraps, every head."""
+    w = synth.workload("fp8_kv")
+    rows = np.concatenate([np.arange(0, w.Lc, 9), [w.Lc - 1]])
+    _stream(w, {0, 19, 20, 40, 59}, rows=rows)

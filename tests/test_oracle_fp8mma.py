@@ -67,7 +67,7 @@ def _replay(q, k, v, mask, scale, vs, delta, bound_fn=None, gain=OF.P_GAIN_LOG2)
 
 
 @pytest.mark.parametrize("peak", [0.3, 3.0, 12.0])
-@pytest.mark.parametrize("delta", [0, 1, 2])
+@pytest.mark.parametrize("delta", [0, 2, 4])
 def test_bound_holds_under_brute_force_rounding(peak, delta):
     rng = np.random.default_rng(int(peak * 10) + delta)
     Nk, D = 600, 64
@@ -111,10 +111,10 @@ def test_bound_without_the_scale_factor_fails():
 
 
 def test_gain_shrinks_the_subnormal_term():
-    """With the kernel's gain the same coherent case is 64x tighter and still
-    covered."""
+    """With the kernel's gain the same coherent case is 2^g times tighter and
+    still covered."""
     D, Nk = 32, 400
-    p0 = 1.49 * 2.0 ** -9 * 40.0 / 64.0  # P r 2^6 = 1.49 * 2^-9
+    p0 = 1.49 * 2.0 ** -9 * 40.0 / 2.0 ** OF.P_GAIN_LOG2  # P r 2^g = 1.49 * 2^-9
     q = np.zeros((4, D), dtype=np.float32)
     q[:, 0] = 1.0
     k = np.zeros((Nk, D))
@@ -129,3 +129,23 @@ def test_gain_shrinks_the_subnormal_term():
     assert np.all(err <= bound + 1e-12)
     err0, bound0 = _replay(q, k, v, mask, 1.0, vs, 0, gain=0)
     assert np.all(bound < bound0)
+
+
+@pytest.mark.parametrize("peak", [0.3, 3.0])
+def test_sigma_predicts_the_replayed_error(peak):
+    """The uniform-rounding model's sigma matches the RMS of the replayed
+    rounding error (random keys: errors independent across keys)."""
+    rng = np.random.default_rng(11 + int(peak))
+    Nk, D = 800, 64
+    q = (rng.standard_normal((64, D)) * peak).astype(np.float32)
+    k = rng.standard_normal((Nk, D))
+    v = rng.standard_normal((Nk, D))
+    vs = np.repeat([0.3, 1.0], Nk // 2)
+    mask = np.ones((64, Nk), dtype=bool)
+    err, _ = _replay(q, k, v, mask, 1.0 / np.sqrt(D), vs, 0)
+    sigma = OF.rounding_sigma(q, k, v, mask, 1.0 / np.sqrt(D), vs)
+    ratio = np.sqrt(np.mean(err ** 2)) / np.sqrt(np.mean(sigma ** 2))
+    assert 0.7 < ratio < 1.3, ratio
+    # and the mean magnitude is about sqrt(2/pi) sigma
+    ratio_abs = np.mean(err) / np.mean(np.sqrt(2 / np.pi) * sigma)
+    assert 0.7 < ratio_abs < 1.3, ratio_abs
