@@ -366,12 +366,16 @@ def run_ours(args):
 
 def run_attn_only(args):
     """Small profiling case: one layer of the Wan-1.3B stream at chunk 2
-    (4608 keys), N back-to-back attention calls over 4 input sets."""
+    (4608 keys), N back-to-back attention calls over 4 input sets; with
+    ``--case fp8_kv_e4m3_mma`` N calls of the E4M3-product kernel on the
+    long-window FP8 workload (sink + 20 slots, 8505 keys)."""
     import torch
 
     import streaming_attention_block_gb300 as sab
     from streaming_attention_block_gb300 import synth
 
+    if args.case == "fp8_kv_e4m3_mma":
+        return run_attn_only_fp8mma(args)
     dev = torch.device("cuda", 0)
     w = synth.workload("wan13b")
     g = synth.generator(w.seed, device="cuda")
@@ -399,6 +403,38 @@ def run_attn_only(args):
     tail = us[min(3, len(us) - 1):]
     print(json.dumps({"attn_only_calls": len(us), "us_median": statistics.median(tail),
                       "tflops_median": flops / (statistics.median(tail) * 1e-6) / 1e12, "splits": args.splits}))
+    assert sab.get_last_device_error(stream) == 0
+
+
+def run_attn_only_fp8mma(args):
+    import torch
+
+    import streaming_attention_block_gb300 as sab
+    from streaming_attention_block_gb300 import synth
+
+    w = synth.workload("fp8_kv")
+    g = synth.generator(w.seed, device="cuda")
+    ring = sab.KVRing(1, w.B, w.H, w.D, w.Lc, w.R, has_sink=w.sink, kv_dtype=sab.KV_FP8_E4M3)
+    sk, sv = synth.sink_kv(w, g, "cuda")
+    ring.set_sink(0, sk, sv)
+    for c in range(w.W + 1):  # first chunk with a full window
+        q, k, v = synth.chunk_qkv(w, g, "cuda")
+        ring.append(0, c, k, v)
+    O = torch.empty_like(q)
+    LSE = torch.empty((w.B, w.H, w.Lc), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    times = []
+    for _ in range(args.attn_only):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        sab.chunk_attention_fp8mma(ring.handle, 0, w.W, q, w.W, w.sink, w.scale, O, LSE, stream)
+        b.record(stream)
+        times.append((a, b))
+    torch.cuda.synchronize()
+    us = [a.elapsed_time(b) * 1e3 for a, b in times]
+    tail = us[min(3, len(us) - 1):]
+    print(json.dumps({"attn_only_calls": len(us), "case": args.case, "us_median": statistics.median(tail)}))
     assert sab.get_last_device_error(stream) == 0
 
 
@@ -660,6 +696,8 @@ def main():
     ap.add_argument("--no-graph", action="store_true", help="skip the graph-replay measurement")
     ap.add_argument("--splits", type=int, default=0, help="KV splits per attention call (0: library's choice)")
     ap.add_argument("--sweep", action="store_true", help="time one attention call of every workload")
+    ap.add_argument("--case", default="wan13b", choices=["wan13b", "fp8_kv_e4m3_mma"],
+                    help="workload of --attn-only")
     ap.add_argument("--attn-only", type=int, default=0, metavar="N",
                     help="profiling case: N steady-state attention calls on one layer, then exit")
     args = ap.parse_args()
