@@ -376,6 +376,8 @@ def run_attn_only(args):
 
     if args.case == "fp8_kv_e4m3_mma":
         return run_attn_only_fp8mma(args)
+    if args.case == "block_causal_backward":
+        return run_attn_only_backward(args)
     dev = torch.device("cuda", 0)
     w = synth.workload("wan13b")
     g = synth.generator(w.seed, device="cuda")
@@ -403,6 +405,41 @@ def run_attn_only(args):
     tail = us[min(3, len(us) - 1):]
     print(json.dumps({"attn_only_calls": len(us), "us_median": statistics.median(tail),
                       "tflops_median": flops / (statistics.median(tail) * 1e-6) / 1e12, "splits": args.splits}))
+    assert sab.get_last_device_error(stream) == 0
+
+
+def run_attn_only_backward(args):
+    """One sample of the training shape (30720 tokens, H12, D128, window 2):
+    one forward, then N backward calls (delta, key-tile and query-tile
+    kernels each)."""
+    import torch
+
+    import streaming_attention_block_gb300 as sab
+    from streaming_attention_block_gb300 import synth
+
+    w = synth.workload("block_causal", B=1)
+    g = synth.generator(w.seed, device="cuda")
+    q, k, v = synth.full_sequence_qkv(w, g, "cuda")
+    do = synth.randn_bf16(g, tuple(q.shape), "cuda")
+    Lt = q.shape[1]
+    O = torch.empty_like(q)
+    LSE = torch.empty((w.B, w.H, Lt), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    sab.block_causal_attention(q, k, v, w.Lc, w.W, 0, w.scale, O, LSE, None, stream)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(sab.block_causal_attention_backward_workspace(w.B, Lt, w.H), dtype=torch.uint8, device="cuda")
+    times = []
+    for _ in range(args.attn_only):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        sab.block_causal_attention_backward(q, k, v, O, do, LSE, w.Lc, w.W, w.scale, dq, dk, dv, ws, stream)
+        b.record(stream)
+        times.append((a, b))
+    torch.cuda.synchronize()
+    us = [a.elapsed_time(b) * 1e3 for a, b in times]
+    tail = us[min(1, len(us) - 1):]
+    print(json.dumps({"attn_only_calls": len(us), "case": args.case, "us_median": statistics.median(tail)}))
     assert sab.get_last_device_error(stream) == 0
 
 
@@ -696,7 +733,7 @@ def main():
     ap.add_argument("--no-graph", action="store_true", help="skip the graph-replay measurement")
     ap.add_argument("--splits", type=int, default=0, help="KV splits per attention call (0: library's choice)")
     ap.add_argument("--sweep", action="store_true", help="time one attention call of every workload")
-    ap.add_argument("--case", default="wan13b", choices=["wan13b", "fp8_kv_e4m3_mma"],
+    ap.add_argument("--case", default="wan13b", choices=["wan13b", "fp8_kv_e4m3_mma", "block_causal_backward"],
                     help="workload of --attn-only")
     ap.add_argument("--attn-only", type=int, default=0, metavar="N",
                     help="profiling case: N steady-state attention calls on one layer, then exit")

@@ -1807,8 +1807,8 @@ struct BwdCfg {
   static constexpr int kBarRes = 0;
   static constexpr int kBarFull = 1;                      // [kStages]
   static constexpr int kBarEmpty = kBarFull + kStages;    // [kStages]
-  static constexpr int kBarSFull = kBarEmpty + kStages;
-  static constexpr int kBarPFull = kBarSFull + 1;         // [2 halves]
+  static constexpr int kBarSFull = kBarEmpty + kStages;   // [2 halves]
+  static constexpr int kBarPFull = kBarSFull + 2;         // [2 halves]
   static constexpr int kBarFinal = kBarPFull + 2;
   static constexpr int kBarDrain = kBarFinal + 1;
   static constexpr int kNumBars = kBarDrain + 1;
@@ -1907,7 +1907,8 @@ attn_bwd_kernel(const __grid_constant__ BwdParams p) {
       mbar_init(bar(C::kBarFull + s), 1);
       mbar_init(bar(C::kBarEmpty + s), 1);
     }
-    mbar_init(bar(C::kBarSFull), 1);
+    mbar_init(bar(C::kBarSFull + 0), 1);
+    mbar_init(bar(C::kBarSFull + 1), 1);
     mbar_init(bar(C::kBarPFull + 0), 128);
     mbar_init(bar(C::kBarPFull + 1), 128);
     mbar_init(bar(C::kBarFinal), 1);
@@ -1987,7 +1988,11 @@ attn_bwd_kernel(const __grid_constant__ BwdParams p) {
     __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0);  // scores: N = 128 rows of the streamed tile
+    // The streamed tile is taken in two halves of 64 rows, each with its own
+    // TMEM buffer (columns 128h .. 128h + 127: scores in the first 64, dP in
+    // the next 64), so the gradient products of one half and the scores of
+    // the next tile's same half run while the other half's softmax works.
+    constexpr uint32_t idesc_s = idesc_bf16_f32(128, 64, 0);   // scores: N = 64 rows of a streamed half
     constexpr uint32_t idesc_acc = idesc_bf16_f32(128, D, 1);  // accumulators: B MN-major, N = D
     constexpr uint32_t kStageStep = C::kStageBytes >> 4;
     bool ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarRes), 0, abort_flag, 1));
@@ -1999,47 +2004,70 @@ attn_bwd_kernel(const __grid_constant__ BwdParams p) {
     const uint64_t dm0 = smem_desc_sw128(base_u32 + C::kStageOff, C::kBoxBytes, 1024);  // streamed tile 0, MN-major
     const uint64_t dm1 = smem_desc_sw128(base_u32 + C::kStageOff + C::kTileBytes, C::kBoxBytes, 1024);
     const uint32_t hi_k = (uint32_t)(dr0 >> 32), hi_mn = (uint32_t)(dm0 >> 32);
-    // scores of the resident tile against a streamed tile: d = A_res . B_str^T
-    auto scores = [&](uint32_t d, uint64_t a, uint64_t bdesc, uint32_t st) {
+    // scores of the resident tile against rows [64h, 64h + 64) of a streamed
+    // tile: d = A_res . B_str^T (the half starts 64 rows = 8 KB into each box)
+    auto scores = [&](uint32_t d, uint64_t a, uint64_t bdesc, uint32_t st, int h) {
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t koff = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
-        mma_ss_e(d, make_desc((uint32_t)a + koff, hi_k), make_desc((uint32_t)bdesc + st * kStageStep + koff, hi_k),
+        mma_ss_e(d, make_desc((uint32_t)a + koff, hi_k),
+                 make_desc((uint32_t)bdesc + st * kStageStep + (uint32_t)h * ((64u * 128u) >> 4) + koff, hi_k),
                  idesc_s, kk > 0 ? 1u : 0u);
       }
     };
-    // acc += X . streamed tile (X: bf16 rows of 128 written to TMEM at column
-    // a_col, half h in columns [64h, 64h + 32); the streamed tile as the
-    // MN-major B operand, K = its 128 rows)
-    auto accum = [&](uint32_t d, uint32_t a_col, uint64_t bmn, uint32_t st, bool first) {
+    // acc += X_h . rows [64h, 64h + 64) of a streamed tile (X_h: bf16 rows
+    // of 64 written to TMEM from column a_col; the streamed tile as the
+    // MN-major B operand, K = 64)
+    auto accum = [&](uint32_t d, uint32_t a_col, uint64_t bmn, uint32_t st, int h, bool first) {
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t ac = a_col + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
-        mma_ts_e(d, tmem + ac, make_desc((uint32_t)bmn + st * kStageStep + ((kk * 16 * 128) >> 4), hi_mn),
-                 idesc_acc, (first && kk == 0) ? 0u : 1u);
+      for (int kk = 0; kk < 4; ++kk) {
+        mma_ts_e(d, tmem + a_col + kk * 8,
+                 make_desc((uint32_t)bmn + st * kStageStep + (((64 * h + 16 * kk) * 128) >> 4), hi_mn), idesc_acc,
+                 (first && kk == 0) ? 0u : 1u);
       }
     };
-    for (int j = 0; ok && j < nt; ++j) {
+    auto issue_scores = [&](int j, int h) {
       const uint32_t st = (uint32_t)(j % C::kStages);
-      if (!(ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarFull + st), (uint32_t)(j / C::kStages) & 1u,
-                                                      abort_flag, 5))))
-        break;
-      tc_fence_after();
-      scores(tmem + 0, dr0, ds0, st);    // S^T = K Q^T  (or S = Q K^T)
-      scores(tmem + 128, dr1, ds1, st);  // dP^T = V dO^T (or dP = dO V^T)
-      mma_commit_e(bar(C::kBarSFull));
+      scores(tmem + 128u * h, dr0, ds0, st, h);        // S^T = K Q^T  (or S = Q K^T)
+      scores(tmem + 128u * h + 64u, dr1, ds1, st, h);  // dP^T = V dO^T (or dP = dO V^T)
+      mma_commit_e(bar(C::kBarSFull + h));
+    };
+    auto issue_accum = [&](int j, int h) {
+      const uint32_t st = (uint32_t)(j % C::kStages);
+      const bool first = j == 0 && h == 0;
+      if (KQ) {
+        accum(tmem + 256, 128u * h, dm1, st, h, first);           // dV += P^T dO
+        accum(tmem + 256 + D, 128u * h + 64u, dm0, st, h, first);  // dK += dS^T Q
+      } else {
+        accum(tmem + 256, 128u * h, dm0, st, h, first);           // dQ += dS K
+      }
+    };
+    auto wait_full = [&](int j) -> bool {
+      const bool r = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarFull + j % C::kStages),
+                                                          (uint32_t)(j / C::kStages) & 1u, abort_flag, 5));
+      if (r) tc_fence_after();
+      return r;
+    };
+    // order: S_0(0), S_1(0), then per tile j: G_0(j), S_0(j+1), G_1(j), S_1(j+1)
+    if (ok && nt > 0 && (ok = wait_full(0))) {
+      issue_scores(0, 0);
+      issue_scores(0, 1);
+    }
+    for (int j = 0; ok && j < nt; ++j) {
       if (!(ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarPFull + 0), (uint32_t)j & 1u, abort_flag, 2))))
         break;
+      tc_fence_after();
+      issue_accum(j, 0);
+      if (j + 1 < nt) {
+        if (!(ok = wait_full(j + 1))) break;
+        issue_scores(j + 1, 0);
+      }
       if (!(ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarPFull + 1), (uint32_t)j & 1u, abort_flag, 3))))
         break;
       tc_fence_after();
-      if (KQ) {
-        accum(tmem + 256, 0, dm1, st, j == 0);      // dV += P^T dO
-        accum(tmem + 256 + D, 128, dm0, st, j == 0);  // dK += dS^T Q
-      } else {
-        accum(tmem + 256, 0, dm0, st, j == 0);      // dQ += dS K
-      }
-      mma_commit_e(bar(C::kBarEmpty + st));
+      issue_accum(j, 1);
+      mma_commit_e(bar(C::kBarEmpty + j % C::kStages));  // stage of tile j is read for the last time
+      if (j + 1 < nt) issue_scores(j + 1, 1);
     }
     if (ok) mma_commit_e(bar(C::kBarFinal));
     if (!ok) {
@@ -2054,7 +2082,7 @@ attn_bwd_kernel(const __grid_constant__ BwdParams p) {
     const int row = quad * 32 + lane;  // row of the resident tile
     const int r = r0 + row;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    const uint32_t tS = tmem + lane_off + hf * 64, tdP = tmem + lane_off + 128 + hf * 64;
+    const uint32_t tS = tmem + lane_off + hf * 128, tdP = tS + 64;  // this half's buffer
     // visible streamed rows of this resident row: [lo0, hi0) in run 0 (real
     // memory) and [lo1, hi1) in run 1
     int hi0 = 0, lo1 = 0, hi1 = 0;
@@ -2085,7 +2113,7 @@ attn_bwd_kernel(const __grid_constant__ BwdParams p) {
     const float sc = p.scale_log2;
     bool ok = true;
     for (int j = 0; j < nt; ++j) {
-      ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarSFull), (uint32_t)j & 1u, abort_flag, 6 + hf));
+      ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarSFull + hf), (uint32_t)j & 1u, abort_flag, 6 + hf));
       if (!ok) break;
       tc_fence_after();
       uint32_t s0[32], s1[32], d0[32], d1[32];
