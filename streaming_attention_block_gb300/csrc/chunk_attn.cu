@@ -2116,18 +2116,11 @@ attn_bwd_kernel(const __grid_constant__ BwdParams p) {
       ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarSFull + hf), (uint32_t)j & 1u, abort_flag, 6 + hf));
       if (!ok) break;
       tc_fence_after();
-      uint32_t s0[32], s1[32], d0[32], d1[32];
-      tmem_ld32(tS, s0);
-      tmem_ld32(tS + 32, s1);
-      tmem_ld32(tdP, d0);
-      tmem_ld32(tdP + 32, d1);
       const int c0 = tile_row(j) + hf * 64;  // first streamed row of this half
       const int lo = (j < u.n0 ? 0 : lo1) - c0, hi = (j < u.n0 ? hi0 : hi1) - c0;
       const float* ls = reinterpret_cast<const float*>(base + C::kStageOff + (j % C::kStages) * C::kStageBytes +
                                                        2 * C::kTileBytes) + hf * 64;
       const float* dl = ls + 128;
-      tmem_wait_ld();
-      uint32_t pk[32], dk[32];
       auto one = [&](uint32_t s, uint32_t dpv, int c, float& pv, float& dsv) {
         const bool vis = c >= lo && c < hi;
         const float l2 = KQ ? ls[c] : lse2;
@@ -2135,23 +2128,29 @@ attn_bwd_kernel(const __grid_constant__ BwdParams p) {
         pv = vis ? ex2(fmaf(__uint_as_float(s), sc, -l2)) : 0.f;
         dsv = pv * (__uint_as_float(dpv) - de);
       };
+      // two passes of 32 columns (the packed results of a pass go over
+      // columns its own loads have already read, so the passes never clash)
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        float pa, pb, da, db;
-        one(s0[2 * c], d0[2 * c], 2 * c, pa, da);
-        one(s0[2 * c + 1], d0[2 * c + 1], 2 * c + 1, pb, db);
-        pk[c] = pack_bf16(pa, pb);
-        dk[c] = pack_bf16(da, db);
-        one(s1[2 * c], d1[2 * c], 32 + 2 * c, pa, da);
-        one(s1[2 * c + 1], d1[2 * c + 1], 33 + 2 * c, pb, db);
-        pk[16 + c] = pack_bf16(pa, pb);
-        dk[16 + c] = pack_bf16(da, db);
-      }
-      if (KQ) {
-        tmem_st32(tS, pk);   // P^T over S^T
-        tmem_st32(tdP, dk);  // dS^T over dP^T
-      } else {
-        tmem_st32(tS, dk);   // dS over S
+      for (int pass = 0; pass < 2; ++pass) {
+        uint32_t sv[32], dv[32];
+        tmem_ld32(tS + 32 * pass, sv);
+        tmem_ld32(tdP + 32 * pass, dv);
+        tmem_wait_ld();
+        uint32_t pk[16], dk[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          float pa, pb, da, db;
+          one(sv[2 * c], dv[2 * c], 32 * pass + 2 * c, pa, da);
+          one(sv[2 * c + 1], dv[2 * c + 1], 32 * pass + 2 * c + 1, pb, db);
+          pk[c] = pack_bf16(pa, pb);
+          dk[c] = pack_bf16(da, db);
+        }
+        if (KQ) {
+          tmem_st16(tS + 16 * pass, pk);   // P^T over S^T
+          tmem_st16(tdP + 16 * pass, dk);  // dS^T over dP^T
+        } else {
+          tmem_st16(tS + 16 * pass, dk);   // dS over S
+        }
       }
       tmem_wait_st();
       tc_fence_before();
