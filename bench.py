@@ -34,7 +34,7 @@ METRIC = "chunk-attention TFLOP/s & chunks/s at Wan-1.3B shape; % of roofline"
 # DRAM bytes (read + write) of one attention launch of this workload, from the
 # ncu capture summarised in profiles/chunk_attn_kh_wan13b_ncu.md; None once
 # the kernel has changed since that capture.
-ATTN_DRAM_BYTES_PER_LAUNCH = 33_098_240 + 1_536
+ATTN_DRAM_BYTES_PER_LAUNCH = 33_098_496 + 7_168
 
 
 def _peaks():
