@@ -126,6 +126,23 @@ class ClockSampler:
                 "samples": len(sm), "period_ms": self.period_ms}
 
 
+def max_over_ranks(pg, values, device):
+    """Each timing maxed over the ranks (the slowest rank decides the job's
+    time); ``pg`` is torch.distributed or None for one process."""
+    if pg is None:
+        return [float(x) for x in values]
+    import torch
+
+    t = torch.tensor([float(x) for x in values], device=device, dtype=torch.float64)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_rate(units_per_rank, world, ms):
+    """Units of all ranks per second over the (max-over-ranks) time ``ms``."""
+    return units_per_rank * world / (ms / 1e3)
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -320,15 +337,11 @@ def run_ours(args):
         graph = {"value": round(args.steps * ws / (g_ms / 1e3), 3), "unit": "chunks/s",
                  "ms_per_step": round(g_ms / args.steps, 4), "kernels_per_replay": S * L + L + 1}
 
-    if pg is not None:
-        t = torch.tensor([ms, e2e_ms], device=dev, dtype=torch.float64)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms, e2e_ms = t.tolist()
+    ms, e2e_ms = max_over_ranks(pg, [ms, e2e_ms], dev)
     nkeys = Lc * (w.W + 1)
     flops_call = 4.0 * B * H * D * Lc * nkeys
     calls = S * L * args.steps
-    chunks_total = args.steps * ws
-    value = chunks_total / (ms / 1e3)
+    value = whole_job_rate(args.steps, ws, ms)
     tflops = flops_call * calls * ws / (ms / 1e3) / 1e12
     attn_avg_s = statistics.mean(attn_ms) / 1e3
     peaks, src = _peaks()
@@ -350,7 +363,7 @@ def run_ours(args):
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "traffic": ATTN_DRAM_BYTES_PER_LAUNCH,
                      "peak_source": f"bf16 dense sustained, {src}"},
-        "e2e": {"value": round(chunks_total / (e2e_ms / 1e3), 3), "unit": "chunks/s",
+        "e2e": {"value": round(whole_job_rate(args.steps, ws, e2e_ms), 3), "unit": "chunks/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "clocks": clk.summary(),
     }
