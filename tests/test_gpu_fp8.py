@@ -66,6 +66,41 @@ def test_append_fp8_bit_exact(B, H, D, Lc, R, sink, outliers):
         assert np.array_equal(K[:, :, :Lc], codes) and np.array_equal(KS[:, :, 0], scales)
 
 
+def _e4m3_tie_values():
+    """Every midpoint between adjacent positive E4M3 values, its bf16
+    neighbours on both sides, both signs, and 448 (so the block's absmax scale
+    is exactly 1 and the device rounding decides every tie and near-tie)."""
+    pos = np.unique(np.abs(OF.e4m3_decode(np.arange(0, 127, dtype=np.uint8))))
+    mids = ((pos[:-1] + pos[1:]) / 2).astype(np.float32)  # 4 significant bits: exact in bf16
+    bits = (mids.view(np.uint32) >> 16).astype(np.uint32)
+    near = np.concatenate([bits, bits + 1, bits - 1]) << 16  # bf16 neighbours (positive values)
+    vals = near.astype(np.uint32).view(np.float32)
+    vals = np.concatenate([vals, -vals, [448.0, -448.0]]).astype(np.float32)
+    assert np.max(np.abs(vals)) == 448.0
+    return vals
+
+
+def test_append_fp8_device_rounding_at_ties():
+    """The device conversion against the oracle codec on every E4M3 midpoint
+    and its bf16 neighbours (scale fixed at 1 by a 448 in the block)."""
+    vals = _e4m3_tie_values()
+    Lc, D = 128, 128
+    x = np.zeros(Lc * D, dtype=np.float32)
+    x[:len(vals)] = vals
+    x = torch.from_numpy(x.reshape(1, Lc, 1, D)).to(torch.bfloat16)
+    assert np.array_equal(x.float().numpy().reshape(-1)[:len(vals)], vals)  # all exact in bf16
+    w = synth.Workload("ties", B=1, H=1, D=D, Lc=Lc, R=2, W=1, kv_fp8=True, seed=1)
+    ring = _ring(w)
+    ring.append(0, 0, x.cuda(), (-x).cuda())
+    torch.cuda.synchronize()
+    K, V, KS, VS = (t.cpu().numpy() for t in ring.layer_views(0))
+    for got, gs, src in ((K, KS, x), (V, VS, -x)):
+        codes, scales = OF.quantize_chunk_bhld(f32(src))
+        assert scales[0, 0] == 1.0 and gs[0, 0, 0] == 1.0
+        mism = np.argwhere(got[:, :, :Lc] != codes)
+        assert mism.size == 0, f"{len(mism)} code mismatches at ties, first {mism[:3]}"
+
+
 SMALL = [
     ("fp8_small", synth.Workload("f8", B=1, H=2, D=128, Lc=200, R=3, W=2, chunks=7, sink=True, kcur_separate=False,
                                  kv_fp8=True, outliers=True, seed=51), 1),
