@@ -159,34 +159,50 @@ def streaming_chunk_attention(q_bhld, ring: ListRing, chunk: int, k_cur, v_cur, 
 
 
 def block_causal_attention(q_blhd, k_blhd, v_blhd, chunk_tokens: int, window: int, scale: float,
-                           rows=None, heads=None, batches=None):
+                           rows=None, heads=None, batches=None, restrict_keys: bool = True):
     """Block-causal attention over a whole sequence (training shape).
 
     Inputs are token-major ``[B, L, H, D]``; token t belongs to chunk
     ``t // chunk_tokens``.  ``rows`` (query token indices), ``heads`` and
     ``batches`` select which outputs to evaluate (default: all); each query
-    row is computed independently from the definition over all L keys with the
-    explicit mask.  Returns (O ``[nb, nh, nrows, D]``, LSE ``[nb, nh, nrows]``).
+    row is computed independently from the definition with the explicit mask.
+    Returns (O ``[nb, nh, nrows, D]``, LSE ``[nb, nh, nrows]``).
+
+    The selected rows are taken one query chunk qc at a time.  With
+    ``restrict_keys`` the candidate keys of that group are the tokens of
+    chunks max(0, qc - W) .. qc: every other key is masked for every row of
+    the group, so its term of the definition is an exact zero and leaving it
+    out changes no sum (only the order in which zeros would be added).  The
+    explicit mask is still applied to the candidates.  ``restrict_keys=False``
+    scores every row against all L keys.
     """
     q = np.asarray(q_blhd)
     k = np.asarray(k_blhd)
     v = np.asarray(v_blhd)
     B, L, H, _ = q.shape
+    Lc = int(chunk_tokens)
     rows = np.arange(L) if rows is None else np.asarray(rows, dtype=np.int64)
     heads = range(H) if heads is None else list(heads)
     batches = range(B) if batches is None else list(batches)
-    key_chunk = np.arange(L) // int(chunk_tokens)
+    key_chunk = np.arange(L) // Lc
     O = np.empty((len(batches), len(heads), len(rows), v.shape[3]), dtype=np.float64)
     LSE = np.empty((len(batches), len(heads), len(rows)), dtype=np.float64)
-    step = 2048  # rows evaluated per batch of independent rows (memory bound only)
+    q_chunk = rows // Lc
+    groups = []  # (positions in `rows`, candidate key slice)
+    for qc in np.unique(q_chunk):
+        pos = np.nonzero(q_chunk == qc)[0]
+        kr = slice(max(0, int(qc) - int(window)) * Lc, min(L, (int(qc) + 1) * Lc)) if restrict_keys else slice(0, L)
+        step = 2048  # rows per matmul (memory bound only)
+        for p0 in range(0, len(pos), step):
+            groups.append((pos[p0:p0 + step], kr))
     for bi, b in enumerate(batches):
         for hi, h in enumerate(heads):
             kk = np.asarray(k[b, :, h, :], dtype=np.float64)
             vv = np.asarray(v[b, :, h, :], dtype=np.float64)
-            for r0 in range(0, len(rows), step):
-                rr = rows[r0:r0 + step]
-                mask = chunk_visibility(rr // int(chunk_tokens), key_chunk, window)
-                o, lse = masked_attention(np.asarray(q[b, rr, h, :], dtype=np.float64), kk, vv, mask, scale)
-                O[bi, hi, r0:r0 + len(rr)] = o
-                LSE[bi, hi, r0:r0 + len(rr)] = lse
+            for pos, kr in groups:
+                rr = rows[pos]
+                mask = chunk_visibility(rr // Lc, key_chunk[kr], window)
+                o, lse = masked_attention(np.asarray(q[b, rr, h, :], dtype=np.float64), kk[kr], vv[kr], mask, scale)
+                O[bi, hi, pos] = o
+                LSE[bi, hi, pos] = lse
     return O, LSE

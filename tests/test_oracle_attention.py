@@ -286,3 +286,23 @@ def test_block_causal_row_subset_and_streaming_agree():
         np.testing.assert_allclose(o, o_all[:, :, sl], atol=1e-12)
         np.testing.assert_allclose(l, l_all[:, :, sl], atol=1e-12)
         ring.append(c, kb[:, :, sl], vb[:, :, sl])
+
+
+def test_block_causal_restricted_keys_equal_full_mask():
+    """Leaving out the keys that no selected row can see (restrict_keys)
+    gives the full-mask result: the left-out terms are exact zeros."""
+    rng = np.random.default_rng(32)
+    B, nch, Lc, H, D, W = 2, 7, 5, 2, 8, 2
+    q, k, v = (rng.normal(size=(B, nch * Lc, H, D)) for _ in range(3))
+    rows = np.array([0, 3, 7, 11, 12, 18, 24, 30, 34, 2, 33])  # unsorted, several per chunk
+    o_r, l_r = A.block_causal_attention(q, k, v, Lc, W, 0.45, rows=rows)
+    o_f, l_f = A.block_causal_attention(q, k, v, Lc, W, 0.45, rows=rows, restrict_keys=False)
+    np.testing.assert_allclose(o_r, o_f, atol=1e-13)
+    np.testing.assert_allclose(l_r, l_f, atol=1e-13)
+    # and each row against the scalar-loop brute force over all keys
+    mask_all = A.chunk_visibility(rows // Lc, np.arange(nch * Lc) // Lc, W)
+    for b in range(B):
+        for h in range(H):
+            ob, lb = _brute(q[b, rows, h], k[b, :, h], v[b, :, h], mask_all, 0.45)
+            np.testing.assert_allclose(o_r[b, h], ob, atol=1e-12)
+            np.testing.assert_allclose(l_r[b, h], lb, atol=1e-12)
