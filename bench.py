@@ -31,10 +31,12 @@ sys.path.insert(0, ROOT)
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 METRIC = "chunk-attention TFLOP/s & chunks/s at Wan-1.3B shape; % of roofline"
-# DRAM bytes (read + write) of one attention launch of this workload, from the
-# ncu capture summarised in profiles/chunk_attn_kh_wan13b_ncu.md; None once
-# the kernel has changed since that capture.
+# DRAM bytes (read + write) of one attention launch of this workload, from an
+# ncu capture of the same kernel build (dram__bytes_read.sum +
+# dram__bytes_write.sum, small case of one layer); None once the kernel has
+# changed since that capture.
 ATTN_DRAM_BYTES_PER_LAUNCH = 33_098_496 + 7_168
+ATTN_DRAM_BYTES_SOURCE = "ncu --set full capture of chunk_attn_kh_kernel<128,0,0>, one Wan-1.3B call"
 
 
 def _peaks():
@@ -345,11 +347,27 @@ def run_ours(args):
     tflops = flops_call * calls * ws / (ms / 1e3) / 1e12
     attn_avg_s = statistics.mean(attn_ms) / 1e3
     peaks, src = _peaks()
-    peak = peaks["bf16_tflops_sustained"]
+    # the kernel is timed in groups of 30 back-to-back launches (about 1 ms),
+    # not in a seconds-long loop: the burst peak is its denominator
+    peak = peaks["bf16_tflops"]
     achieved = flops_call / attn_avg_s / 1e12
+    configs = None
+    if rank == 0 and not args.no_configs:
+        configs = config_records(peaks, src, stream)
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        cpu = cpu_baseline_sample(w, seconds_budget=args.cpu_seconds)
+        base = oracle_baselines()
+        calls_per_chunk = S * L
+        hb = base.pop("wan13b")
+        cpu = {"value": round(hb["value"] / calls_per_chunk, 6), "unit": "chunks/s", "cores": hb["cores"],
+               "kind": "oracle", "sample": hb["sample"] + f"; x{calls_per_chunk} calls per chunk",
+               "single_thread": {"value": round(hb["single_thread"]["value"] / calls_per_chunk, 6),
+                                 "unit": "chunks/s", "cores": 1,
+                                 "sample": hb["single_thread"]["sample"] + f"; x{calls_per_chunk} calls per chunk"}}
+        if configs is not None:
+            for name, b in base.items():
+                if name in configs:
+                    configs[name]["cpu_baseline"] = b
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "chunks/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True,
@@ -362,7 +380,8 @@ def run_ours(args):
         "gpu_launches": gpu_launches,
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "traffic": ATTN_DRAM_BYTES_PER_LAUNCH,
-                     "peak_source": f"bf16 dense sustained, {src}"},
+                     "traffic_source": ATTN_DRAM_BYTES_SOURCE,
+                     "peak_source": f"bf16 dense burst, {src}"},
         "e2e": {"value": round(whole_job_rate(args.steps, ws, e2e_ms), 3), "unit": "chunks/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "clocks": clk.summary(),
@@ -371,10 +390,200 @@ def run_ours(args):
         line["graph_replay"] = graph
     if cpu is not None:
         line["cpu_baseline"] = cpu
+    if configs is not None:
+        line["configs"] = configs
     if rank == 0:
         print(json.dumps(line), flush=True)
     if pg is not None:
         pg.destroy_process_group()
+
+
+# ------------------------------------------------------ per-config records
+# Every workload besides the headline one, timed the way the headline is:
+# CUDA events around groups of back-to-back calls on the launching stream
+# (median over groups), the library's own launch choice (num_splits = 0).
+# Streaming workloads rotate over enough layers that one call's inputs and
+# ring rows are out of L2 when its turn comes again; the full-sequence
+# workloads move more than 4x L2 per call.
+
+def _group_us(calls, per_group, groups, stream):
+    import torch
+
+    n = len(calls)
+    i = 0
+    for _ in range(3 * per_group):  # warm-up
+        calls[i % n]()
+        i += 1
+    res = []
+    for _ in range(groups):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(per_group):
+            calls[i % n]()
+            i += 1
+        b.record(stream)
+        res.append((a, b))
+    torch.cuda.synchronize()
+    return statistics.median(x.elapsed_time(y) * 1e3 / per_group for x, y in res)
+
+
+def _stream_setup(name, layers, sab, synth, torch):
+    """A ring of ``layers`` layers filled up to the first chunk whose window
+    is full, the queries (and current K/V) of that chunk per layer."""
+    w = synth.workload(name)
+    kv = (sab.KV_INT8K_FP8V if w.kv_int8k else sab.KV_FP8_E4M3) if w.kv_fp8 else sab.KV_BF16
+    ring = sab.KVRing(layers, w.B, w.H, w.D, w.Lc, w.R, has_sink=w.sink, kv_dtype=kv)
+    g = synth.generator(w.seed + 17, device="cuda")
+    if w.sink:
+        for l in range(layers):
+            ring.set_sink(l, *synth.sink_kv(w, g, "cuda"))
+    steady = w.R - 1 if not w.kcur_separate else w.W
+    cur = [None] * layers
+    for c in range(steady + 1):
+        for l in range(layers):
+            q, k, v = synth.chunk_qkv(w, g, "cuda")
+            if not w.kcur_separate or c < steady:
+                ring.append(l, c, k, v)
+            cur[l] = (q, k, v)
+    return w, ring, steady, cur
+
+
+def config_records(peaks, src, stream):
+    import torch
+
+    import streaming_attention_block_gb300 as sab
+    from streaming_attention_block_gb300 import synth
+
+    bf16_peak = peaks["bf16_tflops"]
+    out = {}
+
+    def rec(name, workload, us, flops, extra=None, peak=None, peak_note=None):
+        tf = flops / (us * 1e-6) / 1e12
+        pk = bf16_peak if peak is None else peak
+        r = {"workload": workload, "us_per_call": round(us, 2), "calls_per_s": round(1e6 / us, 1),
+             "tflops": round(tf, 1), "gflop_per_call": round(flops / 1e9, 3),
+             "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": pk, "unit": "TFLOP/s",
+                          "frac": round(tf / pk, 4),
+                          "peak_source": peak_note or f"bf16 dense burst, {src}"}}
+        if extra:
+            r.update(extra)
+        out[name] = r
+
+    # streaming workloads: tiny (launch-bound), the long window with sink in
+    # bf16, E4M3 and INT8-key caches, and the E4M3-product variant
+    for name, layers in (("tiny", 1), ("long_sink", 4), ("fp8_kv", 8), ("int8k_kv", 8)):
+        w, ring, c, cur = _stream_setup(name, layers, sab, synth, torch)
+        nkeys = w.Lc * (w.W + 1) + (w.Lc if w.sink else 0)
+        flops = 4.0 * w.B * w.H * w.D * w.Lc * nkeys
+        O = [torch.empty_like(cur[l][0]) for l in range(layers)]
+        L = [torch.empty((w.B, w.H, w.Lc), dtype=torch.float32, device="cuda") for _ in range(layers)]
+        ws = ring.workspace(0)
+
+        def make(l, splits, work):
+            q, k, v = cur[l]
+            kc, vc = (k, v) if w.kcur_separate else (None, None)
+            return lambda: sab.chunk_attention(ring.handle, l, c, q, kc, vc, w.W, w.sink, splits, w.scale, O[l],
+                                               L[l], work, stream)
+
+        us = _group_us([make(l, 0, ws) for l in range(layers)], 20, 8, stream)
+        desc = (f"B{w.B} H{w.H} D{w.D}, {w.Lc} tokens/chunk, {'sink + ' if w.sink else ''}ring {w.R} slots, "
+                f"window current+{w.W} ({nkeys} keys)"
+                + (", E4M3 K/V cache" if w.kv_fp8 and not w.kv_int8k else "")
+                + (", INT8 K / E4M3 V cache" if w.kv_int8k else "")
+                + f"; {layers} layer(s) rotated")
+        extra = {"keys": nkeys, "splits": "library choice (0)"}
+        if w.splits > 1:  # the split count the workload names, merged by LSE in-kernel
+            ws8 = ring.workspace(w.splits)
+            extra[f"us_per_call_splits{w.splits}"] = round(
+                _group_us([make(l, w.splits, ws8) for l in range(layers)], 20, 8, stream), 2)
+        rec(name, desc, us, flops, extra)
+        if name == "fp8_kv":
+            def make8(l):
+                q = cur[l][0]
+                return lambda: sab.chunk_attention_fp8mma(ring.handle, l, c, q, w.W, w.sink, w.scale, O[l], L[l],
+                                                          stream)
+
+            us8 = _group_us([make8(l) for l in range(layers)], 20, 8, stream)
+            rec("fp8_kv_e4m3_mma", desc + "; Q and P rounded to E4M3, kind::f8f6f4 products", us8, flops,
+                {"keys": nkeys}, peak=2 * bf16_peak,
+                peak_note=f"fp8 dense = 2 x bf16 dense burst (nominal ratio), {src}")
+        del ring, cur, O, L
+        torch.cuda.empty_cache()
+
+    # block-causal full sequence (training shape) and its gradients
+    w = synth.workload("block_causal")
+    g = synth.generator(w.seed, device="cuda")
+    q, k, v = synth.full_sequence_qkv(w, g, "cuda")
+    Lt = w.seq_chunks * w.Lc
+    O = torch.empty_like(q)
+    L = torch.empty((w.B, w.H, Lt), dtype=torch.float32, device="cuda")
+    flops = 4.0 * w.D * _visible_pairs_block_causal(w)
+    us = _group_us([lambda: sab.block_causal_attention(q, k, v, w.Lc, w.W, 0, w.scale, O, L, None, stream)], 3, 5,
+                   stream)
+    desc = f"B{w.B} x {Lt} tokens ({w.seq_chunks} chunks of {w.Lc}), H{w.H} D{w.D}, window {w.W}"
+    rec("block_causal", desc, us, flops, {"tokens": Lt})
+    do = synth.randn_bf16(g, tuple(q.shape), "cuda")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    bws = torch.empty(sab.block_causal_attention_backward_workspace(w.B, Lt, w.H), dtype=torch.uint8, device="cuda")
+    us = _group_us([lambda: sab.block_causal_attention_backward(q, k, v, O, do, L, w.Lc, w.W, w.scale, dq, dk, dv,
+                                                                bws, stream)], 2, 5, stream)
+    rec("block_causal_backward", desc + "; dQ, dK, dV (algorithmic 10 D flops per visible pair)", us, 2.5 * flops,
+        {"tokens": Lt})
+    del q, k, v, O, L, do, dq, dk, dv, bws
+    torch.cuda.empty_cache()
+
+    # memory prefix (compressed-memory training shape), forward and gradients
+    w = synth.workload("memory_prefix")
+    q, k, v = synth.full_sequence_qkv(w, g, "cuda")
+    Lt = q.shape[1]
+    ml = torch.tensor(w.mem_lens, dtype=torch.int32, device="cuda")
+    O = torch.empty_like(q)
+    L = torch.empty((w.B, w.H, Lt), dtype=torch.float32, device="cuda")
+    pairs = sum(P * P + sum(w.Lc * (P + w.Lc * (min(c, w.W) + 1)) for c in range(w.seq_chunks)) for P in w.mem_lens)
+    flops = 4.0 * w.H * w.D * pairs
+    desc = (f"B{w.B} x {Lt} tokens: memory of {w.mem_pad} positions ({w.mem_lens} real) + {w.seq_chunks} chunks of "
+            f"{w.Lc}, H{w.H} D{w.D}, window {w.W}")
+    us = _group_us([lambda: sab.memory_prefix_attention(q, k, v, w.mem_pad, ml, w.Lc, w.W, w.scale, O, L, stream)],
+                   5, 5, stream)
+    rec("memory_prefix", desc, us, flops, {"tokens": Lt})
+    do = synth.randn_bf16(g, tuple(q.shape), "cuda")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    bws = torch.empty(sab.block_causal_attention_backward_workspace(w.B, Lt, w.H), dtype=torch.uint8, device="cuda")
+    us = _group_us([lambda: sab.memory_prefix_attention_backward(q, k, v, O, do, L, w.mem_pad, ml, w.Lc, w.W, w.scale,
+                                                                 dq, dk, dv, bws, stream)], 3, 5, stream)
+    rec("memory_prefix_backward", desc + "; gradients", us, 2.5 * flops, {"tokens": Lt})
+    del q, k, v, O, L, do, dq, dk, dv, bws
+    torch.cuda.empty_cache()
+
+    # fused Q/K RMSNorm + rotary embedding + BF16 ring append (HBM-bound)
+    w = synth.workload("wan13b")
+    shape = (w.B, w.Lc, w.H, w.D)
+    nsets = 16  # 16 x 18.9 MB of inputs rotate: every call reads from HBM
+    sets = [tuple(synth.randn_bf16(g, shape, "cuda") for _ in range(3)) for _ in range(nsets)]
+    qouts = [torch.empty(shape, dtype=torch.bfloat16, device="cuda") for _ in range(nsets)]
+    ring = sab.KVRing(1, w.B, w.H, w.D, w.Lc, w.R)
+    rope = sab.RopeDesc(2, 24, 32, 44, 42, 42, 10000.0, 1e-6)
+    state = {"c": 0}
+
+    def producer(i):
+        def f():
+            q_, k_, v_ = sets[i]
+            sab.qk_norm_rope(ring.handle, 0, state["c"], q_, k_, v_, rope, qouts[i], append=True, stream=stream)
+            state["c"] += 1
+        return f
+
+    us = _group_us([producer(i) for i in range(nsets)], 32, 5, stream)
+    nbytes = 6 * w.B * w.Lc * w.H * w.D * 2  # read q, k, v; write q', ring k', ring v
+    gbs = nbytes / (us * 1e-6) / 1e9
+    out["qk_norm_rope_append"] = {
+        "workload": "one Wan-1.3B chunk (B1 H12 D128, 1536 tokens, latent grid 2x24x32, rotary bands 44/42/42), "
+                    "fused append into a BF16 ring", "us_per_call": round(us, 2),
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(gbs / peaks["hbm_gbs"], 4), "peak_source": f"hbm copy, {src}"},
+        "bytes_per_call": nbytes}
+    assert sab.get_last_device_error(stream) == 0
+    return out
 
 
 def run_attn_only(args):
@@ -489,203 +698,196 @@ def run_attn_only_fp8mma(args):
 
 
 def run_sweep(args):
-    """One JSON line per workload: device time per attention call (median
-    of CUDA-event-timed back-to-back calls after warm-up), algorithmic
-    TFLOP/s and the fraction of the bf16 peak.  Not the default bench line."""
+    """One JSON line per workload (the per-config records of the bench line,
+    without the oracle timings)."""
     import torch
 
-    import streaming_attention_block_gb300 as sab
-    from streaming_attention_block_gb300 import synth
-
     peaks, src = _peaks()
-    stream = torch.cuda.current_stream()
-
-    def timed(fn, n):
-        for _ in range(3):
-            fn()
-        ev = []
-        for _ in range(n):
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            fn()
-            b.record(stream)
-            ev.append((a, b))
-        torch.cuda.synchronize()
-        return statistics.median(x.elapsed_time(y) for x, y in ev) * 1e3
-
-    def report(name, us, flops, splits, extra=None):
-        line = {"sweep": name, "us_per_call": round(us, 2), "tflops": round(flops / (us * 1e-6) / 1e12, 1),
-                "frac_of_bf16_peak": round(flops / (us * 1e-6) / 1e12 / peaks["bf16_tflops"], 4),
-                "peak_source": f"bf16 dense burst, {src}", "splits": splits}
-        if extra:
-            line.update(extra)
-        print(json.dumps(line), flush=True)
-
-    for name in ("tiny", "wan13b", "long_sink", "fp8_kv", "int8k_kv"):
-        w = synth.workload(name)
-        g = synth.generator(w.seed, device="cuda")
-        ring = sab.KVRing(1, w.B, w.H, w.D, w.Lc, w.R, has_sink=w.sink,
-                          kv_dtype=(sab.KV_INT8K_FP8V if w.kv_int8k else sab.KV_FP8_E4M3) if w.kv_fp8 else sab.KV_BF16)
-        if w.sink:
-            sk, sv = synth.sink_kv(w, g, "cuda")
-            ring.set_sink(0, sk, sv)
-        steady = w.R if not w.kcur_separate else w.W  # first chunk with a full window
-        q = k = v = None
-        for c in range(steady + 1):
-            q, k, v = synth.chunk_qkv(w, g, "cuda")
-            if not w.kcur_separate or c < steady:
-                ring.append(0, c, k, v)
-        nkeys = w.Lc * (w.W + 1) + (w.Lc if w.sink else 0)
-        flops = 4.0 * w.B * w.H * w.D * w.Lc * nkeys
-        for splits in sorted({0, 1, w.splits}):
-            work = ring.workspace(splits) if splits != 1 else None
-            O = torch.empty_like(q)
-            L = torch.empty((w.B, w.H, w.Lc), dtype=torch.float32, device="cuda")
-            kc, vc = (k, v) if w.kcur_separate else (None, None)
-
-            def call():
-                sab.chunk_attention(ring.handle, 0, steady, q, kc, vc, w.W, w.sink, splits, w.scale, O, L, work,
-                                    stream)
-
-            report(name, timed(call, 50), flops, splits, {"keys": nkeys})
-        if w.kv_fp8 and not w.kv_int8k:
-            # E4M3 tensor-core products (Q and P rounded to E4M3): the peak is
-            # the bf16 one x 2, the nominal fp8 / bf16 dense ratio
-            O = torch.empty_like(q)
-            L = torch.empty((w.B, w.H, w.Lc), dtype=torch.float32, device="cuda")
-
-            def call_f8():
-                sab.chunk_attention_fp8mma(ring.handle, 0, steady, q, w.W, w.sink, w.scale, O, L, stream)
-
-            us = timed(call_f8, 50)
-            tf = flops / (us * 1e-6) / 1e12
-            print(json.dumps({"sweep": name + "_e4m3_mma", "us_per_call": round(us, 2), "tflops": round(tf, 1),
-                              "frac_of_fp8_peak": round(tf / (2 * peaks["bf16_tflops"]), 4),
-                              "peak_source": f"2 x bf16 dense burst, {src}", "splits": 1, "keys": nkeys}),
-                  flush=True)
-    # fused Q/K RMSNorm + rotary embedding + BF16 ring append at the Wan-1.3B
-    # chunk shape (latent grid 2 x 24 x 32, rotary bands 44/42/42); 16 input
-    # sets rotate so that every call reads from HBM (16 x 18.9 MB > L2)
-    w = synth.workload("wan13b")
-    g = synth.generator(w.seed, device="cuda")
-    shape = (w.B, w.Lc, w.H, w.D)
-    nsets = 16
-    sets = [tuple(synth.randn_bf16(g, shape, "cuda") for _ in range(3)) for _ in range(nsets)]
-    qouts = [torch.empty(shape, dtype=torch.bfloat16, device="cuda") for _ in range(nsets)]
-    ring = sab.KVRing(1, w.B, w.H, w.D, w.Lc, w.R)
-    rope = sab.RopeDesc(2, 24, 32, 44, 42, 42, 10000.0, 1e-6)
-    state = {"i": 0, "c": 0}
-
-    def producer():
-        i = state["i"] % nsets
-        q, k, v = sets[i]
-        sab.qk_norm_rope(ring.handle, 0, state["c"], q, k, v, rope, qouts[i], append=True, stream=stream)
-        state["i"] += 1
-        state["c"] += 1
-
-    for _ in range(8):
-        producer()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(64):  # back to back, like the attention calls of a denoise step
-        producer()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    us = e0.elapsed_time(e1) * 1e3 / 64
-    nbytes = 6 * w.B * w.Lc * w.H * w.D * 2  # read q, k, v; write q', ring k', ring v
-    gbs = nbytes / (us * 1e-6) / 1e9
-    print(json.dumps({"sweep": "qk_norm_rope_append", "us_per_call": round(us, 2), "GB_per_s": round(gbs, 1),
-                      "frac_of_hbm_peak": round(gbs / peaks["hbm_gbs"], 4), "peak_source": f"hbm copy, {src}",
-                      "bytes_per_call": nbytes}), flush=True)
-
-    w = synth.workload("block_causal")
-    g = synth.generator(w.seed, device="cuda")
-    q, k, v = synth.full_sequence_qkv(w, g, "cuda")
-    Lt = w.seq_chunks * w.Lc
-    O = torch.empty_like(q)
-    L = torch.empty((w.B, w.H, Lt), dtype=torch.float32, device="cuda")
-    pairs = sum(w.Lc * w.Lc * (min(c, w.W) + 1) for c in range(w.seq_chunks))
-    flops = 4.0 * w.B * w.H * w.D * pairs
-
-    def bc():
-        sab.block_causal_attention(q, k, v, w.Lc, w.W, 0, w.scale, O, L, None, stream)
-
-    report("block_causal", timed(bc, 10), flops, 0, {"tokens": Lt})
-    # backward of the same shape: algorithmic 10 D flops per visible pair
-    # (S recompute, dP, dV, dK, dQ); the kernels recompute S and dP once more
-    do = synth.randn_bf16(g, tuple(q.shape), "cuda")
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    bws = torch.empty(sab.block_causal_attention_backward_workspace(w.B, Lt, w.H), dtype=torch.uint8, device="cuda")
-
-    def bwd():
-        sab.block_causal_attention_backward(q, k, v, O, do, L, w.Lc, w.W, w.scale, dq, dk, dv, bws, stream)
-
-    report("block_causal_backward", timed(bwd, 10), 2.5 * flops, 0, {"tokens": Lt})
-    del q, k, v, O, L, do, dq, dk, dv
-    # memory prefix (compressed-memory training shape): visible pairs counted
-    # per sample -- real memory x real memory, and each target chunk against
-    # the real memory plus its window of target chunks
-    w = synth.workload("memory_prefix")
-    q, k, v = synth.full_sequence_qkv(w, g, "cuda")
-    Lt = q.shape[1]
-    ml = torch.tensor(w.mem_lens, dtype=torch.int32, device="cuda")
-    O = torch.empty_like(q)
-    L = torch.empty((w.B, w.H, Lt), dtype=torch.float32, device="cuda")
-    pairs = sum(P * P + sum(w.Lc * (P + w.Lc * (min(c, w.W) + 1)) for c in range(w.seq_chunks))
-                for P in w.mem_lens)
-    flops = 4.0 * w.H * w.D * pairs
-
-    def mp():
-        sab.memory_prefix_attention(q, k, v, w.mem_pad, ml, w.Lc, w.W, w.scale, O, L, stream)
-
-    report("memory_prefix", timed(mp, 10), flops, 1, {"tokens": Lt, "mem_pad": w.mem_pad})
-    do = synth.randn_bf16(g, tuple(q.shape), "cuda")
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    bws = torch.empty(sab.block_causal_attention_backward_workspace(w.B, Lt, w.H), dtype=torch.uint8, device="cuda")
-
-    def mpb():
-        sab.memory_prefix_attention_backward(q, k, v, O, do, L, w.mem_pad, ml, w.Lc, w.W, w.scale, dq, dk, dv, bws,
-                                             stream)
-
-    report("memory_prefix_backward", timed(mpb, 10), 2.5 * flops, 0, {"tokens": Lt, "mem_pad": w.mem_pad})
-    assert sab.get_last_device_error(stream) == 0
+    for name, r in config_records(peaks, src, torch.cuda.current_stream()).items():
+        print(json.dumps(dict(sweep=name, **r)), flush=True)
 
 
-def cpu_baseline_sample(w, seconds_budget=20.0):
-    """Time the oracle on one steady-state attention call (all heads, all rows,
-    4608 keys) on the host cores; scale to chunks/s."""
-    import numpy as np
-
-    from oracle import attention as OA
-    from oracle.ring import ListRing
-    from streaming_attention_block_gb300 import synth
-
-    gen = synth.generator(w.seed)
-    ring = ListRing(w.R)
-    qs = None
-    t_calls = []
-    for c in range(3):
-        q, k, v = synth.chunk_qkv(w, gen)
-        qb, kb, vb = (np.transpose(x.float().numpy().astype(np.float64), (0, 2, 1, 3)) for x in (q, k, v))
-        if c == 2:
-            t = time.perf_counter()
-            OA.streaming_chunk_attention(qb, ring, c, kb, vb, w.W, False, w.scale)
-            t_calls.append(time.perf_counter() - t)
-        ring.append(c, kb, vb)
-    t_call = statistics.mean(t_calls)
-    per_chunk = t_call * w.steps * w.layers
-    return {"value": round(1.0 / per_chunk, 6), "unit": "chunks/s", "cores": _cpu_threads(), "kind": "oracle",
-            "sample": f"1 oracle call (chunk 2: 12 heads x 1536 queries x 4608 keys, fp64) took {t_call:.2f} s; "
-                      f"scaled x{w.steps * w.layers} calls per chunk"}
-
+# ------------------------------------------------------------------ oracle
+# The CPU baseline: the oracle as it stands, timed on the host cores on a
+# bounded sample of each workload (query rows are independent, so a subset of
+# rows scaled by the visible query-key pairs of a full call gives its time).
+# Run in child processes so that the BLAS thread count can be fixed before
+# numpy loads: once with every core the process may use, once with 1 thread.
 
 def _cpu_threads():
     try:
         return len(os.sched_getaffinity(0))
     except Exception:
         return os.cpu_count()
+
+
+def _visible_pairs_block_causal(w):
+    return w.B * w.H * sum(w.Lc * w.Lc * (min(c, w.W) + 1) for c in range(w.seq_chunks))
+
+
+def _timed_rows(fn, n_rows, frac):
+    """Seconds of one full oracle call whose cost grows with the query rows.
+    ``fn(r)`` runs the call on the first r rows.  frac >= 1: the full call is
+    timed.  Otherwise r = frac * n_rows and 2r rows are timed and the full
+    call is extrapolated linearly (fixed cost per call + cost per row)."""
+    if frac >= 1.0:
+        t = time.perf_counter()
+        fn(n_rows)
+        return time.perf_counter() - t, f"all {n_rows} query rows"
+    r = max(4, int(n_rows * frac))
+    t = time.perf_counter()
+    fn(r)
+    t1 = time.perf_counter() - t
+    t = time.perf_counter()
+    fn(2 * r)
+    t2 = time.perf_counter() - t
+    slope = max(0.0, (t2 - t1) / r)
+    fixed = max(0.0, t1 - slope * r)
+    return fixed + slope * n_rows, f"{r} and {2 * r} of {n_rows} query rows, extrapolated linearly"
+
+
+def oracle_samples(frac):
+    """Seconds per full call of every workload's oracle ({name: {"seconds",
+    "sample"}}); ``frac`` < 1 samples that fraction of the query rows."""
+    import numpy as np
+
+    from oracle import attention as OA
+    from oracle import backward as OB
+    from oracle import fp8 as OF
+    from oracle import fp8mma as OM
+    from oracle import int8 as OI
+    from oracle.ring import ListRing
+    from streaming_attention_block_gb300 import synth
+
+    def bhld(t):
+        return np.ascontiguousarray(np.transpose(t.float().numpy().astype(np.float64), (0, 2, 1, 3)))
+
+    def deq(t, int8=False):
+        x = t.float().numpy()
+        if int8:
+            c, sc = OI.quantize_chunk_bhld(x)
+            return c.astype(np.float64) * sc.astype(np.float64)[:, :, None, None], sc
+        c, sc = OF.quantize_chunk_bhld(x)
+        return OF.e4m3_decode(c) * sc.astype(np.float64)[:, :, None, None], sc
+
+    out = {}
+    # Wan-1.3B streaming call at chunk 2 (4608 keys: 2 cached chunks + the current one)
+    w = synth.workload("wan13b")
+    gen = synth.generator(w.seed)
+    ring = ListRing(w.R)
+    for c in range(2):
+        _, k, v = synth.chunk_qkv(w, gen)
+        ring.append(c, bhld(k), bhld(v))
+    q, k, v = (bhld(x) for x in synth.chunk_qkv(w, gen))
+    sec, how = _timed_rows(lambda r: OA.streaming_chunk_attention(q[:, :, :r], ring, 2, k, v, w.W, False, w.scale),
+                           w.Lc, frac)
+    out["wan13b"] = {"seconds": sec, "sample": f"one call at chunk 2 (12 heads x 4608 keys): {how}"}
+    # tiny: the whole 6-chunk stream
+    w = synth.workload("tiny")
+    gen = synth.generator(w.seed)
+    ring = ListRing(w.R)
+    el = 0.0
+    for c in range(w.chunks):
+        q, k, v = (bhld(x) for x in synth.chunk_qkv(w, gen))
+        t = time.perf_counter()
+        OA.streaming_chunk_attention(q, ring, c, k, v, w.W, False, w.scale)
+        el += time.perf_counter() - t
+        ring.append(c, k, v)
+    out["tiny"] = {"seconds": el / w.chunks, "sample": "the whole 6-chunk stream, averaged per call"}
+    # long window with sink (bf16, E4M3 and INT8-key caches): the first chunk with a full window
+    for name in ("long_sink", "fp8_kv", "int8k_kv"):
+        w = synth.workload(name)
+        gen = synth.generator(w.seed)
+        ring = ListRing(w.R)
+        vsc = {}
+        sk, sv = synth.sink_kv(w, gen)
+        if w.kv_fp8:
+            (ksd, _), (svd, vss) = deq(sk, w.kv_int8k), deq(sv)
+            ring.set_sink(ksd, svd)
+            vsc[OA.SINK_CHUNK] = vss
+        else:
+            ring.set_sink(bhld(sk), bhld(sv))
+        for c in range(w.R):
+            q, k, v = synth.chunk_qkv(w, gen)
+            if w.kv_fp8:
+                (kd, _), (vd, vss) = deq(k, w.kv_int8k), deq(v)
+                ring.append(c, kd, vd)
+                vsc[c] = vss
+            else:
+                ring.append(c, bhld(k), bhld(v))
+        qb = bhld(q)
+        c = w.R - 1
+        sec, how = _timed_rows(lambda r: OA.streaming_chunk_attention(qb[:, :, :r], ring, c, None, None, w.W, True,
+                                                                      w.scale), w.Lc, frac)
+        out[name] = {"seconds": sec, "sample": f"one call at chunk {c} ({w.H} heads x 8505 keys"
+                                               + (", dequantised cache" if w.kv_fp8 else "") + f"): {how}"}
+        if name == "fp8_kv":  # E4M3 products: the oracle of that variant on the same cache
+            K, V, kid, ksink = OA.streaming_key_set(ring, c, None, None, w.W, True)
+            vs_keys = [np.array([vsc[int(i)][b, h] for i in kid], dtype=np.float64)
+                       for b in range(w.B) for h in range(w.H)]
+
+            def f8(r):
+                mask = OA.chunk_visibility(np.full(r, c), kid, w.W, ksink)
+                for b in range(w.B):
+                    for h in range(w.H):
+                        OM.head_attention(qb[b, h, :r].astype(np.float32), K[b, h], V[b, h], mask, w.scale,
+                                          vs_keys[b * w.H + h])
+
+            sec, how = _timed_rows(f8, w.Lc, frac)
+            out["fp8_kv_e4m3_mma"] = {"seconds": sec, "sample": f"one call at chunk {c} (24 heads x 8505 keys, "
+                                                                f"with the rounding bound): {how}"}
+    # block-causal full sequence: the third chunk of a 3-chunk sequence has
+    # the steady-state key set (4608 keys); scaled by visible pairs
+    w = synth.workload("block_causal")
+    w3 = synth.workload("block_causal", B=1, seq_chunks=3)
+    q, k, v = synth.full_sequence_qkv(w3, synth.generator(w.seed))
+    qf, kf, vf = (x.float().numpy() for x in (q, k, v))
+    rows = np.arange(2 * w.Lc, 3 * w.Lc)
+    sec, how = _timed_rows(lambda r: OA.block_causal_attention(qf, kf, vf, w.Lc, w.W, w.scale, rows=rows[:r]),
+                           w.Lc, frac)
+    pairs = w.H * w.Lc * 3 * w.Lc
+    out["block_causal"] = {"seconds": sec * _visible_pairs_block_causal(w) / pairs,
+                           "sample": f"the 1536 rows of one steady-state chunk x 12 heads x 4608 keys ({how}), "
+                                     f"scaled by visible pairs to B2 x 30720 tokens"}
+    # gradients: one head of a 3-chunk sequence, chunk by chunk over the keys
+    # each chunk sees; scaled by visible pairs
+    do = synth.randn_bf16(synth.generator(w.seed + 1), tuple(q.shape)).float().numpy()
+    n_tok = 3 * w.Lc
+    t = time.perf_counter()
+    OB.block_causal_attention_backward_rows(qf, kf, vf, do, w.Lc, w.W, w.scale, 0, 0, np.arange(n_tok),
+                                            np.arange(n_tok))
+    el = time.perf_counter() - t
+    pairs = w.Lc * w.Lc * (1 + 2 + 3)
+    out["block_causal_backward"] = {"seconds": el * _visible_pairs_block_causal(w) / pairs,
+                                    "sample": f"dQ, dK, dV of every row of one head of a {n_tok}-token sequence, "
+                                              f"scaled by visible pairs to B2 x 30720 tokens x 12 heads"}
+    return out
+
+
+def oracle_baselines(seconds_budget_hint=None):
+    """All-core and single-thread oracle timings ({name: cpu_baseline dict}),
+    each from a child process with its BLAS thread count fixed."""
+    res = {}
+    ncores = _cpu_threads()
+    runs = []
+    for threads, frac in ((ncores, 1.0), (1, 0.125)):
+        env = dict(os.environ)
+        for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+            env[var] = str(threads)
+        env["CUDA_VISIBLE_DEVICES"] = ""
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-samples", str(frac)], env=env,
+                           capture_output=True, text=True, timeout=900)
+        if r.returncode != 0:
+            raise RuntimeError(f"oracle sample run failed:\n{r.stderr[-2000:]}")
+        runs.append((threads, json.loads(r.stdout.strip().splitlines()[-1])))
+    (nc, full), (_, single) = runs
+    for name, d in full.items():
+        one = single[name]
+        res[name] = {"value": round(1.0 / d["seconds"], 6), "unit": "calls/s", "cores": nc, "kind": "oracle",
+                     "sample": d["sample"] + " (numpy fp64; BLAS threads = cores, elementwise numpy single-threaded)",
+                     "single_thread": {"value": round(1.0 / one["seconds"], 6), "unit": "calls/s", "cores": 1,
+                                       "sample": one["sample"]}}
+    return res
 
 
 def run_reference(args):
@@ -742,7 +944,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-config records")
+    ap.add_argument("--oracle-samples", type=float, default=None, help=argparse.SUPPRESS)
     ap.add_argument("--no-graph", action="store_true", help="skip the graph-replay measurement")
     ap.add_argument("--splits", type=int, default=0, help="KV splits per attention call (0: library's choice)")
     ap.add_argument("--sweep", action="store_true", help="time one attention call of every workload")
@@ -751,6 +954,9 @@ def main():
     ap.add_argument("--attn-only", type=int, default=0, metavar="N",
                     help="profiling case: N steady-state attention calls on one layer, then exit")
     args = ap.parse_args()
+    if args.oracle_samples is not None:  # child process of oracle_baselines()
+        print(json.dumps(oracle_samples(args.oracle_samples)), flush=True)
+        return
     if args.attn_only:
         return run_attn_only(args)
     if args.sweep:

@@ -183,7 +183,9 @@ sab_status sab_kv_ring_set_state(sab_ring* ring, const long long* newest_chunk, 
  * (0 when num_splits == 1; num_splits == 0 sizes it for any automatic choice).  The workspace holds per-split partial outputs
  * and LSEs plus one arrival counter per query tile; the counters must be zero
  * before the first call (zero-fill the workspace once after allocating it);
- * every successful call leaves them zero again.
+ * every call leaves them zero again, also one whose device waits gave up
+ * (SAB_ERR_TIMEOUT from sab_get_last_device_error: its outputs are then not
+ * valid, but the workspace needs no re-zeroing).
  */
 size_t sab_chunk_attention_workspace(const sab_ring* ring, int num_splits);
 
@@ -199,10 +201,13 @@ size_t sab_chunk_attention_workspace(const sab_ring* ring, int num_splits);
  *   num_splits >= 1: KV partitions computed in parallel and merged by
  *          log-sum-exp inside the same kernel ("Matrix-Game 4.0", section
  *          "技术新颖性": the window is cut into intervals whose partial outputs
- *          are merged with log-sum-exp); 1 runs one 128-query tile per CTA
- *          over the whole key set (no merge).  0 lets the library choose: no
- *          split when the B * H * ceil(Lc / 128) query tiles cover at least a
- *          quarter of the SMs, else up to 8 partitions.
+ *          are merged with log-sum-exp): one CTA per (128-query tile, b, h,
+ *          partition); each partition writes its normalised partial rows and
+ *          LSEs to the workspace and the last one of a query tile to finish
+ *          merges them.  1 runs each query tile over the whole key set (no
+ *          merge).  0 lets the library choose S in 1..8 to fill the SMs: the
+ *          S that minimises ceil(tiles * S / SMs) * ceil(key tiles / S) (+2
+ *          key tiles for the merge when S > 1), tiles = B * H * ceil(Lc / 128).
  *   softmax_scale  usually 1/sqrt(D).
  *   O      device, token-major [B, Lc, H, D] bf16 (output).
  *   LSE    device, [B, H, Lc] fp32, natural log of sum exp(s) (output; may be NULL).
@@ -387,7 +392,7 @@ sab_status sab_chunk_counter_add(long long* d_chunk, long long delta, void* stre
  * LSEs and arrival counters of the split merge live in one library-owned
  * device array of 8 MiB (a file-scope __device__ array: every GPU that loads
  * the library holds it until the process exits).  A request whose merge
- * needs more -- num_splits * B * H * ceil-to-256(Lc) * (D + 1) * 4 bytes,
+ * needs more -- num_splits * B * H * ceil-to-128(Lc) * (D + 1) * 4 bytes,
  * roughly -- returns SAB_ERR_WORKSPACE and launches nothing.
  * The call allocates nothing (no cudaMalloc/cudaFree or allocating library
  * routine); it clears the counters with cudaMemsetAsync on `stream`.
@@ -436,6 +441,24 @@ sab_status sab_get_last_device_error(void* stream);
  * usable.
  */
 sab_status sab_selftest_bounded_wait(unsigned long long timeout_ns, void* stream);
+
+/*
+ * Self-test of the split merge's recovery (no counterpart in the method):
+ * runs sab_chunk_attention with the same arguments and num_splits >= 2 (the
+ * merge through the caller's workspace), in which split `abort_split`
+ * (0 <= abort_split < num_splits) reports itself at the merge exactly as a
+ * split whose bounded wait gave up does.  The merge of every query tile is
+ * then skipped (O and LSE of this call are not valid),
+ * sab_get_last_device_error reports SAB_ERR_TIMEOUT, and every arrival
+ * counter of the workspace is zero again, so the next call on the same
+ * workspace needs no re-zeroing.  Nothing faults, traps or hangs.
+ * Errors: INVALID_ARG (num_splits < 2 or > 256, abort_split out of range),
+ * then those of sab_chunk_attention.
+ */
+sab_status sab_selftest_split_abort(const sab_ring* ring, int layer, long long chunk, const void* Q,
+                                    const void* K_cur, const void* V_cur, int window, int use_sink, int num_splits,
+                                    float softmax_scale, void* O, float* LSE, void* workspace, size_t ws_bytes,
+                                    int abort_split, void* stream);
 
 /* Static, human-readable name of a status code. */
 const char* sab_status_string(sab_status status);

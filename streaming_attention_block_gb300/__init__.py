@@ -43,6 +43,7 @@ from ._abi import (  # noqa: F401
     memory_prefix_attention_backward,
     qk_norm_rope,
     selftest_bounded_wait,
+    selftest_split_abort,
     status_string,
     version,
 )

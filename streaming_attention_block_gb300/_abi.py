@@ -73,6 +73,7 @@ def library() -> ctypes.CDLL:
         "sab_block_causal_attention": (I, [P, P, P, I, I, I, I, I, I, I, F, P, P, P, SZ, P]),
         "sab_get_last_device_error": (I, [P]),
         "sab_selftest_bounded_wait": (I, [ctypes.c_ulonglong, P]),
+        "sab_selftest_split_abort": (I, [P, I, LL, P, P, P, I, I, I, F, P, P, P, SZ, I, P]),
         "sab_qk_norm_rope": (I, [P, I, LL, P, P, P, P, P, P, P, P, P, I, P]),
         "sab_block_causal_attention_backward_workspace": (SZ, [I, I, I]),
         "sab_block_causal_attention_backward": (I, [P, P, P, P, P, P, I, I, I, I, I, I, F, P, P, P, P, SZ, P]),
@@ -330,6 +331,18 @@ def selftest_bounded_wait(timeout_ns: int, stream=None):
     """sab_selftest_bounded_wait: a device wait that nothing completes gives up
     after timeout_ns; read the result with get_last_device_error."""
     _check(library().sab_selftest_bounded_wait(int(timeout_ns), _stream(stream)), "selftest_bounded_wait")
+
+
+def selftest_split_abort(handle, layer: int, chunk: int, Q, K_cur, V_cur, window: int, use_sink: bool,
+                         num_splits: int, softmax_scale: float, O, LSE, workspace, abort_split: int, stream=None):
+    """sab_selftest_split_abort: a split call (num_splits > 8, workspace merge)
+    whose split ``abort_split`` reports itself as having given up a wait."""
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(library().sab_selftest_split_abort(
+        handle, int(layer), int(chunk), _ptr(Q, torch.bfloat16, "Q"), _ptr(K_cur, torch.bfloat16, "K_cur"),
+        _ptr(V_cur, torch.bfloat16, "V_cur"), int(window), int(bool(use_sink)), int(num_splits),
+        float(softmax_scale), _ptr(O, torch.bfloat16, "O"), _ptr(LSE, torch.float32, "LSE"),
+        _ptr(workspace, None, "workspace"), ws_bytes, int(abort_split), _stream(stream)), "selftest_split_abort")
 
 
 class RopeDesc(ctypes.Structure):

@@ -16,29 +16,21 @@
 // masked; in block-causal mode each row derives its key interval from its
 // chunk index.
 //
-// Two kernels.  chunk_attn_kh_kernel (further down) serves every unsplit
-// call: one query tile per CTA, key-half softmax warpgroups, double-buffered
-// S.  chunk_attn_kernel below serves split calls; its design (one CTA = QT
-// query tiles of 128 rows x one (b, h) x one KV split):
-//   warp 0      TMA producer: Q once, then K/V tiles through a smem ring of
-//               kStages stages (128-byte swizzle, 64-column boxes).
-//   warp 1      TMEM allocator and tcgen05 MMA issuer (one elected lane):
-//               S_t = Q_t K^T (M=128, N=128) into TMEM, then O_t += P_t V with
-//               P_t read from TMEM (it overwrites S_t in place, as bf16).
-//   warps 4..   one softmax warpgroup per query tile: thread = row = TMEM
-//               lane; loads S, updates the running max (a rescale of O in
-//               TMEM only when the max grows by more than 2^8, exact in real
-//               arithmetic), writes P, and runs the epilogue.
-// The MMA thread interleaves the two tiles (S_0, PV_1, S_1, PV_0, ...), so one
-// warpgroup's exponentials overlap the other tile's MMAs.  Split partials go
-// to a workspace; the last CTA of a query tile to finish (atomic ticket)
-// merges them by log-sum-exp ("Matrix-Game 4.0", section "技术新颖性": KV
-// window intervals computed in parallel and merged with log-sum-exp).
+// One forward kernel, chunk_attn_kh_kernel (below): one CTA = one tile of
+// 128 query rows x one (b, h) x one KV split; each 128-key tile's scores are
+// handled by two softmax warpgroups, one per 64-key half, double-buffered S
+// in TMEM.  With more than one split, each split writes its normalised
+// partial rows and LSE to the workspace and the last split of a query tile
+// to finish (atomic ticket) merges them by log-sum-exp ("Matrix-Game 4.0",
+// section "技术新颖性": KV window intervals computed in parallel and merged
+// with log-sum-exp).  Further down: the backward kernels.
 //
 // Every mbarrier wait is bounded: on expiry the kernel records the wait site
 // in a device error word, raises a CTA-wide abort flag, drains its own TMA
 // copies and MMAs (again with bounded waits), frees TMEM and returns.
 #include <math.h>
+
+#include <mutex>
 
 #include "ptx.cuh"
 #include "sab_internal.h"
@@ -56,61 +48,6 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows by > 2^8
 constexpr float kRescaleThresholdF8 = 4.0f;  // E4M3 P: by > 2^4 (P' = P * 2^4 * vs / vs_ref <= 2^8)
-
-template <int D_, int QT_, bool FP8_>
-struct Cfg {
-  static constexpr int D = D_, QT = QT_;
-  static constexpr int kBoxes = D / 64;                  // 64-column (128-byte) boxes per row
-  static constexpr uint32_t kBoxBytes = 128u * 128u;     // 128 rows x 128 bytes
-  static constexpr uint32_t kTileBytes = kBoxBytes * kBoxes;
-  static constexpr int kStages = (D == 128) ? 2 : 4;
-  // K stages, V stages, then Q: every operand region is followed by another
-  // operand region inside the allocation.
-  static constexpr uint32_t kKOff = 0;
-  static constexpr uint32_t kVOff = kKOff + kStages * kTileBytes;
-  static constexpr uint32_t kQOff = kVOff + kStages * kTileBytes;
-  static constexpr uint32_t kBarOff = kQOff + QT * kTileBytes;
-  static constexpr int kBarQ = 0;
-  static constexpr int kBarKFull = 1;                      // [kStages] K and V tile landed
-  static constexpr int kBarKVEmpty = kBarKFull + kStages;
-  static constexpr int kBarSFull = kBarKVEmpty + kStages;  // [2]
-  static constexpr int kBarPFull = kBarSFull + 2;          // [2 tiles][2 key halves]
-  static constexpr int kBarOFinal = kBarPFull + 4;         // [2]
-  static constexpr int kBarDrain = kBarOFinal + 2;
-  static constexpr int kBarRawFull = kBarDrain + 1;          // [kStages] FP8 codes landed
-  static constexpr int kBarPairReady = kBarRawFull + kStages;  // pair merge: the peer can receive
-  static constexpr int kBarPairIn = kBarPairReady + 1;         // pair merge: the peer's rows landed
-  static constexpr int kBarPairDone = kBarPairIn + 1;          // pair merge: the peer has our rows
-  static constexpr int kNumBars = kBarPairDone + 1;
-  static constexpr int kConvThreads = 64;                    // warps 2-3 expand E4M3 tiles
-  static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
-  static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;  // + alignment slack
-  static constexpr int kThreads = 128 + 128 * QT;
-  static constexpr uint32_t kTmemS = 0;          // S_t / P_t at column t * 128
-  static constexpr uint32_t kTmemO = QT * 128;   // O_t at column kTmemO + t * D
-  static constexpr uint32_t kTmemCols = (QT * 128 + QT * D <= 256) ? 256u : 512u;
-  // Cluster merge reuses the operand region (K, V, Q are dead by then): the
-  // rows this CTA merges, one slot per split, fp32 with a pitch of D + 4
-  // floats (bank-conflict free float4 access), then one LSE per slot row.
-  // At most QT*128 + 7 slot rows (rows per CTA rounded up, 8 splits).
-  static constexpr uint32_t kMergePitch = D + 4;
-  static constexpr uint32_t kMergeRows = QT * 128 + 8;
-  static constexpr uint32_t kMergeOOff = kKOff;
-  static constexpr uint32_t kMergeLseOff = kMergeOOff + kMergeRows * kMergePitch * 4;
-  static_assert(kMergeLseOff + kMergeRows * 4 <= kBarOff, "merge buffer fits in the operand region");
-  // Two-split pair merge (QT == 2), also in the dead operand region: the
-  // peer's normalised partial rows of the tile this CTA owns (128 rows of D
-  // fp32, 16-byte chunks XOR-swizzled by row, then 128 LSEs), the merged bf16
-  // tile in the output tensor map's layout, and this CTA's partial rows of
-  // the tile the peer owns (same layout as the received block).
-  static constexpr uint32_t kPairBytes = 128u * D * 4u + 128u * 4u;
-  static constexpr uint32_t kPairRecvOff = 0;
-  static constexpr uint32_t kPairOutOff = (kPairRecvOff + kPairBytes + 1023u) & ~1023u;
-  static constexpr uint32_t kPairSendOff = kPairOutOff + kTileBytes;
-  static_assert(QT != 2 || kPairSendOff + kPairBytes <= kBarOff, "pair merge buffers fit");
-  static_assert(kPairBytes % 16 == 0 && kPairSendOff % 16 == 0, "bulk copy alignment");
-  static_assert(kSmemBytes <= 232448, "shared memory budget");
-};
 
 __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
@@ -232,885 +169,44 @@ __device__ __forceinline__ void plan_prefix_runs(const AttnParams& p, int b, int
   kp.total_tiles = t1 + (khi - klo + kTileN - 1) / kTileN;
 }
 
-// Expand one key/value row of 128 8-bit codes in place into 128 bf16 values.
-// The codes sit in the second 128-byte box of the row (where its upper bf16
-// half goes); all of them are read before any bf16 chunk is written, and the
-// bf16 row is written in the 128-byte-swizzled layout of the MMA operands.
-// E4M3 codes and INT8 codes (K8) both convert exactly.
+// Expand one key/value row of 128 8-bit codes in place into 128 fp16 values
+// (the operand type of the 8-bit-cache path).  The codes sit in the second
+// 128-byte box of the row (where its upper 16-bit half goes); all of them are
+// read before any fp16 chunk is written, and the row is written in the
+// 128-byte-swizzled layout of the MMA operands.  One conversion instruction
+// per pair of E4M3 codes; two integer and two half-precision instructions per
+// four INT8 codes.  Exact for every code.
 template <bool K8>
-__device__ __forceinline__ void expand_code_row(uint8_t* tile, int r, uint32_t box_bytes) {
-  const uint4* src = reinterpret_cast<const uint4*>(tile + box_bytes + r * 128);
+__device__ __forceinline__ void expand_code_row_f16(uint8_t* tile, int r, uint32_t box_bytes) {
+  // The row's 16-byte code chunks are visited starting at chunk (r & 7), so
+  // the eight rows of a quarter-warp read eight different bank groups, and
+  // write eight different ones through the swizzle: no bank conflicts.
+  const int rot = r & 7;
+  const uint8_t* src = tile + box_bytes + r * 128;
   uint4 raw[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) raw[i] = src[i];
+  for (int i = 0; i < 8; ++i) raw[i] = *reinterpret_cast<const uint4*>(src + (((i + rot) & 7) << 4));
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
+    const int c = (i + rot) & 7;  // codes 16c .. 16c + 15
     const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
     uint32_t out[8];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       if constexpr (K8) {
-        s8x4_to_bf16x4(w[q], out[2 * q], out[2 * q + 1]);
+        s8x4_to_f16x4(w[q], out[2 * q], out[2 * q + 1]);
       } else {
-        float a0, a1, a2, a3;
-        e4m3x2_to_f32x2((uint16_t)(w[q] & 0xFFFFu), a0, a1);
-        e4m3x2_to_f32x2((uint16_t)(w[q] >> 16), a2, a3);
-        out[2 * q] = pack_bf16(a0, a1);  // exact: every E4M3 value is a bf16 value
-        out[2 * q + 1] = pack_bf16(a2, a3);
+        out[2 * q] = e4m3x2_to_f16x2((uint16_t)(w[q] & 0xFFFFu));
+        out[2 * q + 1] = e4m3x2_to_f16x2((uint16_t)(w[q] >> 16));
       }
     }
-    // codes 16i .. 16i+15 -> 16-byte chunks 2i, 2i+1 of the bf16 row
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
-      const int k = 2 * i + hh;
-      *reinterpret_cast<uint4*>(tile + (k >> 3) * box_bytes + r * 128 + (((k & 7) ^ (r & 7)) << 4)) =
+      const int k = 2 * c + hh;  // 16-byte fp16 chunk of the row
+      *reinterpret_cast<uint4*>(tile + (k >> 3) * box_bytes + r * 128 + (((k & 7) ^ rot) << 4)) =
           make_uint4(out[4 * hh], out[4 * hh + 1], out[4 * hh + 2], out[4 * hh + 3]);
     }
   }
-}
-
-template <int D, int QT, bool FP8>
-__global__ void __launch_bounds__(Cfg<D, QT, FP8>::kThreads, 1)
-chunk_attn_kernel(const __grid_constant__ AttnParams p) {
-  using C = Cfg<D, QT, FP8>;
-  static_assert(!FP8 || D == 128, "the FP8 cache path expands 128-byte code rows in place");
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw_u32 = smem_u32(smem_raw);
-  const uint32_t base_u32 = (raw_u32 + 1023u) & ~1023u;
-  uint8_t* base = smem_raw + (base_u32 - raw_u32);
-  const uint32_t sQ = base_u32 + C::kQOff;
-  const uint32_t sK = base_u32 + C::kKOff;
-  const uint32_t sV = base_u32 + C::kVOff;
-  const uint32_t bars = base_u32 + C::kBarOff;
-  uint32_t* misc = reinterpret_cast<uint32_t*>(base + C::kMiscOff);  // [0] tmem, [1] abort, [2] ticket
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
-  volatile uint32_t* ticket = misc + 2;
-  auto bar = [&](int i) -> uint32_t { return bars + 8u * (uint32_t)i; };
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int qg = blockIdx.x;
-  const int bh = blockIdx.y;
-  const int split = blockIdx.z;
-  const int b = bh / p.H;
-  const int h = bh - b * p.H;
-  const int q0 = qg * QT * kTileM;
-
-
-  if (threadIdx.x == 0) {
-    mbar_init(bar(C::kBarQ), 1);
-    for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(bar(C::kBarKFull + s), FP8 ? C::kConvThreads : 1);
-      mbar_init(bar(C::kBarRawFull + s), 1);
-      mbar_init(bar(C::kBarKVEmpty + s), 1);
-    }
-    for (int t = 0; t < 2; ++t) {
-      mbar_init(bar(C::kBarSFull + t), 1);
-      mbar_init(bar(C::kBarPFull + 2 * t), 128);
-      mbar_init(bar(C::kBarPFull + 2 * t + 1), 128);
-      mbar_init(bar(C::kBarOFinal + t), 1);
-    }
-    mbar_init(bar(C::kBarDrain), 1);
-    mbar_init(bar(C::kBarPairReady), 1);
-    mbar_init(bar(C::kBarPairIn), 1);
-    mbar_init(bar(C::kBarPairDone), 1);
-    misc[1] = 0;
-    misc[2] = 0;
-    fence_mbar_init();
-    fence_proxy_async_smem();
-  }
-  if (warp == 1) {
-    tmem_alloc(smem_u32(misc), C::kTmemCols);
-    tmem_relinquish();
-  }
-  if (warp == 0 && lane == 0) {
-    prefetch_tmap(&p.q_map);
-    prefetch_tmap(&p.k_map[0]);
-    prefetch_tmap(&p.v_map[0]);
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = misc[0];
-  const bool pair_merge = QT == 2 && p.cluster_merge == 2;
-  if (pair_merge) cluster_arrive_relaxed();  // barriers initialised (waited on before remote use)
-  // Everything above (barriers, TMEM, tensor-map prefetch) overlaps the tail
-  // of the previous kernel in the stream; no global memory is touched before
-  // the previous grid has completed.
-  griddep_launch_dependents();
-  griddep_wait();
-  // key runs: planned on the host, or (graph mode) by every thread from the
-  // chunk index in device memory, read only after the previous grid completed
-  KeyPlan kp;
-  if (p.mode == kModeStreaming && p.d_chunk != nullptr)
-    plan_key_runs(*p.d_chunk, p.window, p.ring_slots, p.chunk_tokens, p.has_sink, p.use_sink, p.kcur, kp);
-  else
-    kp = p.plan;
-  int first = 0, n_tiles = 0;
-  kv_range(p, kp, q0, QT * kTileM, split, first, n_tiles);
-
-  // softmax-thread state handed to the cluster merge in the common tail
-  bool sm_ok = false;
-  float sm_inv_l = 0.f, sm_lse = -INFINITY;
-  uint32_t sm_tO = 0;
-  int sm_rcta = 0;
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      mbar_arrive_expect_tx(bar(C::kBarQ), QT * C::kTileBytes);
-#pragma unroll
-      for (int t = 0; t < QT; ++t)
-#pragma unroll
-        for (int bx = 0; bx < C::kBoxes; ++bx)
-          tma_load_4d(sQ + t * C::kTileBytes + bx * C::kBoxBytes, &p.q_map, bar(C::kBarQ), bx * 64,
-                      q0 + t * kTileM, h, b);
-      int j = 0;
-      for (; j < n_tiles; ++j) {
-        const int st = j % C::kStages;
-        const uint32_t round = (uint32_t)(j / C::kStages);
-        if (j >= C::kStages &&
-            !wait_bounded(bar(C::kBarKVEmpty + st), (round - 1u) & 1u, abort_flag, 0))
-          break;
-        const Tile ti = tile_at(p, kp, first + j);
-        if (FP8) {
-          // E4M3 code rows (128 bytes each) land in the upper half of the bf16
-          // stage buffers; the converter warps expand them in place
-          mbar_arrive_expect_tx(bar(C::kBarRawFull + st), 2 * 128 * D);
-          tma_load_4d(sK + st * C::kTileBytes + C::kBoxBytes, &p.k_map[0], bar(C::kBarRawFull + st), 0, ti.row,
-                      h, b);
-          tma_load_4d(sV + st * C::kTileBytes + C::kBoxBytes, &p.v_map[0], bar(C::kBarRawFull + st), 0, ti.row,
-                      h, b);
-        } else {
-          mbar_arrive_expect_tx(bar(C::kBarKFull + st), 2 * C::kTileBytes);
-#pragma unroll
-          for (int bx = 0; bx < C::kBoxes; ++bx)
-            tma_load_4d(sK + st * C::kTileBytes + bx * C::kBoxBytes, &p.k_map[ti.src],
-                        bar(C::kBarKFull + st), bx * 64, ti.row, h, b);
-#pragma unroll
-          for (int bx = 0; bx < C::kBoxes; ++bx)
-            tma_load_4d(sV + st * C::kTileBytes + bx * C::kBoxBytes, &p.v_map[ti.src],
-                        bar(C::kBarKFull + st), bx * 64, ti.row, h, b);
-        }
-      }
-      if (*abort_flag) {
-        // let every copy this thread issued land before the CTA exits
-        wait_drain(bar(C::kBarQ), 0);
-        for (int jj = max(0, j - C::kStages); jj < j; ++jj) {
-          const int st = jj % C::kStages;
-          const uint32_t ph = (uint32_t)(jj / C::kStages) & 1u;
-          wait_drain(bar((FP8 ? C::kBarRawFull : C::kBarKFull) + st), ph);
-        }
-      }
-    }
-    __syncwarp();
-  } else if (FP8 && (warp == 2 || warp == 3)) {
-    // ------------------------------------------------ E4M3 -> bf16 expansion
-    // Each thread owns whole rows: it reads a row's 128 codes (which sit
-    // exactly where the row's upper bf16 half goes), then writes the 128
-    // code values as bf16 (exact) in the 128-byte-swizzled layout the MMA
-    // descriptors expect.  No other thread touches those bytes, so the
-    // in-place expansion needs no barrier.  The per-(batch, head, chunk)
-    // scales are applied in fp32 by the softmax: the K scale on the scores,
-    // the V scale on P.
-    const int ct = threadIdx.x - 64;
-    for (int j = 0; j < n_tiles; ++j) {
-      const int st = j % C::kStages;
-      if (!wait_bounded(bar(C::kBarRawFull + st), (uint32_t)(j / C::kStages) & 1u, abort_flag, 12)) break;
-      const int row0 = tile_at(p, kp, first + j).row;
-#pragma unroll 1
-      for (int job = ct; job < 2 * kTileN; job += C::kConvThreads) {
-        const int r = job & (kTileN - 1);
-        const bool isv = job >= kTileN;
-        uint8_t* tile = base + (isv ? C::kVOff : C::kKOff) + st * C::kTileBytes;
-        if (p.k_int8 && !isv) expand_code_row<true>(tile, r, C::kBoxBytes);  // INT8 keys
-        else expand_code_row<false>(tile, r, C::kBoxBytes);
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(bar(C::kBarKFull + st));
-    }
-  } else if (warp == 1) {
-    // ---------------------------------------------------------- MMA issuer
-    // The whole warp runs the issue loop (its values stay warp-uniform);
-    // one elected lane issues each MMA and commit.
-    {
-      constexpr uint32_t idesc_qk = idesc_bf16_f32(128, kTileN, 0);
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 1);
-      bool ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarQ), 0, abort_flag, 1));
-      if (ok) tc_fence_after();
-      // Descriptors are built once: every operand tile of a kind shares the
-      // high word, and stepping K (or a stage) only adds a small constant to
-      // the 14-bit start-address field of the low word (no carry: shared
-      // addresses stay below 256 KB).
-      const uint64_t dq = smem_desc_sw128(sQ, 16, 1024);
-      const uint64_t dk = smem_desc_sw128(sK, 16, 1024);
-      const uint64_t dv = smem_desc_sw128(sV, C::kBoxBytes, 1024);
-      const uint32_t q_lo = (uint32_t)dq, k_lo = (uint32_t)dk, v_lo = (uint32_t)dv;
-      const uint32_t kq_hi = (uint32_t)(dq >> 32), v_hi = (uint32_t)(dv >> 32);
-      constexpr uint32_t kTileStep = C::kTileBytes >> 4;
-      // The issuing thread blocks on each MMA until the tensor pipe accepts
-      // it, so a barrier check between MMA groups leaves the pipe idle for
-      // its latency.  Barriers needed next are therefore probed without
-      // blocking in the middle of the preceding MMA group (the probe's latency
-      // hides behind the MMA issue stall); a later wait is skipped when its
-      // probe already saw the phase complete.  A probe can never observe a
-      // stale phase: each barrier's next phase depends on work this thread
-      // has not issued yet.
-      auto issue_s = [&](int t, int j, uint32_t pbar, uint32_t ppar, bool& pout) {
-        const uint32_t st = (uint32_t)(j % C::kStages);
-        const uint32_t d = tmem + C::kTmemS + t * 128;
-        const uint32_t a0 = q_lo + (uint32_t)t * kTileStep;
-        const uint32_t b0 = k_lo + st * kTileStep;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t koff = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
-          mma_ss_e(d, make_desc(a0 + koff, kq_hi), make_desc(b0 + koff, kq_hi), idesc_qk, kk > 0 ? 1u : 0u);
-          if (kk == D / 32 && pbar != 0) pout = mbar_test_wait(pbar, ppar);
-        }
-      };
-      // one half (64 keys) of O_t += P_t V
-      auto issue_pv_half = [&](int t, int j, int half, uint32_t pbar, uint32_t ppar, bool& pout) {
-        const uint32_t st = (uint32_t)(j % C::kStages);
-        const uint32_t d = tmem + C::kTmemO + t * D;
-        const uint32_t b0 = v_lo + st * kTileStep;
-        const uint32_t acc0 = j > 0 ? 1u : 0u;
-#pragma unroll
-        for (int kk = half * 4; kk < half * 4 + 4; ++kk) {
-          const uint32_t a_t = tmem + C::kTmemS + t * 128 + kk * 8;
-          mma_ts_e(d, a_t, make_desc(b0 + ((kk * 16 * 128) >> 4), v_hi), idesc_pv, kk > 0 ? 1u : acc0);
-          if (kk == half * 4 + 1 && pbar != 0) pout = mbar_test_wait(pbar, ppar);
-        }
-      };
-      auto wait_probed = [&](uint32_t b, uint32_t par, bool probed, unsigned site) -> bool {
-        if (probed) return true;
-        return __all_sync(0xffffffffu, wait_bounded(b, par, abort_flag, site));
-      };
-      auto kbar = [&](int j) { return bar(C::kBarKFull + j % C::kStages); };
-      auto kpar = [&](int j) { return (uint32_t)(j / C::kStages) & 1u; };
-      auto pbar = [&](int t, int half) { return bar(C::kBarPFull + 2 * t + half); };
-      // PV_t(j): both halves, with the probes for what follows
-      // (V of tile j landed with K of tile j: one barrier covers both)
-      auto issue_pv = [&](int t, int j, bool pr_h0, uint32_t nbar, uint32_t npar, bool& nout) -> bool {
-        if (!wait_probed(pbar(t, 0), (uint32_t)j & 1u, pr_h0, 2 + t)) return false;
-        tc_fence_after();
-        bool pr_h1 = false;
-        issue_pv_half(t, j, 0, pbar(t, 1), (uint32_t)j & 1u, pr_h1);
-        if (!wait_probed(pbar(t, 1), (uint32_t)j & 1u, pr_h1, 2 + t)) return false;
-        tc_fence_after();
-        issue_pv_half(t, j, 1, nbar, npar, nout);
-        return true;
-      };
-      bool pr_p0 = false;  // probe for PV_0 of the previous tile
-      // A stage is released by a commit right after the last PV that reads
-      // it (before the next S is issued), so the release does not also wait
-      // for that S.
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        bool pr_k = false;
-        if (j > 0 && !(ok = issue_pv(0, j - 1, pr_p0, kbar(j), kpar(j), pr_k))) break;
-        if (QT == 1 && j > 0) mma_commit_e(bar(C::kBarKVEmpty + (j - 1) % C::kStages));
-        if (!(ok = wait_probed(kbar(j), kpar(j), pr_k, 5))) break;
-        tc_fence_after();
-        if (QT == 2) {
-          bool pr_p1 = false;
-          issue_s(0, j, j > 0 ? pbar(1, 0) : 0u, (uint32_t)(j - 1) & 1u, pr_p1);
-          mma_commit_e(bar(C::kBarSFull + 0));
-          bool unused = false;
-          if (j > 0) {
-            if (!(ok = issue_pv(1, j - 1, pr_p1, 0u, 0u, unused))) break;
-            mma_commit_e(bar(C::kBarKVEmpty + (j - 1) % C::kStages));
-          }
-          issue_s(1, j, pbar(0, 0), (uint32_t)j & 1u, pr_p0);
-          mma_commit_e(bar(C::kBarSFull + 1));
-        } else {
-          bool unused = false;
-          issue_s(0, j, 0u, 0u, unused);
-          mma_commit_e(bar(C::kBarSFull + 0));
-          pr_p0 = false;
-        }
-      }
-      if (ok) {
-        if (n_tiles > 0) {
-          bool unused = false;
-          ok = issue_pv(0, n_tiles - 1, pr_p0, 0u, 0u, unused);
-          if (ok) mma_commit_e(bar(C::kBarOFinal + 0));
-          if (ok && QT == 2) {
-            ok = issue_pv(1, n_tiles - 1, false, 0u, 0u, unused);
-            if (ok) mma_commit_e(bar(C::kBarOFinal + 1));
-          }
-          if (ok) mma_commit_e(bar(C::kBarKVEmpty + (n_tiles - 1) % C::kStages));
-        } else {
-          mma_commit_e(bar(C::kBarOFinal + 0));
-          if (QT == 2) mma_commit_e(bar(C::kBarOFinal + 1));
-        }
-      }
-      if (!ok) {
-        mma_commit_e(bar(C::kBarDrain));
-        if (lane == 0) wait_drain(bar(C::kBarDrain), 0);
-      }
-    }
-    __syncwarp();
-  } else if (warp >= 4) {
-    // ---------------------------------------------- softmax + epilogue
-    const int t = (warp - 4) >> 2;   // query tile of this warpgroup
-    const int quad = warp & 3;       // TMEM lane quadrant this warp may access
-    const int row = quad * 32 + lane;
-    const int q_row = q0 + t * kTileM + row;
-    const bool row_valid = q_row < p.Lq;
-    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    const uint32_t tS = tmem + lane_off + C::kTmemS + t * 128;
-    const uint32_t tO = tmem + lane_off + C::kTmemO + t * D;
-    int klo = 0, khi = 0;  // block-causal: visible key rows [klo, khi)
-    if (p.mode == kModeBlockCausal && row_valid) {
-      const int qc = q_row / p.chunk_tokens;
-      klo = max(0, qc - p.window) * p.chunk_tokens;
-      khi = min(p.Lk, (qc + 1) * p.chunk_tokens);
-    }
-    const float sl = p.scale_log2;
-    // streaming: the key runs in registers (the last tile of a run is partial)
-    int seg_tile0[kMaxSegments], seg_rows[kMaxSegments], seg_row0[kMaxSegments];
-#pragma unroll
-    for (int i = 0; i < kMaxSegments; ++i) {
-      seg_tile0[i] = (i < kp.nseg) ? kp.seg[i].tile0 : 0x7fffffff;
-      seg_rows[i] = kp.seg[i].nrows;
-      seg_row0[i] = kp.seg[i].row0;
-    }
-    const long long srow = (long long)bh * p.scale_stride;  // FP8 scale row of this (b, h)
-    float m_run = -INFINITY, l_run = 0.f;
-    bool ok = true;
-    for (int j = 0; j < n_tiles; ++j) {
-      ok = wait_bounded(bar(C::kBarSFull + t), (uint32_t)j & 1u, abort_flag, 6 + t);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t s0[32], s1[32], s2[32], s3[32];
-      tmem_ld32(tS + 0, s0);
-      tmem_ld32(tS + 32, s1);
-      tmem_ld32(tS + 64, s2);
-      tmem_ld32(tS + 96, s3);
-      int lo, hi;
-      int tile_row0 = 0;
-      const int g = first + j;
-      if (p.mode == kModeStreaming) {
-        int sg = 0;
-#pragma unroll
-        for (int i = 1; i < kMaxSegments; ++i) sg = (g >= seg_tile0[i]) ? i : sg;
-        int t0 = seg_tile0[0], nr = seg_rows[0], r0 = seg_row0[0];
-#pragma unroll
-        for (int i = 1; i < kMaxSegments; ++i) {
-          t0 = (sg == i) ? seg_tile0[i] : t0;
-          nr = (sg == i) ? seg_rows[i] : nr;
-          r0 = (sg == i) ? seg_row0[i] : r0;
-        }
-        lo = 0;
-        hi = nr - (g - t0) * kTileN;
-        tile_row0 = r0 + (g - t0) * kTileN;
-      } else {
-        lo = klo - g * kTileN;
-        hi = khi - g * kTileN;
-      }
-      tmem_wait_ld();
-      // FP8 cache: the keys of this tile belong to at most two chunks
-      // (chunk_tokens >= 128): columns [0, bnd) to the first, the rest to the
-      // next.  Score coefficient c = softmax_scale*log2(e)*k_scale; V scale
-      // folded into P (exponent offset d = log2 v_scale when uniform).
-      float c0 = sl, c1 = sl, d0 = 0.f, v0 = 1.f, v1 = 1.f, iv0 = 1.f;
-      int bnd = kTileN;
-      if constexpr (FP8) {
-        const int si0 = min(tile_row0 / p.chunk_tokens, p.scale_stride - 1);
-        const int si1 = min(si0 + 1, p.scale_stride - 1);
-        bnd = (si0 + 1) * p.chunk_tokens - tile_row0;
-        c0 = sl * __ldg(p.k_scale + srow + si0);
-        c1 = sl * __ldg(p.k_scale + srow + si1);
-        v0 = __ldg(p.v_scale + srow + si0);
-        v1 = __ldg(p.v_scale + srow + si1);
-        d0 = __log2f(v0);
-        iv0 = 1.f / v0;
-      }
-      const bool straddle = FP8 && bnd < kTileN;
-      if (straddle) {
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          s0[c] = __float_as_uint(__uint_as_float(s0[c]) * (c < bnd ? c0 : c1));
-          s1[c] = __float_as_uint(__uint_as_float(s1[c]) * (c + 32 < bnd ? c0 : c1));
-          s2[c] = __float_as_uint(__uint_as_float(s2[c]) * (c + 64 < bnd ? c0 : c1));
-          s3[c] = __float_as_uint(__uint_as_float(s3[c]) * (c + 96 < bnd ? c0 : c1));
-        }
-      }
-      // mask after any per-column scaling (an unwritten FP8 slot has scale 0,
-      // and -inf * 0 would be NaN)
-      if (!(lo <= 0 && hi >= kTileN)) {
-        const uint32_t ninf = 0xff800000u;
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          s0[c] = (c >= lo && c < hi) ? s0[c] : ninf;
-          s1[c] = (c + 32 >= lo && c + 32 < hi) ? s1[c] : ninf;
-          s2[c] = (c + 64 >= lo && c + 64 < hi) ? s2[c] : ninf;
-          s3[c] = (c + 96 >= lo && c + 96 < hi) ? s3[c] : ninf;
-        }
-      }
-      // row max: 8 independent chains of three-input maxima
-      float pm[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        float m = fmax3(__uint_as_float(s0[k]), __uint_as_float(s0[k + 8]), __uint_as_float(s0[k + 16]));
-        m = fmax3(m, __uint_as_float(s0[k + 24]), __uint_as_float(s1[k]));
-        m = fmax3(m, __uint_as_float(s1[k + 8]), __uint_as_float(s1[k + 16]));
-        m = fmax3(m, __uint_as_float(s1[k + 24]), __uint_as_float(s2[k]));
-        m = fmax3(m, __uint_as_float(s2[k + 8]), __uint_as_float(s2[k + 16]));
-        m = fmax3(m, __uint_as_float(s2[k + 24]), __uint_as_float(s3[k]));
-        m = fmax3(m, __uint_as_float(s3[k + 8]), __uint_as_float(s3[k + 16]));
-        pm[k] = fmaxf(m, __uint_as_float(s3[k + 24]));
-      }
-      const float mx = fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7]));
-      const float m_new = fmaxf(m_run, straddle ? mx : mx * c0);
-      const bool need = m_new > m_run + kRescaleThreshold;
-      float alpha = 1.f;
-      if (need) {
-        alpha = ex2(m_run - m_new);  // 0 when m_run is -inf
-        l_run *= alpha;
-        m_run = m_new;
-      }
-      if (j > 0 && __any_sync(0xffffffffu, need)) {
-        // S_t(j) completion implies PV_t(j-1) completed (same-thread commit
-        // order); the rescale lands before the first half of P is published.
-#pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 16) {
-          uint32_t o[16];
-          tmem_ld16(tO + c0, o);
-          tmem_wait_ld();
-#pragma unroll
-          for (int c = 0; c < 16; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-          tmem_st16(tO + c0, o);
-        }
-      }
-      const float mb = (m_run == -INFINITY) ? 0.f : m_run;
-      float ps[4] = {0.f, 0.f, 0.f, 0.f};
-      // P (bf16 pairs) overwrites the first 64 columns of S: column k holds
-      // keys 2k (low half) and 2k+1 (high half).  Keys 0..63 are published
-      // first so the PV MMA on them overlaps the exponentials of keys 64..127.
-      // e = 2^(x) with x = s*c0 + d0 - m (bf16 cache: c0 = scale*log2(e),
-      // d0 = 0); a straddling FP8 tile has its scores pre-scaled per column
-      // and multiplies P by the column's V scale instead.
-      const float xa = straddle ? 1.f : c0;
-      const float xb = d0 - mb;
-      const float xs = straddle ? -mb : xb;
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t pk[32];
-        const uint32_t* sa = hf ? s2 : s0;
-        const uint32_t* sb = hf ? s3 : s1;
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          float a0 = ex2(fmaf(__uint_as_float(sa[2 * c]), xa, xs));
-          float a1 = ex2(fmaf(__uint_as_float(sa[2 * c + 1]), xa, xs));
-          float b0 = ex2(fmaf(__uint_as_float(sb[2 * c]), xa, xs));
-          float b1 = ex2(fmaf(__uint_as_float(sb[2 * c + 1]), xa, xs));
-          ps[c & 3] += (a0 + a1) + (b0 + b1);
-          if (straddle) {
-            const int k = hf * 64 + 2 * c;  // key index of a0
-            a0 *= (k < bnd ? v0 : v1);
-            a1 *= (k + 1 < bnd ? v0 : v1);
-            b0 *= (k + 32 < bnd ? v0 : v1);
-            b1 *= (k + 33 < bnd ? v0 : v1);
-          }
-          pk[c] = pack_bf16(a0, a1);
-          pk[16 + c] = pack_bf16(b0, b1);
-        }
-        tmem_st32(tS + hf * 32, pk);
-        if (hf == 0) {
-          tmem_wait_st();
-          tc_fence_before();
-          mbar_arrive(bar(C::kBarPFull + 2 * t));
-        }
-      }
-      l_run += ((ps[0] + ps[1]) + (ps[2] + ps[3])) * (straddle ? 1.f : iv0);
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar(C::kBarPFull + 2 * t + 1));
-    }
-    if (ok) {
-      ok = wait_bounded(bar(C::kBarOFinal + t), 0, abort_flag, 8 + t);
-      // the cluster merge overwrites operand smem: every MMA must be done
-      if (ok && QT == 2 && p.cluster_merge)
-        ok = wait_bounded(bar(C::kBarOFinal + (1 - t)), 0, abort_flag, 9 - t);
-      // (the pair merge also reuses operand smem: same condition)
-      ok = __all_sync(0xffffffffu, ok);
-    }
-    const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
-    const float lse = (l_run > 0.f) ? (m_run + __log2f(l_run)) * kLn2 : -INFINITY;
-    const int BH = p.B * p.H;
-    if (ok) {
-      tc_fence_after();
-      if (p.splits == 1) {
-        // stage the bf16 row in this tile's (now dead) Q slot, in the
-        // 128-byte-swizzled layout of the output tensor map, for a TMA store
-        uint8_t* stage = base + C::kQOff + t * C::kTileBytes;
-#pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t o[32];
-          if (n_tiles > 0) {
-            tmem_ld32(tO + c0, o);
-            tmem_wait_ld();
-          } else {
-#pragma unroll
-            for (int c = 0; c < 32; ++c) o[c] = 0u;
-          }
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint4 w;
-            w.x = pack_bf16(__uint_as_float(o[8 * v + 0]) * inv_l, __uint_as_float(o[8 * v + 1]) * inv_l);
-            w.y = pack_bf16(__uint_as_float(o[8 * v + 2]) * inv_l, __uint_as_float(o[8 * v + 3]) * inv_l);
-            w.z = pack_bf16(__uint_as_float(o[8 * v + 4]) * inv_l, __uint_as_float(o[8 * v + 5]) * inv_l);
-            w.w = pack_bf16(__uint_as_float(o[8 * v + 6]) * inv_l, __uint_as_float(o[8 * v + 7]) * inv_l);
-            const int k = (c0 >> 3) + v;  // 16-byte chunk of the row
-            *reinterpret_cast<uint4*>(stage + (k >> 3) * C::kBoxBytes + row * 128 + (((k & 7) ^ (row & 7)) << 4)) = w;
-          }
-        }
-        if (row_valid && p.LSE != nullptr) p.LSE[(long long)bh * p.Lq + q_row] = lse;
-      } else if (p.cluster_merge == 1) {
-        // the common tail pushes this row once every CTA of the cluster is
-        // done with its operand shared memory
-        sm_ok = true;
-        sm_inv_l = inv_l;
-        sm_lse = lse;
-        sm_tO = tO;
-        sm_rcta = t * 128 + row;
-      } else if (p.cluster_merge == 0) {
-        const long long prow = ((long long)split * BH + bh) * p.lq_pad + (q_row);
-        float* wrow = p.ws_o + prow * D;
-#pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t o[32];
-          if (n_tiles > 0) {
-            tmem_ld32(tO + c0, o);
-            tmem_wait_ld();
-          } else {
-#pragma unroll
-            for (int c = 0; c < 32; ++c) o[c] = 0u;
-          }
-          float4* dst = reinterpret_cast<float4*>(wrow + c0);
-#pragma unroll
-          for (int v = 0; v < 8; ++v)
-            dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv_l, __uint_as_float(o[4 * v + 1]) * inv_l,
-                                 __uint_as_float(o[4 * v + 2]) * inv_l, __uint_as_float(o[4 * v + 3]) * inv_l);
-        }
-        p.ws_lse[prow] = lse;
-      }
-    }
-    if (p.splits == 1) {
-      // every row of the tile is staged: one thread stores the tile with TMA
-      // (rows past the end of the sequence are clipped by the tensor map)
-      fence_proxy_async_smem();
-      named_bar_sync(2 + t, 128);
-      if (warp == 4 + 4 * t && lane == 0 && !*abort_flag && q0 + t * kTileM < p.Lq) {
-#pragma unroll
-        for (int bx = 0; bx < C::kBoxes; ++bx)
-          tma_store_4d(&p.o_map, base_u32 + C::kQOff + t * C::kTileBytes + bx * C::kBoxBytes, bx * 64,
-                       q0 + t * kTileM, h, b);
-        tma_store_commit_and_wait_read();
-      }
-    }
-    if (pair_merge) {
-      // ---------------- two-split log-sum-exp merge inside a CTA pair
-      // CTA rank r of the pair owns query tile r.  The warpgroup of the other
-      // tile normalises its partial rows into smem and sends them to the peer
-      // in one bulk copy, once the peer reports that its operand smem is free
-      // (all its MMAs done).  The owning warpgroup keeps its partial in TMEM,
-      // waits for the peer's rows, merges by log-sum-exp, and stores the bf16
-      // tile with TMA.  Three point-to-point mbarriers carry the handshake,
-      // each wait bounded; the sender keeps its source smem alive until the
-      // peer confirms receipt.
-      const uint32_t rank = cluster_ctarank();
-      const uint32_t peer = rank ^ 1u;
-      cluster_wait();  // the peer's barriers are initialised
-      tc_fence_after();
-      const bool leader = lane == 0 && quad == 0;
-      const uint32_t sw = (uint32_t)(row & 7);  // 16-byte chunk swizzle of this row
-      uint32_t o[D];
-      if (ok) {
-        if (n_tiles > 0) {
-#pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 32) tmem_ld32(tO + c0, *reinterpret_cast<uint32_t(*)[32]>(o + c0));
-          tmem_wait_ld();
-        } else {
-#pragma unroll
-          for (int c = 0; c < D; ++c) o[c] = 0u;
-        }
-      }
-      if (t != (int)rank) {
-        uint8_t* snd = base + C::kPairSendOff;
-        if (ok) {
-#pragma unroll
-          for (int k = 0; k < D / 4; ++k)
-            *reinterpret_cast<float4*>(snd + row * (D * 4) + ((k ^ sw) << 4)) =
-                make_float4(__uint_as_float(o[4 * k]) * inv_l, __uint_as_float(o[4 * k + 1]) * inv_l,
-                            __uint_as_float(o[4 * k + 2]) * inv_l, __uint_as_float(o[4 * k + 3]) * inv_l);
-          reinterpret_cast<float*>(snd + 128 * D * 4)[row] = lse;
-        }
-        fence_proxy_async_smem();
-        named_bar_sync(2 + t, 128);
-        if (leader && ok && wait_bounded<true>(bar(C::kBarPairReady), 0, abort_flag, 10) && !*abort_flag) {
-          bulk_copy_to_cta(mapa(base_u32 + C::kPairRecvOff, peer), base_u32 + C::kPairSendOff, C::kPairBytes,
-                           mapa(bar(C::kBarPairIn), peer));
-          wait_bounded<true>(bar(C::kBarPairDone), 0, abort_flag, 10);
-        }
-      } else {
-        if (leader) {
-          mbar_arrive_expect_tx(bar(C::kBarPairIn), C::kPairBytes);
-          if (ok) mbar_arrive_remote(mapa(bar(C::kBarPairReady), peer));
-        }
-        const bool got = __all_sync(0xffffffffu, ok && wait_bounded(bar(C::kBarPairIn), 0, abort_flag, 11));
-        if (got && leader) mbar_arrive_remote(mapa(bar(C::kBarPairDone), peer));
-        if (got) {
-          const uint8_t* rcv = base + C::kPairRecvOff;
-          const float lse_p = reinterpret_cast<const float*>(rcv + 128 * D * 4)[row];
-          const float M = fmaxf(lse, lse_p);
-          float w_own = 0.f, w_peer = 0.f, L = -INFINITY;
-          if (M != -INFINITY) {
-            const float e_own = ex2((lse - M) * kLog2e), e_peer = ex2((lse_p - M) * kLog2e);
-            const float tot = e_own + e_peer;
-            w_own = e_own / tot * inv_l;
-            w_peer = e_peer / tot;
-            L = M + __logf(tot);
-          }
-          uint8_t* ost = base + C::kPairOutOff;
-#pragma unroll
-          for (int k = 0; k < D / 8; ++k) {  // 16-byte bf16 chunks of the output row
-            const float4 a = *reinterpret_cast<const float4*>(rcv + row * (D * 4) + (((2 * k) ^ sw) << 4));
-            const float4 c = *reinterpret_cast<const float4*>(rcv + row * (D * 4) + (((2 * k + 1) ^ sw) << 4));
-            uint4 w;
-            w.x = pack_bf16(fmaf(__uint_as_float(o[8 * k + 0]), w_own, a.x * w_peer),
-                            fmaf(__uint_as_float(o[8 * k + 1]), w_own, a.y * w_peer));
-            w.y = pack_bf16(fmaf(__uint_as_float(o[8 * k + 2]), w_own, a.z * w_peer),
-                            fmaf(__uint_as_float(o[8 * k + 3]), w_own, a.w * w_peer));
-            w.z = pack_bf16(fmaf(__uint_as_float(o[8 * k + 4]), w_own, c.x * w_peer),
-                            fmaf(__uint_as_float(o[8 * k + 5]), w_own, c.y * w_peer));
-            w.w = pack_bf16(fmaf(__uint_as_float(o[8 * k + 6]), w_own, c.z * w_peer),
-                            fmaf(__uint_as_float(o[8 * k + 7]), w_own, c.w * w_peer));
-            *reinterpret_cast<uint4*>(ost + (k >> 3) * C::kBoxBytes + row * 128 + (((k & 7) ^ sw) << 4)) = w;
-          }
-          if (row_valid && p.LSE != nullptr) p.LSE[(long long)bh * p.Lq + q_row] = L;
-        }
-        fence_proxy_async_smem();
-        named_bar_sync(2 + t, 128);
-        if (leader && !*abort_flag && q0 + t * kTileM < p.Lq) {
-#pragma unroll
-          for (int bx = 0; bx < C::kBoxes; ++bx)
-            tma_store_4d(&p.o_map, base_u32 + C::kPairOutOff + bx * C::kBoxBytes, bx * 64, q0 + t * kTileM, h, b);
-          tma_store_commit_and_wait_read();
-        }
-      }
-    }
-    if (p.splits > 1 && !p.cluster_merge) {
-      // ------------------------- log-sum-exp merge of the splits through global memory
-      __threadfence();
-      named_bar_sync(1, 128 * QT);
-      if (threadIdx.x == 128) {
-        *ticket = (*abort_flag) ? 0xffffffffu
-                                : atomicAdd(&p.ws_count[(long long)bh * p.n_qgroups + qg], 1u);
-      }
-      named_bar_sync(1, 128 * QT);
-      if (*ticket == (uint32_t)(p.splits - 1)) {
-        __threadfence();
-        if (row_valid) {
-          const long long stride = (long long)BH * p.lq_pad;
-          const long long r0 = (long long)bh * p.lq_pad + q_row;
-          float M = -INFINITY;
-          for (int s = 0; s < p.splits; ++s) M = fmaxf(M, __ldcg(p.ws_lse + s * stride + r0));
-          float tot = 0.f;
-          if (M != -INFINITY)
-            for (int s = 0; s < p.splits; ++s) tot += ex2((__ldcg(p.ws_lse + s * stride + r0) - M) * kLog2e);
-          const float L = (M == -INFINITY) ? -INFINITY : M + __logf(tot);
-          uint16_t* orow = p.O + (((long long)b * p.Lq + q_row) * p.H + h) * D;
-#pragma unroll 1
-          for (int c0 = 0; c0 < D; c0 += 32) {
-            float acc[32];
-#pragma unroll
-            for (int c = 0; c < 32; ++c) acc[c] = 0.f;
-            if (L != -INFINITY) {
-#pragma unroll 1
-              for (int s = 0; s < p.splits; ++s) {
-                const float ls = __ldcg(p.ws_lse + s * stride + r0);
-                if (ls == -INFINITY) continue;
-                const float w = ex2((ls - L) * kLog2e);
-                const float4* src = reinterpret_cast<const float4*>(p.ws_o + (s * stride + r0) * D + c0);
-#pragma unroll
-                for (int v = 0; v < 8; ++v) {
-                  const float4 x = __ldcg(src + v);
-                  acc[4 * v] = fmaf(w, x.x, acc[4 * v]);
-                  acc[4 * v + 1] = fmaf(w, x.y, acc[4 * v + 1]);
-                  acc[4 * v + 2] = fmaf(w, x.z, acc[4 * v + 2]);
-                  acc[4 * v + 3] = fmaf(w, x.w, acc[4 * v + 3]);
-                }
-              }
-            }
-            uint4* dst = reinterpret_cast<uint4*>(orow + c0);
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              uint4 w;
-              w.x = pack_bf16(acc[8 * v + 0], acc[8 * v + 1]);
-              w.y = pack_bf16(acc[8 * v + 2], acc[8 * v + 3]);
-              w.z = pack_bf16(acc[8 * v + 4], acc[8 * v + 5]);
-              w.w = pack_bf16(acc[8 * v + 6], acc[8 * v + 7]);
-              dst[v] = w;
-            }
-          }
-          if (p.LSE != nullptr) p.LSE[(long long)bh * p.Lq + q_row] = L;
-        }
-        if (threadIdx.x == 128) p.ws_count[(long long)bh * p.n_qgroups + qg] = 0u;
-      }
-    }
-  }
-
-  tc_fence_before();
-  if (pair_merge && warp < 4) cluster_wait();
-  if (p.cluster_merge == 1) {
-    // ------------- log-sum-exp merge of the splits through distributed smem
-    // CTA rank r of the cluster owns rows [r * rows_per, (r + 1) * rows_per)
-    // of the query group.  Barrier A: every CTA is done with its operand
-    // smem (all MMAs complete).  Each softmax thread whose row another CTA
-    // owns pushes its normalised partial row and LSE into the owner's smem
-    // (slot = this split) with fire-and-forget distributed-shared-memory
-    // stores; rows this CTA owns stay in TMEM.  Barrier B: every push has
-    // landed; each owning thread merges its TMEM row with the received
-    // slots and writes the output row.  TMEM loads are warp-collective, so
-    // the branches are warp-uniform and only the stores are predicated per
-    // lane (a warp's rows may straddle two owners).
-    const int S = p.splits;
-    const int rows_per = (QT * 128 + S - 1) / S;
-    const uint32_t rank = cluster_ctarank();
-    const uint32_t owner = (uint32_t)(sm_rcta / rows_per);
-    const int lr = sm_rcta - (int)owner * rows_per;
-    const bool push = owner != rank;
-    cluster_sync_all();
-    if (warp >= 4 && sm_ok && __any_sync(0xffffffffu, push)) {
-      tc_fence_after();
-      const int slot_row = split * rows_per + lr;
-      const uint32_t o_dst = mapa(base_u32 + C::kMergeOOff + slot_row * C::kMergePitch * 4, owner);
-#pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t o[32];
-        if (n_tiles > 0) {
-          tmem_ld32(sm_tO + c0, o);
-          tmem_wait_ld();
-        } else {
-#pragma unroll
-          for (int c = 0; c < 32; ++c) o[c] = 0u;
-        }
-        if (push) {
-#pragma unroll
-          for (int v = 0; v < 8; ++v)
-            st_dsmem_v4(o_dst + (c0 + 4 * v) * 4, __uint_as_float(o[4 * v]) * sm_inv_l,
-                        __uint_as_float(o[4 * v + 1]) * sm_inv_l, __uint_as_float(o[4 * v + 2]) * sm_inv_l,
-                        __uint_as_float(o[4 * v + 3]) * sm_inv_l);
-        }
-      }
-      if (push) st_dsmem_f32(mapa(base_u32 + C::kMergeLseOff + slot_row * 4, owner), sm_lse);
-    }
-    cluster_sync_all();
-    if (warp >= 4 && sm_ok && __any_sync(0xffffffffu, !push)) {
-      tc_fence_after();
-      const int q_row = q0 + sm_rcta;
-      const float* lse_buf = reinterpret_cast<const float*>(base + C::kMergeLseOff);
-      const float* o_buf = reinterpret_cast<const float*>(base + C::kMergeOOff);
-      float ls[8];
-      float M = -INFINITY;
-#pragma unroll
-      for (int s = 0; s < 8; ++s) {
-        ls[s] = (s >= S || push) ? -INFINITY : (s == (int)rank ? sm_lse : lse_buf[s * rows_per + lr]);
-        M = fmaxf(M, ls[s]);
-      }
-      float tot = 0.f;
-#pragma unroll
-      for (int s = 0; s < 8; ++s) {
-        ls[s] = (M == -INFINITY || ls[s] == -INFINITY) ? 0.f : ex2((ls[s] - M) * kLog2e);
-        tot += ls[s];
-      }
-      const float inv_tot = tot > 0.f ? 1.f / tot : 0.f;
-      const float L = (M == -INFINITY) ? -INFINITY : M + __logf(tot);
-      const bool row_valid = !push && q_row < p.Lq;
-      uint16_t* orow = p.O + (((long long)b * p.Lq + q_row) * p.H + h) * D;
-      float l_own = 0.f;
-#pragma unroll
-      for (int s = 0; s < 8; ++s) l_own = (s == (int)rank) ? ls[s] : l_own;
-      const float w_own = l_own * inv_tot * sm_inv_l;
-#pragma unroll 1
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t o[32];
-        if (n_tiles > 0) {
-          tmem_ld32(sm_tO + c0, o);
-          tmem_wait_ld();
-        } else {
-#pragma unroll
-          for (int c = 0; c < 32; ++c) o[c] = 0u;
-        }
-        float acc[32];
-#pragma unroll
-        for (int c = 0; c < 32; ++c) acc[c] = __uint_as_float(o[c]) * w_own;
-#pragma unroll
-        for (int s = 0; s < 8; ++s) {
-          if (s < S && s != (int)rank && !push) {
-            const float wgt = ls[s] * inv_tot;
-            const float4* src = reinterpret_cast<const float4*>(o_buf + (s * rows_per + lr) * C::kMergePitch + c0);
-#pragma unroll
-            for (int v = 0; v < 8; ++v) {
-              const float4 x = src[v];
-              acc[4 * v] = fmaf(wgt, x.x, acc[4 * v]);
-              acc[4 * v + 1] = fmaf(wgt, x.y, acc[4 * v + 1]);
-              acc[4 * v + 2] = fmaf(wgt, x.z, acc[4 * v + 2]);
-              acc[4 * v + 3] = fmaf(wgt, x.w, acc[4 * v + 3]);
-            }
-          }
-        }
-        if (row_valid) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c0);
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint4 w;
-            w.x = pack_bf16(acc[8 * v + 0], acc[8 * v + 1]);
-            w.y = pack_bf16(acc[8 * v + 2], acc[8 * v + 3]);
-            w.z = pack_bf16(acc[8 * v + 4], acc[8 * v + 5]);
-            w.w = pack_bf16(acc[8 * v + 6], acc[8 * v + 7]);
-            dst[v] = w;
-          }
-        }
-      }
-      if (row_valid && p.LSE != nullptr) p.LSE[(long long)bh * p.Lq + q_row] = L;
-    }
-  }
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, C::kTmemCols);
-  }
-}
-
-template <int D, int QT, bool FP8>
-cudaError_t launch_impl(const AttnParams& p, cudaStream_t s) {
-  using C = Cfg<D, QT, FP8>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(chunk_attn_kernel<D, QT, FP8>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.n_qgroups, p.B * p.H, p.splits);
-  cfg.blockDim = dim3(C::kThreads, 1, 1);
-  cfg.dynamicSmemBytes = C::kSmemBytes;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[2];
-  // programmatic dependent launch: the kernel waits for its predecessor in
-  // griddepcontrol.wait, after its own set-up
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = 1;
-  attr[1].val.clusterDim.y = 1;
-  attr[1].val.clusterDim.z = (unsigned)p.splits;
-  cfg.attrs = attr;
-  cfg.numAttrs = p.cluster_merge ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, chunk_attn_kernel<D, QT, FP8>, p);
 }
 
 // ===========================================================================
@@ -1135,7 +231,10 @@ struct KhCfg {
   static constexpr int D = D_;
   // F8MMA: E4M3 K/V tiles go to the tensor core as stored (no expansion);
   // Q is quantised per row on chip and P is rounded to E4M3
-  static constexpr bool kConv = FP8_ && !F8MMA_;  // E4M3 -> bf16 expansion warps
+  // 8-bit cache with 16-bit products: the codes are expanded to fp16 on
+  // chip (exact), Q is converted to fp16 with a per-row power-of-two scale
+  // (exact) and P is rounded to fp16; kind::f16 products with fp16 operands
+  static constexpr bool kConv = FP8_ && !F8MMA_;  // 8-bit -> fp16 expansion warps
   static constexpr int kBoxes = D / 64;
   static constexpr uint32_t kBoxBytes = 128u * 128u;
   static constexpr uint32_t kTileBytes = kBoxBytes * kBoxes;                  // bf16 tile of 128 rows
@@ -1146,7 +245,7 @@ struct KhCfg {
   static constexpr uint32_t kQOff = kVOff + kStages * kKVTileBytes;
   static constexpr uint32_t kQ8Off = kQOff + kTileBytes;                        // E4M3 Q (F8MMA)
   static constexpr uint32_t kQmaxOff = kQ8Off + (F8MMA_ ? 128u * D : 0u);       // 2 x 128 row maxima
-  static constexpr uint32_t kBarOff = kQmaxOff + (F8MMA_ ? 1024u : 0u);
+  static constexpr uint32_t kBarOff = kQmaxOff + (FP8_ ? 1024u : 0u);
   static constexpr int kBarQ = 0;
   static constexpr int kBarKFull = 1;                         // [kStages]
   static constexpr int kBarKVEmpty = kBarKFull + kStages;     // [kStages]
@@ -1156,7 +255,7 @@ struct KhCfg {
   static constexpr int kBarPVDone = kBarPFull + 4;            // [2 halves] one phase per tile
   static constexpr int kBarOFinal = kBarPVDone + 2;           // every MMA complete
   static constexpr int kBarDrain = kBarOFinal + 1;
-  static constexpr int kBarQ8 = kBarDrain + 1;                // F8MMA: E4M3 Q written
+  static constexpr int kBarQ8 = kBarDrain + 1;                // 8-bit cache: converted Q written
   static constexpr int kNumBars = kBarQ8 + 1;
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
   static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;
@@ -1194,6 +293,7 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
   const int b = bh / p.H;
   const int h = bh - b * p.H;
   const int q0 = blockIdx.x * kTileM;
+  const int split = blockIdx.z;  // KV partition (p.splits of them, merged through the workspace)
 
 
   if (threadIdx.x == 0) {
@@ -1213,6 +313,7 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
     mbar_init(bar(C::kBarDrain), 1);
     mbar_init(bar(C::kBarQ8), 256);
     misc[1] = 0;
+    misc[2] = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
   }
@@ -1242,7 +343,7 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
   else
     kp = p.plan;
   int first = 0, n_tiles = 0;
-  kv_range(p, kp, q0, kTileM, 0, first, n_tiles);
+  kv_range(p, kp, q0, kTileM, split, first, n_tiles);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -1312,18 +413,20 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
         const int r = job & (kTileN - 1);
         const bool isv = job >= kTileN;
         uint8_t* tile = base + (isv ? C::kVOff : C::kKOff) + st * C::kTileBytes;
-        if (p.k_int8 && !isv) expand_code_row<true>(tile, r, C::kBoxBytes);  // INT8 keys
-        else expand_code_row<false>(tile, r, C::kBoxBytes);
+        if (p.k_int8 && !isv) expand_code_row_f16<true>(tile, r, C::kBoxBytes);  // INT8 keys
+        else expand_code_row_f16<false>(tile, r, C::kBoxBytes);
       }
       fence_proxy_async_smem();
       mbar_arrive(bar(C::kBarKFull + st));
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    constexpr uint32_t idesc_qk = F8MMA ? idesc_e4m3_f32(128, kTileN, 0) : idesc_bf16_f32(128, kTileN, 0);
-    constexpr uint32_t idesc_pv = F8MMA ? idesc_e4m3_f32(128, D, 1) : idesc_bf16_f32(128, D, 1);
-    // F8MMA: the A operand is the E4M3 Q the softmax warps write
-    bool ok = __all_sync(0xffffffffu, wait_bounded(bar(F8MMA ? C::kBarQ8 : C::kBarQ), 0, abort_flag, 1));
+    constexpr uint32_t idesc_qk = F8MMA ? idesc_e4m3_f32(128, kTileN, 0)
+                                        : (C::kConv ? idesc_f16_f32(128, kTileN, 0) : idesc_bf16_f32(128, kTileN, 0));
+    constexpr uint32_t idesc_pv = F8MMA ? idesc_e4m3_f32(128, D, 1)
+                                        : (C::kConv ? idesc_f16_f32(128, D, 1) : idesc_bf16_f32(128, D, 1));
+    // 8-bit cache: the A operand is the converted Q the softmax warps write
+    bool ok = __all_sync(0xffffffffu, wait_bounded(bar(FP8 ? C::kBarQ8 : C::kBarQ), 0, abort_flag, 1));
     if (ok) tc_fence_after();
     const uint64_t dq = smem_desc_sw128(F8MMA ? base_u32 + C::kQ8Off : sQ, 16, 1024);
     const uint64_t dk = smem_desc_sw128(sK, 16, 1024);
@@ -1462,16 +565,25 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
     const long long srow = (long long)bh * p.scale_stride;
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
-    // E4M3 products: this thread quantises its half of the row's Q (one
-    // absmax scale per row, as the cache's quantiser does per chunk; the
-    // division in fp32), and P is formed as P * (vs / vs_ref) * 2^4 so that
-    // the codes of V are used as stored and P stays out of the subnormals
-    // (the running max lags by at most 2^4, so P' <= 2^8 < 448).
+    // 8-bit cache: this thread converts its half of the row's Q in shared
+    // memory before the first product (the two halves of a row agree on the
+    // row's absmax through shared memory).
+    //  * E4M3 products: Q quantised to E4M3 with one absmax scale per row (as
+    //    the cache's quantiser does per chunk; the division in fp32), into a
+    //    separate buffer; P is formed as P * (vs / vs_ref) * 2^4 so that the
+    //    codes of V are used as stored and P stays out of the subnormals (the
+    //    running max lags by at most 2^4, so P' <= 2^8 < 448).
+    //  * 16-bit products: Q converted in place to fp16 times 2^e, with e
+    //    chosen per row so that the row's absmax lands in [2^14, 2^15): exact
+    //    for every value down to 2^-28 of the row's absmax (and below that an
+    //    error under 2^-39 of it); 2^-e goes into the score coefficient.  P is
+    //    formed as P * (vs / vs_ref) * 2^6 <= 2^14 (the running max lags by at
+    //    most 2^8) and rounded to fp16.
     float slq = sl, vgain = 1.f, ofac = 1.f;
-    if constexpr (F8MMA) {
+    if constexpr (FP8) {
       ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarQ), 0, abort_flag, 10));
       float* qmax = reinterpret_cast<float*>(base + C::kQmaxOff);
-      const uint8_t* qrow = base + C::kQOff + hf * C::kBoxBytes + row * 128;  // bf16 columns 64hf ..
+      uint8_t* qrow = base + C::kQOff + hf * C::kBoxBytes + row * 128;  // bf16 columns 64hf ..
       uint4 qv[8];
       float amax = 0.f;
       if (ok) {
@@ -1487,28 +599,48 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
       qmax[hf * 128 + row] = amax;
       named_bar_sync(1, 256);
       amax = fmaxf(amax, qmax[(1 - hf) * 128 + row]);
-      const float qs = amax == 0.f ? 1.f : __fdiv_rn(amax, 448.f);
-      if (ok) {
-        uint8_t* q8row = base + C::kQ8Off + row * 128;
+      if constexpr (F8MMA) {
+        const float qs = amax == 0.f ? 1.f : __fdiv_rn(amax, 448.f);
+        if (ok) {
+          uint8_t* q8row = base + C::kQ8Off + row * 128;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {  // 16 codes: bf16 chunks 2i, 2i + 1 of this half
-          uint32_t o[4];
+          for (int i = 0; i < 4; ++i) {  // 16 codes: bf16 chunks 2i, 2i + 1 of this half
+            uint32_t o[4];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint4 src = qv[2 * i + (k >> 1)];
-            const uint32_t wa = (k & 1) ? src.z : src.x, wb = (k & 1) ? src.w : src.y;
-            o[k] = pack_e4m3x2(__fdiv_rn(__uint_as_float(wa << 16), qs),
-                               __fdiv_rn(__uint_as_float(wa & 0xFFFF0000u), qs)) |
-                   (pack_e4m3x2(__fdiv_rn(__uint_as_float(wb << 16), qs),
-                                __fdiv_rn(__uint_as_float(wb & 0xFFFF0000u), qs))
-                    << 16);
+            for (int k = 0; k < 4; ++k) {
+              const uint4 src = qv[2 * i + (k >> 1)];
+              const uint32_t wa = (k & 1) ? src.z : src.x, wb = (k & 1) ? src.w : src.y;
+              o[k] = pack_e4m3x2(__fdiv_rn(__uint_as_float(wa << 16), qs),
+                                 __fdiv_rn(__uint_as_float(wa & 0xFFFF0000u), qs)) |
+                     (pack_e4m3x2(__fdiv_rn(__uint_as_float(wb << 16), qs),
+                                  __fdiv_rn(__uint_as_float(wb & 0xFFFF0000u), qs))
+                      << 16);
+            }
+            *reinterpret_cast<uint4*>(q8row + (((4 * hf + i) ^ (row & 7)) << 4)) =
+                make_uint4(o[0], o[1], o[2], o[3]);
           }
-          *reinterpret_cast<uint4*>(q8row + (((4 * hf + i) ^ (row & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
         }
+        slq = sl * qs;
+      } else {
+        int e = 0;
+        if (amax > 0.f) e = min(max(14 - ((int)((__float_as_uint(amax) >> 23) & 0xFFu) - 127), -126), 126);
+        const float up = __uint_as_float((uint32_t)(127 + e) << 23);    // 2^e
+        const float down = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e
+        if (ok) {
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {  // in place: the same 16-byte chunk, bf16 -> fp16
+            const uint32_t w[4] = {qv[c].x, qv[c].y, qv[c].z, qv[c].w};
+            uint32_t o[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              o[k] = pack_f16(__uint_as_float(w[k] << 16) * up, __uint_as_float(w[k] & 0xFFFF0000u) * up);
+            *reinterpret_cast<uint4*>(qrow + ((c ^ (row & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+          }
+        }
+        slq = sl * down;
       }
       fence_proxy_async_smem();
       mbar_arrive(bar(C::kBarQ8));
-      slq = sl * qs;
       // largest V scale over the chunks of the key runs
       float vmax = 0.f;
 #pragma unroll 1
@@ -1519,8 +651,9 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
         for (int c = kp.seg[i].row0 / p.chunk_tokens; c <= c_hi; ++c) vmax = fmaxf(vmax, __ldg(p.v_scale + srow + c));
       }
       const float vref = vmax > 0.f ? vmax : 1.f;
-      vgain = __fdiv_rn(16.f, vref);
-      ofac = vref * (1.f / 16.f);
+      constexpr float kGain = F8MMA ? 16.f : 64.f;
+      vgain = __fdiv_rn(kGain, vref);
+      ofac = vref * (1.f / kGain);
     }
     for (int j = 0; ok && j < n_tiles; ++j) {
       ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarSFull + (j & 1)), (uint32_t)(j >> 1) & 1u,
@@ -1576,7 +709,7 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
         // keep the coefficients finite and non-zero so that -inf stays -inf
         c0 = ks0 > 0.f ? slq * ks0 : slq;
         c1 = ks1 > 0.f ? slq * ks1 : slq;
-        v0 = vs0 * vgain;  // vgain = 1 unless the product is E4M3
+        v0 = vs0 * vgain;  // the P gain of the 8-bit paths
         v1 = vs1 * vgain;
         d0 = vs0 > 0.f ? __log2f(v0) : 0.f;
         iv0 = vs0 > 0.f ? 1.f / v0 : 0.f;
@@ -1625,6 +758,8 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
             const uint32_t h2 = pack_e4m3x2(e0, e1);
             if (c & 1) pko[c >> 1] = lo16 | (h2 << 16);
             else lo16 = h2;
+          } else if constexpr (C::kConv) {
+            pko[c] = pack_f16(e0, e1);
           } else {
             pko[c] = pack_bf16(e0, e1);
           }
@@ -1703,7 +838,7 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
     const float w1 = (M == -INFINITY) ? 0.f : ex2(m1 - M);
     const float L = l0 * w0 + l1 * w1;
     const float inv = L > 0.f ? 1.f / L : 0.f;
-    const float sc0 = w0 * inv * ofac, sc1 = w1 * inv * ofac;  // ofac undoes the E4M3 P gain
+    const float sc0 = w0 * inv * ofac, sc1 = w1 * inv * ofac;  // ofac undoes the 8-bit paths' P gain
     constexpr int kHalfCols = D / 2;
     uint8_t* stage = base + C::kQOff;
     if (ok) {
@@ -1721,26 +856,109 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
 #pragma unroll
         for (int c = 0; c < kHalfCols; ++c) oa[c] = ob[c] = 0u;
       }
+      const float lse = L > 0.f ? (M + __log2f(L)) * kLn2 : -INFINITY;
+      if (p.splits == 1) {
 #pragma unroll
-      for (int i = 0; i < kHalfCols / 8; ++i) {
-        float v[8];
+        for (int i = 0; i < kHalfCols / 8; ++i) {
+          float v[8];
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
-          v[c] = fmaf(__uint_as_float(oa[8 * i + c]), sc0, __uint_as_float(ob[8 * i + c]) * sc1);
-        uint4 w;
-        w.x = pack_bf16(v[0], v[1]);
-        w.y = pack_bf16(v[2], v[3]);
-        w.z = pack_bf16(v[4], v[5]);
-        w.w = pack_bf16(v[6], v[7]);
-        const int k = hf * (kHalfCols / 8) + i;  // 16-byte chunk of the output row
-        *reinterpret_cast<uint4*>(stage + (k >> 3) * C::kBoxBytes + row * 128 + (((k & 7) ^ (row & 7)) << 4)) = w;
+          for (int c = 0; c < 8; ++c)
+            v[c] = fmaf(__uint_as_float(oa[8 * i + c]), sc0, __uint_as_float(ob[8 * i + c]) * sc1);
+          uint4 w;
+          w.x = pack_bf16(v[0], v[1]);
+          w.y = pack_bf16(v[2], v[3]);
+          w.z = pack_bf16(v[4], v[5]);
+          w.w = pack_bf16(v[6], v[7]);
+          const int k = hf * (kHalfCols / 8) + i;  // 16-byte chunk of the output row
+          *reinterpret_cast<uint4*>(stage + (k >> 3) * C::kBoxBytes + row * 128 + (((k & 7) ^ (row & 7)) << 4)) = w;
+        }
+        if (hf == 0 && row_valid && p.LSE != nullptr) p.LSE[(long long)bh * p.Lq + q_row] = lse;
+      } else {
+        // this split's normalised partial row (fp32) and its LSE go to the
+        // workspace (rows past the sequence too: the pitch is whole tiles)
+        const long long prow = ((long long)split * p.B * p.H + bh) * p.lq_pad + q_row;
+        float4* dst = reinterpret_cast<float4*>(p.ws_o + prow * D + hf * kHalfCols);
+#pragma unroll
+        for (int i = 0; i < kHalfCols / 4; ++i)
+          __stcg(dst + i, make_float4(fmaf(__uint_as_float(oa[4 * i]), sc0, __uint_as_float(ob[4 * i]) * sc1),
+                                      fmaf(__uint_as_float(oa[4 * i + 1]), sc0, __uint_as_float(ob[4 * i + 1]) * sc1),
+                                      fmaf(__uint_as_float(oa[4 * i + 2]), sc0, __uint_as_float(ob[4 * i + 2]) * sc1),
+                                      fmaf(__uint_as_float(oa[4 * i + 3]), sc0, __uint_as_float(ob[4 * i + 3]) * sc1)));
+        if (hf == 0) __stcg(p.ws_lse + prow, lse);
       }
-      if (hf == 0 && row_valid && p.LSE != nullptr)
-        p.LSE[(long long)bh * p.Lq + q_row] = L > 0.f ? (M + __log2f(L)) * kLn2 : -INFINITY;
+    }
+    bool store = p.splits == 1;
+    if (p.splits > 1) {
+      // ------------------------------ log-sum-exp merge of the KV splits
+      // ("Matrix-Game 4.0", section 技术新颖性: window intervals computed in
+      // parallel, merged by log-sum-exp).  Every split of the query tile
+      // arrives on its counter, also one that gave up on a wait: the low 16
+      // bits count arrivals, the high 16 bits aborts.  The last arriver resets
+      // the counter (the workspace stays usable after a reported timeout) and,
+      // if no split aborted, merges the partial rows and stores the tile.
+      __threadfence();
+      named_bar_sync(1, 256);
+      volatile uint32_t* ticket = misc + 2;
+      if (warp == C::kSoftmaxWarp0 && lane == 0) {
+        unsigned* cnt = &p.ws_count[(long long)bh * p.n_qgroups + blockIdx.x];
+        if (split + 1 == p.inject_abort) {  // self-test: behave as a split whose wait gave up
+          atomicOr(&g_sab_error_word, 1u << 29);
+          *abort_flag = 1;
+        }
+        const bool aborted = *abort_flag != 0;
+        const unsigned old = atomicAdd(cnt, aborted ? 0x10001u : 1u);
+        const bool last = (old & 0xFFFFu) == (unsigned)(p.splits - 1);
+        if (last) *cnt = 0u;
+        *ticket = (last && !aborted && (old >> 16) == 0u) ? 1u : 0u;
+      }
+      named_bar_sync(1, 256);
+      store = *ticket == 1u;
+      if (store) {
+        __threadfence();
+        const long long stride = (long long)p.B * p.H * p.lq_pad;
+        const long long r0 = (long long)bh * p.lq_pad + q_row;
+        float Mx = -INFINITY;
+        for (int sp = 0; sp < p.splits; ++sp) Mx = fmaxf(Mx, __ldcg(p.ws_lse + sp * stride + r0));
+        float tot = 0.f;
+        if (Mx != -INFINITY)
+          for (int sp = 0; sp < p.splits; ++sp) tot += ex2((__ldcg(p.ws_lse + sp * stride + r0) - Mx) * kLog2e);
+        const float Lm = (Mx == -INFINITY) ? -INFINITY : Mx + __logf(tot);
+        float acc[kHalfCols];
+#pragma unroll
+        for (int c = 0; c < kHalfCols; ++c) acc[c] = 0.f;
+        if (Lm != -INFINITY) {
+#pragma unroll 1
+          for (int sp = 0; sp < p.splits; ++sp) {
+            const float ls = __ldcg(p.ws_lse + sp * stride + r0);
+            if (ls == -INFINITY) continue;
+            const float wgt = ex2((ls - Lm) * kLog2e);
+            const float4* src = reinterpret_cast<const float4*>(p.ws_o + (sp * stride + r0) * D + hf * kHalfCols);
+#pragma unroll
+            for (int i = 0; i < kHalfCols / 4; ++i) {
+              const float4 x = __ldcg(src + i);
+              acc[4 * i] = fmaf(wgt, x.x, acc[4 * i]);
+              acc[4 * i + 1] = fmaf(wgt, x.y, acc[4 * i + 1]);
+              acc[4 * i + 2] = fmaf(wgt, x.z, acc[4 * i + 2]);
+              acc[4 * i + 3] = fmaf(wgt, x.w, acc[4 * i + 3]);
+            }
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < kHalfCols / 8; ++i) {
+          uint4 w;
+          w.x = pack_bf16(acc[8 * i + 0], acc[8 * i + 1]);
+          w.y = pack_bf16(acc[8 * i + 2], acc[8 * i + 3]);
+          w.z = pack_bf16(acc[8 * i + 4], acc[8 * i + 5]);
+          w.w = pack_bf16(acc[8 * i + 6], acc[8 * i + 7]);
+          const int k = hf * (kHalfCols / 8) + i;
+          *reinterpret_cast<uint4*>(stage + (k >> 3) * C::kBoxBytes + row * 128 + (((k & 7) ^ (row & 7)) << 4)) = w;
+        }
+        if (hf == 0 && row_valid && p.LSE != nullptr) p.LSE[(long long)bh * p.Lq + q_row] = Lm;
+      }
     }
     fence_proxy_async_smem();
     named_bar_sync(1, 256);
-    if (warp == C::kSoftmaxWarp0 && lane == 0 && !*abort_flag) {
+    if (store && warp == C::kSoftmaxWarp0 && lane == 0 && !*abort_flag) {
 #pragma unroll
       for (int bx = 0; bx < C::kBoxes; ++bx)
         tma_store_4d(&p.o_map, base_u32 + C::kQOff + bx * C::kBoxBytes, bx * 64, q0, h, b);
@@ -1766,7 +984,7 @@ cudaError_t launch_kh_impl(const AttnParams& p, cudaStream_t s) {
     attr_set = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.n_qgroups, p.B * p.H, 1);
+  cfg.gridDim = dim3(p.n_qgroups, p.B * p.H, p.splits);
   cfg.blockDim = dim3(C::kThreads, 1, 1);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = s;
@@ -2272,21 +1490,13 @@ cudaError_t launch_wait_timeout_probe(unsigned long long timeout_ns, cudaStream_
 }
 
 cudaError_t launch_chunk_attention_kh(const AttnParams& p, cudaStream_t s) {
-  if (p.splits != 1) return cudaErrorInvalidValue;
+  if (p.splits < 1 || p.splits > 65535 || (p.splits > 1 && (p.ws_o == nullptr || p.ws_lse == nullptr ||
+                                                             p.ws_count == nullptr)))
+    return cudaErrorInvalidValue;
   if (p.f8mma) return (p.fp8 && !p.k_int8 && p.D == 128) ? launch_kh_impl<128, true, true>(p, s) : cudaErrorInvalidValue;
   if (p.fp8) return p.D == 128 ? launch_kh_impl<128, true>(p, s) : cudaErrorInvalidValue;
   if (p.D == 128) return launch_kh_impl<128, false>(p, s);
   if (p.D == 64) return launch_kh_impl<64, false>(p, s);
-  return cudaErrorInvalidValue;
-}
-
-cudaError_t launch_chunk_attention(const AttnParams& p, int q_tiles_per_cta, cudaStream_t s) {
-  if (p.fp8) {
-    if (p.D != 128) return cudaErrorInvalidValue;
-    return q_tiles_per_cta == 2 ? launch_impl<128, 2, true>(p, s) : launch_impl<128, 1, true>(p, s);
-  }
-  if (p.D == 128) return q_tiles_per_cta == 2 ? launch_impl<128, 2, false>(p, s) : launch_impl<128, 1, false>(p, s);
-  if (p.D == 64) return q_tiles_per_cta == 2 ? launch_impl<64, 2, false>(p, s) : launch_impl<64, 1, false>(p, s);
   return cudaErrorInvalidValue;
 }
 
@@ -2297,22 +1507,47 @@ cudaError_t launch_chunk_attention(const AttnParams& p, int q_tiles_per_cta, cud
 constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;  // 8 MiB
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+
 cudaError_t noalloc_scratch(void** ptr, size_t* bytes) {
   // In host code the array's name is only a stand-in: the device address is
-  // looked up once per device (with that device current) and cached.
+  // looked up with the device current and cached per device together with
+  // the context it belongs to.  A call under another context (the primary
+  // context was reset and re-created, which reloads the module) looks the
+  // address up again; a lock keeps concurrent first calls from racing.
   constexpr int kMaxDevices = 64;
-  static void* addr[kMaxDevices] = {};
+  struct Entry {
+    CUcontext ctx;
+    void* addr;
+  };
+  static std::mutex mu;
+  static Entry cache[kMaxDevices] = {};
+  static CtxGetCurrentFn get_ctx = nullptr;
+  static bool get_ctx_tried = false;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  if (addr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess) return e;
-    addr[dev] = p;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!get_ctx_tried) {
+    get_ctx_tried = true;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_ctx = reinterpret_cast<CtxGetCurrentFn>(fn);
   }
-  *ptr = addr[dev];
+  CUcontext ctx = nullptr;
+  if (cache[dev].addr != nullptr && get_ctx != nullptr && get_ctx(&ctx) != CUDA_SUCCESS) ctx = nullptr;
+  if (cache[dev].addr == nullptr || ctx != cache[dev].ctx) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);  // makes the device's context current
+    if (e != cudaSuccess) return e;
+    CUcontext now = nullptr;
+    if (get_ctx != nullptr && get_ctx(&now) != CUDA_SUCCESS) now = nullptr;
+    cache[dev] = Entry{now, p};
+  }
+  *ptr = cache[dev].addr;
   *bytes = kNoAllocScratchBytes;
   return cudaSuccess;
 }

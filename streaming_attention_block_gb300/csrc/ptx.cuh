@@ -272,6 +272,32 @@ __device__ __forceinline__ void s8x4_to_bf16x4(uint32_t w, uint32_t& lo, uint32_
   asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(lo) : "r"(__float_as_uint(f01.x)), "r"(__float_as_uint(f01.y)));
   asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(hi) : "r"(__float_as_uint(f23.x)), "r"(__float_as_uint(f23.y)));
 }
+// Two E4M3 codes (low byte = first) -> two fp16 values (exact: every E4M3
+// value, subnormals included, is a normal fp16 value); `codes`' first code in
+// the low half of the result.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t codes) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(codes));
+  return h2;
+}
+// Four INT8 codes (two's complement bytes, low byte first) -> four fp16
+// values, exactly: each byte, offset by 128, becomes the low mantissa byte of
+// the fp16 1024 + (n + 128) (spacing 1 there); subtracting 1152 leaves n.
+// `lo` holds codes 0, 1; `hi` codes 2, 3.
+__device__ __forceinline__ void s8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t t = w ^ 0x80808080u;
+  uint32_t a, b;
+  asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(a) : "r"(t), "r"(0x64646464u));
+  asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(b) : "r"(t), "r"(0x64646464u));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(0x64806480u));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(0x64806480u));
+}
+// pack two fp32 into fp16x2 (round to nearest even); `lo` in the low half
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
 // three-input maximum
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float r;
@@ -386,6 +412,10 @@ __device__ __forceinline__ uint64_t make_desc(uint32_t lo, uint32_t hi) {
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, uint32_t b_mn_major) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn_major << 16) | ((N >> 3) << 17) |
          ((M >> 4) << 24);
+}
+// kind::f16 with fp16 A/B (format 0) and fp32 accumulator
+__host__ __device__ constexpr uint32_t idesc_f16_f32(uint32_t M, uint32_t N, uint32_t b_mn_major) {
+  return (1u << 4) | (b_mn_major << 16) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 // kind::f8f6f4 with A and B E4M3 (format 0), fp32 accumulator
 __host__ __device__ constexpr uint32_t idesc_e4m3_f32(uint32_t M, uint32_t N, uint32_t b_mn_major) {

@@ -114,36 +114,25 @@ Geometry geometry(const sab_ring_desc& d) {
   return g;
 }
 
-// Query tiling shared by the workspace size and the launch.
-struct QTiling {
-  int n_qtiles, qt, n_qgroups, lq_pad;
-};
-QTiling qtiling(int Lq) {
-  QTiling t;
-  t.n_qtiles = (Lq + kTileM - 1) / kTileM;
-  t.qt = t.n_qtiles >= 2 ? 2 : 1;
-  t.n_qgroups = (t.n_qtiles + t.qt - 1) / t.qt;
-  t.lq_pad = t.n_qgroups * t.qt * kTileM;
-  return t;
-}
-
+// Split workspace: one arrival counter per (b, h, query tile), then the
+// fp32 partial rows [S][B*H][n_qtiles*128][D] and partial LSEs [S][B*H][n_qtiles*128].
 struct WsLayout {
   size_t count_off, o_off, lse_off, total;
 };
 WsLayout ws_layout(int BH, int Lq, int D, int splits) {
   WsLayout w{0, 0, 0, 0};
   if (splits <= 1) return w;
-  const QTiling t = qtiling(Lq);
+  const size_t n_qtiles = (size_t)(Lq + kTileM - 1) / kTileM;
+  const size_t lq_pad = n_qtiles * kTileM;
   w.count_off = 0;
-  w.o_off = align_up((size_t)BH * t.n_qgroups * sizeof(unsigned), kAlign);
-  w.lse_off = w.o_off + align_up((size_t)splits * BH * t.lq_pad * D * sizeof(float), kAlign);
-  w.total = w.lse_off + align_up((size_t)splits * BH * t.lq_pad * sizeof(float), kAlign);
+  w.o_off = align_up((size_t)BH * n_qtiles * sizeof(unsigned), kAlign);
+  w.lse_off = w.o_off + align_up((size_t)splits * BH * lq_pad * D * sizeof(float), kAlign);
+  w.total = w.lse_off + align_up((size_t)splits * BH * lq_pad * sizeof(float), kAlign);
   return w;
 }
 
 constexpr int kMaxSplits = 256;
 constexpr int kMaxAutoSplits = 8;
-constexpr int kMaxClusterSplits = 8;
 
 int device_sms() {
   static int n = 0;
@@ -158,14 +147,23 @@ int device_sms() {
   return n;
 }
 
-// num_splits == 0: fill the GPU with one wave of CTAs (one CTA per SM fits):
-// the largest S with (query CTAs x S) <= SMs, at least 1, at most 16 and at
-// most half the KV tiles.
-int auto_splits(int base_ctas, int kv_tiles) {
-  int s = device_sms() / std::max(1, base_ctas);
-  s = std::min(s, kMaxAutoSplits);
-  s = std::min(s, std::max(1, kv_tiles / 2));
-  return std::max(1, s);
+// num_splits == 0: the KV split count S (1..8) that minimises the modelled
+// time of one call: CTAs of one query tile x one split run one per SM, so the
+// call takes ceil(tiles x S / SMs) waves of ceil(kv_tiles / S) key tiles each,
+// plus about two key tiles' time for the log-sum-exp merge when S > 1.
+int auto_splits(long long q_tiles, int kv_tiles) {
+  const long long sms = device_sms();
+  int best = 1;
+  long long best_cost = ((q_tiles + sms - 1) / sms) * (long long)kv_tiles;
+  for (int s = 2; s <= kMaxAutoSplits && s <= kv_tiles / 2; ++s) {
+    const long long waves = (q_tiles * s + sms - 1) / sms;
+    const long long cost = waves * ((kv_tiles + s - 1) / s) + 2;
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  return best;
 }
 
 }  // namespace
@@ -356,36 +354,25 @@ size_t sab_chunk_attention_workspace(const sab_ring* ring, int num_splits) {
 }
 
 static sab_status launch_attention(AttnParams& p, int Lq, int splits, void* workspace, size_t ws_bytes,
-                                   void* stream, bool allow_cluster = true) {
+                                   void* stream) {
   if ((long long)p.B * p.H > 65535) return SAB_ERR_UNSUPPORTED;
-  // One query tile per CTA without a KV split (key-half kernel, no merge)
-  // whenever the caller asks for one split, or on auto once the query tiles
-  // alone occupy a quarter of the SMs: its per-SM rate is about twice the
-  // split kernel's, which more than pays for the idle SMs.
+  // One CTA per (128-query tile, (b, h), KV split), key-half softmax.  Splits
+  // (explicit, or chosen on auto to fill the SMs) merge their partial rows by
+  // log-sum-exp through the workspace.
   const int n_qtiles = (Lq + kTileM - 1) / kTileM;
-  if (splits == 1 || (splits == 0 && (long long)n_qtiles * p.B * p.H * 4 >= device_sms())) {
-    p.Lq = Lq;
-    p.n_qtiles = n_qtiles;
-    p.n_qgroups = n_qtiles;
-    p.lq_pad = n_qtiles * kTileM;
-    p.splits = 1;
-    p.cluster_merge = 0;
-    return launch_chunk_attention_kh(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SAB_OK
-                                                                                          : SAB_ERR_CUDA;
-  }
-  const QTiling t = qtiling(Lq);
   if (splits == 0) {
-    // block-causal: a CTA sees at most (window + 1) chunks plus one straddled tile
+    // block-causal: a query tile sees at most (window + 1) chunks plus one straddled tile
     const int tiles = p.mode == kModeStreaming
                           ? p.plan.total_tiles
                           : ((p.window + 1) * p.chunk_tokens + 2 * kTileN - 1) / kTileN;
-    splits = auto_splits(t.n_qgroups * p.B * p.H, tiles);
+    splits = auto_splits((long long)n_qtiles * p.B * p.H, tiles);
   }
   p.Lq = Lq;
-  p.n_qtiles = t.n_qtiles;
-  p.n_qgroups = t.n_qgroups;
-  p.lq_pad = t.lq_pad;
+  p.n_qtiles = n_qtiles;
+  p.n_qgroups = n_qtiles;
+  p.lq_pad = n_qtiles * kTileM;
   p.splits = splits;
+  p.cluster_merge = 0;
   if (splits > 1) {
     const WsLayout w = ws_layout(p.B * p.H, Lq, p.D, splits);
     if (workspace == nullptr || ws_bytes < w.total) return SAB_ERR_WORKSPACE;
@@ -395,18 +382,7 @@ static sab_status launch_attention(AttnParams& p, int Lq, int splits, void* work
     p.ws_o = reinterpret_cast<float*>(ws + w.o_off);
     p.ws_lse = reinterpret_cast<float*>(ws + w.lse_off);
   }
-  if ((long long)p.B * p.H > 65535) return SAB_ERR_UNSUPPORTED;
-  // 2..8 splits of a query group merge inside a thread-block cluster; more
-  // splits (or a device refusing the cluster) merge through the workspace.
-  p.cluster_merge = (allow_cluster && splits >= 2 && splits <= kMaxClusterSplits) ? 1 : 0;
-  if (p.cluster_merge && splits == 2 && t.qt == 2) p.cluster_merge = 2;
-  cudaError_t e = launch_chunk_attention(p, t.qt, static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess && p.cluster_merge) {
-    (void)cudaGetLastError();
-    p.cluster_merge = 0;
-    e = launch_chunk_attention(p, t.qt, static_cast<cudaStream_t>(stream));
-  }
-  return e == cudaSuccess ? SAB_OK : SAB_ERR_CUDA;
+  return launch_chunk_attention_kh(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SAB_OK : SAB_ERR_CUDA;
 }
 
 // Validation and key-set planning shared by both chunk-attention entry points.
@@ -640,7 +616,7 @@ sab_status sab_chunk_attention_noalloc(const sab_ring* ring, int layer, long lon
   if (w.total > cap) return SAB_ERR_WORKSPACE;
   // the arrival counters must start at zero; the partial rows are fully rewritten
   if (cudaMemsetAsync(scratch, 0, w.o_off, static_cast<cudaStream_t>(stream)) != cudaSuccess) return SAB_ERR_CUDA;
-  return launch_attention(p, ring->d.chunk_tokens, num_splits, scratch, cap, stream, /*allow_cluster=*/false);
+  return launch_attention(p, ring->d.chunk_tokens, num_splits, scratch, cap, stream);
 }
 
 size_t sab_block_causal_attention_workspace(int B, int L, int H, int D, int num_splits) {
@@ -777,6 +753,20 @@ sab_status sab_memory_prefix_attention_backward(const void* Q, const void* K, co
                                                 size_t ws_bytes, void* stream) {
   return attention_backward(Q, K, V, O, dO, LSE, B, L, H, D, mem_pad, mem_len, chunk_tokens, window, softmax_scale,
                             dQ, dK, dV, workspace, ws_bytes, stream);
+}
+
+sab_status sab_selftest_split_abort(const sab_ring* ring, int layer, long long chunk, const void* Q,
+                                    const void* K_cur, const void* V_cur, int window, int use_sink, int num_splits,
+                                    float softmax_scale, void* O, float* LSE, void* workspace, size_t ws_bytes,
+                                    int abort_split, void* stream) {
+  if (num_splits < 2 || num_splits > kMaxSplits) return SAB_ERR_INVALID_ARG;
+  if (abort_split < 0 || abort_split >= num_splits) return SAB_ERR_INVALID_ARG;
+  AttnParams p;
+  const sab_status st =
+      plan_chunk_attention(ring, layer, chunk, Q, K_cur, V_cur, window, use_sink, num_splits, softmax_scale, O, LSE, p);
+  if (st != SAB_OK) return st;
+  p.inject_abort = abort_split + 1;
+  return launch_attention(p, ring->d.chunk_tokens, num_splits, workspace, ws_bytes, stream);
 }
 
 sab_status sab_selftest_bounded_wait(unsigned long long timeout_ns, void* stream) {

@@ -132,6 +132,9 @@ struct AttnParams {
   // outputs
   uint16_t* O;            // bf16 [B, Lq, H, D]
   float* LSE;             // [B, H, Lq] or null
+  // failure-detection self-test: 0, or 1 + the index of a split that
+  // reports itself at the workspace merge as if one of its waits had given up
+  int inject_abort;
   // split workspace
   float* ws_o;            // [splits][B*H][lq_pad][D]
   float* ws_lse;          // [splits][B*H][lq_pad]
@@ -201,12 +204,10 @@ cudaError_t launch_counter_add(long long* counter, long long delta, cudaStream_t
 cudaError_t launch_qk_rope(const RopeParams& p, cudaStream_t s);
 cudaError_t launch_attention_backward(const BwdParams& p, cudaStream_t s);
 cudaError_t launch_wait_timeout_probe(unsigned long long timeout_ns, cudaStream_t s);
-cudaError_t launch_chunk_attention(const AttnParams& p, int q_tiles_per_cta, cudaStream_t s);
 // One query tile per CTA, key-half softmax warpgroups; unsplit KV only.
 cudaError_t launch_chunk_attention_kh(const AttnParams& p, cudaStream_t s);
 cudaError_t read_and_clear_device_error(unsigned int* value);
 // Device address and size of the library's own split-merge scratch.
 cudaError_t noalloc_scratch(void** ptr, size_t* bytes);
-int attention_q_tiles_per_cta(int D);
 
 }  // namespace sab

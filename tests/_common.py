@@ -14,8 +14,9 @@ from streaming_attention_block_gb300 import synth
 
 # Tolerances fixed by the acceptance criteria of the method: BF16 outputs
 # within max-abs 1e-2 and mean-abs 1e-3 of the fp64 oracle on the same
-# bf16-rounded inputs; FP8-KV outputs within max-abs 5e-2.  LSE (not covered
-# there) within 1e-3 (bf16) / 5e-2 (fp8): see the design doc's readings.
+# bf16-rounded inputs; FP8-KV outputs within max-abs 5e-2.  LSE, which the
+# criteria do not cover, within 1e-3 (bf16) / 5e-2 (fp8): the kernel
+# accumulates the row sum in fp32 and takes one logarithm.
 BF16_MAX, BF16_MEAN, BF16_LSE = 1e-2, 1e-3, 1e-3
 FP8_MAX, FP8_LSE = 5e-2, 5e-2
 
@@ -95,7 +96,7 @@ def run_stream(w, ring, check_chunks, rows=None, layers=1, splits=None, device="
     gen = synth.generator(w.seed)
     orings = [ListRing(w.R) for _ in range(layers)]
     orings_raw = [ListRing(w.R) for _ in range(layers)]  # un-quantised K/V (fp8 primary check)
-    ws = ring.workspace(splits) if splits > 1 else None
+    ws = ring.workspace(splits) if splits != 1 else None  # 0: the library's choice may split
     results = []
     if w.sink:
         sk, sv = synth.sink_kv(w, gen)

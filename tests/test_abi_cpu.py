@@ -62,8 +62,8 @@ def test_ring_bytes(lib):
 def test_workspace_sizes(lib):
     assert sab.block_causal_attention_workspace(2, 30720, 12, 128, 1) == 0
     n = sab.block_causal_attention_workspace(1, 405, 24, 128, 8)
-    # 405 rows -> 4 query tiles -> 2 CTAs of 2 tiles -> 512 padded rows
-    cnt = (24 * 2 * 4 + 255) // 256 * 256
+    # 405 rows -> 4 query tiles of 128 -> 512 padded rows; one counter per (b, h, tile)
+    cnt = (24 * 4 * 4 + 255) // 256 * 256
     o = (8 * 24 * 512 * 128 * 4 + 255) // 256 * 256
     lse = (8 * 24 * 512 * 4 + 255) // 256 * 256
     assert n == cnt + o + lse

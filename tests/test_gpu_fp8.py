@@ -2,9 +2,10 @@
 against the oracle's quantiser) and attention over the quantised ring.
 
 Attention is compared with the oracle run on the dequantised cache
-(x_hat = E4M3 value * scale, in fp64): max-abs 5e-2 plus one bf16 ulp of the
-reference value (2^-7 relative; outlier rows reach |O| > 16, where a bf16
-output's ulp alone is 0.125), and mean-abs 2e-3.
+(x_hat = E4M3 value * scale, in fp64): max-abs 5e-2 plus half a bf16 ulp of
+the reference value (2^-8 relative: outlier rows reach |O| > 16, where the
+single rounding of the fp32 result to bf16 alone may move it by up to 2^-8
+|O| = 0.0625), and mean-abs 2e-3.
 Against the un-quantised inputs the quantisation itself moves the outputs of
 these outlier-heavy inputs by up to ~1 (mean ~9e-3; measured with the oracle
 alone), so that comparison is checked only in the mean: the kernel may not
@@ -111,7 +112,7 @@ SMALL = [
 
 def _fp8(O, L, o_ref, l_ref, rows=None, what=""):
     return compare(O, L, o_ref, l_ref, rows=rows, max_tol=FP8_MAX, mean_tol=2e-3, lse_tol=FP8_LSE, what=what,
-                   rel_ulp=2.0 ** -7)
+                   rel_ulp=2.0 ** -8)
 
 
 def _raw(O, L, o_ref, l_ref, rows=None, what=""):
@@ -135,6 +136,16 @@ def test_fp8_long_window_sampled_rows():
     ring = _ring(w)
     res, _ = run_stream(w, ring, check_chunks={0, 19, 20, 40, 59}, rows=rows, on_check=_fp8)
     assert len(res) == 5
+    assert sab.get_last_device_error() == 0
+
+
+def test_fp8_long_window_auto_sampled_rows():
+    """The same stream through the library's own launch choice
+    (num_splits = 0, as the benchmark times it) at the wrap chunks."""
+    w = synth.workload("fp8_kv")
+    rows = np.concatenate([np.arange(0, 405, 7), [404]])
+    res, _ = run_stream(w, _ring(w), check_chunks={0, 19, 20, 39, 40, 59}, rows=rows, splits=0, on_check=_fp8)
+    assert len(res) == 6
     assert sab.get_last_device_error() == 0
 
 

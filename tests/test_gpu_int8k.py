@@ -81,7 +81,7 @@ CASES = [
 
 def _deq(O, L, o_ref, l_ref, rows=None, what=""):
     return compare(O, L, o_ref, l_ref, rows=rows, max_tol=FP8_MAX, mean_tol=2e-3, lse_tol=FP8_LSE, what=what,
-                   rel_ulp=2.0 ** -7)
+                   rel_ulp=2.0 ** -8)
 
 
 def _raw(O, L, o_ref, l_ref, rows=None, what=""):
@@ -97,9 +97,10 @@ def test_int8k_attention_small(name, w, splits):
 
 
 def test_int8k_long_window_sampled_rows():
-    """INT8-key cache at the sink + 20-slot ring shape, 60 chunks, library's split choice."""
+    """INT8-key cache at the sink + 20-slot ring shape, 60 chunks, library's
+    launch choice (as the benchmark times it), at the wrap chunks."""
     w = synth.workload("int8k_kv")
-    rows = np.concatenate([np.arange(0, 405, 9), [404]])
-    res, _ = run_stream(w, _ring(w), check_chunks={0, 19, 20, 40, 59}, rows=rows, splits=0, on_check=_deq)
-    assert len(res) == 5
+    rows = np.concatenate([np.arange(0, 405, 7), [404]])
+    res, _ = run_stream(w, _ring(w), check_chunks={0, 19, 20, 39, 40, 59}, rows=rows, splits=0, on_check=_deq)
+    assert len(res) == 6
     assert sab.get_last_device_error() == 0

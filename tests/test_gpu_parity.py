@@ -229,19 +229,39 @@ def test_long_sink_stream_sampled_rows():
     _check_device_error()
 
 
-def test_block_causal_full_size_sampled_rows():
-    """B2 x 30720 tokens, H12, D128, window 2: rows sampled in every chunk."""
+def test_long_sink_stream_auto_sampled_rows():
+    """The same stream through the library's own launch choice
+    (num_splits = 0, the configuration the benchmark times), checked at the
+    wrap chunks {0, 19, 20, 39, 40, 59}."""
+    w = synth.workload("long_sink")
+    ring = _ring(w)
+    rows = np.concatenate([np.arange(0, 405, 5), [383, 384, 404]])
+    res, _ = run_stream(w, ring, check_chunks={0, 19, 20, 39, 40, 59}, rows=rows, splits=0, on_check=compare)
+    assert len(res) == 6
+    _check_device_error()
+
+
+def test_block_causal_full_size_rows():
+    """B2 x 30720 tokens, H12, D128, window 2, every head: in batch 0 four
+    rows of every one of the 240 query tiles (its first and last row and two
+    drawn at random); in batch 1, 512 random rows of every chunk."""
     w = synth.workload("block_causal")
     q, k, v = synth.full_sequence_qkv(w, synth.generator(w.seed))
     L = w.seq_chunks * w.Lc
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
     O = torch.empty_like(qd)
     LSE = torch.empty((w.B, w.H, L), dtype=torch.float32, device="cuda")
-    sab.block_causal_attention(qd, kd, vd, w.Lc, w.W, 1, w.scale, O, LSE, None)
+    sab.block_causal_attention(qd, kd, vd, w.Lc, w.W, 0, w.scale, O, LSE, None)
     torch.cuda.synchronize()
     rng = np.random.default_rng(5)
-    rows = np.unique(np.concatenate([[c * w.Lc, c * w.Lc + w.Lc - 1] for c in range(w.seq_chunks)] +
-                                    [rng.integers(0, L, 24)]))
-    o_ref, l_ref = OA.block_causal_attention(f32(q), f32(k), f32(v), w.Lc, w.W, w.scale, rows=rows)
-    compare(O, LSE, o_ref, l_ref, rows=rows, what="block-causal full")
+    tiles = L // 128
+    rows0 = np.unique(np.concatenate([np.arange(tiles) * 128, np.arange(tiles) * 128 + 127,
+                                      np.arange(tiles) * 128 + rng.integers(1, 127, tiles),
+                                      np.arange(tiles) * 128 + rng.integers(1, 127, tiles)]))
+    assert len(np.unique(rows0 // 128)) == tiles
+    rows1 = np.unique(np.concatenate([c * w.Lc + rng.choice(w.Lc, 512, replace=False) for c in range(w.seq_chunks)]))
+    qf, kf, vf = f32(q), f32(k), f32(v)
+    for b, rows in ((0, rows0), (1, rows1)):
+        o_ref, l_ref = OA.block_causal_attention(qf, kf, vf, w.Lc, w.W, w.scale, rows=rows, batches=[b])
+        compare(O[b:b + 1], LSE[b:b + 1], o_ref, l_ref, rows=rows, what=f"block-causal full, batch {b}")
     _check_device_error()
