@@ -252,11 +252,12 @@ struct KhCfg {
   static constexpr int kBarRawFull = kBarKVEmpty + kStages;   // [kStages] FP8 codes landed
   static constexpr int kBarSFull = kBarRawFull + kStages;     // [2 buffers]
   static constexpr int kBarPFull = kBarSFull + 2;             // [2 buffers][2 halves]
-  static constexpr int kBarPVDone = kBarPFull + 4;            // [2 halves] one phase per tile
-  static constexpr int kBarOFinal = kBarPVDone + 2;           // every MMA complete
+  static constexpr int kBarPVLast = kBarPFull + 4;            // PV of the last tile but one complete
+  static constexpr int kBarOFinal = kBarPVLast + 1;           // every MMA complete
   static constexpr int kBarDrain = kBarOFinal + 1;
   static constexpr int kBarQ8 = kBarDrain + 1;                // 8-bit cache: converted Q written
-  static constexpr int kNumBars = kBarQ8 + 1;
+  static constexpr int kBarMerge = kBarQ8 + 1;                // split merge: partial tiles landed
+  static constexpr int kNumBars = kBarMerge + 1;
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
   static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;
   static constexpr int kConvThreads = 64;
@@ -307,11 +308,12 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
       mbar_init(bar(C::kBarSFull + i), 1);
       mbar_init(bar(C::kBarPFull + 2 * i), 128);
       mbar_init(bar(C::kBarPFull + 2 * i + 1), 128);
-      mbar_init(bar(C::kBarPVDone + i), 1);
     }
+    mbar_init(bar(C::kBarPVLast), 1);
     mbar_init(bar(C::kBarOFinal), 1);
     mbar_init(bar(C::kBarDrain), 1);
     mbar_init(bar(C::kBarQ8), 256);
+    mbar_init(bar(C::kBarMerge), 1);
     misc[1] = 0;
     misc[2] = 0;
     fence_mbar_init();
@@ -505,13 +507,14 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
       tc_fence_after();
       pr = false;
       issue_pv(j, 0, pbar(j, 1), ppar(j), pr);
-      mma_commit_e(bar(C::kBarPVDone + 0));
       if (!(ok = wait_probed(pbar(j, 1), ppar(j), pr, 3))) break;
       tc_fence_after();
       pr = false;
       if (j + 2 < n_tiles) issue_pv(j, 1, kbar(j + 2), kpar(j + 2), pr);
       else issue_pv(j, 1, 0u, 0u, pr);
-      mma_commit_e(bar(C::kBarPVDone + 1));
+      // the softmax of the last tile learns from this that O holds every
+      // earlier tile (other tiles learn it from the next tile's S)
+      if (j + 2 == n_tiles) mma_commit_e(bar(C::kBarPVLast));
       // stage j + 1 (K(j + 1), V(j)) is free once PV(j) completes: S(j + 1)
       // was issued before it
       mma_commit_e(bar(C::kBarKVEmpty + (j + 1) % C::kStages));
@@ -663,6 +666,7 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
       const uint32_t tS = tSh + (uint32_t)(j & 1) * 128u;
       uint32_t s0[32], s1[32];
       tmem_ld32(tS + 0, s0);
+      tmem_ld32(tS + 32, s1);  // both loads in flight while the key range is worked out
       int lo, hi;
       int tile_row0 = 0;
       const int g = first + j;
@@ -774,11 +778,9 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
       uint32_t pk[32];
       float2 psa = make_float2(0.f, 0.f), psb = make_float2(0.f, 0.f);
       tmem_wait_ld();
-      tmem_ld32(tS + 32, s1);
       prep(s0, 0);
       const float mx0 = max32(s0);
       exps32(s0, 0, xa, straddle ? -mb0 : d0 - mb0, pk, psa);
-      tmem_wait_ld();
       prep(s1, 32);
       const float mx1 = max32(s1);
       exps32(s1, 32, xa, straddle ? -mb0 : d0 - mb0, pk + (F8MMA ? 8 : 16), psb);
@@ -793,9 +795,12 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
           m_run = m_new;
         }
         if (j > 0) {
-          // O_hf holds PV_hf(j-1) only once that MMA group has completed
-          ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarPVDone + hf), (uint32_t)(j - 1) & 1u, abort_flag,
-                                                    8 + hf));
+          // O_hf holds PV_hf(j-1) only once that MMA group has completed:
+          // S(j+1) was issued after it (one tensor pipe, in order), and for
+          // the last tile a commit follows PV(j-1) itself
+          const uint32_t wb = j + 1 < n_tiles ? bar(C::kBarSFull + ((j + 1) & 1)) : bar(C::kBarPVLast);
+          const uint32_t wp = j + 1 < n_tiles ? (uint32_t)((j + 1) >> 1) & 1u : 0u;
+          ok = __all_sync(0xffffffffu, wait_bounded(wb, wp, abort_flag, 8 + hf));
           if (!ok) break;
           tc_fence_after();
 #pragma unroll 1
@@ -874,17 +879,20 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
         }
         if (hf == 0 && row_valid && p.LSE != nullptr) p.LSE[(long long)bh * p.Lq + q_row] = lse;
       } else {
-        // this split's normalised partial row (fp32) and its LSE go to the
-        // workspace (rows past the sequence too: the pitch is whole tiles)
-        const long long prow = ((long long)split * p.B * p.H + bh) * p.lq_pad + q_row;
-        float4* dst = reinterpret_cast<float4*>(p.ws_o + prow * D + hf * kHalfCols);
+        // this split's normalised partial tile (fp32) and its LSEs go to the
+        // workspace: a tile is 128 x D floats stored as [D / 4][128 rows]
+        // float4s, so the 32 rows of a warp write 512 contiguous bytes
+        const long long tile = ((long long)split * p.B * p.H + bh) * p.n_qtiles + blockIdx.x;
+        float4* dst = reinterpret_cast<float4*>(p.ws_o) + tile * (kTileM * D / 4) + hf * (kHalfCols / 4) * kTileM + row;
 #pragma unroll
         for (int i = 0; i < kHalfCols / 4; ++i)
-          __stcg(dst + i, make_float4(fmaf(__uint_as_float(oa[4 * i]), sc0, __uint_as_float(ob[4 * i]) * sc1),
-                                      fmaf(__uint_as_float(oa[4 * i + 1]), sc0, __uint_as_float(ob[4 * i + 1]) * sc1),
-                                      fmaf(__uint_as_float(oa[4 * i + 2]), sc0, __uint_as_float(ob[4 * i + 2]) * sc1),
-                                      fmaf(__uint_as_float(oa[4 * i + 3]), sc0, __uint_as_float(ob[4 * i + 3]) * sc1)));
-        if (hf == 0) __stcg(p.ws_lse + prow, lse);
+          __stcg(dst + i * kTileM,
+                 make_float4(fmaf(__uint_as_float(oa[4 * i]), sc0, __uint_as_float(ob[4 * i]) * sc1),
+                             fmaf(__uint_as_float(oa[4 * i + 1]), sc0, __uint_as_float(ob[4 * i + 1]) * sc1),
+                             fmaf(__uint_as_float(oa[4 * i + 2]), sc0, __uint_as_float(ob[4 * i + 2]) * sc1),
+                             fmaf(__uint_as_float(oa[4 * i + 3]), sc0, __uint_as_float(ob[4 * i + 3]) * sc1)));
+        if (hf == 0) __stcg(p.ws_lse + tile * kTileM + row, lse);
+        fence_proxy_async_global();  // the merging CTA reads the partials with bulk copies
       }
     }
     bool store = p.splits == 1;
@@ -897,10 +905,11 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
       // the counter (the workspace stays usable after a reported timeout) and,
       // if no split aborted, merges the partial rows and stores the tile.
       __threadfence();
+      fence_proxy_async_smem();  // the operand region may be overwritten by bulk copies below
       named_bar_sync(1, 256);
       volatile uint32_t* ticket = misc + 2;
       if (warp == C::kSoftmaxWarp0 && lane == 0) {
-        unsigned* cnt = &p.ws_count[(long long)bh * p.n_qgroups + blockIdx.x];
+        unsigned* cnt = &p.ws_count[(long long)bh * p.n_qtiles + blockIdx.x];
         if (split + 1 == p.inject_abort) {  // self-test: behave as a split whose wait gave up
           atomicOr(&g_sab_error_word, 1u << 29);
           *abort_flag = 1;
@@ -915,33 +924,78 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
       store = *ticket == 1u;
       if (store) {
         __threadfence();
-        const long long stride = (long long)p.B * p.H * p.lq_pad;
-        const long long r0 = (long long)bh * p.lq_pad + q_row;
+        fence_proxy_async_global();
+        // partial tiles of this query tile: split sp at tile index t0 + sp * tstride
+        const long long tstride = (long long)p.B * p.H * p.n_qtiles;
+        const long long t0 = (long long)bh * p.n_qtiles + blockIdx.x;
+        auto lse_of = [&](int sp) { return __ldcg(p.ws_lse + (t0 + sp * tstride) * kTileM + row); };
         float Mx = -INFINITY;
-        for (int sp = 0; sp < p.splits; ++sp) Mx = fmaxf(Mx, __ldcg(p.ws_lse + sp * stride + r0));
+        for (int s8 = 0; s8 < p.splits; s8 += 8) {  // eight loads in flight
+          float l8[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) l8[k] = s8 + k < p.splits ? lse_of(s8 + k) : -INFINITY;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) Mx = fmaxf(Mx, l8[k]);
+        }
         float tot = 0.f;
-        if (Mx != -INFINITY)
-          for (int sp = 0; sp < p.splits; ++sp) tot += ex2((__ldcg(p.ws_lse + sp * stride + r0) - Mx) * kLog2e);
+        if (Mx != -INFINITY) {
+          for (int s8 = 0; s8 < p.splits; s8 += 8) {
+            float l8[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) l8[k] = s8 + k < p.splits ? lse_of(s8 + k) : -INFINITY;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) tot += l8[k] == -INFINITY ? 0.f : ex2((l8[k] - Mx) * kLog2e);
+          }
+        }
         const float Lm = (Mx == -INFINITY) ? -INFINITY : Mx + __logf(tot);
         float acc[kHalfCols];
 #pragma unroll
         for (int c = 0; c < kHalfCols; ++c) acc[c] = 0.f;
-        if (Lm != -INFINITY) {
-#pragma unroll 1
-          for (int sp = 0; sp < p.splits; ++sp) {
-            const float ls = __ldcg(p.ws_lse + sp * stride + r0);
-            if (ls == -INFINITY) continue;
-            const float wgt = ex2((ls - Lm) * kLog2e);
-            const float4* src = reinterpret_cast<const float4*>(p.ws_o + (sp * stride + r0) * D + hf * kHalfCols);
+        // The partial tiles come into the (dead) K/V stage region by bulk
+        // copies, as many at a time as it holds; each thread then reads its
+        // row's half from shared memory (a warp's 32 rows: 512 contiguous bytes).
+        constexpr uint32_t kPartBytes = kTileM * D * 4;
+        constexpr int kBatch = (int)((2u * C::kStages * C::kKVTileBytes) / kPartBytes);
+        static_assert(kBatch >= 1, "one partial tile fits in the operand region");
+        const bool leader = warp == C::kSoftmaxWarp0 && lane == 0;
+        bool got = true;
+        int batch = 0;
+        for (int b0 = 0; got && b0 < p.splits; b0 += kBatch, ++batch) {
+          const int nb = min(kBatch, p.splits - b0);
+          if (leader) {
+            mbar_arrive_expect_tx(bar(C::kBarMerge), (uint32_t)nb * kPartBytes);
+            for (int k = 0; k < nb; ++k)
+              bulk_copy_g2s(base_u32 + C::kKOff + (uint32_t)k * kPartBytes,
+                            reinterpret_cast<const float4*>(p.ws_o) + (t0 + (b0 + k) * tstride) * (kTileM * D / 4),
+                            kPartBytes, bar(C::kBarMerge));
+          }
+          float lb[kBatch];
 #pragma unroll
-            for (int i = 0; i < kHalfCols / 4; ++i) {
-              const float4 x = __ldcg(src + i);
-              acc[4 * i] = fmaf(wgt, x.x, acc[4 * i]);
-              acc[4 * i + 1] = fmaf(wgt, x.y, acc[4 * i + 1]);
-              acc[4 * i + 2] = fmaf(wgt, x.z, acc[4 * i + 2]);
-              acc[4 * i + 3] = fmaf(wgt, x.w, acc[4 * i + 3]);
+          for (int k = 0; k < kBatch; ++k) lb[k] = k < nb ? lse_of(b0 + k) : -INFINITY;
+          got = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarMerge), (uint32_t)batch & 1u, abort_flag, 13));
+          if (got) {
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+              if (k >= nb || lb[k] == -INFINITY || Lm == -INFINITY) continue;
+              const float wgt = ex2((lb[k] - Lm) * kLog2e);
+              const float4* src = reinterpret_cast<const float4*>(base + C::kKOff + k * kPartBytes) +
+                                  hf * (kHalfCols / 4) * kTileM + row;
+#pragma unroll
+              for (int i = 0; i < kHalfCols / 4; ++i) {
+                const float4 x = src[i * kTileM];
+                acc[4 * i] = fmaf(wgt, x.x, acc[4 * i]);
+                acc[4 * i + 1] = fmaf(wgt, x.y, acc[4 * i + 1]);
+                acc[4 * i + 2] = fmaf(wgt, x.z, acc[4 * i + 2]);
+                acc[4 * i + 3] = fmaf(wgt, x.w, acc[4 * i + 3]);
+              }
             }
           }
+          named_bar_sync(1, 256);  // the batch is read before the next one lands
+        }
+        if (!got) {
+          // a bulk copy did not land in time: drain it before the CTA exits
+          if (leader) wait_drain(bar(C::kBarMerge), (uint32_t)(batch - 1) & 1u);
+          store = false;
         }
 #pragma unroll
         for (int i = 0; i < kHalfCols / 8; ++i) {
@@ -984,7 +1038,7 @@ cudaError_t launch_kh_impl(const AttnParams& p, cudaStream_t s) {
     attr_set = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.n_qgroups, p.B * p.H, p.splits);
+  cfg.gridDim = dim3(p.n_qtiles, p.B * p.H, p.splits);
   cfg.blockDim = dim3(C::kThreads, 1, 1);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = s;

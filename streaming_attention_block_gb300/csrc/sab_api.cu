@@ -148,17 +148,21 @@ int device_sms() {
 }
 
 // num_splits == 0: the KV split count S (1..8) that minimises the modelled
-// time of one call: CTAs of one query tile x one split run one per SM, so the
-// call takes ceil(tiles x S / SMs) waves of ceil(kv_tiles / S) key tiles each,
-// plus about two key tiles' time for the log-sum-exp merge when S > 1.
+// time of one call, in key-tile periods.  CTAs (one query tile x one split)
+// run one per SM, so the call takes ceil(tiles * S / SMs) waves of
+// ceil(kv_tiles / S) key tiles each; every wave after the first also pays a
+// CTA's set-up and epilogue (about 5 key tiles: the first wave's overlaps the
+// previous kernel), and S > 1 adds the partial-tile write and the merge (about
+// 1 + 0.4 S key tiles).
 int auto_splits(long long q_tiles, int kv_tiles) {
   const long long sms = device_sms();
   int best = 1;
-  long long best_cost = ((q_tiles + sms - 1) / sms) * (long long)kv_tiles;
-  for (int s = 2; s <= kMaxAutoSplits && s <= kv_tiles / 2; ++s) {
+  double best_cost = 0.0;
+  for (int s = 1; s <= kMaxAutoSplits && (s == 1 || s <= kv_tiles / 2); ++s) {
     const long long waves = (q_tiles * s + sms - 1) / sms;
-    const long long cost = waves * ((kv_tiles + s - 1) / s) + 2;
-    if (cost < best_cost) {
+    double cost = (double)waves * ((kv_tiles + s - 1) / s) + 5.0 * (double)(waves - 1);
+    if (s > 1) cost += 1.0 + 0.4 * s;
+    if (s == 1 || cost < best_cost) {
       best_cost = cost;
       best = s;
     }
@@ -369,10 +373,7 @@ static sab_status launch_attention(AttnParams& p, int Lq, int splits, void* work
   }
   p.Lq = Lq;
   p.n_qtiles = n_qtiles;
-  p.n_qgroups = n_qtiles;
-  p.lq_pad = n_qtiles * kTileM;
   p.splits = splits;
-  p.cluster_merge = 0;
   if (splits > 1) {
     const WsLayout w = ws_layout(p.B * p.H, Lq, p.D, splits);
     if (workspace == nullptr || ws_bytes < w.total) return SAB_ERR_WORKSPACE;

@@ -109,14 +109,7 @@ struct AttnParams {
   int B, H, D;
   int Lq;                 // query rows per (b, h)
   int n_qtiles;           // ceil(Lq / 128)
-  int n_qgroups;          // CTAs along the query axis (q tiles per CTA: 1 or 2)
-  int lq_pad;             // n_qgroups * tiles per CTA * 128 (workspace row pitch)
   int splits;
-  int cluster_merge;      // 0: splits merge through the workspace; 1: the splits
-                          // of a query group form a thread-block cluster and
-                          // merge through distributed shared memory; 2: two
-                          // splits of a two-tile group merge as a CTA pair
-                          // (one bulk copy each way)
   float scale_log2;       // softmax_scale * log2(e)
   // streaming: key runs planned on the host, or (d_chunk != null: graph mode)
   // planned by every CTA from the chunk index in device memory
@@ -135,10 +128,10 @@ struct AttnParams {
   // failure-detection self-test: 0, or 1 + the index of a split that
   // reports itself at the workspace merge as if one of its waits had given up
   int inject_abort;
-  // split workspace
-  float* ws_o;            // [splits][B*H][lq_pad][D]
-  float* ws_lse;          // [splits][B*H][lq_pad]
-  unsigned int* ws_count; // [B*H][n_qgroups]
+  // split workspace: tile t = (split * B*H + bh) * n_qtiles + query tile
+  float* ws_o;            // [tiles][D / 4][128 rows] float4: normalised partial rows
+  float* ws_lse;          // [tiles][128 rows]: partial LSEs
+  unsigned int* ws_count; // [B*H][n_qtiles] arrival counters
 };
 
 // FP8 append: per (b, h) block of one chunk.
