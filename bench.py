@@ -582,6 +582,38 @@ def config_records(peaks, src, stream):
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(gbs / peaks["hbm_gbs"], 4), "peak_source": f"hbm copy, {src}"},
         "bytes_per_call": nbytes}
+    del sets, qouts, ring
+
+    # ring append alone: BF16 copy (Wan-1.3B chunk) and E4M3 absmax
+    # quantisation (long-window chunk); 16 layers and 16 input sets rotate, so
+    # reads and writes both leave L2
+    for name, wname, kvd in (("ring_append_bf16", "wan13b", sab.KV_BF16),
+                             ("ring_append_fp8", "fp8_kv", sab.KV_FP8_E4M3)):
+        w = synth.workload(wname)
+        shape = (w.B, w.Lc, w.H, w.D)
+        sets = [tuple(synth.randn_bf16(g, shape, "cuda") for _ in range(2)) for _ in range(nsets)]
+        ring = sab.KVRing(nsets, w.B, w.H, w.D, w.Lc, w.R, has_sink=w.sink, kv_dtype=kvd)
+        chunk = [0] * nsets
+
+        def appender(i):
+            def f():
+                k_, v_ = sets[i]
+                sab.kv_ring_append(ring.handle, i, chunk[i], k_, v_, stream)
+                chunk[i] += 1
+            return f
+
+        us = _group_us([appender(i) for i in range(nsets)], 32, 5, stream)
+        elems = 2 * w.B * w.Lc * w.H * w.D
+        nbytes = elems * 2 + elems * (2 if kvd == sab.KV_BF16 else 1)  # read bf16 K, V; write the ring's codes
+        gbs = nbytes / (us * 1e-6) / 1e9
+        out[name] = {
+            "workload": f"B{w.B} H{w.H} D{w.D}, {w.Lc} tokens/chunk, token-major K, V -> head-major ring slot"
+                        + ("" if kvd == sab.KV_BF16 else ", E4M3 codes + per-(b, h) scales"),
+            "us_per_call": round(us, 2),
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(gbs / peaks["hbm_gbs"], 4), "peak_source": f"hbm copy, {src}"},
+            "bytes_per_call": nbytes}
+        del sets, ring
     assert sab.get_last_device_error(stream) == 0
     return out
 

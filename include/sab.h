@@ -63,7 +63,8 @@ typedef enum {
   SAB_ERR_OUT_OF_RANGE = 3,  /* chunk not held by the ring / bad chunk order  */
   SAB_ERR_WORKSPACE = 4,     /* workspace missing or smaller than required    */
   SAB_ERR_CUDA = 5,          /* a CUDA runtime/driver call failed             */
-  SAB_ERR_TIMEOUT = 6        /* a device-side pipeline wait gave up (see sab_get_last_device_error) */
+  SAB_ERR_TIMEOUT = 6,       /* a device-side pipeline wait gave up (see sab_get_last_device_error) */
+  SAB_ERR_BOUNDS = 7         /* debug builds: a device-side index check failed (ditto) */
 } sab_status;
 
 /*
@@ -425,10 +426,44 @@ sab_status sab_block_causal_attention(const void* Q, const void* K, const void* 
 
 /*
  * Synchronise `stream`, then report and clear the device error word that
- * bounded pipeline waits set when they give up (SAB_ERR_TIMEOUT), or
- * SAB_ERR_CUDA if the stream itself reports an error.  SAB_OK otherwise.
+ * bounded pipeline waits set when they give up (SAB_ERR_TIMEOUT) and that the
+ * index checks of a debug build set (SAB_ERR_BOUNDS, reported first when both
+ * are recorded), or SAB_ERR_CUDA if the stream itself reports an error.
+ * SAB_OK otherwise.
  */
 sab_status sab_get_last_device_error(void* stream);
+
+/*
+ * Debug builds (no counterpart in the method).  A library compiled with
+ * -DSAB_DEBUG_BOUNDS (libsab_debug.so) checks, in every kernel before it
+ * issues a copy or a store, each global index it is about to form: the ring
+ * slot rows of an append (inside the (batch, head) block, on a slot
+ * boundary), the scale entry of an 8-bit append, every key run of an
+ * attention CTA against the rows of its source, the FP8 scale entries it
+ * reads, its workspace tile and counter, and the row ranges of the backward
+ * tiles.  The checks are uniform over a CTA: a CTA that fails one records
+ * SAB_ERR_BOUNDS in the device error word and leaves through the same path as
+ * a CTA whose wait gave up (no copy, no store; split-merge counters still
+ * return to zero).  Nothing traps.  Release builds compile the checks out.
+ *
+ * sab_debug_bounds_enabled: 1 in a debug build, 0 otherwise.
+ * sab_debug_inject_bounds_error: makes the next launch of the named kind
+ * carry an index past its buffer, so that its device check has to catch it
+ * (the forged index points inside memory the caller owns in the forms the
+ * self-test uses: one slot past the ring rows for an append, one slot past
+ * the ring for an attention key run, one tile fewer than the workspace holds
+ * for a split tile).  what: SAB_DEBUG_INJECT_APPEND_SLOT,
+ * SAB_DEBUG_INJECT_KEY_ROW or SAB_DEBUG_INJECT_WS_TILE; 0 cancels a pending
+ * injection.  Host-side only: nothing is launched.  Errors: UNSUPPORTED in a
+ * release build, INVALID_ARG for another `what`.
+ */
+enum {
+  SAB_DEBUG_INJECT_APPEND_SLOT = 1, /* next ring append (BF16 or 8-bit) */
+  SAB_DEBUG_INJECT_KEY_ROW = 2,     /* next streaming chunk attention */
+  SAB_DEBUG_INJECT_WS_TILE = 3      /* next split (num_splits >= 2) chunk attention */
+};
+int sab_debug_bounds_enabled(void);
+sab_status sab_debug_inject_bounds_error(int what);
 
 /*
  * Self-test of the device-side failure detection (no counterpart in the

@@ -8,6 +8,12 @@ is missing.
 """
 
 from ._abi import (  # noqa: F401
+    DEBUG_INJECT_APPEND_SLOT,
+    DEBUG_INJECT_KEY_ROW,
+    DEBUG_INJECT_WS_TILE,
+    ERR_BOUNDS,
+    ERR_TIMEOUT,
+    GUARD_BYTE,
     KV_BF16,
     KV_FP8_E4M3,
     KV_INT8K_FP8V,
@@ -24,6 +30,10 @@ from ._abi import (  # noqa: F401
     chunk_attention_fp8mma,
     chunk_attention_noalloc,
     chunk_counter_add,
+    debug_bounds_enabled,
+    debug_inject_bounds_error,
+    guard_watch_begin,
+    guard_watch_end,
     chunk_attention_workspace,
     get_last_device_error,
     kv_ring_append,

@@ -17,8 +17,14 @@ KV_INT8K_FP8V = 2
 
 _STATUS = {
     0: "SAB_OK", 1: "SAB_ERR_INVALID_ARG", 2: "SAB_ERR_UNSUPPORTED", 3: "SAB_ERR_OUT_OF_RANGE",
-    4: "SAB_ERR_WORKSPACE", 5: "SAB_ERR_CUDA", 6: "SAB_ERR_TIMEOUT",
+    4: "SAB_ERR_WORKSPACE", 5: "SAB_ERR_CUDA", 6: "SAB_ERR_TIMEOUT", 7: "SAB_ERR_BOUNDS",
 }
+ERR_TIMEOUT = 6
+ERR_BOUNDS = 7
+# sab_debug_inject_bounds_error kinds
+DEBUG_INJECT_APPEND_SLOT = 1
+DEBUG_INJECT_KEY_ROW = 2
+DEBUG_INJECT_WS_TILE = 3
 
 
 class SabError(RuntimeError):
@@ -72,6 +78,8 @@ def library() -> ctypes.CDLL:
         "sab_block_causal_attention_workspace": (SZ, [I, I, I, I, I]),
         "sab_block_causal_attention": (I, [P, P, P, I, I, I, I, I, I, I, F, P, P, P, SZ, P]),
         "sab_get_last_device_error": (I, [P]),
+        "sab_debug_bounds_enabled": (I, []),
+        "sab_debug_inject_bounds_error": (I, [I]),
         "sab_selftest_bounded_wait": (I, [ctypes.c_ulonglong, P]),
         "sab_selftest_split_abort": (I, [P, I, LL, P, P, P, I, I, I, F, P, P, P, SZ, I, P]),
         "sab_qk_norm_rope": (I, [P, I, LL, P, P, P, P, P, P, P, P, P, I, P]),
@@ -327,6 +335,59 @@ def get_last_device_error(stream=None) -> int:
     return int(library().sab_get_last_device_error(_stream(stream)))
 
 
+def debug_bounds_enabled() -> bool:
+    """True when the loaded library is the debug build (device index checks)."""
+    return bool(library().sab_debug_bounds_enabled())
+
+
+def debug_inject_bounds_error(what: int):
+    """sab_debug_inject_bounds_error (debug builds only)."""
+    _check(library().sab_debug_inject_bounds_error(int(what)), "debug_inject_bounds_error")
+
+
+# Canary bands: a device buffer can be allocated between two bands of
+# GUARD_BYTE that no call may write.  While a watch is open every guarded
+# allocation is recorded, and closing the watch counts the band bytes that
+# changed (buffer overruns or underruns by any kernel that wrote near it).
+GUARD_BYTE = 0xA5
+_guard_watch = None
+
+
+def _guarded(nbytes: int, guard: int, device, zero: bool = False):
+    """(storage, view): ``view`` is ``nbytes`` of 256-byte-aligned device
+    memory, with ``guard`` bytes (rounded up to 256) of canaries on each side."""
+    g = (int(guard) + 255) // 256 * 256
+    mem = torch.empty(nbytes + 2 * g + 256, dtype=torch.uint8, device=device)
+    off = (-mem.data_ptr()) % 256 + g
+    buf = mem[off:off + nbytes]
+    if zero:
+        buf.zero_()
+    if g:
+        mem[:off].fill_(GUARD_BYTE)
+        mem[off + nbytes:].fill_(GUARD_BYTE)
+        if _guard_watch is not None:
+            _guard_watch.append((mem, ((0, off), (off + nbytes, mem.numel()))))
+    return mem, buf
+
+
+def guard_watch_begin():
+    """Start recording guarded allocations."""
+    global _guard_watch
+    _guard_watch = []
+
+
+def guard_watch_end() -> int:
+    """Stop recording; return how many canary bytes of the recorded
+    allocations no longer hold GUARD_BYTE (0: no call wrote outside them)."""
+    global _guard_watch
+    watched, _guard_watch = _guard_watch or [], None
+    bad = 0
+    for mem, bands in watched:
+        for lo, hi in bands:
+            bad += int((mem[lo:hi] != GUARD_BYTE).sum().item())
+    return bad
+
+
 def selftest_bounded_wait(timeout_ns: int, stream=None):
     """sab_selftest_bounded_wait: a device wait that nothing completes gives up
     after timeout_ns; read the result with get_last_device_error."""
@@ -362,18 +423,23 @@ def qk_norm_rope(handle, layer: int, chunk: int, Q, K, V, rope: RopeDesc, Q_out,
 
 
 class KVRing:
-    """A ring KV cache on torch-owned device memory (memory + handle)."""
+    """A ring KV cache on torch-owned device memory (memory + handle).
+
+    ``guard_bytes`` (default ``KVRing.default_guard_bytes``, 0) puts canary
+    bands of that many bytes around the ring memory and around every
+    workspace ``workspace()`` allocates (see ``guard_watch_begin``)."""
+
+    default_guard_bytes = 0
 
     def __init__(self, num_layers, batch, heads, head_dim, chunk_tokens, ring_slots, has_sink=False,
-                 kv_dtype=KV_BF16, device="cuda", stream=None):
+                 kv_dtype=KV_BF16, device="cuda", stream=None, guard_bytes=None):
         self.desc = RingDesc(num_layers, batch, heads, head_dim, chunk_tokens, ring_slots, int(bool(has_sink)),
                              int(kv_dtype))
         nbytes = kv_ring_bytes(self.desc)
         if nbytes == 0:
             raise SabError(1, "invalid ring shape")
-        self.mem = torch.empty(nbytes + 256, dtype=torch.uint8, device=device)
-        off = (-self.mem.data_ptr()) % 256
-        self.buf = self.mem[off:off + nbytes]
+        self.guard_bytes = self.default_guard_bytes if guard_bytes is None else int(guard_bytes)
+        self.mem, self.buf = _guarded(nbytes, self.guard_bytes, device)
         self.handle = kv_ring_create(self.desc, self.buf, stream)
         self.rows = (self.desc.has_sink + ring_slots) * chunk_tokens
 
@@ -416,7 +482,7 @@ class KVRing:
         n = chunk_attention_workspace(self.handle, num_splits)
         if n == 0:
             return None
-        return torch.zeros(n, dtype=torch.uint8, device=self.buf.device)
+        return _guarded(n, self.guard_bytes, self.buf.device, zero=True)[1]
 
     def attention(self, layer, chunk, Q, K_cur=None, V_cur=None, window=2, use_sink=False, num_splits=1,
                   softmax_scale=None, O=None, LSE=None, workspace=None, stream=None):

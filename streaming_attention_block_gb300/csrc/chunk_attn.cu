@@ -48,6 +48,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows by > 2^8
 constexpr float kRescaleThresholdF8 = 4.0f;  // E4M3 P: by > 2^4 (P' = P * 2^4 * vs / vs_ref <= 2^8)
+constexpr int kScaleTab = 64;  // per-chunk coefficient table entries (1 KB of shared memory)
 
 __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
@@ -140,6 +141,30 @@ __device__ __forceinline__ void kv_range(const AttnParams& p, const KeyPlan& kp,
   const long long e = (long long)total * (split + 1) / p.splits;
   first = base + (int)a;
   count = (int)(e - a);
+}
+
+// Debug builds: every global index a forward CTA will form, checked before it
+// issues any copy or store.  Uniform over the CTA (it depends on the launch
+// parameters, the block index and the key plan only).
+__device__ bool attn_indices_ok(const AttnParams& p, const KeyPlan& kp, int b, int q0, int split, int first,
+                                int n_tiles) {
+  if (b >= p.B || q0 >= p.Lq || (int)blockIdx.x >= p.n_qtiles || split >= p.splits) return false;
+  if (first < 0 || n_tiles < 0) return false;
+  for (int g = first; g < first + n_tiles; ++g) {
+    const Tile t = tile_at(p, kp, g);
+    if (t.src < 0 || t.src > 1 || (t.src == 1 && !(p.mode == kModeStreaming && p.kcur))) return false;
+    if (t.row < 0 || t.row >= p.src_rows[t.src] || t.valid < 1) return false;
+    // streaming key runs end inside their source (block-causal tiles may run
+    // past the last key: the copy fills zeros and the mask drops them)
+    if (p.mode != kModeBlockCausal && t.row + t.valid > p.src_rows[t.src]) return false;
+    if (p.fp8 && (t.row + t.valid - 1) / p.chunk_tokens >= p.scale_stride) return false;
+  }
+  if (p.splits > 1) {
+    const long long tile = ((long long)split * p.B * p.H + blockIdx.y) * p.n_qtiles + blockIdx.x;
+    if (tile >= p.ws_tiles || (long long)blockIdx.y * p.n_qtiles + blockIdx.x >= (long long)p.B * p.H * p.n_qtiles)
+      return false;
+  }
+  return true;
 }
 
 // Key runs of the query rows [q0, q0 + qrows) behind a memory prefix
@@ -260,7 +285,8 @@ struct KhCfg {
   static constexpr int kNumBars = kBarMerge + 1;
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
   static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;
-  static constexpr int kConvThreads = 64;
+  // 8-bit cache: warps 2 and 3 expand codes, softmax warps 4..11
+  static constexpr int kConvThreads = kConv ? 64 : 0;
   static constexpr int kSoftmaxWarp0 = kConv ? 4 : 2;
   static constexpr int kThreads = 32 * (kSoftmaxWarp0 + 8);
   static constexpr uint32_t kTmemO = 256;
@@ -346,195 +372,20 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
     kp = p.plan;
   int first = 0, n_tiles = 0;
   kv_range(p, kp, q0, kTileM, split, first, n_tiles);
+  if constexpr (kDebugBounds) {
+    if (!attn_indices_ok(p, kp, b, q0, split, first, n_tiles)) {  // the whole CTA takes this branch
+      n_tiles = 0;
+      if (threadIdx.x == 0) {
+        atomicOr(&g_sab_error_word, kErrBoundsBit);
+        *abort_flag = 1;  // every role leaves as after a wait that gave up
+      }
+      __syncthreads();
+    }
+  }
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      mbar_arrive_expect_tx(bar(C::kBarQ), C::kTileBytes);
-#pragma unroll
-      for (int bx = 0; bx < C::kBoxes; ++bx)
-        tma_load_4d(sQ + bx * C::kBoxBytes, &p.q_map, bar(C::kBarQ), bx * 64, q0, h, b);
-      int u = 0;
-      for (; u <= n_tiles && n_tiles > 0; ++u) {
-        const int st = u % C::kStages;
-        if (u >= C::kStages &&
-            !wait_bounded(bar(C::kBarKVEmpty + st), (uint32_t)(u / C::kStages - 1) & 1u, abort_flag, 0))
-          break;
-        const bool has_k = u < n_tiles, has_v = u > 0;
-        const Tile tk = tile_at(p, kp, first + (has_k ? u : u - 1));
-        const Tile tv = tile_at(p, kp, first + (has_v ? u - 1 : u));
-        if constexpr (F8MMA) {  // E4M3 code tiles, used by the MMA as stored
-          mbar_arrive_expect_tx(bar(C::kBarKFull + st),
-                                (has_k ? C::kKVTileBytes : 0u) + (has_v ? C::kKVTileBytes : 0u));
-          if (has_k)
-            tma_load_4d(sK + st * C::kKVTileBytes, &p.k_map[0], bar(C::kBarKFull + st), 0, tk.row, h, b);
-          if (has_v)
-            tma_load_4d(sV + st * C::kKVTileBytes, &p.v_map[0], bar(C::kBarKFull + st), 0, tv.row, h, b);
-        } else if (FP8) {
-          mbar_arrive_expect_tx(bar(C::kBarRawFull + st), (has_k ? 128 * D : 0) + (has_v ? 128 * D : 0));
-          if (has_k)
-            tma_load_4d(sK + st * C::kTileBytes + C::kBoxBytes, &p.k_map[0], bar(C::kBarRawFull + st), 0, tk.row,
-                        h, b);
-          if (has_v)
-            tma_load_4d(sV + st * C::kTileBytes + C::kBoxBytes, &p.v_map[0], bar(C::kBarRawFull + st), 0, tv.row,
-                        h, b);
-        } else {
-          mbar_arrive_expect_tx(bar(C::kBarKFull + st), (has_k ? C::kTileBytes : 0) + (has_v ? C::kTileBytes : 0));
-          if (has_k) {
-#pragma unroll
-            for (int bx = 0; bx < C::kBoxes; ++bx)
-              tma_load_4d(sK + st * C::kTileBytes + bx * C::kBoxBytes, &p.k_map[tk.src], bar(C::kBarKFull + st),
-                          bx * 64, tk.row, h, b);
-          }
-          if (has_v) {
-#pragma unroll
-            for (int bx = 0; bx < C::kBoxes; ++bx)
-              tma_load_4d(sV + st * C::kTileBytes + bx * C::kBoxBytes, &p.v_map[tv.src], bar(C::kBarKFull + st),
-                          bx * 64, tv.row, h, b);
-          }
-        }
-      }
-      if (*abort_flag) {
-        wait_drain(bar(C::kBarQ), 0);
-        for (int uu = max(0, u - C::kStages); uu < u; ++uu)
-          wait_drain(bar((C::kConv ? C::kBarRawFull : C::kBarKFull) + uu % C::kStages),
-                     (uint32_t)(uu / C::kStages) & 1u);
-      }
-    }
-    __syncwarp();
-  } else if (C::kConv && (warp == 2 || warp == 3)) {
-    // ------------------------------------------------ E4M3 -> bf16 expansion
-    // (same in-place row expansion as the two-tile kernel)
-    const int ct = threadIdx.x - 64;
-    for (int u = 0; u <= n_tiles && n_tiles > 0; ++u) {
-      const int st = u % C::kStages;
-      if (!wait_bounded(bar(C::kBarRawFull + st), (uint32_t)(u / C::kStages) & 1u, abort_flag, 12)) break;
-      const int job0 = u < n_tiles ? 0 : kTileN, job1 = u > 0 ? 2 * kTileN : kTileN;  // K rows, then V rows
-#pragma unroll 1
-      for (int job = job0 + ct; job < job1; job += C::kConvThreads) {
-        const int r = job & (kTileN - 1);
-        const bool isv = job >= kTileN;
-        uint8_t* tile = base + (isv ? C::kVOff : C::kKOff) + st * C::kTileBytes;
-        if (p.k_int8 && !isv) expand_code_row_f16<true>(tile, r, C::kBoxBytes);  // INT8 keys
-        else expand_code_row_f16<false>(tile, r, C::kBoxBytes);
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(bar(C::kBarKFull + st));
-    }
-  } else if (warp == 1) {
-    // ---------------------------------------------------------- MMA issuer
-    constexpr uint32_t idesc_qk = F8MMA ? idesc_e4m3_f32(128, kTileN, 0)
-                                        : (C::kConv ? idesc_f16_f32(128, kTileN, 0) : idesc_bf16_f32(128, kTileN, 0));
-    constexpr uint32_t idesc_pv = F8MMA ? idesc_e4m3_f32(128, D, 1)
-                                        : (C::kConv ? idesc_f16_f32(128, D, 1) : idesc_bf16_f32(128, D, 1));
-    // 8-bit cache: the A operand is the converted Q the softmax warps write
-    bool ok = __all_sync(0xffffffffu, wait_bounded(bar(FP8 ? C::kBarQ8 : C::kBarQ), 0, abort_flag, 1));
-    if (ok) tc_fence_after();
-    const uint64_t dq = smem_desc_sw128(F8MMA ? base_u32 + C::kQ8Off : sQ, 16, 1024);
-    const uint64_t dk = smem_desc_sw128(sK, 16, 1024);
-    const uint64_t dv = smem_desc_sw128(sV, C::kBoxBytes, 1024);
-    const uint32_t q_lo = (uint32_t)dq, k_lo = (uint32_t)dk, v_lo = (uint32_t)dv;
-    const uint32_t kq_hi = (uint32_t)(dq >> 32), v_hi = (uint32_t)(dv >> 32);
-    constexpr uint32_t kTileStep = C::kKVTileBytes >> 4;
-    // As in the two-tile kernel, the barrier needed next is probed without
-    // blocking in the middle of the preceding MMA group.
-    auto issue_s = [&](int j, uint32_t pb, uint32_t pp, bool& pout) {
-      const uint32_t d = tmem + (uint32_t)(j & 1) * 128u;
-      const uint32_t b0 = k_lo + (uint32_t)(j % C::kStages) * kTileStep;
-      if constexpr (F8MMA) {  // 128-byte code rows: K = 32 codes (32 bytes) a step
-#pragma unroll
-        for (int kk = 0; kk < D / 32; ++kk) {
-          const uint32_t koff = (uint32_t)(kk * 32) >> 4;
-          mma_ss_f8_e(d, make_desc(q_lo + koff, kq_hi), make_desc(b0 + koff, kq_hi), idesc_qk, kk > 0 ? 1u : 0u);
-          if (kk == D / 64 && pb != 0) pout = mbar_test_wait(pb, pp);
-        }
-      } else {
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t koff = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
-          mma_ss_e(d, make_desc(q_lo + koff, kq_hi), make_desc(b0 + koff, kq_hi), idesc_qk, kk > 0 ? 1u : 0u);
-          if (kk == D / 32 && pb != 0) pout = mbar_test_wait(pb, pp);
-        }
-      }
-    };
-    // O_hf += P_hf V[64 hf .. 64 hf + 63]
-    auto issue_pv = [&](int j, int hf, uint32_t pb, uint32_t pp, bool& pout) {
-      const uint32_t d = tmem + C::kTmemO + (uint32_t)hf * D;
-      const uint32_t b0 = v_lo + (uint32_t)((j + 1) % C::kStages) * kTileStep;
-      const uint32_t a0 = tmem + (uint32_t)(j & 1) * 128u + (uint32_t)hf * 64u;
-      if constexpr (F8MMA) {  // P_hf: 64 E4M3 keys in 16 columns, 32 keys (8 columns) a step
-#pragma unroll
-        for (int kk = 0; kk < 2; ++kk) {
-          const int kr = hf * 64 + kk * 32;  // first key row of the step
-          mma_ts_f8_e(d, a0 + kk * 8, make_desc(b0 + ((kr * 128) >> 4), v_hi), idesc_pv,
-                      (kk > 0 || j > 0) ? 1u : 0u);
-          if (kk == 0 && pb != 0) pout = mbar_test_wait(pb, pp);
-        }
-      } else {
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const int kg = hf * 4 + kk;  // group of 16 keys
-          mma_ts_e(d, a0 + kk * 8, make_desc(b0 + ((kg * 16 * 128) >> 4), v_hi), idesc_pv,
-                   (kk > 0 || j > 0) ? 1u : 0u);
-          if (kk == 1 && pb != 0) pout = mbar_test_wait(pb, pp);
-        }
-      }
-    };
-    auto wait_probed = [&](uint32_t bb, uint32_t par, bool probed, unsigned site) -> bool {
-      if (probed) return true;
-      return __all_sync(0xffffffffu, wait_bounded(bb, par, abort_flag, site));
-    };
-    auto kbar = [&](int j) { return bar(C::kBarKFull + j % C::kStages); };
-    auto kpar = [&](int j) { return (uint32_t)(j / C::kStages) & 1u; };
-    auto pbar = [&](int j, int hf) { return bar(C::kBarPFull + 2 * (j & 1) + hf); };
-    auto ppar = [&](int j) { return (uint32_t)(j >> 1) & 1u; };
-    bool pr = false;
-    // prologue: S(0), S(1)
-    for (int j = 0; ok && j < 2 && j < n_tiles; ++j) {
-      if (!(ok = wait_probed(kbar(j), kpar(j), pr, 5))) break;
-      tc_fence_after();
-      pr = false;
-      if (j + 1 < 2 && j + 1 < n_tiles) issue_s(j, kbar(j + 1), kpar(j + 1), pr);
-      else issue_s(j, pbar(0, 0), ppar(0), pr);
-      mma_commit_e(bar(C::kBarSFull + (j & 1)));
-      if (j == 0) mma_commit_e(bar(C::kBarKVEmpty + 0));  // stage 0 holds K(0) only
-    }
-    for (int j = 0; ok && j < n_tiles; ++j) {
-      // V(j) sits in stage j + 1 with K(j + 1): already waited for before
-      // S(j + 1), except after the last tile
-      if (j + 1 >= n_tiles && !(ok = wait_probed(kbar(j + 1), kpar(j + 1), false, 5))) break;
-      if (!(ok = wait_probed(pbar(j, 0), ppar(j), pr, 2))) break;
-      tc_fence_after();
-      pr = false;
-      issue_pv(j, 0, pbar(j, 1), ppar(j), pr);
-      if (!(ok = wait_probed(pbar(j, 1), ppar(j), pr, 3))) break;
-      tc_fence_after();
-      pr = false;
-      if (j + 2 < n_tiles) issue_pv(j, 1, kbar(j + 2), kpar(j + 2), pr);
-      else issue_pv(j, 1, 0u, 0u, pr);
-      // the softmax of the last tile learns from this that O holds every
-      // earlier tile (other tiles learn it from the next tile's S)
-      if (j + 2 == n_tiles) mma_commit_e(bar(C::kBarPVLast));
-      // stage j + 1 (K(j + 1), V(j)) is free once PV(j) completes: S(j + 1)
-      // was issued before it
-      mma_commit_e(bar(C::kBarKVEmpty + (j + 1) % C::kStages));
-      if (j + 2 < n_tiles) {
-        if (!(ok = wait_probed(kbar(j + 2), kpar(j + 2), pr, 5))) break;
-        tc_fence_after();
-        pr = false;
-        issue_s(j + 2, pbar(j + 1, 0), ppar(j + 1), pr);
-        mma_commit_e(bar(C::kBarSFull + (j & 1)));
-      } else {
-        pr = false;
-      }
-    }
-    if (ok) mma_commit_e(bar(C::kBarOFinal));
-    if (!ok) {
-      mma_commit_e(bar(C::kBarDrain));
-      if (lane == 0) wait_drain(bar(C::kBarDrain), 0);
-    }
-    __syncwarp();
-  } else if (warp >= C::kSoftmaxWarp0) {
+  // Roles: softmax warps (and their epilogue); producer, MMA issuer and
+  // (8-bit cache) conversion warps.
+  if (warp >= C::kSoftmaxWarp0) {
     // ---------------------------------------------- softmax + epilogue
     const int hf = (warp - C::kSoftmaxWarp0) >> 2;  // key half of every tile
     const int quad = warp & 3;                        // TMEM lane quadrant of this warp
@@ -657,6 +508,20 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
       constexpr float kGain = F8MMA ? 16.f : 64.f;
       vgain = __fdiv_rn(kGain, vref);
       ofac = vref * (1.f / kGain);
+      // The per-chunk coefficients of this (b, h) go to a shared table (over
+      // the row maxima, dead now) so that no tile waits on a global load:
+      // {K scale, V scale * gain, log2 of it, its reciprocal}
+      if (p.scale_stride <= kScaleTab) {
+        named_bar_sync(1, 256);  // every thread has read the row maxima
+        float4* tab = reinterpret_cast<float4*>(base + C::kQmaxOff);
+        const int t = hf * 128 + row;
+        if (t < p.scale_stride) {
+          const float ks = __ldg(p.k_scale + srow + t), vs = __ldg(p.v_scale + srow + t);
+          const float v = vs * vgain;
+          tab[t] = make_float4(ks, v, vs > 0.f ? __log2f(v) : 0.f, vs > 0.f ? 1.f / v : 0.f);
+        }
+        named_bar_sync(1, 256);
+      }
     }
     for (int j = 0; ok && j < n_tiles; ++j) {
       ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarSFull + (j & 1)), (uint32_t)(j >> 1) & 1u,
@@ -703,20 +568,27 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
         const int si0 = min(tile_row0 / p.chunk_tokens, p.scale_stride - 1);
         const int si1 = min(si0 + 1, p.scale_stride - 1);
         bnd = (si0 + 1) * p.chunk_tokens - tile_row0 - kofs;
-        float ks0 = __ldg(p.k_scale + srow + si0), ks1 = __ldg(p.k_scale + srow + si1);
-        float vs0 = __ldg(p.v_scale + srow + si0), vs1 = __ldg(p.v_scale + srow + si1);
-        if (bnd <= 0) {  // the whole half lies in the second chunk
-          ks0 = ks1;
-          vs0 = vs1;
+        // the half's keys before `bnd` belong to chunk si0, the rest to si1
+        float4 e0, e1;
+        if (p.scale_stride <= kScaleTab) {
+          const float4* tab = reinterpret_cast<const float4*>(base + C::kQmaxOff);
+          e0 = tab[bnd <= 0 ? si1 : si0];  // the whole half in the second chunk
+          e1 = tab[si1];
+        } else {
+          const int a = bnd <= 0 ? si1 : si0;
+          const float ks0 = __ldg(p.k_scale + srow + a), ks1 = __ldg(p.k_scale + srow + si1);
+          const float vs0 = __ldg(p.v_scale + srow + a), vs1 = __ldg(p.v_scale + srow + si1);
+          e0 = make_float4(ks0, vs0 * vgain, vs0 > 0.f ? __log2f(vs0 * vgain) : 0.f, vs0 > 0.f ? 1.f / (vs0 * vgain) : 0.f);
+          e1 = make_float4(ks1, vs1 * vgain, 0.f, 0.f);
         }
         // a zero scale marks a slot never written, whose keys are all masked:
         // keep the coefficients finite and non-zero so that -inf stays -inf
-        c0 = ks0 > 0.f ? slq * ks0 : slq;
-        c1 = ks1 > 0.f ? slq * ks1 : slq;
-        v0 = vs0 * vgain;  // the P gain of the 8-bit paths
-        v1 = vs1 * vgain;
-        d0 = vs0 > 0.f ? __log2f(v0) : 0.f;
-        iv0 = vs0 > 0.f ? 1.f / v0 : 0.f;
+        c0 = e0.x > 0.f ? slq * e0.x : slq;
+        c1 = e1.x > 0.f ? slq * e1.x : slq;
+        v0 = e0.y;  // V scale times the P gain of the 8-bit paths
+        v1 = e1.y;
+        d0 = e0.z;
+        iv0 = e0.w;
       }
       const bool straddle = FP8 && bnd > 0 && bnd < 64;
       const bool masked = !(lo <= 0 && hi >= 64);
@@ -829,7 +701,9 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
     // (the other half's softmax may still be a tile behind, so completion is
     // read from the single-phase final barrier, not from the per-tile ones)
     if (ok) ok = wait_bounded(bar(C::kBarOFinal), 0, abort_flag, 8);
-    ok = __all_sync(0xffffffffu, ok);
+    // a completed barrier does not clear an abort raised elsewhere in the CTA
+    // (another role's wait, or a failed index check): nothing is stored then
+    ok = __all_sync(0xffffffffu, ok && !*abort_flag);
     // every MMA is complete: the operand region is free.  Exchange (m, l) of
     // the two halves of each row, then each half finishes D/2 columns.
     float2* xch = reinterpret_cast<float2*>(base + C::kXchOff);
@@ -911,7 +785,7 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
       if (warp == C::kSoftmaxWarp0 && lane == 0) {
         unsigned* cnt = &p.ws_count[(long long)bh * p.n_qtiles + blockIdx.x];
         if (split + 1 == p.inject_abort) {  // self-test: behave as a split whose wait gave up
-          atomicOr(&g_sab_error_word, 1u << 29);
+          atomicOr(&g_sab_error_word, kErrInjectedAbortBit);
           *abort_flag = 1;
         }
         const bool aborted = *abort_flag != 0;
@@ -1017,6 +891,194 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
       for (int bx = 0; bx < C::kBoxes; ++bx)
         tma_store_4d(&p.o_map, base_u32 + C::kQOff + bx * C::kBoxBytes, bx * 64, q0, h, b);
       tma_store_commit_and_wait_read();
+    }
+  } else {
+    if (warp == 0) {
+      // ------------------------------------------------------------ producer
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar(C::kBarQ), C::kTileBytes);
+  #pragma unroll
+        for (int bx = 0; bx < C::kBoxes; ++bx)
+          tma_load_4d(sQ + bx * C::kBoxBytes, &p.q_map, bar(C::kBarQ), bx * 64, q0, h, b);
+        int u = 0;
+        for (; u <= n_tiles && n_tiles > 0; ++u) {
+          const int st = u % C::kStages;
+          if (u >= C::kStages &&
+              !wait_bounded(bar(C::kBarKVEmpty + st), (uint32_t)(u / C::kStages - 1) & 1u, abort_flag, 0))
+            break;
+          const bool has_k = u < n_tiles, has_v = u > 0;
+          const Tile tk = tile_at(p, kp, first + (has_k ? u : u - 1));
+          const Tile tv = tile_at(p, kp, first + (has_v ? u - 1 : u));
+          if constexpr (F8MMA) {  // E4M3 code tiles, used by the MMA as stored
+            mbar_arrive_expect_tx(bar(C::kBarKFull + st),
+                                  (has_k ? C::kKVTileBytes : 0u) + (has_v ? C::kKVTileBytes : 0u));
+            if (has_k)
+              tma_load_4d(sK + st * C::kKVTileBytes, &p.k_map[0], bar(C::kBarKFull + st), 0, tk.row, h, b);
+            if (has_v)
+              tma_load_4d(sV + st * C::kKVTileBytes, &p.v_map[0], bar(C::kBarKFull + st), 0, tv.row, h, b);
+          } else if (FP8) {
+            mbar_arrive_expect_tx(bar(C::kBarRawFull + st), (has_k ? 128 * D : 0) + (has_v ? 128 * D : 0));
+            if (has_k)
+              tma_load_4d(sK + st * C::kTileBytes + C::kBoxBytes, &p.k_map[0], bar(C::kBarRawFull + st), 0, tk.row,
+                          h, b);
+            if (has_v)
+              tma_load_4d(sV + st * C::kTileBytes + C::kBoxBytes, &p.v_map[0], bar(C::kBarRawFull + st), 0, tv.row,
+                          h, b);
+          } else {
+            mbar_arrive_expect_tx(bar(C::kBarKFull + st), (has_k ? C::kTileBytes : 0) + (has_v ? C::kTileBytes : 0));
+            if (has_k) {
+  #pragma unroll
+              for (int bx = 0; bx < C::kBoxes; ++bx)
+                tma_load_4d(sK + st * C::kTileBytes + bx * C::kBoxBytes, &p.k_map[tk.src], bar(C::kBarKFull + st),
+                            bx * 64, tk.row, h, b);
+            }
+            if (has_v) {
+  #pragma unroll
+              for (int bx = 0; bx < C::kBoxes; ++bx)
+                tma_load_4d(sV + st * C::kTileBytes + bx * C::kBoxBytes, &p.v_map[tv.src], bar(C::kBarKFull + st),
+                            bx * 64, tv.row, h, b);
+            }
+          }
+        }
+        if (*abort_flag) {
+          wait_drain(bar(C::kBarQ), 0);
+          for (int uu = max(0, u - C::kStages); uu < u; ++uu)
+            wait_drain(bar((C::kConv ? C::kBarRawFull : C::kBarKFull) + uu % C::kStages),
+                       (uint32_t)(uu / C::kStages) & 1u);
+        }
+      }
+      __syncwarp();
+    } else if (warp == 1) {
+      // ---------------------------------------------------------- MMA issuer
+      constexpr uint32_t idesc_qk = F8MMA ? idesc_e4m3_f32(128, kTileN, 0)
+                                          : (C::kConv ? idesc_f16_f32(128, kTileN, 0) : idesc_bf16_f32(128, kTileN, 0));
+      constexpr uint32_t idesc_pv = F8MMA ? idesc_e4m3_f32(128, D, 1)
+                                          : (C::kConv ? idesc_f16_f32(128, D, 1) : idesc_bf16_f32(128, D, 1));
+      // 8-bit cache: the A operand is the converted Q the softmax warps write
+      bool ok = __all_sync(0xffffffffu, wait_bounded(bar(FP8 ? C::kBarQ8 : C::kBarQ), 0, abort_flag, 1));
+      if (ok) tc_fence_after();
+      const uint64_t dq = smem_desc_sw128(F8MMA ? base_u32 + C::kQ8Off : sQ, 16, 1024);
+      const uint64_t dk = smem_desc_sw128(sK, 16, 1024);
+      const uint64_t dv = smem_desc_sw128(sV, C::kBoxBytes, 1024);
+      const uint32_t q_lo = (uint32_t)dq, k_lo = (uint32_t)dk, v_lo = (uint32_t)dv;
+      const uint32_t kq_hi = (uint32_t)(dq >> 32), v_hi = (uint32_t)(dv >> 32);
+      constexpr uint32_t kTileStep = C::kKVTileBytes >> 4;
+      // As in the two-tile kernel, the barrier needed next is probed without
+      // blocking in the middle of the preceding MMA group.
+      auto issue_s = [&](int j, uint32_t pb, uint32_t pp, bool& pout) {
+        const uint32_t d = tmem + (uint32_t)(j & 1) * 128u;
+        const uint32_t b0 = k_lo + (uint32_t)(j % C::kStages) * kTileStep;
+        if constexpr (F8MMA) {  // 128-byte code rows: K = 32 codes (32 bytes) a step
+  #pragma unroll
+          for (int kk = 0; kk < D / 32; ++kk) {
+            const uint32_t koff = (uint32_t)(kk * 32) >> 4;
+            mma_ss_f8_e(d, make_desc(q_lo + koff, kq_hi), make_desc(b0 + koff, kq_hi), idesc_qk, kk > 0 ? 1u : 0u);
+            if (kk == D / 64 && pb != 0) pout = mbar_test_wait(pb, pp);
+          }
+        } else {
+  #pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t koff = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
+            mma_ss_e(d, make_desc(q_lo + koff, kq_hi), make_desc(b0 + koff, kq_hi), idesc_qk, kk > 0 ? 1u : 0u);
+            if (kk == D / 32 && pb != 0) pout = mbar_test_wait(pb, pp);
+          }
+        }
+      };
+      // O_hf += P_hf V[64 hf .. 64 hf + 63]
+      auto issue_pv = [&](int j, int hf, uint32_t pb, uint32_t pp, bool& pout) {
+        const uint32_t d = tmem + C::kTmemO + (uint32_t)hf * D;
+        const uint32_t b0 = v_lo + (uint32_t)((j + 1) % C::kStages) * kTileStep;
+        const uint32_t a0 = tmem + (uint32_t)(j & 1) * 128u + (uint32_t)hf * 64u;
+        if constexpr (F8MMA) {  // P_hf: 64 E4M3 keys in 16 columns, 32 keys (8 columns) a step
+  #pragma unroll
+          for (int kk = 0; kk < 2; ++kk) {
+            const int kr = hf * 64 + kk * 32;  // first key row of the step
+            mma_ts_f8_e(d, a0 + kk * 8, make_desc(b0 + ((kr * 128) >> 4), v_hi), idesc_pv,
+                        (kk > 0 || j > 0) ? 1u : 0u);
+            if (kk == 0 && pb != 0) pout = mbar_test_wait(pb, pp);
+          }
+        } else {
+  #pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const int kg = hf * 4 + kk;  // group of 16 keys
+            mma_ts_e(d, a0 + kk * 8, make_desc(b0 + ((kg * 16 * 128) >> 4), v_hi), idesc_pv,
+                     (kk > 0 || j > 0) ? 1u : 0u);
+            if (kk == 1 && pb != 0) pout = mbar_test_wait(pb, pp);
+          }
+        }
+      };
+      auto wait_probed = [&](uint32_t bb, uint32_t par, bool probed, unsigned site) -> bool {
+        if (probed) return true;
+        return __all_sync(0xffffffffu, wait_bounded(bb, par, abort_flag, site));
+      };
+      auto kbar = [&](int j) { return bar(C::kBarKFull + j % C::kStages); };
+      auto kpar = [&](int j) { return (uint32_t)(j / C::kStages) & 1u; };
+      auto pbar = [&](int j, int hf) { return bar(C::kBarPFull + 2 * (j & 1) + hf); };
+      auto ppar = [&](int j) { return (uint32_t)(j >> 1) & 1u; };
+      bool pr = false;
+      // prologue: S(0), S(1)
+      for (int j = 0; ok && j < 2 && j < n_tiles; ++j) {
+        if (!(ok = wait_probed(kbar(j), kpar(j), pr, 5))) break;
+        tc_fence_after();
+        pr = false;
+        if (j + 1 < 2 && j + 1 < n_tiles) issue_s(j, kbar(j + 1), kpar(j + 1), pr);
+        else issue_s(j, pbar(0, 0), ppar(0), pr);
+        mma_commit_e(bar(C::kBarSFull + (j & 1)));
+        if (j == 0) mma_commit_e(bar(C::kBarKVEmpty + 0));  // stage 0 holds K(0) only
+      }
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        // V(j) sits in stage j + 1 with K(j + 1): already waited for before
+        // S(j + 1), except after the last tile
+        if (j + 1 >= n_tiles && !(ok = wait_probed(kbar(j + 1), kpar(j + 1), false, 5))) break;
+        if (!(ok = wait_probed(pbar(j, 0), ppar(j), pr, 2))) break;
+        tc_fence_after();
+        pr = false;
+        issue_pv(j, 0, pbar(j, 1), ppar(j), pr);
+        if (!(ok = wait_probed(pbar(j, 1), ppar(j), pr, 3))) break;
+        tc_fence_after();
+        pr = false;
+        if (j + 2 < n_tiles) issue_pv(j, 1, kbar(j + 2), kpar(j + 2), pr);
+        else issue_pv(j, 1, 0u, 0u, pr);
+        // the softmax of the last tile learns from this that O holds every
+        // earlier tile (other tiles learn it from the next tile's S)
+        if (j + 2 == n_tiles) mma_commit_e(bar(C::kBarPVLast));
+        // stage j + 1 (K(j + 1), V(j)) is free once PV(j) completes: S(j + 1)
+        // was issued before it
+        mma_commit_e(bar(C::kBarKVEmpty + (j + 1) % C::kStages));
+        if (j + 2 < n_tiles) {
+          if (!(ok = wait_probed(kbar(j + 2), kpar(j + 2), pr, 5))) break;
+          tc_fence_after();
+          pr = false;
+          issue_s(j + 2, pbar(j + 1, 0), ppar(j + 1), pr);
+          mma_commit_e(bar(C::kBarSFull + (j & 1)));
+        } else {
+          pr = false;
+        }
+      }
+      if (ok) mma_commit_e(bar(C::kBarOFinal));
+      if (!ok) {
+        mma_commit_e(bar(C::kBarDrain));
+        if (lane == 0) wait_drain(bar(C::kBarDrain), 0);
+      }
+      __syncwarp();
+    } else if (C::kConv) {
+      // ----------------------------------------- 8-bit -> fp16 expansion
+      const int ct = threadIdx.x - 64;
+      for (int u = 0; u <= n_tiles && n_tiles > 0; ++u) {
+        const int st = u % C::kStages;
+        if (!wait_bounded(bar(C::kBarRawFull + st), (uint32_t)(u / C::kStages) & 1u, abort_flag, 12)) break;
+        const int job0 = u < n_tiles ? 0 : kTileN, job1 = u > 0 ? 2 * kTileN : kTileN;  // K rows, then V rows
+  #pragma unroll 1
+        for (int job = job0 + ct; job < job1; job += C::kConvThreads) {
+          const int r = job & (kTileN - 1);
+          const bool isv = job >= kTileN;
+          uint8_t* tile = base + (isv ? C::kVOff : C::kKOff) + st * C::kTileBytes;
+          if (p.k_int8 && !isv) expand_code_row_f16<true>(tile, r, C::kBoxBytes);  // INT8 keys
+          else expand_code_row_f16<false>(tile, r, C::kBoxBytes);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(bar(C::kBarKFull + st));
+      }
     }
   }
   tc_fence_before();
@@ -1201,8 +1263,22 @@ attn_bwd_kernel(const __grid_constant__ BwdParams p) {
   griddep_wait();
   const int P = p.mem_pad > 0 ? min(max(__ldg(p.mem_len + b), 0), p.mem_pad) : 0;  // real memory
   const BwdRuns u = bwd_runs<KQ>(p, P, r0);
-  const int nt = u.n0 + u.n1;  // streamed tiles
+  int nt = u.n0 + u.n1;  // streamed tiles
   auto tile_row = [&](int j) { return j < u.n0 ? j * 128 : u.row1 + (j - u.n0) * 128; };
+  if constexpr (kDebugBounds) {
+    // the resident tile and every streamed tile start inside [0, L) of an
+    // existing (b, h); checked by the whole CTA before any copy or store
+    bool in = b < p.B && r0 < p.L && u.n0 >= 0 && u.n1 >= 0;
+    for (int j = 0; in && j < nt; ++j) in = tile_row(j) >= 0 && tile_row(j) < p.L;
+    if (!in) {
+      nt = 0;
+      if (threadIdx.x == 0) {
+        atomicOr(&g_sab_error_word, kErrBoundsBit);
+        *abort_flag = 1;
+      }
+      __syncthreads();
+    }
+  }
   // resident: K, V (key-tile kernel) or Q, dO (query-tile kernel);
   // streamed: Q_j, dO_j or K_j, V_j
   const CUtensorMap* res0 = KQ ? &p.k_map : &p.q_map;
@@ -1430,7 +1506,7 @@ attn_bwd_kernel(const __grid_constant__ BwdParams p) {
     }
     // ------------------------------------------------------------ epilogue
     if (ok) ok = wait_bounded(bar(C::kBarFinal), 0, abort_flag, 8);
-    ok = __all_sync(0xffffffffu, ok);
+    ok = __all_sync(0xffffffffu, ok && !*abort_flag);  // an abort anywhere in the CTA: no store
     if (ok) {  // warp-uniform: tcgen05.ld is warp-collective, rows past L only skip the store
       tc_fence_after();
       // key-tile kernel: half 0 writes the dV row, half 1 the dK row;
@@ -1508,7 +1584,7 @@ __global__ void wait_timeout_probe_kernel(uint64_t timeout_ns) {
     fence_mbar_init();
   }
   __syncthreads();
-  if (threadIdx.x == 0) (void)wait_bounded(bar, 0, reinterpret_cast<volatile int*>(&abort_), 30, timeout_ns);
+  if (threadIdx.x == 0) (void)wait_bounded(bar, 0, reinterpret_cast<volatile int*>(&abort_), kErrProbeSite, timeout_ns);
   __syncthreads();
 }
 
@@ -1604,6 +1680,15 @@ cudaError_t noalloc_scratch(void** ptr, size_t* bytes) {
   *ptr = cache[dev].addr;
   *bytes = kNoAllocScratchBytes;
   return cudaSuccess;
+}
+
+unsigned int* device_error_word() {
+  static unsigned int* ptr = nullptr;
+  if (ptr == nullptr) {
+    void* a = nullptr;
+    if (cudaGetSymbolAddress(&a, g_sab_error_word) == cudaSuccess) ptr = static_cast<unsigned int*>(a);
+  }
+  return ptr;
 }
 
 cudaError_t read_and_clear_device_error(unsigned int* value) {

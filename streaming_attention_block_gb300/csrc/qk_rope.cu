@@ -33,6 +33,15 @@ qk_rope_kernel(const __grid_constant__ RopeParams p) {
   ptx::griddep_launch_dependents();
   ptx::griddep_wait();
   const int lane = threadIdx.x & 31;
+  if constexpr (kDebugBounds) {
+    // the appended chunk's ring rows lie inside each (b, h) block, on a slot
+    // boundary; checked by the whole CTA before any load or store
+    if (p.ring_k != nullptr &&
+        !(p.Lc > 0 && p.slot_row0 >= 0 && p.slot_row0 % p.Lc == 0 && p.slot_row0 + p.Lc <= p.rows)) {
+      if (threadIdx.x == 0 && p.err_word != nullptr) atomicOr(p.err_word, kErrBoundsBit);
+      return;
+    }
+  }
   const long long tok = (long long)blockIdx.x * kRopeWarps + (threadIdx.x >> 5);  // b * Lc + t
   if (tok >= (long long)p.B * p.Lc) return;
   const int t = (int)(tok % p.Lc);

@@ -8,6 +8,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <atomic>
 #include <new>
 #include <vector>
 
@@ -19,6 +20,15 @@ using namespace sab;
 namespace {
 
 constexpr size_t kAlign = 256;
+
+// Debug builds: the kind of launch whose next instance carries a forged index
+// (sab_debug_inject_bounds_error); 0 when none is pending.
+std::atomic<int> g_inject{0};
+bool take_injection(int what) {
+  if (!kDebugBounds) return false;
+  int expect = what;
+  return g_inject.compare_exchange_strong(expect, 0);
+}
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -278,6 +288,11 @@ static sab_status write_chunk(sab_ring* r, int layer, int slot_row0, int scale_i
   p.d_chunk = d_chunk;
   p.ring_slots = r->d.ring_slots;
   p.has_sink = r->d.has_sink;
+  p.err_word = device_error_word();
+  if (d_chunk == nullptr && take_injection(SAB_DEBUG_INJECT_APPEND_SLOT)) {
+    p.slot_row0 = p.rows;  // one slot past the (b, h) block
+    p.scale_idx = p.scale_stride;
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const cudaError_t e = r->d.kv_dtype == SAB_KV_BF16 ? launch_append_bf16(p, s) : launch_append_fp8(p, s);
   return e == cudaSuccess ? SAB_OK : SAB_ERR_CUDA;
@@ -382,6 +397,13 @@ static sab_status launch_attention(AttnParams& p, int Lq, int splits, void* work
     p.ws_count = reinterpret_cast<unsigned*>(ws + w.count_off);
     p.ws_o = reinterpret_cast<float*>(ws + w.o_off);
     p.ws_lse = reinterpret_cast<float*>(ws + w.lse_off);
+    p.ws_tiles = (long long)((w.lse_off - w.o_off) / ((size_t)kTileM * p.D * sizeof(float)));
+    if (take_injection(SAB_DEBUG_INJECT_WS_TILE)) p.ws_tiles -= 1;  // the last tile "past" the workspace
+  }
+  if (p.mode == kModeStreaming && p.d_chunk == nullptr && p.plan.nseg > 0 &&
+      take_injection(SAB_DEBUG_INJECT_KEY_ROW)) {
+    KvSegment& sg = p.plan.seg[p.plan.nseg - 1];
+    sg.row0 += p.src_rows[sg.src];  // the last key run moved past the end of its source
   }
   return launch_chunk_attention_kh(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SAB_OK : SAB_ERR_CUDA;
 }
@@ -429,6 +451,8 @@ static sab_status plan_common(const sab_ring* ring, int layer, const void* Q, co
   p.has_sink = d.has_sink;
   p.use_sink = use_sink;
   p.kcur = kcur ? 1 : 0;
+  p.src_rows[0] = (int)ring->g.rows;
+  p.src_rows[1] = kcur ? Lc : 0;
   p.k_map[0] = ring->kmap[layer];
   p.v_map[0] = ring->vmap[layer];
   p.k_map[1] = ring->kmap[layer];
@@ -558,6 +582,8 @@ sab_status sab_qk_norm_rope(sab_ring* ring, int layer, long long chunk, const vo
   rp.Lc = d.chunk_tokens;
   rp.rows = (int)ring->g.rows;
   rp.slot_row0 = (d.has_sink + slot) * d.chunk_tokens;
+  rp.err_word = device_error_word();
+  if (rp.ring_k != nullptr && take_injection(SAB_DEBUG_INJECT_APPEND_SLOT)) rp.slot_row0 = rp.rows;
   rp.chunk = chunk;
   rp.F = rope->frames;
   rp.Hp = rope->height;
@@ -646,6 +672,7 @@ sab_status sab_block_causal_attention(const void* Q, const void* K, const void* 
   p.chunk_tokens = chunk_tokens;
   p.window = window;
   p.Lk = L;
+  p.src_rows[0] = L;
   p.O = static_cast<uint16_t*>(O);
   p.LSE = LSE;
   if (!encode_token_major(&p.q_map, Q, B, L, H, D) || !encode_token_major(&p.k_map[0], K, B, L, H, D) ||
@@ -678,6 +705,7 @@ sab_status sab_memory_prefix_attention(const void* Q, const void* K, const void*
   p.chunk_tokens = chunk_tokens;
   p.window = window;
   p.Lk = L;
+  p.src_rows[0] = L;
   p.mem_pad = mem_pad;
   p.mem_len = mem_len;
   p.O = static_cast<uint16_t*>(O);
@@ -780,7 +808,17 @@ sab_status sab_get_last_device_error(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return SAB_ERR_CUDA;
   unsigned v = 0;
   if (read_and_clear_device_error(&v) != cudaSuccess) return SAB_ERR_CUDA;
+  if (v & kErrBoundsBit) return SAB_ERR_BOUNDS;
   return v ? SAB_ERR_TIMEOUT : SAB_OK;
+}
+
+int sab_debug_bounds_enabled(void) { return kDebugBounds ? 1 : 0; }
+
+sab_status sab_debug_inject_bounds_error(int what) {
+  if (!kDebugBounds) return SAB_ERR_UNSUPPORTED;
+  if (what < 0 || what > SAB_DEBUG_INJECT_WS_TILE) return SAB_ERR_INVALID_ARG;
+  g_inject.store(what);
+  return SAB_OK;
 }
 
 const char* sab_status_string(sab_status status) {
@@ -792,6 +830,7 @@ const char* sab_status_string(sab_status status) {
     case SAB_ERR_WORKSPACE: return "SAB_ERR_WORKSPACE";
     case SAB_ERR_CUDA: return "SAB_ERR_CUDA";
     case SAB_ERR_TIMEOUT: return "SAB_ERR_TIMEOUT";
+    case SAB_ERR_BOUNDS: return "SAB_ERR_BOUNDS";
   }
   return "SAB_ERR_UNKNOWN";
 }

@@ -12,6 +12,19 @@ constexpr int kTileM = 128;    // query rows per tile (one TMEM lane per row)
 constexpr int kTileN = 128;    // keys per KV tile
 constexpr int kMaxSegments = 4;
 
+// Device error word bits: bit k < 16, a bounded wait at site k gave up; bit
+// 28, the bounded-wait self-test's wait gave up; bit 29, a split reported
+// itself as aborted on request (self-test); bit 30, a debug-build index check
+// failed; bit 31, a drain after an abort gave up.
+constexpr unsigned kErrProbeSite = 28;
+constexpr unsigned kErrInjectedAbortBit = 1u << 29;
+constexpr unsigned kErrBoundsBit = 1u << 30;
+#ifdef SAB_DEBUG_BOUNDS
+constexpr bool kDebugBounds = true;
+#else
+constexpr bool kDebugBounds = false;
+#endif
+
 // One contiguous run of key rows inside one K/V source.
 //   src 0: the layer's ring (rows along the [B,H,rows,D] row axis),
 //   src 1: the current chunk passed in (token axis of [B,L,H,D]).
@@ -132,6 +145,10 @@ struct AttnParams {
   float* ws_o;            // [tiles][D / 4][128 rows] float4: normalised partial rows
   float* ws_lse;          // [tiles][128 rows]: partial LSEs
   unsigned int* ws_count; // [B*H][n_qtiles] arrival counters
+  // debug-build index checks: rows of each key source's row axis, and the
+  // partial tiles the workspace holds
+  int src_rows[2];
+  long long ws_tiles;
 };
 
 // FP8 append: per (b, h) block of one chunk.
@@ -148,6 +165,7 @@ struct AppendParams {
   // graph mode: the slot is chunk mod R with the chunk read on the device
   const long long* d_chunk;
   int ring_slots, has_sink;
+  unsigned int* err_word;   // the library's device error word (debug-build index checks)
 };
 
 // Fused Q/K RMSNorm + rotary embedding of one chunk (token-major [B, Lc, H, D]).
@@ -170,6 +188,7 @@ struct RopeParams {
   int bt, bh, bw;           // rotary bands of the head dimension (even, sum D)
   float log2_base;          // log2(rotary base)
   float eps;
+  unsigned int* err_word;   // the library's device error word (debug-build index checks)
 };
 
 // Backward of block-causal attention (token-major [B, L, H, D] tensors).
@@ -200,6 +219,8 @@ cudaError_t launch_wait_timeout_probe(unsigned long long timeout_ns, cudaStream_
 // One query tile per CTA, key-half softmax warpgroups; unsplit KV only.
 cudaError_t launch_chunk_attention_kh(const AttnParams& p, cudaStream_t s);
 cudaError_t read_and_clear_device_error(unsigned int* value);
+// Device address of the error word (for kernels of other translation units).
+unsigned int* device_error_word();
 // Device address and size of the library's own split-merge scratch.
 cudaError_t noalloc_scratch(void** ptr, size_t* bytes);
 

@@ -40,7 +40,30 @@ def test_every_declared_symbol_is_exported(lib):
 def test_status_strings_and_version(lib):
     assert sab.status_string(0) == "SAB_OK"
     assert sab.status_string(6) == "SAB_ERR_TIMEOUT"
+    assert sab.status_string(7) == "SAB_ERR_BOUNDS"
     assert "sm_103a" in sab.version()
+
+
+def test_release_build_has_no_index_checks(lib):
+    assert not sab.debug_bounds_enabled()
+    # the injection hook exists in every build but is refused outside a debug build
+    assert lib.sab_debug_inject_bounds_error(sab.DEBUG_INJECT_APPEND_SLOT) == 2  # SAB_ERR_UNSUPPORTED
+
+
+def test_debug_build_exports_the_same_boundary_with_checks_on():
+    """libsab_debug.so (-DSAB_DEBUG_BOUNDS): same exports; the checks are on and
+    the injection hook validates its argument (host-only calls, no GPU)."""
+    from streaming_attention_block_gb300.build import DEBUG_LIB, build
+    build(debug_bounds=True)
+    dl = ctypes.CDLL(DEBUG_LIB)
+    for name in _declared():
+        assert hasattr(dl, name), name
+    dl.sab_debug_inject_bounds_error.argtypes = [ctypes.c_int]
+    assert dl.sab_debug_bounds_enabled() == 1
+    assert dl.sab_debug_inject_bounds_error(99) == 1   # SAB_ERR_INVALID_ARG
+    assert dl.sab_debug_inject_bounds_error(-1) == 1
+    assert dl.sab_debug_inject_bounds_error(sab.DEBUG_INJECT_WS_TILE) == 0
+    assert dl.sab_debug_inject_bounds_error(0) == 0    # cancels it
 
 
 def test_ring_bytes(lib):

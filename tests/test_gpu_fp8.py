@@ -35,8 +35,13 @@ def _ring(w, layers=1):
     return KVRing(layers, w.B, w.H, w.D, w.Lc, w.R, has_sink=w.sink, kv_dtype=sab.KV_FP8_E4M3)
 
 
+# block sizes for every launch form of the 8-bit append: a cluster of CTAs
+# per (tensor, b, h) block holding 2, 4, 8 or 16 vectors a thread, and one CTA
+# per block (two passes) beyond that
 @pytest.mark.parametrize("B,H,D,Lc,R,sink,outliers", [(1, 2, 128, 32, 2, False, False), (2, 3, 128, 200, 3, True, True),
-                                                      (1, 4, 64, 405, 4, True, True)])
+                                                      (1, 4, 64, 405, 4, True, True), (1, 3, 128, 405, 2, True, True),
+                                                      (1, 1, 128, 700, 2, False, True), (1, 2, 128, 1536, 2, False, True),
+                                                      (1, 1, 128, 4160, 2, False, False)])
 def test_append_fp8_bit_exact(B, H, D, Lc, R, sink, outliers):
     w = synth.Workload("t", B=B, H=H, D=D, Lc=Lc, R=R, W=1, sink=sink, outliers=outliers, kv_fp8=True, seed=9)
     ring = _ring(w)

@@ -34,7 +34,8 @@ def _ring(w, layers=1):
 
 
 @pytest.mark.parametrize("B,H,D,Lc,R,sink", [(1, 2, 128, 32, 2, False), (2, 3, 128, 200, 3, True),
-                                             (1, 4, 64, 405, 4, True)])
+                                             (1, 4, 64, 405, 4, True), (1, 2, 128, 1536, 2, False),
+                                             (1, 1, 128, 4160, 2, False)])
 def test_append_int8k_bit_exact(B, H, D, Lc, R, sink):
     w = synth.Workload("t", B=B, H=H, D=D, Lc=Lc, R=R, W=1, sink=sink, outliers=True, kv_fp8=True, kv_int8k=True,
                        seed=19)
