@@ -1238,7 +1238,7 @@ attn_bwd_kernel(const __grid_constant__ BwdParams p) {
   if (threadIdx.x == 0) {
     mbar_init(bar(C::kBarRes), 1);
     for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(bar(C::kBarFull + s), 1);
+      mbar_init(bar(C::kBarFull + s), KQ ? 2 : 1);  // key-tile kernel: copies + LSE/delta
       mbar_init(bar(C::kBarEmpty + s), 1);
     }
     mbar_init(bar(C::kBarSFull + 0), 1);
@@ -1306,6 +1306,17 @@ attn_bwd_kernel(const __grid_constant__ BwdParams p) {
       if (!ok) break;
       const uint32_t so = C::kStageOff + st * C::kStageBytes;
       const int row = tile_row(j);
+      // the tile copies first; the LSE and delta loads (key-tile kernel) take
+      // their global-memory latency while the copies are in flight
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar(C::kBarFull + st), 2 * C::kTileBytes);
+#pragma unroll
+        for (int bx = 0; bx < C::kBoxes; ++bx) {
+          tma_load_4d(base_u32 + so + bx * C::kBoxBytes, str0, bar(C::kBarFull + st), bx * 64, row, h, b);
+          tma_load_4d(base_u32 + so + C::kTileBytes + bx * C::kBoxBytes, str1, bar(C::kBarFull + st), bx * 64,
+                      row, h, b);
+        }
+      }
       if (KQ) {  // lse * log2(e) and delta of the stage's 128 queries (plain loads, whole warp)
         float* ls = reinterpret_cast<float*>(base + so + 2 * C::kTileBytes);
         float* dl = ls + 128;
@@ -1316,15 +1327,7 @@ attn_bwd_kernel(const __grid_constant__ BwdParams p) {
           dl[i] = in ? __ldg(p.delta + (long long)bh * p.L + q) : 0.f;
         }
         __syncwarp();
-      }
-      if (lane == 0) {
-        mbar_arrive_expect_tx(bar(C::kBarFull + st), 2 * C::kTileBytes);
-#pragma unroll
-        for (int bx = 0; bx < C::kBoxes; ++bx) {
-          tma_load_4d(base_u32 + so + bx * C::kBoxBytes, str0, bar(C::kBarFull + st), bx * 64, row, h, b);
-          tma_load_4d(base_u32 + so + C::kTileBytes + bx * C::kBoxBytes, str1, bar(C::kBarFull + st), bx * 64,
-                      row, h, b);
-        }
+        if (lane == 0) mbar_arrive(bar(C::kBarFull + st));  // second arrival: the stage's LSE and delta
       }
       __syncwarp();
     }
