@@ -1296,6 +1296,22 @@ attn_bwd_kernel(const __grid_constant__ BwdParams p) {
         tma_load_4d(base_u32 + C::kR1Off + bx * C::kBoxBytes, res1, bar(C::kBarRes), bx * 64, r0, h, b);
       }
     }
+    // key-tile kernel: the 128 LSE * log2(e) and delta values of a streamed
+    // tile are loaded into registers (four of each per lane) one tile ahead,
+    // so their global-memory latency passes while the producer waits for a
+    // free stage; they go to the stage after its tile copies are issued
+    float lsr[4], dlr[4];
+    auto load_lse = [&](int jj) {
+      const int row = tile_row(jj);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int q = row + lane + 32 * i;
+        const bool in = q < p.L;
+        lsr[i] = in ? -__ldg(p.LSE + (long long)bh * p.L + q) * kLog2e : -INFINITY;  // stored negated
+        dlr[i] = in ? -__ldg(p.delta + (long long)bh * p.L + q) : 0.f;
+      }
+    };
+    if (KQ && nt > 0) load_lse(0);
     int j = 0;
     for (; j < nt; ++j) {
       const int st = j % C::kStages;
@@ -1306,8 +1322,6 @@ attn_bwd_kernel(const __grid_constant__ BwdParams p) {
       if (!ok) break;
       const uint32_t so = C::kStageOff + st * C::kStageBytes;
       const int row = tile_row(j);
-      // the tile copies first; the LSE and delta loads (key-tile kernel) take
-      // their global-memory latency while the copies are in flight
       if (lane == 0) {
         mbar_arrive_expect_tx(bar(C::kBarFull + st), 2 * C::kTileBytes);
 #pragma unroll
@@ -1317,17 +1331,17 @@ attn_bwd_kernel(const __grid_constant__ BwdParams p) {
                       row, h, b);
         }
       }
-      if (KQ) {  // lse * log2(e) and delta of the stage's 128 queries (plain loads, whole warp)
+      if (KQ) {
         float* ls = reinterpret_cast<float*>(base + so + 2 * C::kTileBytes);
         float* dl = ls + 128;
-        for (int i = lane; i < 128; i += 32) {
-          const int q = row + i;
-          const bool in = q < p.L;
-          ls[i] = in ? __ldg(p.LSE + (long long)bh * p.L + q) * kLog2e : INFINITY;
-          dl[i] = in ? __ldg(p.delta + (long long)bh * p.L + q) : 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          ls[lane + 32 * i] = lsr[i];
+          dl[lane + 32 * i] = dlr[i];
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(C::kBarFull + st));  // second arrival: the stage's LSE and delta
+        if (j + 1 < nt) load_lse(j + 1);
       }
       __syncwarp();
     }
@@ -1457,8 +1471,8 @@ attn_bwd_kernel(const __grid_constant__ BwdParams p) {
           lo1 = M + max(0, c - p.window) * Lc;
           hi1 = min(p.L, M + (c + 1) * Lc);
         }
-        lse2 = __ldg(p.LSE + (long long)bh * p.L + r) * kLog2e;
-        dlt = __ldg(p.delta + (long long)bh * p.L + r);
+        lse2 = -__ldg(p.LSE + (long long)bh * p.L + r) * kLog2e;  // negated, as the stages hold them
+        dlt = -__ldg(p.delta + (long long)bh * p.L + r);
       }
     }
     const float sc = p.scale_log2;
@@ -1472,13 +1486,18 @@ attn_bwd_kernel(const __grid_constant__ BwdParams p) {
       const float* ls = reinterpret_cast<const float*>(base + C::kStageOff + (j % C::kStages) * C::kStageBytes +
                                                        2 * C::kTileBytes) + hf * 64;
       const float* dl = ls + 128;
+      // ls, dl (and lse2, dlt) hold -lse * log2(e) and -delta
       auto one = [&](uint32_t s, uint32_t dpv, int c, float& pv, float& dsv) {
         const bool vis = c >= lo && c < hi;
-        const float l2 = KQ ? ls[c] : lse2;
-        const float de = KQ ? dl[c] : dlt;
-        pv = vis ? ex2(fmaf(__uint_as_float(s), sc, -l2)) : 0.f;
-        dsv = pv * (__uint_as_float(dpv) - de);
+        const float nl2 = KQ ? ls[c] : lse2;
+        const float nde = KQ ? dl[c] : dlt;
+        pv = vis ? ex2(fmaf(__uint_as_float(s), sc, nl2)) : 0.f;
+        dsv = pv * (__uint_as_float(dpv) + nde);
       };
+      // every row of this warp sees all 64 columns of the half: no mask,
+      // pairs of columns in packed fp32 arithmetic
+      const bool whole = __all_sync(0xffffffffu, lo <= 0 && hi >= 64);
+      const float2 sc2 = make_float2(sc, sc);
       // two passes of 32 columns (the packed results of a pass go over
       // columns its own loads have already read, so the passes never clash)
 #pragma unroll
@@ -1488,13 +1507,39 @@ attn_bwd_kernel(const __grid_constant__ BwdParams p) {
         tmem_ld32(tdP + 32 * pass, dv);
         tmem_wait_ld();
         uint32_t pk[16], dk[16];
+        if (whole) {
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          float pa, pb, da, db;
-          one(sv[2 * c], dv[2 * c], 32 * pass + 2 * c, pa, da);
-          one(sv[2 * c + 1], dv[2 * c + 1], 32 * pass + 2 * c + 1, pb, db);
-          pk[c] = pack_bf16(pa, pb);
-          dk[c] = pack_bf16(da, db);
+          for (int c4 = 0; c4 < 8; ++c4) {  // four columns: one 16-byte read of the stage's values
+            float4 nl4, nd4;
+            if (KQ) {
+              nl4 = *reinterpret_cast<const float4*>(ls + 32 * pass + 4 * c4);
+              nd4 = *reinterpret_cast<const float4*>(dl + 32 * pass + 4 * c4);
+            } else {
+              nl4 = make_float4(lse2, lse2, lse2, lse2);
+              nd4 = make_float4(dlt, dlt, dlt, dlt);
+            }
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int c = 2 * c4 + e;
+              const float2 x = __ffma2_rn(make_float2(__uint_as_float(sv[2 * c]), __uint_as_float(sv[2 * c + 1])), sc2,
+                                          e ? make_float2(nl4.z, nl4.w) : make_float2(nl4.x, nl4.y));
+              const float2 pv = make_float2(ex2(x.x), ex2(x.y));
+              const float2 dd = __fadd2_rn(make_float2(__uint_as_float(dv[2 * c]), __uint_as_float(dv[2 * c + 1])),
+                                           e ? make_float2(nd4.z, nd4.w) : make_float2(nd4.x, nd4.y));
+              const float2 ds = __fmul2_rn(pv, dd);
+              pk[c] = pack_bf16(pv.x, pv.y);
+              dk[c] = pack_bf16(ds.x, ds.y);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            float pa, pb, da, db;
+            one(sv[2 * c], dv[2 * c], 32 * pass + 2 * c, pa, da);
+            one(sv[2 * c + 1], dv[2 * c + 1], 32 * pass + 2 * c + 1, pb, db);
+            pk[c] = pack_bf16(pa, pb);
+            dk[c] = pack_bf16(da, db);
+          }
         }
         if (KQ) {
           tmem_st16(tS + 16 * pass, pk);   // P^T over S^T
