@@ -9,9 +9,12 @@ change.  Tolerance per element: that bound, plus one bf16 ulp of the result
 exponential; LSE within 2e-3 (P is not rounded in the row sums, so LSE only
 sees the fp32 score accumulation of exact E4M3 products).  The bulk is held
 to the oracle's statistical model of the rounding: over each checked call,
-mean |error| <= 1.5 x mean(sqrt(2/pi) sigma) + 2^-10 mean |O| + 1e-4, with
+mean |error| <= 1.25 x mean(sqrt(2/pi) sigma) + 2^-10 mean |O| + 1e-4, with
 sigma the standard deviation of uniform rounding of every P to E4M3 and the
-second term the bf16 rounding of the output."""
+second term the bf16 rounding of the output.  The kernel's mean error is
+0.82-1.03 of the model's on these workloads; a P rounding toward zero
+instead of to nearest lands at 1.23-1.34 of the limit
+(``tests/test_oracle_fp8mma.py::test_mean_check_rejects_truncated_p``)."""
 
 import numpy as np
 import pytest
@@ -27,6 +30,8 @@ import streaming_attention_block_gb300 as sab
 from ._common import bhld, f64
 
 pytestmark = pytest.mark.gpu
+
+MEAN_FACTOR = 1.25  # mean error allowed, in units of the uniform-rounding model's mean
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -97,7 +102,7 @@ def _stream(w, check_chunks, rows=None):
                 assert np.max(np.abs(l_gpu[b, h] - lse)) <= 2e-3, f"chunk {c} b{b} h{h}: LSE"
         n = w.B * w.H
         stats.append((c, e_sum / n, p_sum / n))
-        assert e_sum <= 1.5 * p_sum + 2.0 ** -10 * o_sum + 1e-4 * n, (c, e_sum / n, p_sum / n)
+        assert e_sum <= MEAN_FACTOR * p_sum + 2.0 ** -10 * o_sum + 1e-4 * n, (c, e_sum / n, p_sum / n)
     return worst, stats
 
 

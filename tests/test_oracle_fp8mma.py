@@ -149,3 +149,40 @@ def test_sigma_predicts_the_replayed_error(peak):
     # and the mean magnitude is about sqrt(2/pi) sigma
     ratio_abs = np.mean(err) / np.mean(np.sqrt(2 / np.pi) * sigma)
     assert 0.7 < ratio_abs < 1.3, ratio_abs
+
+
+def _e4m3_truncate(x):
+    """Round positive float32 values toward zero onto the E4M3 grid (the
+    grid taken from torch's float8_e4m3fn codes 0..126)."""
+    grid = torch.arange(0, 127, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    x = np.asarray(x, dtype=np.float64)
+    return grid[np.searchsorted(grid, x, side="right") - 1]
+
+
+@pytest.mark.parametrize("peak", [0.3, 3.0])
+def test_mean_check_rejects_truncated_p(peak):
+    """The GPU test's mean check (mean |error| <= 1.25 x mean(sqrt(2/pi) sigma)
+    + 2^-10 mean |O| + 1e-4) has teeth: a P path that rounds toward zero
+    instead of to nearest -- a plausible conversion bug that the per-element
+    bound alone lets through -- doubles the mean-square rounding error and
+    fails it, while round-to-nearest passes on the same inputs."""
+    rng = np.random.default_rng(23 + int(peak))
+    Nk, D = 800, 64
+    q = (rng.standard_normal((64, D)) * peak).astype(np.float32)
+    k = rng.standard_normal((Nk, D))
+    v = rng.standard_normal((Nk, D))
+    vs = np.repeat([0.3, 1.0], Nk // 2)
+    mask = np.ones((64, Nk), dtype=bool)
+    scale = 1.0 / np.sqrt(D)
+    o, _, bound = OF.head_attention(q, k, v, mask, scale, vs)
+    sigma = OF.rounding_sigma(q, k, v, mask, scale, vs)
+    q_hat, _ = OF.quantize_rows(q)
+    s = scale * (q_hat @ k.T)
+    p = np.exp(s - s.max(axis=1, keepdims=True))
+    f = (vs / vs.max())[None, :] * 2.0 ** OF.P_GAIN_LOG2
+    limit = 1.25 * np.mean(np.sqrt(2.0 / np.pi) * sigma) + 2.0 ** -10 * np.mean(np.abs(o)) + 1e-4
+    for rounder, passes in ((_e4m3_round, True), (_e4m3_truncate, False)):
+        o_sim = ((rounder(p * f) / f) @ v) / p.sum(axis=1, keepdims=True)
+        err = np.abs(o_sim - o)
+        assert np.all(err <= bound + 2.0 ** -8 * np.abs(o) + 1e-3)  # the per-element bound holds for both
+        assert (np.mean(err) <= limit) == passes, (rounder.__name__, float(np.mean(err)), float(limit))
