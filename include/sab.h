@@ -206,9 +206,11 @@ size_t sab_chunk_attention_workspace(const sab_ring* ring, int num_splits);
  *          partition); each partition writes its normalised partial rows and
  *          LSEs to the workspace and the last one of a query tile to finish
  *          merges them.  1 runs each query tile over the whole key set (no
- *          merge).  0 lets the library choose S in 1..8 to fill the SMs: the
- *          S that minimises ceil(tiles * S / SMs) * ceil(key tiles / S) (+2
- *          key tiles for the merge when S > 1), tiles = B * H * ceil(Lc / 128).
+ *          merge).  0 lets the library choose S in 1..8 (and at most half the
+ *          key tiles) to fill the SMs: the S that minimises, in units of one
+ *          key tile's time, waves * ceil(key tiles / S) + 5 (waves - 1) plus
+ *          1 + 0.4 S for the merge when S > 1, where waves =
+ *          ceil(tiles * S / SMs) and tiles = B * H * ceil(Lc / 128).
  *   softmax_scale  usually 1/sqrt(D).
  *   O      device, token-major [B, Lc, H, D] bf16 (output).
  *   LSE    device, [B, H, Lc] fp32, natural log of sum exp(s) (output; may be NULL).
