@@ -1139,9 +1139,11 @@ struct BwdCfg {
   static constexpr uint32_t kStageBytes = 2 * kTileBytes + 1024;
   static constexpr uint32_t kBarOff = kStageOff + kStages * kStageBytes;
   static constexpr int kBarRes = 0;
-  static constexpr int kBarFull = 1;                      // [kStages]
-  static constexpr int kBarEmpty = kBarFull + kStages;    // [kStages]
-  static constexpr int kBarSFull = kBarEmpty + kStages;   // [2 halves]
+  // a stage fills and frees per 64-row half of the streamed tiles: half h of
+  // a stage is read by S_h, dP_h and the accumulations of half h only
+  static constexpr int kBarFull = 1;                          // [kStages][2 halves]
+  static constexpr int kBarEmpty = kBarFull + 2 * kStages;    // [kStages][2 halves]
+  static constexpr int kBarSFull = kBarEmpty + 2 * kStages;   // [2 halves]
   static constexpr int kBarPFull = kBarSFull + 2;         // [2 halves]
   static constexpr int kBarFinal = kBarPFull + 2;
   static constexpr int kBarDrain = kBarFinal + 1;
@@ -1238,8 +1240,10 @@ attn_bwd_kernel(const __grid_constant__ BwdParams p) {
   if (threadIdx.x == 0) {
     mbar_init(bar(C::kBarRes), 1);
     for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(bar(C::kBarFull + s), KQ ? 2 : 1);  // key-tile kernel: copies + LSE/delta
-      mbar_init(bar(C::kBarEmpty + s), 1);
+      for (int hh = 0; hh < 2; ++hh) {
+        mbar_init(bar(C::kBarFull + 2 * s + hh), KQ ? 2 : 1);  // key-tile kernel: copies + LSE/delta
+        mbar_init(bar(C::kBarEmpty + 2 * s + hh), 1);
+      }
     }
     mbar_init(bar(C::kBarSFull + 0), 1);
     mbar_init(bar(C::kBarSFull + 1), 1);
@@ -1312,43 +1316,52 @@ attn_bwd_kernel(const __grid_constant__ BwdParams p) {
       }
     };
     if (KQ && nt > 0) load_lse(0);
-    int j = 0;
-    for (; j < nt; ++j) {
+    // streamed rows come in 64-row halves (their own tensor maps), each as
+    // soon as the same half of the stage is free
+    const CUtensorMap* str0h = KQ ? &p.q_map_h : &p.k_map_h;
+    const CUtensorMap* str1h = KQ ? &p.do_map_h : &p.v_map_h;
+    int nh = 0;  // half-stage loads issued
+    bool ok = true;
+    for (int j = 0; ok && j < nt; ++j) {
       const int st = j % C::kStages;
-      bool ok = true;
-      if (j >= C::kStages)
-        ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarEmpty + st), (uint32_t)(j / C::kStages - 1) & 1u,
-                                                  abort_flag, 0));
-      if (!ok) break;
       const uint32_t so = C::kStageOff + st * C::kStageBytes;
       const int row = tile_row(j);
-      if (lane == 0) {
-        mbar_arrive_expect_tx(bar(C::kBarFull + st), 2 * C::kTileBytes);
 #pragma unroll
-        for (int bx = 0; bx < C::kBoxes; ++bx) {
-          tma_load_4d(base_u32 + so + bx * C::kBoxBytes, str0, bar(C::kBarFull + st), bx * 64, row, h, b);
-          tma_load_4d(base_u32 + so + C::kTileBytes + bx * C::kBoxBytes, str1, bar(C::kBarFull + st), bx * 64,
-                      row, h, b);
-        }
-      }
-      if (KQ) {
-        float* ls = reinterpret_cast<float*>(base + so + 2 * C::kTileBytes);
-        float* dl = ls + 128;
+      for (int hh = 0; hh < 2; ++hh) {
+        const uint32_t fb = bar(C::kBarFull + 2 * st + hh);
+        if (j >= C::kStages)
+          ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarEmpty + 2 * st + hh),
+                                                    (uint32_t)(j / C::kStages - 1) & 1u, abort_flag, 0));
+        if (!ok) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(fb, 2u * C::kBoxes * (C::kBoxBytes / 2));
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          ls[lane + 32 * i] = lsr[i];
-          dl[lane + 32 * i] = dlr[i];
+          for (int bx = 0; bx < C::kBoxes; ++bx) {
+            const uint32_t off = so + bx * C::kBoxBytes + hh * (C::kBoxBytes / 2);
+            tma_load_4d(base_u32 + off, str0h, fb, bx * 64, row + 64 * hh, h, b);
+            tma_load_4d(base_u32 + off + C::kTileBytes, str1h, fb, bx * 64, row + 64 * hh, h, b);
+          }
         }
+        if (KQ) {
+          float* ls = reinterpret_cast<float*>(base + so + 2 * C::kTileBytes);
+          float* dl = ls + 128;
+#pragma unroll
+          for (int i = 2 * hh; i < 2 * hh + 2; ++i) {
+            ls[lane + 32 * i] = lsr[i];
+            dl[lane + 32 * i] = dlr[i];
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(fb);  // second arrival: the half's LSE and delta
+        }
+        ++nh;
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(C::kBarFull + st));  // second arrival: the stage's LSE and delta
-        if (j + 1 < nt) load_lse(j + 1);
       }
-      __syncwarp();
+      if (KQ && ok && j + 1 < nt) load_lse(j + 1);
     }
     if (lane == 0 && *abort_flag) {
       wait_drain(bar(C::kBarRes), 0);
-      for (int jj = max(0, j - C::kStages); jj < j; ++jj)
-        wait_drain(bar(C::kBarFull + jj % C::kStages), (uint32_t)(jj / C::kStages) & 1u);
+      for (int k = max(0, nh - 2 * C::kStages); k < nh; ++k)
+        wait_drain(bar(C::kBarFull + 2 * ((k >> 1) % C::kStages) + (k & 1)), (uint32_t)((k >> 1) / C::kStages) & 1u);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -1407,32 +1420,37 @@ attn_bwd_kernel(const __grid_constant__ BwdParams p) {
         accum(tmem + 256, 128u * h, dm0, st, h, first);           // dQ += dS K
       }
     };
-    auto wait_full = [&](int j) -> bool {
-      const bool r = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarFull + j % C::kStages),
+    auto wait_full = [&](int j, int hh) -> bool {
+      const bool r = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarFull + 2 * (j % C::kStages) + hh),
                                                           (uint32_t)(j / C::kStages) & 1u, abort_flag, 5));
       if (r) tc_fence_after();
       return r;
     };
     // order: S_0(0), S_1(0), then per tile j: G_0(j), S_0(j+1), G_1(j), S_1(j+1)
-    if (ok && nt > 0 && (ok = wait_full(0))) {
+    if (ok && nt > 0 && (ok = wait_full(0, 0))) {
       issue_scores(0, 0);
-      issue_scores(0, 1);
+      if ((ok = wait_full(0, 1))) issue_scores(0, 1);
     }
     for (int j = 0; ok && j < nt; ++j) {
+      const int st = j % C::kStages;
       if (!(ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarPFull + 0), (uint32_t)j & 1u, abort_flag, 2))))
         break;
       tc_fence_after();
       issue_accum(j, 0);
+      mma_commit_e(bar(C::kBarEmpty + 2 * st + 0));  // half 0 of tile j's stage is read for the last time
       if (j + 1 < nt) {
-        if (!(ok = wait_full(j + 1))) break;
+        if (!(ok = wait_full(j + 1, 0))) break;
         issue_scores(j + 1, 0);
       }
       if (!(ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarPFull + 1), (uint32_t)j & 1u, abort_flag, 3))))
         break;
       tc_fence_after();
       issue_accum(j, 1);
-      mma_commit_e(bar(C::kBarEmpty + j % C::kStages));  // stage of tile j is read for the last time
-      if (j + 1 < nt) issue_scores(j + 1, 1);
+      mma_commit_e(bar(C::kBarEmpty + 2 * st + 1));
+      if (j + 1 < nt) {
+        if (!(ok = wait_full(j + 1, 1))) break;
+        issue_scores(j + 1, 1);
+      }
     }
     if (ok) mma_commit_e(bar(C::kBarFinal));
     if (!ok) {

@@ -52,12 +52,12 @@ EncodeTiledFn encode_fn() {
 
 // 4-D bf16 map with coordinates (d, row, h, b) and a 64 x 128 box, 128-byte swizzle.
 bool encode_map(CUtensorMap* m, const void* ptr, int D, long long rows, int H, int B, size_t s_row,
-                size_t s_h, size_t s_b) {
+                size_t s_h, size_t s_b, int box_rows = kTileN) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
   const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)rows, (cuuint64_t)H, (cuuint64_t)B};
   const cuuint64_t strides[3] = {(cuuint64_t)s_row, (cuuint64_t)s_h, (cuuint64_t)s_b};
-  const cuuint32_t box[4] = {64, (cuuint32_t)kTileN, 1, 1};
+  const cuuint32_t box[4] = {64, (cuuint32_t)box_rows, 1, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -80,9 +80,9 @@ bool encode_head_major_u8(CUtensorMap* m, const void* ptr, int B, int H, long lo
 }
 
 // Token-major [B, L, H, D] bf16.
-bool encode_token_major(CUtensorMap* m, const void* ptr, int B, int L, int H, int D) {
+bool encode_token_major(CUtensorMap* m, const void* ptr, int B, int L, int H, int D, int box_rows = kTileN) {
   const size_t e = 2;
-  return encode_map(m, ptr, D, L, H, B, (size_t)H * D * e, (size_t)D * e, (size_t)L * H * D * e);
+  return encode_map(m, ptr, D, L, H, B, (size_t)H * D * e, (size_t)D * e, (size_t)L * H * D * e, box_rows);
 }
 
 // Head-major [B, H, rows, D] bf16.
@@ -761,7 +761,9 @@ static sab_status attention_backward(const void* Q, const void* K, const void* V
   p.scale = softmax_scale;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
   if (!encode_token_major(&p.q_map, Q, B, L, H, D) || !encode_token_major(&p.k_map, K, B, L, H, D) ||
-      !encode_token_major(&p.v_map, V, B, L, H, D) || !encode_token_major(&p.do_map, dO, B, L, H, D))
+      !encode_token_major(&p.v_map, V, B, L, H, D) || !encode_token_major(&p.do_map, dO, B, L, H, D) ||
+      !encode_token_major(&p.q_map_h, Q, B, L, H, D, 64) || !encode_token_major(&p.k_map_h, K, B, L, H, D, 64) ||
+      !encode_token_major(&p.v_map_h, V, B, L, H, D, 64) || !encode_token_major(&p.do_map_h, dO, B, L, H, D, 64))
     return SAB_ERR_CUDA;
   return launch_attention_backward(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SAB_OK : SAB_ERR_CUDA;
 }

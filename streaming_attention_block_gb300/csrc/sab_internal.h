@@ -194,6 +194,7 @@ struct RopeParams {
 // Backward of block-causal attention (token-major [B, L, H, D] tensors).
 struct BwdParams {
   CUtensorMap q_map, k_map, v_map, do_map;  // dims (D, L, H, B), box (64, 128, 1, 1), SW128
+  CUtensorMap q_map_h, k_map_h, v_map_h, do_map_h;  // the same with 64-row boxes (streamed halves)
   const uint16_t* O;      // forward output
   const uint16_t* dO;
   const float* LSE;       // [B, H, L] natural-log LSE of the forward
