@@ -194,42 +194,50 @@ __device__ __forceinline__ void plan_prefix_runs(const AttnParams& p, int b, int
   kp.total_tiles = t1 + (khi - klo + kTileN - 1) / kTileN;
 }
 
-// Expand one key/value row of 128 8-bit codes in place into 128 fp16 values
-// (the operand type of the 8-bit-cache path).  The codes sit in the second
-// 128-byte box of the row (where its upper 16-bit half goes); all of them are
-// read before any fp16 chunk is written, and the row is written in the
-// 128-byte-swizzled layout of the MMA operands.  One conversion instruction
-// per pair of E4M3 codes; two integer and two half-precision instructions per
-// four INT8 codes.  Exact for every code.
+// Expand two key/value rows (both K rows or both V rows of one tile) of 128
+// 8-bit codes each in place into 128 fp16 values (the operand type of the
+// 8-bit-cache path).  The codes sit in the second 128-byte box of a row
+// (where its upper 16-bit half goes); every code of both rows is read before
+// any fp16 chunk is written (the two rows' shared-memory latencies overlap),
+// and the rows are written in the 128-byte-swizzled layout of the MMA
+// operands.  A row's 16-byte code chunks are visited from chunk (row mod 8),
+// so the eight rows a quarter-warp touches read eight different bank groups
+// and write eight different ones through the swizzle.  One conversion
+// instruction per pair of E4M3 codes; two integer and two half-precision
+// instructions per four INT8 codes.  Exact for every code.
 template <bool K8>
-__device__ __forceinline__ void expand_code_row_f16(uint8_t* tile, int r, uint32_t box_bytes) {
-  // The row's 16-byte code chunks are visited starting at chunk (r & 7), so
-  // the eight rows of a quarter-warp read eight different bank groups, and
-  // write eight different ones through the swizzle: no bank conflicts.
-  const int rot = r & 7;
-  const uint8_t* src = tile + box_bytes + r * 128;
-  uint4 raw[8];
+__device__ __forceinline__ void expand_code_rows2_f16(uint8_t* tile, int ra, int rb, uint32_t box_bytes) {
+  const int rot[2] = {ra & 7, rb & 7};
+  const int rr[2] = {ra, rb};
+  uint4 raw[2][8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) raw[i] = *reinterpret_cast<const uint4*>(src + (((i + rot) & 7) << 4));
+  for (int w = 0; w < 2; ++w) {
+    const uint8_t* src = tile + box_bytes + rr[w] * 128;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int c = (i + rot) & 7;  // codes 16c .. 16c + 15
-    const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
-    uint32_t out[8];
+    for (int i = 0; i < 8; ++i) raw[w][i] = *reinterpret_cast<const uint4*>(src + (((i + rot[w]) & 7) << 4));
+  }
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      if constexpr (K8) {
-        s8x4_to_f16x4(w[q], out[2 * q], out[2 * q + 1]);
-      } else {
-        out[2 * q] = e4m3x2_to_f16x2((uint16_t)(w[q] & 0xFFFFu));
-        out[2 * q + 1] = e4m3x2_to_f16x2((uint16_t)(w[q] >> 16));
+  for (int w = 0; w < 2; ++w) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int c = (i + rot[w]) & 7;  // codes 16c .. 16c + 15
+      const uint32_t wd[4] = {raw[w][i].x, raw[w][i].y, raw[w][i].z, raw[w][i].w};
+      uint32_t out[8];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if constexpr (K8) {
+          s8x4_to_f16x4(wd[q], out[2 * q], out[2 * q + 1]);
+        } else {
+          out[2 * q] = e4m3x2_to_f16x2((uint16_t)(wd[q] & 0xFFFFu));
+          out[2 * q + 1] = e4m3x2_to_f16x2((uint16_t)(wd[q] >> 16));
+        }
       }
-    }
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      const int k = 2 * c + hh;  // 16-byte fp16 chunk of the row
-      *reinterpret_cast<uint4*>(tile + (k >> 3) * box_bytes + r * 128 + (((k & 7) ^ rot) << 4)) =
-          make_uint4(out[4 * hh], out[4 * hh + 1], out[4 * hh + 2], out[4 * hh + 3]);
+      for (int hh = 0; hh < 2; ++hh) {
+        const int k = 2 * c + hh;
+        *reinterpret_cast<uint4*>(tile + (k >> 3) * box_bytes + rr[w] * 128 + (((k & 7) ^ rot[w]) << 4)) =
+            make_uint4(out[4 * hh], out[4 * hh + 1], out[4 * hh + 2], out[4 * hh + 3]);
+      }
     }
   }
 }
@@ -1068,13 +1076,15 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
         const int st = u % C::kStages;
         if (!wait_bounded(bar(C::kBarRawFull + st), (uint32_t)(u / C::kStages) & 1u, abort_flag, 12)) break;
         const int job0 = u < n_tiles ? 0 : kTileN, job1 = u > 0 ? 2 * kTileN : kTileN;  // K rows, then V rows
+        // rows job and job + 64 of the same tensor (the job range is a
+        // multiple of 128 long)
   #pragma unroll 1
-        for (int job = job0 + ct; job < job1; job += C::kConvThreads) {
+        for (int job = job0 + ct; job < job1; job += 2 * C::kConvThreads) {
           const int r = job & (kTileN - 1);
           const bool isv = job >= kTileN;
           uint8_t* tile = base + (isv ? C::kVOff : C::kKOff) + st * C::kTileBytes;
-          if (p.k_int8 && !isv) expand_code_row_f16<true>(tile, r, C::kBoxBytes);  // INT8 keys
-          else expand_code_row_f16<false>(tile, r, C::kBoxBytes);
+          if (p.k_int8 && !isv) expand_code_rows2_f16<true>(tile, r, r + C::kConvThreads, C::kBoxBytes);  // INT8 keys
+          else expand_code_rows2_f16<false>(tile, r, r + C::kConvThreads, C::kBoxBytes);
         }
         fence_proxy_async_smem();
         mbar_arrive(bar(C::kBarKFull + st));
