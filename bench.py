@@ -500,15 +500,16 @@ def config_records(peaks, src, stream):
                 _group_us([make(l, w.splits, ws8) for l in range(layers)], 20, 8, stream), 2)
         rec(name, desc, us, flops, extra)
         if name == "fp8_kv":
-            def make8(l):
+            def make8(l, splits):
                 q = cur[l][0]
                 return lambda: sab.chunk_attention_fp8mma(ring.handle, l, c, q, w.W, w.sink, w.scale, O[l], L[l],
-                                                          stream)
+                                                          stream, num_splits=splits, workspace=ws)
 
-            us8 = _group_us([make8(l) for l in range(layers)], 20, 8, stream)
+            us8 = _group_us([make8(l, 0) for l in range(layers)], 20, 8, stream)
+            us8_1 = _group_us([make8(l, 1) for l in range(layers)], 20, 8, stream)
             rec("fp8_kv_e4m3_mma", desc + "; Q and P rounded to E4M3, kind::f8f6f4 products", us8, flops,
-                {"keys": nkeys}, peak=2 * bf16_peak,
-                peak_note=f"fp8 dense = 2 x bf16 dense burst (nominal ratio), {src}")
+                {"keys": nkeys, "splits": "library choice (0)", "us_per_call_unsplit": round(us8_1, 2)},
+                peak=2 * bf16_peak, peak_note=f"fp8 dense = 2 x bf16 dense burst (nominal ratio), {src}")
         del ring, cur, O, L
         torch.cuda.empty_cache()
 
@@ -714,13 +715,15 @@ def run_attn_only_fp8mma(args):
         ring.append(0, c, k, v)
     O = torch.empty_like(q)
     LSE = torch.empty((w.B, w.H, w.Lc), dtype=torch.float32, device="cuda")
+    ws = ring.workspace(0)
     stream = torch.cuda.current_stream()
     times = []
     for _ in range(args.attn_only):
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        sab.chunk_attention_fp8mma(ring.handle, 0, w.W, q, w.W, w.sink, w.scale, O, LSE, stream)
+        sab.chunk_attention_fp8mma(ring.handle, 0, w.W, q, w.W, w.sink, w.scale, O, LSE, stream, num_splits=0,
+                                   workspace=ws)
         b.record(stream)
         times.append((a, b))
     torch.cuda.synchronize()

@@ -236,20 +236,23 @@ sab_status sab_chunk_attention(const sab_ring* ring, int layer, long long chunk,
  * Worlds", sections 前置知识 / FP8 量化与 CUDA Graph and 技术新颖性: attention in
  * FP8 over an 8-bit KV cache).  Same key set and arguments as
  * sab_chunk_attention with K_cur = V_cur = NULL (the current chunk appended
- * first) and one split; the cached codes are used by the tensor cores as
- * stored.  Each query row is quantised on chip to E4M3 with its own absmax
- * scale (amax / 448, fp32 division, round to nearest even, satfinite -- the
- * cache's rule applied per row); the probabilities are rounded to E4M3 as
+ * first); num_splits, workspace and ws_bytes as there (0 = the library picks
+ * the split count, and a workspace of sab_chunk_attention_workspace bytes is
+ * then required).  The cached codes are used by the tensor cores as stored.
+ * Each query row is quantised on chip to E4M3 with its own absmax scale
+ * (amax / 448, fp32 division, round to nearest even, satfinite -- the cache's
+ * rule applied per row); the probabilities are rounded to E4M3 as
  * P * (vs / vs_ref) * 2^4 (vs: the key's V scale, vs_ref: the largest V scale
- * of the key set; the running max lags by at most 2^4, so the values stay
- * below 2^8) and the row sums are kept in fp32 from the unrounded values.
- * S = Q8 K8^T and O += P8 V8 accumulate in fp32.  O and LSE as in
- * sab_chunk_attention.
+ * of the key set; the running max lags by at most 2^4.75, so the values stay
+ * below 2^8.75 < 448) and the row sums are kept in fp32 from the unrounded
+ * values.  S = Q8 K8^T and O += P8 V8 accumulate in fp32; the splits' partial
+ * rows merge by log-sum-exp in fp32.  O and LSE as in sab_chunk_attention.
  * Requires a SAB_KV_FP8_E4M3 ring (UNSUPPORTED otherwise), D = 128.
  * Errors: as sab_chunk_attention.
  */
 sab_status sab_chunk_attention_fp8mma(const sab_ring* ring, int layer, long long chunk, const void* Q, int window,
-                                      int use_sink, float softmax_scale, void* O, float* LSE, void* stream);
+                                      int use_sink, int num_splits, float softmax_scale, void* O, float* LSE,
+                                      void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * Gradients of block-causal attention (training / causal adaptation:

@@ -86,7 +86,7 @@ def library() -> ctypes.CDLL:
         "sab_block_causal_attention_backward_workspace": (SZ, [I, I, I]),
         "sab_block_causal_attention_backward": (I, [P, P, P, P, P, P, I, I, I, I, I, I, F, P, P, P, P, SZ, P]),
         "sab_memory_prefix_attention": (I, [P, P, P, I, I, I, I, I, P, I, I, F, P, P, P]),
-        "sab_chunk_attention_fp8mma": (I, [P, I, LL, P, I, I, F, P, P, P]),
+        "sab_chunk_attention_fp8mma": (I, [P, I, LL, P, I, I, I, F, P, P, P, SZ, P]),
         "sab_memory_prefix_attention_backward": (I, [P, P, P, P, P, P, I, I, I, I, I, P, I, I, F, P, P, P, P, SZ,
                                                      P]),
         "sab_status_string": (ctypes.c_char_p, [I]),
@@ -276,13 +276,15 @@ def block_causal_attention_backward(Q, K, V, O, dO, LSE, chunk_tokens: int, wind
 
 
 def chunk_attention_fp8mma(handle, layer: int, chunk: int, Q, window: int, use_sink: bool, softmax_scale: float,
-                           O, LSE=None, stream=None):
+                           O, LSE=None, stream=None, num_splits: int = 1, workspace=None):
     """sab_chunk_attention_fp8mma: chunk attention over an E4M3 ring with Q and
-    P rounded to E4M3 for the tensor-core products (see include/sab.h)."""
+    P rounded to E4M3 for the tensor-core products (see include/sab.h);
+    ``num_splits`` and ``workspace`` as in ``chunk_attention``."""
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(library().sab_chunk_attention_fp8mma(
         handle, int(layer), int(chunk), _ptr(Q, torch.bfloat16, "Q"), int(window), 1 if use_sink else 0,
-        float(softmax_scale), _ptr(O, torch.bfloat16, "O"), _ptr(LSE, torch.float32, "LSE"), _stream(stream)),
-        "chunk_attention_fp8mma")
+        int(num_splits), float(softmax_scale), _ptr(O, torch.bfloat16, "O"), _ptr(LSE, torch.float32, "LSE"),
+        _ptr(workspace, None, "workspace"), ws_bytes, _stream(stream)), "chunk_attention_fp8mma")
 
 
 def memory_prefix_attention(Q, K, V, mem_pad: int, mem_len, chunk_tokens: int, window: int, softmax_scale: float,

@@ -47,7 +47,9 @@ constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per pipeline wait
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows by > 2^8
-constexpr float kRescaleThresholdF8 = 4.0f;  // E4M3 P: by > 2^4 (P' = P * 2^4 * vs / vs_ref <= 2^8)
+// E4M3 P: by > 2^4.75, so that P' = P * 2^4 * vs / vs_ref <= 2^8.75 ~ 430.5
+// stays below the largest code 448 = 2^8.807
+constexpr float kRescaleThresholdF8 = 4.75f;
 constexpr int kScaleTab = 64;  // per-chunk coefficient table entries (1 KB of shared memory)
 
 __device__ __forceinline__ uint64_t global_ns() {
@@ -434,7 +436,7 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
     //    the cache's quantiser does per chunk; the division in fp32), into a
     //    separate buffer; P is formed as P * (vs / vs_ref) * 2^4 so that the
     //    codes of V are used as stored and P stays out of the subnormals (the
-    //    running max lags by at most 2^4, so P' <= 2^8 < 448).
+    //    running max lags by at most 2^4.75, so P' <= 2^8.75 < 448).
     //  * 16-bit products: Q converted in place to fp16 times 2^e, with e
     //    chosen per row so that the row's absmax lands in [2^14, 2^15): exact
     //    for every value down to 2^-28 of the row's absmax (and below that an
@@ -649,10 +651,14 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
           }
         }
       };
-      // Exponentials are taken against the running max m_run right away, in
-      // parallel with the row max; only when the max grows by more than the
-      // rescale threshold (always on a row's first visible tile) are they
-      // recomputed against the new max, with O and l rescaled.
+      // 16-bit P: exponentials are taken against the running max m_run right
+      // away, in parallel with the row max; only when the max grows by more
+      // than the rescale threshold (always on a row's first visible tile) are
+      // they recomputed against the new max, with O and l rescaled.  E4M3 P:
+      // the narrow range makes rescales frequent (a warp rescales when any of
+      // its 32 rows does), so the max comes first and the exponentials are
+      // taken once.
+      constexpr bool kSpeculate = !F8MMA;
       const float mb0 = (m_run == -INFINITY) ? 0.f : m_run;
       const float xa = straddle ? 1.f : c0;
       uint32_t pk[32];
@@ -660,10 +666,10 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
       tmem_wait_ld();
       prep(s0, 0);
       const float mx0 = max32(s0);
-      exps32(s0, 0, xa, straddle ? -mb0 : d0 - mb0, pk, psa);
+      if constexpr (kSpeculate) exps32(s0, 0, xa, straddle ? -mb0 : d0 - mb0, pk, psa);
       prep(s1, 32);
       const float mx1 = max32(s1);
-      exps32(s1, 32, xa, straddle ? -mb0 : d0 - mb0, pk + (F8MMA ? 8 : 16), psb);
+      if constexpr (kSpeculate) exps32(s1, 32, xa, straddle ? -mb0 : d0 - mb0, pk + 16, psb);
       const float mx = fmaxf(mx0, mx1);
       const float m_new = fmaxf(m_run, straddle ? mx : mx * c0);
       const bool need = m_new > m_run + (F8MMA ? kRescaleThresholdF8 : kRescaleThreshold);
@@ -684,19 +690,26 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
           if (!ok) break;
           tc_fence_after();
 #pragma unroll 1
-          for (int cc = 0; cc < D; cc += 16) {
-            uint32_t o[16];
-            tmem_ld16(tO + cc, o);
+          for (int cc = 0; cc < D; cc += 32) {
+            uint32_t o[32];
+            tmem_ld32(tO + cc, o);
             tmem_wait_ld();
 #pragma unroll
-            for (int c = 0; c < 16; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-            tmem_st16(tO + cc, o);
+            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+            tmem_st32(tO + cc, o);
           }
         }
+        if constexpr (kSpeculate) {
+          const float mb = (m_run == -INFINITY) ? 0.f : m_run;
+          psa = psb = make_float2(0.f, 0.f);
+          exps32(s0, 0, xa, straddle ? -mb : d0 - mb, pk, psa);
+          exps32(s1, 32, xa, straddle ? -mb : d0 - mb, pk + 16, psb);
+        }
+      }
+      if constexpr (!kSpeculate) {
         const float mb = (m_run == -INFINITY) ? 0.f : m_run;
-        psa = psb = make_float2(0.f, 0.f);
         exps32(s0, 0, xa, straddle ? -mb : d0 - mb, pk, psa);
-        exps32(s1, 32, xa, straddle ? -mb : d0 - mb, pk + (F8MMA ? 8 : 16), psb);
+        exps32(s1, 32, xa, straddle ? -mb : d0 - mb, pk + 8, psb);
       }
       if constexpr (F8MMA) tmem_st16(tS, *reinterpret_cast<const uint32_t(*)[16]>(pk));
       else tmem_st32(tS, pk);

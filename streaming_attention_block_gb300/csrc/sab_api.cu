@@ -499,12 +499,13 @@ sab_status sab_chunk_attention(const sab_ring* ring, int layer, long long chunk,
 }
 
 sab_status sab_chunk_attention_fp8mma(const sab_ring* ring, int layer, long long chunk, const void* Q, int window,
-                                      int use_sink, float softmax_scale, void* O, float* LSE, void* stream) {
+                                      int use_sink, int num_splits, float softmax_scale, void* O, float* LSE,
+                                      void* workspace, size_t ws_bytes, void* stream) {
   if (ring == nullptr) return SAB_ERR_INVALID_ARG;
   if (ring->d.kv_dtype != SAB_KV_FP8_E4M3) return SAB_ERR_UNSUPPORTED;
   AttnParams p;
-  const sab_status st =
-      plan_chunk_attention(ring, layer, chunk, Q, nullptr, nullptr, window, use_sink, 1, softmax_scale, O, LSE, p);
+  const sab_status st = plan_chunk_attention(ring, layer, chunk, Q, nullptr, nullptr, window, use_sink, num_splits,
+                                             softmax_scale, O, LSE, p);
   if (st != SAB_OK) return st;
   p.f8mma = 1;
   // the tensor cores read the code tiles as K-major / MN-major operands in
@@ -513,7 +514,7 @@ sab_status sab_chunk_attention_fp8mma(const sab_ring* ring, int layer, long long
   if (!encode_head_major_u8(&p.k_map[0], ring->k(layer), d.batch, d.heads, ring->g.rows, d.head_dim, true) ||
       !encode_head_major_u8(&p.v_map[0], ring->v(layer), d.batch, d.heads, ring->g.rows, d.head_dim, true))
     return SAB_ERR_CUDA;
-  return launch_attention(p, ring->d.chunk_tokens, 1, nullptr, 0, stream);
+  return launch_attention(p, ring->d.chunk_tokens, num_splits, workspace, ws_bytes, stream);
 }
 
 sab_status sab_chunk_attention_dev(const sab_ring* ring, int layer, const long long* d_chunk, const void* Q,

@@ -50,9 +50,10 @@ def _quantised(x_blhd):
     return deq, scales
 
 
-def _stream(w, check_chunks, rows=None):
-    """Append-first stream over an E4M3 ring; at ``check_chunks`` compare every
-    (b, h) on ``rows``.  Returns the worst error / tolerance ratio and, per
+def _stream(w, check_chunks, rows=None, splits=1):
+    """Append-first stream over an E4M3 ring (``splits`` KV partitions, 0 =
+    the library's choice); at ``check_chunks`` compare every (b, h) on
+    ``rows``.  Returns the worst error / tolerance ratio and, per
     checked chunk, the mean error and the predicted mean rounding error."""
     gen = synth.generator(w.seed)
     ring = sab.KVRing(1, w.B, w.H, w.D, w.Lc, w.R, has_sink=w.sink, kv_dtype=sab.KV_FP8_E4M3)
@@ -65,6 +66,7 @@ def _stream(w, check_chunks, rows=None):
         oring.set_sink(kq, vq)
         vscale[OA.SINK_CHUNK] = vsc
     worst, stats = 0.0, []
+    ws = ring.workspace(splits) if splits != 1 else None
     rsel = slice(None) if rows is None else rows
     for c in range(w.chunks):
         q, k, v = synth.chunk_qkv(w, gen)
@@ -74,7 +76,8 @@ def _stream(w, check_chunks, rows=None):
         vscale[c] = vsc
         O = torch.empty((w.B, w.Lc, w.H, w.D), dtype=torch.bfloat16, device="cuda")
         LSE = torch.empty((w.B, w.H, w.Lc), dtype=torch.float32, device="cuda")
-        sab.chunk_attention_fp8mma(ring.handle, 0, c, q.cuda(), w.W, w.sink, w.scale, O, LSE)
+        sab.chunk_attention_fp8mma(ring.handle, 0, c, q.cuda(), w.W, w.sink, w.scale, O, LSE, num_splits=splits,
+                                   workspace=ws)
         if c not in check_chunks:
             continue
         torch.cuda.synchronize()
@@ -106,18 +109,23 @@ def _stream(w, check_chunks, rows=None):
     return worst, stats
 
 
-def test_fp8mma_small_elementwise():
+@pytest.mark.parametrize("splits", [1, 3, 0], ids=["unsplit", "3splits", "auto"])
+def test_fp8mma_small_elementwise(splits):
     """Sink + 3-slot ring, 200-token chunks (key tiles straddle chunks),
-    window 2, 1% x8 outliers; every row of chunks 0, 1, 3 and 5."""
+    window 2, 1% x8 outliers; every row of chunks 0, 1, 3 and 5, unsplit, in
+    three KV partitions merged by log-sum-exp, and with the library's split
+    choice."""
     w = synth.Workload("f8s", B=1, H=2, D=128, Lc=200, R=3, W=2, chunks=6, sink=True, kcur_separate=False,
                        kv_fp8=True, outliers=True, seed=41)
-    _stream(w, {0, 1, 3, 5})
+    _stream(w, {0, 1, 3, 5}, splits=splits)
 
 
-def test_fp8mma_full_size_sampled_rows():
+@pytest.mark.parametrize("splits", [1, 0], ids=["unsplit", "auto"])
+def test_fp8mma_full_size_sampled_rows(splits):
     """Long-window FP8 workload (H24, 405-token chunks, sink + 20-slot ring,
     window 19, 60 chunks so the ring wraps 3 times): sampled rows of chunks
-    around the wraps, every head."""
+    around the wraps, every head; unsplit and with the library's split choice
+    (the launch the benchmark times)."""
     w = synth.workload("fp8_kv")
     rows = np.concatenate([np.arange(0, w.Lc, 9), [w.Lc - 1]])
-    _stream(w, {0, 19, 20, 40, 59}, rows=rows)
+    _stream(w, {0, 19, 20, 40, 59}, rows=rows, splits=splits)
