@@ -242,8 +242,8 @@ sab_status sab_chunk_attention(const sab_ring* ring, int layer, long long chunk,
  * Each query row is quantised on chip to E4M3 with its own absmax scale
  * (amax / 448, fp32 division, round to nearest even, satfinite -- the cache's
  * rule applied per row); the probabilities are rounded to E4M3 as
- * P * (vs / vs_ref) * 2^4 (vs: the key's V scale, vs_ref: the largest V scale
- * of the key set; the running max lags by at most 2^4.75, so the values stay
+ * P * (vs / vs_ref) * 2^3 (vs: the key's V scale, vs_ref: the largest V scale
+ * of the key set; the running max lags by at most 2^5.75, so the values stay
  * below 2^8.75 < 448) and the row sums are kept in fp32 from the unrounded
  * values.  S = Q8 K8^T and O += P8 V8 accumulate in fp32; the splits' partial
  * rows merge by log-sum-exp in fp32.  O and LSE as in sab_chunk_attention.

@@ -25,8 +25,8 @@ P'_j = P_j * r_j * 2^(g + delta), where P_j = exp(s_j - max) <= 1,
 r_j = vs_j / vs_ref <= 1 is the key's V scale relative to the largest V scale
 of the visible keys (the V scales are applied before the rounding so that the
 product uses the codes as stored), g is a fixed gain that lifts the values
-out of the subnormal range (the kernel uses g = 4 with a running-max slack
-of at most 2^4.75, so P' <= 2^8.75 < 448), and delta >= 0 accounts for a running
+out of the subnormal range (the kernel uses g = 3 with a running-max slack
+of at most 2^5.75, so P' <= 2^8.75 < 448), and delta >= 0 accounts for a running
 maximum that has not yet caught up (the values are then larger, never
 smaller).  E4M3 rounding to nearest changes a value by at most 2^-4 of itself
 when it is normal (>= 2^-6) and by at most 2^-10 (half the subnormal spacing
@@ -68,7 +68,7 @@ def quantize_rows(q: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
     return out, sc
 
 
-P_GAIN_LOG2 = 4  # g of the module docstring
+P_GAIN_LOG2 = 3  # g of the module docstring
 
 
 def p_rounding_error(p: np.ndarray, r: np.ndarray, gain_log2: int = P_GAIN_LOG2) -> np.ndarray:

@@ -47,9 +47,9 @@ constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per pipeline wait
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows by > 2^8
-// E4M3 P: by > 2^4.75, so that P' = P * 2^4 * vs / vs_ref <= 2^8.75 ~ 430.5
+// E4M3 P: by > 2^5.75, so that P' = P * 2^3 * vs / vs_ref <= 2^8.75 ~ 430.5
 // stays below the largest code 448 = 2^8.807
-constexpr float kRescaleThresholdF8 = 4.75f;
+constexpr float kRescaleThresholdF8 = 5.75f;
 constexpr int kScaleTab = 64;  // per-chunk coefficient table entries (1 KB of shared memory)
 
 __device__ __forceinline__ uint64_t global_ns() {
@@ -434,9 +434,9 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
     // row's absmax through shared memory).
     //  * E4M3 products: Q quantised to E4M3 with one absmax scale per row (as
     //    the cache's quantiser does per chunk; the division in fp32), into a
-    //    separate buffer; P is formed as P * (vs / vs_ref) * 2^4 so that the
+    //    separate buffer; P is formed as P * (vs / vs_ref) * 2^3 so that the
     //    codes of V are used as stored and P stays out of the subnormals (the
-    //    running max lags by at most 2^4.75, so P' <= 2^8.75 < 448).
+    //    running max lags by at most 2^5.75, so P' <= 2^8.75 < 448).
     //  * 16-bit products: Q converted in place to fp16 times 2^e, with e
     //    chosen per row so that the row's absmax lands in [2^14, 2^15): exact
     //    for every value down to 2^-28 of the row's absmax (and below that an
@@ -515,7 +515,7 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
         for (int c = kp.seg[i].row0 / p.chunk_tokens; c <= c_hi; ++c) vmax = fmaxf(vmax, __ldg(p.v_scale + srow + c));
       }
       const float vref = vmax > 0.f ? vmax : 1.f;
-      constexpr float kGain = F8MMA ? 16.f : 64.f;
+      constexpr float kGain = F8MMA ? 8.f : 64.f;
       vgain = __fdiv_rn(kGain, vref);
       ofac = vref * (1.f / kGain);
       // The per-chunk coefficients of this (b, h) go to a shared table (over
@@ -533,6 +533,7 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
         named_bar_sync(1, 256);
       }
     }
+    int rec_si = 0, rec_end = 0;  // 8-bit cache: lane L's record of tile 32 * (j / 32) + L
     for (int j = 0; ok && j < n_tiles; ++j) {
       ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarSFull + (j & 1)), (uint32_t)(j >> 1) & 1u,
                                                 abort_flag, 6 + hf));
@@ -545,17 +546,22 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
       int lo, hi;
       int tile_row0 = 0;
       const int g = first + j;
-      if (p.mode != kModeBlockCausal) {
-        int sg = 0;
+      // key run of plan tile gg: its index, first plan tile, rows and first row
+      auto seg_of = [&](int gg, int& sg, int& t0, int& nr, int& r0) {
+        sg = 0;
 #pragma unroll
-        for (int i = 1; i < kMaxSegments; ++i) sg = (g >= seg_tile0[i]) ? i : sg;
-        int t0 = seg_tile0[0], nr = seg_rows[0], r0 = seg_row0[0];
+        for (int i = 1; i < kMaxSegments; ++i) sg = (gg >= seg_tile0[i]) ? i : sg;
+        t0 = seg_tile0[0], nr = seg_rows[0], r0 = seg_row0[0];
 #pragma unroll
         for (int i = 1; i < kMaxSegments; ++i) {
           t0 = (sg == i) ? seg_tile0[i] : t0;
           nr = (sg == i) ? seg_rows[i] : nr;
           r0 = (sg == i) ? seg_row0[i] : r0;
         }
+      };
+      if (p.mode != kModeBlockCausal) {
+        int sg, t0, nr, r0;
+        seg_of(g, sg, t0, nr, r0);
         tile_row0 = r0 + (g - t0) * kTileN;
         if (p.mode == kModeStreaming) {
           lo = 0;
@@ -575,9 +581,18 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
       float c0 = slq, c1 = slq, d0 = 0.f, v0 = 1.f, v1 = 1.f, iv0 = 1.f;
       int bnd = 64;
       if constexpr (FP8) {
-        const int si0 = min(tile_row0 / p.chunk_tokens, p.scale_stride - 1);
+        if ((j & 31) == 0) {
+          // lane L works out the first chunk of tile j + L and where it ends
+          // (rows from the tile's first), once for the next 32 tiles
+          int sg, t0, nr, r0;
+          seg_of(g + lane, sg, t0, nr, r0);
+          const int tr = r0 + (g + lane - t0) * kTileN;
+          rec_si = min(tr / p.chunk_tokens, p.scale_stride - 1);
+          rec_end = (rec_si + 1) * p.chunk_tokens - tr;
+        }
+        const int si0 = __shfl_sync(0xffffffffu, rec_si, j & 31);
         const int si1 = min(si0 + 1, p.scale_stride - 1);
-        bnd = (si0 + 1) * p.chunk_tokens - tile_row0 - kofs;
+        bnd = __shfl_sync(0xffffffffu, rec_end, j & 31) - kofs;
         // the half's keys before `bnd` belong to chunk si0, the rest to si1
         float4 e0, e1;
         if (p.scale_stride <= kScaleTab) {

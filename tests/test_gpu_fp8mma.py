@@ -12,8 +12,8 @@ to the oracle's statistical model of the rounding: over each checked call,
 mean |error| <= 1.25 x mean(sqrt(2/pi) sigma) + 2^-10 mean |O| + 1e-4, with
 sigma the standard deviation of uniform rounding of every P to E4M3 and the
 second term the bf16 rounding of the output.  The kernel's mean error is
-0.82-1.03 of the model's on these workloads; a P rounding toward zero
-instead of to nearest lands at 1.23-1.34 of the limit
+0.88-0.99 of the model's on these workloads; a P rounding toward zero
+instead of to nearest lands at 1.22-1.32 of the limit
 (``tests/test_oracle_fp8mma.py::test_mean_check_rejects_truncated_p``)."""
 
 import numpy as np
