@@ -129,3 +129,37 @@ def test_fp8mma_full_size_sampled_rows(splits):
     w = synth.workload("fp8_kv")
     rows = np.concatenate([np.arange(0, w.Lc, 9), [w.Lc - 1]])
     _stream(w, {0, 19, 20, 40, 59}, rows=rows, splits=splits)
+
+
+def test_fp8mma_argument_errors():
+    """Host-side refusals of the E4M3-product entry: a bf16 ring is
+    UNSUPPORTED, a split call without a workspace (explicit splits, or the
+    library's choice when it picks more than one) is WORKSPACE, a workspace
+    sized for fewer splits is WORKSPACE, a split count past the limit is
+    INVALID_ARG; nothing is launched for any of them."""
+    w = synth.Workload("f8e", B=1, H=2, D=128, Lc=256, R=3, W=2, kv_fp8=True, seed=43)
+    ring = sab.KVRing(1, w.B, w.H, w.D, w.Lc, w.R, kv_dtype=sab.KV_FP8_E4M3)
+    gen = synth.generator(w.seed)
+    for c in range(3):
+        q, k, v = synth.chunk_qkv(w, gen)
+        ring.append(0, c, k.cuda(), v.cuda())
+    qd = q.cuda()
+    O = torch.full_like(qd, 7.0)
+    LSE = torch.empty((w.B, w.H, w.Lc), dtype=torch.float32, device="cuda")
+    with pytest.raises(sab.SabError) as e:
+        sab.chunk_attention_fp8mma(ring.handle, 0, 2, qd, w.W, False, w.scale, O, LSE, num_splits=3)
+    assert e.value.status == 4  # SAB_ERR_WORKSPACE
+    small = ring.workspace(2)
+    with pytest.raises(sab.SabError) as e:
+        sab.chunk_attention_fp8mma(ring.handle, 0, 2, qd, w.W, False, w.scale, O, LSE, num_splits=3, workspace=small)
+    assert e.value.status == 4
+    with pytest.raises(sab.SabError) as e:
+        sab.chunk_attention_fp8mma(ring.handle, 0, 2, qd, w.W, False, w.scale, O, LSE, num_splits=1 << 20)
+    assert e.value.status == 1  # SAB_ERR_INVALID_ARG
+    bring = sab.KVRing(1, w.B, w.H, w.D, w.Lc, w.R)
+    with pytest.raises(sab.SabError) as e:
+        sab.chunk_attention_fp8mma(bring.handle, 0, 0, qd, w.W, False, w.scale, O, LSE)
+    assert e.value.status == 2  # SAB_ERR_UNSUPPORTED
+    torch.cuda.synchronize()
+    assert bool((O == 7.0).all())
+    assert sab.get_last_device_error() == 0
