@@ -11,6 +11,7 @@ import pytest
 import torch
 
 from oracle import attention as OA
+from oracle import ring as OR
 from oracle.ring import expected_physical_slots
 from streaming_attention_block_gb300 import KVRing, SabError, synth
 import streaming_attention_block_gb300 as sab
@@ -97,6 +98,13 @@ def test_append_order_and_state():
         ring.append(0, 4, k, v)
     ring.append(0, 6, k, v)
     ring.append(0, 7, k, v)
+    # the held chunks map to slot chunk mod R; older, newer or never-appended
+    # chunks are OUT_OF_RANGE (the oracle's ring model: slot_of)
+    assert ring.slot_of(0, 7) == OR.slot_of(7, w.R) and ring.slot_of(0, 6) == OR.slot_of(6, w.R)
+    for layer, chunk in ((0, 5), (0, 8), (1, 0)):
+        with pytest.raises(SabError) as e:
+            ring.slot_of(layer, chunk)
+        assert e.value.status == 3
     n, h, s = sab.kv_ring_get_state(ring.handle, 2)
     assert n == [7, -1] and h == [2, 0] and s == [0, 0]
     sab.kv_ring_set_state(ring.handle, [3, 0], [2, 1], [0, 0])
