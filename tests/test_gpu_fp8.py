@@ -135,12 +135,13 @@ def test_fp8_attention_small(name, w, splits):
 
 
 def test_fp8_long_window_sampled_rows():
-    """FP8 cache at the sink + 20-slot ring shape, 60 chunks, 8 KV splits."""
+    """FP8 cache at the sink + 20-slot ring shape, 60 chunks, 8 KV splits;
+    checked on both sides of every wrap ({0, 1, 18, 19, 20, 21, 39, 40, 59})."""
     w = synth.workload("fp8_kv")
     rows = np.concatenate([np.arange(0, 405, 9), [404]])
     ring = _ring(w)
-    res, _ = run_stream(w, ring, check_chunks={0, 19, 20, 40, 59}, rows=rows, on_check=_fp8)
-    assert len(res) == 5
+    res, _ = run_stream(w, ring, check_chunks={0, 1, 18, 19, 20, 21, 39, 40, 59}, rows=rows, on_check=_fp8)
+    assert len(res) == 9
     assert sab.get_last_device_error() == 0
 
 

@@ -123,12 +123,12 @@ def test_fp8mma_small_elementwise(splits):
 @pytest.mark.parametrize("splits", [1, 0], ids=["unsplit", "auto"])
 def test_fp8mma_full_size_sampled_rows(splits):
     """Long-window FP8 workload (H24, 405-token chunks, sink + 20-slot ring,
-    window 19, 60 chunks so the ring wraps 3 times): sampled rows of chunks
-    around the wraps, every head; unsplit and with the library's split choice
-    (the launch the benchmark times)."""
+    window 19, 60 chunks so the ring wraps 3 times): sampled rows of the
+    chunks on both sides of every wrap, every head; unsplit and with the
+    library's split choice (the launch the benchmark times)."""
     w = synth.workload("fp8_kv")
     rows = np.concatenate([np.arange(0, w.Lc, 9), [w.Lc - 1]])
-    _stream(w, {0, 19, 20, 40, 59}, rows=rows, splits=splits)
+    _stream(w, {0, 1, 18, 19, 20, 21, 39, 40, 59}, rows=rows, splits=splits)
 
 
 def test_fp8mma_argument_errors():
