@@ -147,11 +147,11 @@ def test_fp8_long_window_sampled_rows():
 
 def test_fp8_long_window_auto_sampled_rows():
     """The same stream through the library's own launch choice
-    (num_splits = 0, as the benchmark times it) at the wrap chunks."""
+    (num_splits = 0, as the benchmark times it) on both sides of every wrap."""
     w = synth.workload("fp8_kv")
     rows = np.concatenate([np.arange(0, 405, 7), [404]])
-    res, _ = run_stream(w, _ring(w), check_chunks={0, 19, 20, 39, 40, 59}, rows=rows, splits=0, on_check=_fp8)
-    assert len(res) == 6
+    res, _ = run_stream(w, _ring(w), check_chunks={0, 1, 18, 19, 20, 21, 39, 40, 59}, rows=rows, splits=0, on_check=_fp8)
+    assert len(res) == 9
     assert sab.get_last_device_error() == 0
 
 

@@ -99,9 +99,9 @@ def test_int8k_attention_small(name, w, splits):
 
 def test_int8k_long_window_sampled_rows():
     """INT8-key cache at the sink + 20-slot ring shape, 60 chunks, library's
-    launch choice (as the benchmark times it), at the wrap chunks."""
+    launch choice (as the benchmark times it), on both sides of every wrap."""
     w = synth.workload("int8k_kv")
     rows = np.concatenate([np.arange(0, 405, 7), [404]])
-    res, _ = run_stream(w, _ring(w), check_chunks={0, 19, 20, 39, 40, 59}, rows=rows, splits=0, on_check=_deq)
-    assert len(res) == 6
+    res, _ = run_stream(w, _ring(w), check_chunks={0, 1, 18, 19, 20, 21, 39, 40, 59}, rows=rows, splits=0, on_check=_deq)
+    assert len(res) == 9
     assert sab.get_last_device_error() == 0

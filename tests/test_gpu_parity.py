@@ -240,12 +240,12 @@ def test_long_sink_stream_sampled_rows():
 def test_long_sink_stream_auto_sampled_rows():
     """The same stream through the library's own launch choice
     (num_splits = 0, the configuration the benchmark times), checked at the
-    wrap chunks {0, 19, 20, 39, 40, 59}."""
+    chunks on both sides of every wrap."""
     w = synth.workload("long_sink")
     ring = _ring(w)
     rows = np.concatenate([np.arange(0, 405, 5), [383, 384, 404]])
-    res, _ = run_stream(w, ring, check_chunks={0, 19, 20, 39, 40, 59}, rows=rows, splits=0, on_check=compare)
-    assert len(res) == 6
+    res, _ = run_stream(w, ring, check_chunks={0, 1, 18, 19, 20, 21, 39, 40, 59}, rows=rows, splits=0, on_check=compare)
+    assert len(res) == 9
     _check_device_error()
 
 
