@@ -114,6 +114,8 @@ def test_validation_before_any_cuda_call(lib):
     assert lib.sab_chunk_counter_add(None, 1, None) == 1
     assert lib.sab_chunk_counter_add(ctypes.c_void_p(4100), 1, None) == 1
     assert lib.sab_selftest_bounded_wait(10, None) == 1  # limit outside 1 ms .. 2 s
+    # E4M3-product entry: no ring
+    assert lib.sab_chunk_attention_fp8mma(None, 0, 0, p, 2, 0, 1, 0.1, p, None, None, 0, None) == 1
     assert lib.sab_kv_ring_destroy(None) == 0
 
 
