@@ -942,6 +942,9 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
           if (u >= C::kStages &&
               !wait_bounded(bar(C::kBarKVEmpty + st), (uint32_t)(u / C::kStages - 1) & 1u, abort_flag, 0))
             break;
+          // the first product's operands (Q, K(0)) land before the later
+          // stages are requested
+          if (!FP8 && u == 1 && !wait_bounded(bar(C::kBarKFull + 0), 0, abort_flag, 0)) break;
           const bool has_k = u < n_tiles, has_v = u > 0;
           const Tile tk = tile_at(p, kp, first + (has_k ? u : u - 1));
           const Tile tv = tile_at(p, kp, first + (has_v ? u - 1 : u));
