@@ -129,6 +129,10 @@ SMALL = [
                                             kcur_separate=False, seed=13), 4),
     ("d64_window1", synth.Workload("d64", B=1, H=3, D=64, Lc=160, R=2, W=1, chunks=5, seed=14), 1),
     ("window0_R1", synth.Workload("w0", B=1, H=2, D=128, Lc=130, R=1, W=0, chunks=3, seed=15), 2),
+    # the sink and the current chunk only (window 0), current chunk passed in / appended first
+    ("sink_window0_kcur", synth.Workload("sw0", B=2, H=2, D=64, Lc=96, R=1, W=0, chunks=4, sink=True, seed=17), 1),
+    ("sink_window0_in_ring", synth.Workload("sw1", B=1, H=3, D=128, Lc=200, R=1, W=0, chunks=4, sink=True,
+                                            kcur_separate=False, seed=18), 3),
     ("many_empty_splits", synth.Workload("es", B=1, H=2, D=128, Lc=96, R=2, W=2, chunks=4, seed=16), 9),
 ]
 
