@@ -146,7 +146,9 @@ def test_streaming_small_elementwise(name, w, splits):
 
 
 @pytest.mark.parametrize("Lc,W,L_chunks,H,D,splits", [(200, 2, 5, 2, 128, 1), (256, 2, 6, 2, 128, 2),
-                                                      (128, 1, 7, 3, 64, 1), (96, 3, 5, 1, 128, 3)])
+                                                      (128, 1, 7, 3, 64, 1), (96, 3, 5, 1, 128, 3),
+                                                      (160, 0, 4, 2, 128, 1),   # chunk-local only
+                                                      (64, 8, 5, 2, 64, 2)])   # window past the start: causal
 def test_block_causal_small_elementwise(Lc, W, L_chunks, H, D, splits):
     w = synth.Workload("bc", B=2, H=H, D=D, Lc=Lc, W=W, seq_chunks=L_chunks, seed=21)
     q, k, v = synth.full_sequence_qkv(w, synth.generator(21))
