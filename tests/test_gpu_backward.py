@@ -32,6 +32,8 @@ CASES = [
     ("aligned", 1, 640, 2, 128, 128, 1),
     ("ragged_d64", 2, 500, 2, 64, 100, 2),
     ("long_chunks", 1, 3 * 1536, 2, 128, 1536, 2),
+    ("chunk_local_w0", 1, 384, 2, 128, 128, 0),
+    ("window_past_start", 1, 448, 1, 128, 64, 9),
 ]
 
 
