@@ -173,6 +173,11 @@ ORACLE_CASES = [
     # E4M3 ring, sink, current chunk in the ring, outliers
     ("fp8_sink_inring", synth.Workload("go", B=1, H=2, D=128, Lc=160, R=3, W=2, chunks=8, steps=1, sink=True,
                                        kcur_separate=False, kv_fp8=True, outliers=True, seed=93)),
+    # INT8 keys / E4M3 values, sink, current chunk in the ring
+    ("int8k_sink_inring", synth.Workload("go", B=1, H=2, D=128, Lc=160, R=3, W=2, chunks=8, steps=1, sink=True,
+                                         kcur_separate=False, kv_fp8=True, kv_int8k=True, outliers=True, seed=94)),
+    # a window shorter than the ring: the device planner takes the newest chunks only
+    ("kcur_window1_R4", synth.Workload("go", B=1, H=2, D=128, Lc=192, R=4, W=1, chunks=9, steps=1, seed=95)),
 ]
 
 
@@ -180,6 +185,7 @@ ORACLE_CASES = [
 def test_graph_replay_matches_oracle(name, w):
     layers, S = 2, w.steps
     fp8 = bool(w.kv_fp8)
+    int8k = bool(w.kv_int8k)
     shape = (w.B, w.Lc, w.H, w.D)
     mk = lambda: KVRing(layers, w.B, w.H, w.D, w.Lc, w.R, has_sink=w.sink, kv_dtype=_kv_dtype(w))
     # one-time kernel attribute set-up happens outside the capture
@@ -201,7 +207,7 @@ def test_graph_replay_matches_oracle(name, w):
         sk, sv = synth.sink_kv(w, gen)
         for l in range(layers):
             ring.set_sink(l, sk.cuda(), sv.cuda())
-            orings[l].set_sink(*oracle_kv(sk, sv, fp8))
+            orings[l].set_sink(*oracle_kv(sk, sv, fp8, int8k))
     bufs = {(s, l): [torch.empty(shape, dtype=torch.bfloat16, device="cuda") for _ in range(3)]
             for s in range(S) for l in range(layers)}
     outs = {(s, l): (torch.empty(shape, dtype=torch.bfloat16, device="cuda"),
@@ -249,7 +255,7 @@ def test_graph_replay_matches_oracle(name, w):
             for l in range(layers):
                 q, k, v = host[(s, l)]
                 if not w.kcur_separate:
-                    orings[l].append(c, *oracle_kv(k, v, fp8))
+                    orings[l].append(c, *oracle_kv(k, v, fp8, int8k))
                     o_ref, l_ref = OA.streaming_chunk_attention(bhld(q), orings[l], c, None, None, w.W, w.sink,
                                                                 w.scale)
                 else:
@@ -260,7 +266,7 @@ def test_graph_replay_matches_oracle(name, w):
         if w.kcur_separate:
             for l in range(layers):
                 _, k, v = host[(save, l)]
-                orings[l].append(c, *oracle_kv(k, v, fp8))
+                orings[l].append(c, *oracle_kv(k, v, fp8, int8k))
     assert int(d_chunk.item()) == w.chunks
     assert sab.get_last_device_error() == 0
 
