@@ -623,15 +623,18 @@ def config_records(peaks, src, stream):
 def run_attn_only(args):
     """Small profiling case: one layer of the Wan-1.3B stream at chunk 2
     (4608 keys), N back-to-back attention calls over 4 input sets; with
-    ``--case fp8_kv_e4m3_mma`` N calls of the E4M3-product kernel on the
-    long-window FP8 workload (sink + 20 slots, 8505 keys)."""
+    ``--case fp8_kv_e4m3_mma`` / ``fp8_kv`` / ``int8k_kv`` N calls over the
+    long-window 8-bit workload (sink + 20 slots, 8505 keys), with
+    ``--case ring_append`` N BF16 and N E4M3 ring appends."""
     import torch
 
     import streaming_attention_block_gb300 as sab
     from streaming_attention_block_gb300 import synth
 
-    if args.case == "fp8_kv_e4m3_mma":
+    if args.case in ("fp8_kv_e4m3_mma", "fp8_kv", "int8k_kv"):
         return run_attn_only_fp8mma(args)
+    if args.case == "ring_append":
+        return run_attn_only_append(args)
     if args.case == "block_causal_backward":
         return run_attn_only_backward(args)
     dev = torch.device("cuda", 0)
@@ -699,15 +702,52 @@ def run_attn_only_backward(args):
     assert sab.get_last_device_error(stream) == 0
 
 
-def run_attn_only_fp8mma(args):
+def run_attn_only_append(args):
+    """``--case ring_append``: N BF16 appends of a Wan-1.3B chunk, then N E4M3
+    appends of a long-window chunk, each into its own layer of a 16-layer ring
+    from 16 rotating input sets (reads and writes leave L2)."""
     import torch
 
     import streaming_attention_block_gb300 as sab
     from streaming_attention_block_gb300 import synth
 
-    w = synth.workload("fp8_kv")
+    stream = torch.cuda.current_stream()
+    g = synth.generator(7, device="cuda")
+    res = {}
+    for name, wname, kvd in (("bf16", "wan13b", sab.KV_BF16), ("fp8", "fp8_kv", sab.KV_FP8_E4M3)):
+        w = synth.workload(wname)
+        shape = (w.B, w.Lc, w.H, w.D)
+        sets = [tuple(synth.randn_bf16(g, shape, "cuda") for _ in range(2)) for _ in range(16)]
+        ring = sab.KVRing(16, w.B, w.H, w.D, w.Lc, w.R, has_sink=w.sink, kv_dtype=kvd)
+        times = []
+        for i in range(args.attn_only):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            sab.kv_ring_append(ring.handle, i % 16, i // 16, *sets[i % 16], stream)
+            b.record(stream)
+            times.append((a, b))
+        torch.cuda.synchronize()
+        us = [a.elapsed_time(b) * 1e3 for a, b in times]
+        res[name] = statistics.median(us[min(3, len(us) - 1):])
+        del sets, ring
+    print(json.dumps({"attn_only_calls": args.attn_only, "case": args.case, "us_median": res}))
+    assert sab.get_last_device_error(stream) == 0
+
+
+def run_attn_only_fp8mma(args):
+    """``--case fp8_kv_e4m3_mma``: the E4M3-product entry; ``--case fp8_kv``
+    / ``int8k_kv``: the 8-bit cache through the fp16-expansion path; the
+    library's split choice, over the first chunk with a full window."""
+    import torch
+
+    import streaming_attention_block_gb300 as sab
+    from streaming_attention_block_gb300 import synth
+
+    w = synth.workload("int8k_kv" if args.case == "int8k_kv" else "fp8_kv")
     g = synth.generator(w.seed, device="cuda")
-    ring = sab.KVRing(1, w.B, w.H, w.D, w.Lc, w.R, has_sink=w.sink, kv_dtype=sab.KV_FP8_E4M3)
+    ring = sab.KVRing(1, w.B, w.H, w.D, w.Lc, w.R, has_sink=w.sink,
+                      kv_dtype=sab.KV_INT8K_FP8V if args.case == "int8k_kv" else sab.KV_FP8_E4M3)
     sk, sv = synth.sink_kv(w, g, "cuda")
     ring.set_sink(0, sk, sv)
     for c in range(w.W + 1):  # first chunk with a full window
@@ -722,8 +762,11 @@ def run_attn_only_fp8mma(args):
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        sab.chunk_attention_fp8mma(ring.handle, 0, w.W, q, w.W, w.sink, w.scale, O, LSE, stream, num_splits=0,
-                                   workspace=ws)
+        if args.case == "fp8_kv_e4m3_mma":
+            sab.chunk_attention_fp8mma(ring.handle, 0, w.W, q, w.W, w.sink, w.scale, O, LSE, stream, num_splits=0,
+                                       workspace=ws)
+        else:
+            sab.chunk_attention(ring.handle, 0, w.W, q, None, None, w.W, w.sink, 0, w.scale, O, LSE, ws, stream)
         b.record(stream)
         times.append((a, b))
     torch.cuda.synchronize()
@@ -985,7 +1028,8 @@ def main():
     ap.add_argument("--no-graph", action="store_true", help="skip the graph-replay measurement")
     ap.add_argument("--splits", type=int, default=0, help="KV splits per attention call (0: library's choice)")
     ap.add_argument("--sweep", action="store_true", help="time one attention call of every workload")
-    ap.add_argument("--case", default="wan13b", choices=["wan13b", "fp8_kv_e4m3_mma", "block_causal_backward"],
+    ap.add_argument("--case", default="wan13b",
+                    choices=["wan13b", "fp8_kv_e4m3_mma", "fp8_kv", "int8k_kv", "ring_append", "block_causal_backward"],
                     help="workload of --attn-only")
     ap.add_argument("--attn-only", type=int, default=0, metavar="N",
                     help="profiling case: N steady-state attention calls on one layer, then exit")

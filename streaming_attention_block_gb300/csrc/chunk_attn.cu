@@ -307,7 +307,7 @@ struct KhCfg {
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
-template <int D, bool FP8, bool F8MMA>
+template <int D, bool FP8, bool F8MMA, bool K8>
 __global__ void __launch_bounds__(KhCfg<D, FP8, F8MMA>::kThreads, 1)
 chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
   using C = KhCfg<D, FP8, F8MMA>;
@@ -1114,7 +1114,7 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
           const int r = job & (kTileN - 1);
           const bool isv = job >= kTileN;
           uint8_t* tile = base + (isv ? C::kVOff : C::kKOff) + st * C::kTileBytes;
-          if (p.k_int8 && !isv) expand_code_rows2_f16<true>(tile, r, r + C::kConvThreads, C::kBoxBytes);  // INT8 keys
+          if (K8 && !isv) expand_code_rows2_f16<true>(tile, r, r + C::kConvThreads, C::kBoxBytes);  // INT8 keys
           else expand_code_rows2_f16<false>(tile, r, r + C::kConvThreads, C::kBoxBytes);
         }
         fence_proxy_async_smem();
@@ -1130,12 +1130,12 @@ chunk_attn_kh_kernel(const __grid_constant__ AttnParams p) {
   }
 }
 
-template <int D, bool FP8, bool F8MMA = false>
+template <int D, bool FP8, bool F8MMA = false, bool K8 = false>
 cudaError_t launch_kh_impl(const AttnParams& p, cudaStream_t s) {
   using C = KhCfg<D, FP8, F8MMA>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(chunk_attn_kh_kernel<D, FP8, F8MMA>,
+    cudaError_t e = cudaFuncSetAttribute(chunk_attn_kh_kernel<D, FP8, F8MMA, K8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set = true;
@@ -1150,7 +1150,7 @@ cudaError_t launch_kh_impl(const AttnParams& p, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, chunk_attn_kh_kernel<D, FP8, F8MMA>, p);
+  return cudaLaunchKernelEx(&cfg, chunk_attn_kh_kernel<D, FP8, F8MMA, K8>, p);
 }
 
 // ===========================================================================
@@ -1731,7 +1731,8 @@ cudaError_t launch_chunk_attention_kh(const AttnParams& p, cudaStream_t s) {
                                                              p.ws_count == nullptr)))
     return cudaErrorInvalidValue;
   if (p.f8mma) return (p.fp8 && !p.k_int8 && p.D == 128) ? launch_kh_impl<128, true, true>(p, s) : cudaErrorInvalidValue;
-  if (p.fp8) return p.D == 128 ? launch_kh_impl<128, true>(p, s) : cudaErrorInvalidValue;
+  if (p.fp8 && p.D != 128) return cudaErrorInvalidValue;
+  if (p.fp8) return p.k_int8 ? launch_kh_impl<128, true, false, true>(p, s) : launch_kh_impl<128, true, false, false>(p, s);
   if (p.D == 128) return launch_kh_impl<128, false>(p, s);
   if (p.D == 64) return launch_kh_impl<64, false>(p, s);
   return cudaErrorInvalidValue;
